@@ -1,0 +1,259 @@
+/*
+ * paged_kv.h -- C ABI of the PagedAttention decode library (GB300, sm_103a).
+ *
+ * The library implements the decode-time hot path of PagedAttention: each
+ * running sequence's new query token attends over that sequence's KV cache,
+ * which is stored as fixed 16-token physical blocks scattered through a shared
+ * pool and reached through a per-sequence block table; next to it sit the
+ * write of each step's new K/V into its slot, the copy-on-write block copy,
+ * and a host-side block manager that produces the tables and slot maps.
+ *
+ * Sources (web pages on PagedAttention, by title and section):
+ *  [G]  "PagedAttention（ページドアテンション）" glossary entry (jisaku.com):
+ *       "PagedAttentionの解決策" (16-token blocks, block table logical ->
+ *       physical, blocks need not be contiguous), "コピーオンライト
+ *       （Copy-on-Write）共有" (parallel sampling shares prompt blocks),
+ *       "他のKVキャッシュ最適化との組み合わせ" (GQA + paging).
+ *  [B]  "数万トークンでもVRAMが溢れない！LLM推論を爆速化する「PagedAttention」の全貌"
+ *       (blog): "OSの知恵をGPUへ" (on-demand blocks, waste only in the last
+ *       block, sharing by reference count).
+ *  [S]  abeam.tech summary of "Efficient Memory Management for Large Language
+ *       Model Serving with PagedAttention": "用語解説" (block table,
+ *       Copy-on-Write), "技術の仕組み" (the kernel reads KV through the block
+ *       table), "KV キャッシュマネージャ" (fill the last block, allocate when
+ *       full, return blocks on finish), "並列サンプリングやビームサーチでの共有"
+ *       (copy only when a write reaches a shared block), "よくある質問" (not a
+ *       new attention formula).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - Block size is 16 tokens ([G], [B]); it is fixed at compile time.
+ *  - Element type T is IEEE fp16 or bfloat16 (pkv_dtype_t) for q, out, K, V.
+ *  - Layouts (all row-major, densely packed, element strides implied):
+ *      q, out        : T[num_seqs][num_q_heads][head_dim]
+ *      k_pool, v_pool: T[num_blocks][num_kv_heads][16][head_dim]
+ *                      (one (block, kv head) tile is a contiguous 16*head_dim
+ *                      span, 4 KiB at head_dim 128)
+ *      block_tables  : int32[num_seqs][max_blocks_per_seq]; entries past
+ *                      ceil(context_len/16) are never read (pad with -1)
+ *      context_lens  : int32[num_seqs]; 0 marks an empty (padding) sequence
+ *      slot_mapping  : int64[num_tokens]; slot = block * 16 + offset, < 0 skips
+ *      src_dst_pairs : int64[num_pairs][2]
+ *    Token position p of sequence s lives in block block_tables[s][p / 16],
+ *    slot p % 16 ([G], "PagedAttentionの解決策").
+ *  - GQA: query head h reads KV head h / (num_q_heads / num_kv_heads).
+ *  - Device pointers are owned by the caller; the library never allocates
+ *    device memory. Scratch for split-K decode comes from a caller-provided
+ *    workspace (pkv_paged_attention_workspace_size).
+ *  - Every GPU call is asynchronous on `stream` (a cudaStream_t; NULL means
+ *    the legacy default stream) and returns after the launch. Scalar
+ *    arguments are checked on the host before anything is launched; on a
+ *    failed check nothing is launched and the status says why
+ *    (pkv_last_error_string gives the detail, per calling thread).
+ *  - Device-resident indices (block ids, context lengths, slots, pairs) are
+ *    checked by the kernels. A bad index never faults: the kernel records a
+ *    flag in the device status word (pkv_device_status), skips the access or
+ *    clamps it into range, and the affected output is unspecified.
+ *  - pointers must be 16-byte aligned (q, out, pools, k, v) and 4/8-byte
+ *    aligned for the int32/int64 arrays.
+ */
+#ifndef PAGED_KV_H_
+#define PAGED_KV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PKV_BLOCK_SIZE 16
+
+/* Status of every call. */
+typedef enum {
+  PKV_OK = 0,
+  PKV_ERR_INVALID_ARG = 1,   /* a size, pointer or index argument is out of range */
+  PKV_ERR_UNSUPPORTED = 2,   /* valid, but not built: dtype / head_dim / group size */
+  PKV_ERR_OUT_OF_BLOCKS = 3, /* block manager: free list cannot satisfy the call */
+  PKV_ERR_CUDA = 4,          /* a CUDA runtime call failed (launch, copy, attribute) */
+  PKV_ERR_WORKSPACE = 5      /* workspace missing or smaller than required */
+} pkv_status_t;
+
+typedef enum { PKV_F16 = 0, PKV_BF16 = 1 } pkv_dtype_t;
+
+/* Flags of the device status word (pkv_device_status). */
+#define PKV_DEV_BAD_BLOCK_ID    0x1u  /* block table entry outside [0, num_blocks) */
+#define PKV_DEV_BAD_CONTEXT_LEN 0x2u  /* context_len < 0 or > max_blocks_per_seq*16 */
+#define PKV_DEV_BAD_SLOT        0x4u  /* slot_mapping entry >= num_blocks*16 */
+#define PKV_DEV_BAD_PAIR        0x8u  /* copy pair with src or dst outside the pool */
+#define PKV_DEV_WAIT_TIMEOUT    0x10u /* a bounded wait on a copy gave up */
+
+typedef struct CUstream_st* pkv_stream_t; /* same type as cudaStream_t */
+
+/* Library version string, static storage. */
+const char* pkv_version(void);
+
+/* Detail of the last failing call made by this thread ("" if none). */
+const char* pkv_last_error_string(void);
+
+/*
+ * Reads the device status word of the current CUDA device into *flags_out
+ * (PKV_DEV_* bits, 0 = no device-side check tripped since the last clear),
+ * and clears it when `clear` is non-zero. Synchronises the device.
+ */
+pkv_status_t pkv_device_status(uint32_t* flags_out, int clear);
+
+/* ------------------------------------------------------------------------ */
+/* Decode attention                                                          */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * PagedAttention decode ([S] "技術の仕組み": the kernel follows the block
+ * table to reach each sequence's non-contiguous KV; [S] "よくある質問": the
+ * result is ordinary attention).
+ *
+ * For every sequence s and query head h (g = h / (num_q_heads/num_kv_heads),
+ * L = context_lens[s]):
+ *     out[s][h] = softmax_p( scale * <q[s][h], K_s[p]> ) . V_s[p],  p < L
+ * with K_s[p] = k_pool[block_tables[s][p/16]][g][p%16] (V likewise).
+ * Softmax, dot products and the weighted sum run in fp32 (online maximum and
+ * running sum); out is rounded once to T. L == 0 writes zeros.
+ *
+ * partition_size (tokens): 0 lets the library choose; -1 forces one pass per
+ * (sequence, KV head); any other value must be a positive multiple of 16 and
+ * splits each sequence into partitions of that many tokens, whose partial
+ * (max, sum, weighted V) are merged with a log-sum-exp merge. Sequences that
+ * fit one partition are written directly. The result does not depend on the
+ * partitioning beyond fp32 rounding.
+ *
+ * Supported: T in {fp16, bf16}; head_dim in {64, 128, 256};
+ * num_q_heads % num_kv_heads == 0 with group size <= 8.
+ *
+ * workspace: device memory of at least
+ * pkv_paged_attention_workspace_size(...) bytes for the same arguments, or
+ * NULL when that size is 0. Its contents need no initialisation, and calls
+ * that use one workspace must not overlap on the GPU.
+ */
+pkv_status_t pkv_paged_attention_decode(
+    void* out, const void* q, const void* k_pool, const void* v_pool,
+    const int32_t* block_tables, const int32_t* context_lens,
+    int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+    int max_blocks_per_seq, int num_blocks, float scale, pkv_dtype_t dtype,
+    int partition_size, void* workspace, size_t workspace_bytes,
+    pkv_stream_t stream);
+
+/* Bytes of workspace pkv_paged_attention_decode needs for these sizes
+ * (0 when the call runs in one pass). Returns 0 for invalid sizes as well. */
+size_t pkv_paged_attention_workspace_size(
+    int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+    int max_blocks_per_seq, int partition_size);
+
+/* The partition size (tokens) a call with these sizes runs with: -1 for one
+ * pass, else the split-K partition; resolves partition_size == 0. */
+int pkv_paged_attention_partition(
+    int num_seqs, int num_kv_heads, int max_blocks_per_seq, int partition_size);
+
+/* ------------------------------------------------------------------------ */
+/* Cache writes and copy-on-write                                            */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Writes each new token's K and V into its slot ([S] "KV キャッシュマネージャ":
+ * tokens fill the last block of their sequence).
+ *   k, v: T[num_tokens][num_kv_heads][head_dim]
+ *   for t with slot = slot_mapping[t] >= 0 and every KV head g:
+ *     k_pool[slot/16][g][slot%16][:] = k[t][g][:]   (v likewise)
+ * A pure bit copy. Slots >= num_blocks*16 are skipped and flagged
+ * (PKV_DEV_BAD_SLOT). Two tokens with the same slot race (unspecified winner).
+ */
+pkv_status_t pkv_reshape_and_cache(
+    const void* k, const void* v, void* k_pool, void* v_pool,
+    const int64_t* slot_mapping, int num_tokens, int num_kv_heads,
+    int head_dim, int num_blocks, pkv_dtype_t dtype, pkv_stream_t stream);
+
+/*
+ * Copy-on-write block copies ([S] "並列サンプリングやビームサーチでの共有",
+ * [G] "コピーオンライト（Copy-on-Write）共有"): for each (src, dst) pair,
+ * block src of both pools (all KV heads, all 16 slots) is copied to block dst.
+ * src_dst_pairs is device memory. The pairs must not conflict: dst values
+ * are distinct and no dst is also a src (pkv_check_copy_pairs tests this on
+ * the host; the block manager's pairs satisfy it by construction). Pairs
+ * with an id outside [0, num_blocks) are skipped and flagged.
+ */
+pkv_status_t pkv_copy_blocks(
+    void* k_pool, void* v_pool, const int64_t* src_dst_pairs, int num_pairs,
+    int num_kv_heads, int head_dim, int num_blocks, pkv_dtype_t dtype,
+    pkv_stream_t stream);
+
+/* Host check of a pair list (host memory): ids in range, dst distinct, no dst
+ * used as a src. PKV_OK or PKV_ERR_INVALID_ARG. */
+pkv_status_t pkv_check_copy_pairs(const int64_t* src_dst_pairs_host, int num_pairs,
+                                  int num_blocks);
+
+/* ------------------------------------------------------------------------ */
+/* Host block manager ([S] "KV キャッシュマネージャ", [B] "OSの知恵をGPUへ")  */
+/* ------------------------------------------------------------------------ */
+/*
+ * Host memory only; not thread-safe (one handle per thread or external lock).
+ * Free list: a stack, initially initial_free_order (index 0 at the bottom)
+ * or 0..num_blocks-1; allocation pops the top; a block whose refcount drops
+ * to 0 is pushed back. Within a call, blocks are taken in logical order and
+ * returned in table order. Every failing call leaves the state unchanged.
+ */
+typedef struct pkv_bm pkv_bm_t;
+
+/* block_size must be 16. initial_free_order: NULL or a permutation of
+ * 0..num_blocks-1 (host). */
+pkv_status_t pkv_bm_create(int num_blocks, int block_size,
+                           const int32_t* initial_free_order, pkv_bm_t** out);
+void pkv_bm_destroy(pkv_bm_t* bm);
+
+/* New sequence holding num_tokens tokens: ceil(num_tokens/16) fresh blocks. */
+pkv_status_t pkv_bm_add_seq(pkv_bm_t* bm, int64_t seq_id, int64_t num_tokens);
+
+/* child shares every block of parent (refcount + 1 each); no data moves
+ * ([B]: sharing by reference count only). */
+pkv_status_t pkv_bm_fork(pkv_bm_t* bm, int64_t parent, int64_t child);
+
+/*
+ * Reserves the slot of the sequence's next token. With L tokens:
+ *  - L % 16 == 0: a new block is appended;
+ *  - else if the last block is shared (refcount > 1): copy-on-write -- a new
+ *    block replaces it in this table, the old block's refcount drops by one,
+ *    and (*cow_src_out, *cow_dst_out) = (old, new) must be copied with
+ *    pkv_copy_blocks before the new token is written;
+ *  - else the token goes into the last block in place.
+ * *slot_out = table[L/16]*16 + L%16; the length becomes L+1. The CoW outputs
+ * are -1 when no copy is needed.
+ */
+pkv_status_t pkv_bm_append_slot(pkv_bm_t* bm, int64_t seq_id, int64_t* slot_out,
+                                int64_t* cow_src_out, int64_t* cow_dst_out);
+
+/* append_slot for n sequences in order, all-or-nothing. slots_out[n];
+ * pairs_out[n][2] receives the copy pairs packed at the front and
+ * *num_pairs_out their count. */
+pkv_status_t pkv_bm_append_slots(pkv_bm_t* bm, const int64_t* seq_ids, int n,
+                                 int64_t* slots_out, int64_t* pairs_out,
+                                 int* num_pairs_out);
+
+/* Drop the sequence; blocks whose refcount reaches 0 return to the free list. */
+pkv_status_t pkv_bm_free_seq(pkv_bm_t* bm, int64_t seq_id);
+
+/* Padded block tables and lengths of n sequences (host buffers):
+ * table_out[n][max_blocks_per_seq] (-1 padded), lens_out[n]. */
+pkv_status_t pkv_bm_block_tables(const pkv_bm_t* bm, const int64_t* seq_ids, int n,
+                                 int max_blocks_per_seq, int32_t* table_out,
+                                 int32_t* lens_out);
+
+pkv_status_t pkv_bm_refcount(const pkv_bm_t* bm, int block, int32_t* out);
+pkv_status_t pkv_bm_seq_len(const pkv_bm_t* bm, int64_t seq_id, int64_t* out);
+int pkv_bm_num_free(const pkv_bm_t* bm);
+int pkv_bm_num_seqs(const pkv_bm_t* bm);
+/* Copies the free stack (bottom first) into out[capacity]; returns its size. */
+int pkv_bm_free_stack(const pkv_bm_t* bm, int32_t* out, int capacity);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGED_KV_H_ */

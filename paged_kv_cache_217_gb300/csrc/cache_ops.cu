@@ -1,0 +1,114 @@
+// reshape_and_cache and copy_blocks: bit copies with 16-byte vectors.
+//
+// reshape_and_cache writes each decode step's new K/V row into its slot, the
+// "fill the last block" step of the KV cache manager (abeam.tech summary of
+// "Efficient Memory Management for Large Language Model Serving with
+// PagedAttention", section "KV キャッシュマネージャ"). copy_blocks is the
+// copy-on-write duplication of a shared block (same summary, section
+// "並列サンプリングやビームサーチでの共有"; glossary entry
+// "PagedAttention（ページドアテンション）", "コピーオンライト（Copy-on-Write）共有").
+// Both are HBM-bound copies; each thread moves 16-byte vectors, consecutive
+// threads consecutive vectors, so loads and stores are fully coalesced.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "device_common.cuh"
+#include "launch.h"
+
+namespace pkv {
+namespace {
+
+// One thread per 16-byte vector of a (token, KV head) row.
+__global__ void __launch_bounds__(256)
+reshape_and_cache_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
+                         uint4* __restrict__ k_pool, uint4* __restrict__ v_pool,
+                         const int64_t* __restrict__ slots, int64_t total, int num_kv_heads,
+                         int vec_per_row, int64_t num_slots, unsigned int* status) {
+  const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= total) return;
+  const int c = int(i % vec_per_row);
+  const int64_t tg = i / vec_per_row;
+  const int gh = int(tg % num_kv_heads);
+  const int64_t t = tg / num_kv_heads;
+  const int64_t slot = __ldg(slots + t);
+  if (slot < 0) return;
+  if (slot >= num_slots) {
+    if (gh == 0 && c == 0) flag(status, PKV_DEV_BAD_SLOT);
+    return;
+  }
+  const int64_t blk = slot / kBlock, off = slot % kBlock;
+  const int64_t dst = ((blk * num_kv_heads + gh) * kBlock + off) * vec_per_row + c;
+  k_pool[dst] = __ldg(k + i);
+  v_pool[dst] = __ldg(v + i);
+}
+
+constexpr int kCopyThreads = 256;
+constexpr int kCopyVecPerThread = 4;
+
+// grid.y = pair; grid.x strides over the block's 16-byte vectors (all KV heads).
+__global__ void __launch_bounds__(kCopyThreads)
+copy_blocks_kernel(uint4* __restrict__ k_pool, uint4* __restrict__ v_pool,
+                   const int64_t* __restrict__ pairs, int64_t vec_per_block, int num_blocks,
+                   unsigned int* status) {
+  const int p = blockIdx.y;
+  const int64_t src = __ldg(pairs + 2 * p), dst = __ldg(pairs + 2 * p + 1);
+  if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) flag(status, PKV_DEV_BAD_PAIR);
+    return;
+  }
+  const uint4* ks = k_pool + src * vec_per_block;
+  const uint4* vs = v_pool + src * vec_per_block;
+  uint4* kd = k_pool + dst * vec_per_block;
+  uint4* vd = v_pool + dst * vec_per_block;
+  const int64_t base = int64_t(blockIdx.x) * kCopyThreads * kCopyVecPerThread + threadIdx.x;
+  uint4 kr[kCopyVecPerThread], vr[kCopyVecPerThread];
+#pragma unroll
+  for (int u = 0; u < kCopyVecPerThread; ++u) {
+    const int64_t i = base + int64_t(u) * kCopyThreads;
+    if (i < vec_per_block) {
+      kr[u] = ks[i];
+      vr[u] = vs[i];
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < kCopyVecPerThread; ++u) {
+    const int64_t i = base + int64_t(u) * kCopyThreads;
+    if (i < vec_per_block) {
+      kd[i] = kr[u];
+      vd[i] = vr[u];
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_reshape_and_cache(const void* k, const void* v, void* k_pool, void* v_pool,
+                                     const int64_t* slots, int num_tokens, int num_kv_heads,
+                                     int head_dim, int num_blocks, unsigned int* status,
+                                     cudaStream_t stream) {
+  const int vec_per_row = head_dim / 8;
+  const int64_t total = int64_t(num_tokens) * num_kv_heads * vec_per_row;
+  if (total == 0) return cudaSuccess;
+  const int64_t nblk = (total + 255) / 256;
+  reshape_and_cache_kernel<<<unsigned(nblk), 256, 0, stream>>>(
+      static_cast<const uint4*>(k), static_cast<const uint4*>(v), static_cast<uint4*>(k_pool),
+      static_cast<uint4*>(v_pool), slots, total, num_kv_heads, vec_per_row,
+      int64_t(num_blocks) * kBlock, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_copy_blocks(void* k_pool, void* v_pool, const int64_t* pairs, int num_pairs,
+                               int num_kv_heads, int head_dim, int num_blocks,
+                               unsigned int* status, cudaStream_t stream) {
+  if (num_pairs == 0) return cudaSuccess;
+  const int64_t vec_per_block = int64_t(num_kv_heads) * kBlock * head_dim / 8;
+  const int64_t per_cta = int64_t(kCopyThreads) * kCopyVecPerThread;
+  const dim3 grid(unsigned((vec_per_block + per_cta - 1) / per_cta), unsigned(num_pairs));
+  copy_blocks_kernel<<<grid, kCopyThreads, 0, stream>>>(static_cast<uint4*>(k_pool),
+                                                        static_cast<uint4*>(v_pool), pairs,
+                                                        vec_per_block, num_blocks, status);
+  return cudaGetLastError();
+}
+
+}  // namespace pkv

@@ -186,3 +186,46 @@ def to_numpy_storage(t, dtype):
     if dtype == "f16":
         return t.numpy()
     return t.view(torch.int16).numpy().view(np.uint16)
+
+
+@dataclass
+class SamplingPlan:
+    """What driving a block manager through a ParallelSamplingTrace produced."""
+    seq_ids: list               # sample s of prompt i has id i * n + s
+    prompt_of: list             # prompt index of each sequence
+    step_slots: list            # per decode step: (seq ids appending, int64 slots)
+    pairs: list                 # copy-on-write (src, dst) pairs, in emission order
+    final_lens: dict            # seq id -> tokens after the tails
+
+
+def drive_parallel_sampling(trace, bm):
+    """Runs the parallel-sampling script against any block manager with
+    add_seq / fork / append_slot: add each prompt as sample 0, fork samples
+    1..n-1 from it, then decode the tails one step at a time; in each step
+    every sequence whose tail is not finished appends one token, in
+    ascending sequence id."""
+    n = trace.n
+    seq_ids, prompt_of = [], []
+    for i, plen in enumerate(trace.prompt_lens.tolist()):
+        root = i * n
+        bm.add_seq(root, plen)
+        seq_ids.append(root)
+        prompt_of.append(i)
+        for c in range(1, n):
+            bm.fork(root, root + c)
+            seq_ids.append(root + c)
+            prompt_of.append(i)
+    tails = {i * n + c: int(trace.tail_lens[i, c]) for i in range(trace.prompt_lens.shape[0])
+             for c in range(n)}
+    steps, pairs = [], []
+    for step in range(int(trace.tail_lens.max()) if trace.tail_lens.size else 0):
+        active = [sid for sid in seq_ids if tails[sid] > step]
+        slots = np.empty(len(active), dtype=np.int64)
+        for j, sid in enumerate(active):
+            slot, src, dst = bm.append_slot(sid)
+            slots[j] = slot
+            if src >= 0:
+                pairs.append((src, dst))
+        steps.append((active, slots))
+    final = {sid: int(trace.prompt_lens[sid // n]) + tails[sid] for sid in seq_ids}
+    return SamplingPlan(seq_ids, prompt_of, steps, pairs, final)

@@ -1,0 +1,120 @@
+"""The C-ABI library without a GPU: it loads, exports every function that
+include/paged_kv.h declares, sizes workspaces, picks partitions, and rejects
+bad arguments on the host before anything would be launched."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from paged_kv_cache_217_gb300 import binding as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if not fn.endswith(".h"):
+            continue
+        with open(os.path.join(ROOT, "include", fn)) as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        names |= set(re.findall(r"\b(pkv_[a-z0-9_]+)\s*\(", text))
+    return sorted(names)
+
+
+def test_library_exports_every_declared_function():
+    lib = B.lib()
+    declared = _declared_functions()
+    assert len(declared) >= 20
+    missing = [n for n in declared if not hasattr(lib, n)]
+    assert not missing, f"declared but not exported: {missing}"
+    assert sorted(declared) == B.declared_symbols()
+    assert B.version().startswith("paged_kv")
+
+
+def test_workspace_and_partition_choice():
+    # short contexts run in one pass and need no workspace
+    assert B.resolved_partition(64, 40, 32) == -1
+    assert B.workspace_size(64, 40, 40, 128, 32) == 0
+    # longer contexts split into 512-token partitions by default
+    assert B.resolved_partition(64, 40, 128) == 512
+    parts = 128 * 16 // 512
+    assert B.workspace_size(64, 40, 40, 128, 128) == 64 * 40 * parts * (128 * 4 + 8)
+    # explicit choices
+    assert B.resolved_partition(8, 96, 2048, -1) == -1
+    assert B.resolved_partition(8, 96, 2048, 256) == 256
+    assert B.workspace_size(8, 96, 96, 128, 2048, -1) == 0
+    assert B.workspace_size(8, 96, 96, 128, 2048, 512) == 8 * 96 * 64 * (128 * 4 + 8)
+    # a partition that covers the whole context is one pass
+    assert B.resolved_partition(4, 4, 4, 64) == -1
+    assert B.workspace_size(4, 4, 4, 64, 4, 64) == 0
+    # invalid partition sizes
+    assert B.resolved_partition(4, 4, 4, 24) == 0
+    assert B.workspace_size(0, 4, 4, 64, 4) == 0
+
+
+FAKE = 0x10000  # a 16-byte aligned address; never dereferenced because every call below fails its checks
+
+
+def _decode(**kw):
+    a = dict(out=FAKE, q=FAKE, k=FAKE, v=FAKE, bt=FAKE, cl=FAKE, S=4, Hq=4, Hkv=4, D=64, MB=4, NB=64,
+             scale=0.125, dt=B.PKV_F16, part=0, ws=None, wsb=0)
+    a.update(kw)
+    st = B.lib().pkv_paged_attention_decode(a["out"], a["q"], a["k"], a["v"], a["bt"], a["cl"], a["S"], a["Hq"],
+                                            a["Hkv"], a["D"], a["MB"], a["NB"], a["scale"], a["dt"], a["part"],
+                                            a["ws"], a["wsb"], None)
+    return st, B.lib().pkv_last_error_string().decode()
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(Hq=6, Hkv=4), 1),           # not a multiple
+    (dict(Hq=32, Hkv=2), 2),          # group 16 > 8
+    (dict(D=80), 2),                  # head_dim
+    (dict(dt=7), 2),                  # dtype
+    (dict(MB=0), 1),
+    (dict(NB=0), 1),
+    (dict(S=70000), 2),
+    (dict(scale=float("inf")), 1),
+    (dict(q=None), 1),
+    (dict(q=FAKE + 8), 1),            # misaligned
+    (dict(part=24), 1),               # not a multiple of 16
+    (dict(MB=64, part=16), 5),        # split needs a workspace
+    (dict(MB=64, part=16, ws=FAKE, wsb=100), 5),
+])
+def test_decode_rejects_bad_arguments_before_launch(kw, status):
+    st, msg = _decode(**kw)
+    assert st == status, msg
+    assert msg
+
+
+def test_zero_sequences_is_a_no_op():
+    assert _decode(S=0, out=None, q=None)[0] == 0
+
+
+def test_cache_ops_reject_bad_arguments():
+    L = B.lib()
+    assert L.pkv_reshape_and_cache(FAKE, FAKE, FAKE, FAKE, FAKE, 0, 4, 64, 8, 0, None) == 0   # no tokens
+    assert L.pkv_reshape_and_cache(FAKE, FAKE, FAKE, FAKE, FAKE, -1, 4, 64, 8, 0, None) == 1
+    assert L.pkv_reshape_and_cache(FAKE, FAKE, FAKE, FAKE, FAKE, 2, 4, 60, 8, 0, None) == 2
+    assert L.pkv_reshape_and_cache(FAKE + 4, FAKE, FAKE, FAKE, FAKE, 2, 4, 64, 8, 0, None) == 1
+    assert L.pkv_reshape_and_cache(None, FAKE, FAKE, FAKE, FAKE, 2, 4, 64, 8, 0, None) == 1
+    assert L.pkv_copy_blocks(FAKE, FAKE, FAKE, 0, 4, 64, 8, 0, None) == 0                     # no pairs
+    assert L.pkv_copy_blocks(FAKE, FAKE, FAKE, -1, 4, 64, 8, 0, None) == 1
+    assert L.pkv_copy_blocks(FAKE, FAKE, FAKE, 70000, 4, 64, 8, 0, None) == 2
+    assert L.pkv_copy_blocks(FAKE, FAKE, FAKE + 4, 2, 4, 64, 8, 0, None) == 1
+    assert L.pkv_copy_blocks(FAKE, FAKE, FAKE, 2, 4, 64, 8, 9, None) == 2
+
+
+def test_device_status_needs_an_argument():
+    assert B.lib().pkv_device_status(None, 0) == 1
+
+
+def test_missing_library_fails_loudly(monkeypatch):
+    monkeypatch.setattr(B, "_lib", None)
+    monkeypatch.setattr(B, "LIB_PATH", "/nonexistent/libpaged_kv.so")
+    with pytest.raises(B.LibraryNotBuilt):
+        B.lib()

@@ -1,0 +1,256 @@
+"""GPU parity of paged_attention_decode (through the C ABI) against the fp64 oracle.
+
+Small cases compare every output element; the full-size workloads compare
+sampled (sequence, head) outputs, in the launch configuration the benchmark
+times (automatic partition choice)."""
+
+import numpy as np
+import pytest
+import torch
+
+import helpers as H
+import oracle.attention as OA
+from oracle.block_manager import OracleBlockManager
+import oracle.cache_ops as OC
+from paged_kv_cache_217_gb300 import binding as B
+from paged_kv_cache_217_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    H.ensure_built()
+    B.device_status(clear=True)
+    yield
+    flags = B.device_status(clear=True)
+    assert flags == 0, f"device flags raised: {B.describe_device_flags(flags)}"
+
+
+def _run(case, partition=0):
+    out = case.new_out()
+    B.paged_attention_decode(out, case.q, case.k_pool, case.v_pool, case.tables, case.lens, case.scale,
+                             partition_size=partition)
+    torch.cuda.synchronize()
+    return out
+
+
+# ---------------------------------------------------------------------------
+# tiny decode (batch 4, L = 5, 17, 33, 64, 4 heads, d 64, fp16), tables from
+# the block manager over a seeded permutation of a 64-block pool, then one
+# new token per sequence written with reshape_and_cache
+# ---------------------------------------------------------------------------
+def test_tiny_decode_with_reshape():
+    shape = W.tiny_decode()
+    order = W.shuffled_free_order(64, 0)
+    bm, obm = B.BlockManager(64, order), OracleBlockManager(64, initial_free_order=order)
+    for s, L in enumerate(shape.context_lens.tolist()):
+        bm.add_seq(s, L)
+        obm.add_seq(s, L)
+    tables, lens = bm.block_tables(range(4), 5)
+    dev = "cuda"
+    kp = W.normal_values((64, 4, 16, 64), "f16", 1, dev)
+    vp = W.normal_values((64, 4, 16, 64), "f16", 2, dev)
+    q = W.normal_values((4, 4, 64), "f16", 3, dev)
+    case = H.DecodeCase(q, kp, vp, torch.from_numpy(tables).to(dev), torch.from_numpy(lens).to(dev),
+                        1.0 / 8.0, "f16")
+    want = H.oracle_full(case)
+    for part in (0, -1, 16, 32):
+        e = H.assert_attention_close(H.to_f64(_run(case, part)), want, f"tiny part={part}")
+        assert e["max_abs"] <= 2e-3  # fp16 outputs meet the plain absolute bound
+
+    # one new token per sequence into its next slot (L=64 needs a fifth block)
+    slots, pairs = bm.append_slots(range(4))
+    assert slots.tolist() == [obm.append_slot(s)[0] for s in range(4)] and pairs.size == 0
+    knew = W.normal_values((4, 4, 64), "f16", 4, dev)
+    vnew = W.normal_values((4, 4, 64), "f16", 5, dev)
+    k_before, v_before = W.to_numpy_storage(kp, "f16"), W.to_numpy_storage(vp, "f16")
+    B.reshape_and_cache(knew, vnew, kp, vp, torch.from_numpy(slots).to(dev))
+    torch.cuda.synchronize()
+    ok, ov = OC.reshape_and_cache(W.to_numpy_storage(knew, "f16"), W.to_numpy_storage(vnew, "f16"),
+                                  k_before, v_before, slots)
+    assert np.array_equal(W.to_numpy_storage(kp, "f16").view(np.uint16), ok.view(np.uint16))
+    assert np.array_equal(W.to_numpy_storage(vp, "f16").view(np.uint16), ov.view(np.uint16))
+    tables2, lens2 = bm.block_tables(range(4), 5)
+    assert lens2.tolist() == [6, 18, 34, 65]
+    case2 = H.DecodeCase(q, kp, vp, torch.from_numpy(tables2).to(dev), torch.from_numpy(lens2).to(dev),
+                         1.0 / 8.0, "f16")
+    H.assert_attention_close(H.to_f64(_run(case2)), H.oracle_full(case2), "tiny after reshape")
+
+
+# ---------------------------------------------------------------------------
+# shapes, dtypes, group sizes and partitions, every element compared
+# ---------------------------------------------------------------------------
+RAGGED = [1, 15, 16, 17, 31, 33, 100, 0, 255, 257, 700]
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("hq,hkv", [(4, 4), (8, 2), (32, 8), (6, 2), (16, 2), (3, 1)])
+def test_decode_matches_oracle(dtype, d, hq, hkv):
+    case = H.make_case(RAGGED, hq, hkv, d, dtype, seed=d + hq + hkv, extra_cols=3)
+    want = H.oracle_full(case)
+    for part in (0, -1, 64, 512):
+        H.assert_attention_close(H.to_f64(_run(case, part)), want, f"{dtype} d={d} {hq}/{hkv} part={part}")
+
+
+def test_zero_length_rows_are_zero_and_others_untouched():
+    case = H.make_case([0, 5, 0, 40], 8, 4, 128, "bf16", seed=3)
+    out = _run(case)
+    assert torch.all(out[0] == 0) and torch.all(out[2] == 0)
+    H.assert_attention_close(H.to_f64(out), H.oracle_full(case), "zero rows")
+
+
+def test_scores_large_and_scale_extremes():
+    # large logits: values x 8 make exp() span many orders of magnitude
+    case = H.make_case([300, 47, 1000], 8, 8, 128, "f16", seed=4, scale=1.0)
+    case.q.mul_(4)
+    case.k_pool.mul_(2)
+    H.assert_attention_close(H.to_f64(_run(case)), H.oracle_full(case), "large logits")
+    H.assert_attention_close(H.to_f64(_run(case, 16)), H.oracle_full(case), "large logits split 16")
+
+
+# ---------------------------------------------------------------------------
+# invariants the pages fix
+# ---------------------------------------------------------------------------
+def test_physical_permutation_is_bit_identical():
+    case = H.make_case([37, 300, 1000, 12], 32, 8, 128, "bf16", seed=5, pool_factor=2.0)
+    base = _run(case)
+    nb = case.k_pool.shape[0]
+    pi = torch.from_numpy(np.random.default_rng(9).permutation(nb)).to("cuda")
+    kp2 = torch.empty_like(case.k_pool)
+    vp2 = torch.empty_like(case.v_pool)
+    kp2[pi] = case.k_pool
+    vp2[pi] = case.v_pool
+    t2 = torch.where(case.tables >= 0, pi[case.tables.clamp(min=0).long()].int(), case.tables)
+    moved = H.DecodeCase(case.q, kp2, vp2, t2.contiguous(), case.lens, case.scale, case.dtype)
+    assert torch.equal(_run(moved), base)
+
+
+def test_partition_size_invariance():
+    case = H.make_case([5000, 4097, 513, 64], 8, 8, 128, "f16", seed=6)
+    outs = [H.to_f64(_run(case, p)) for p in (-1, 16, 512, 1024, 0)]
+    want = H.oracle_full(case)
+    for o in outs:
+        H.assert_attention_close(o, want, "partition")
+    for o in outs[1:]:
+        assert np.abs(o - outs[0]).max() <= 4e-3
+
+
+def test_cow_siblings_bit_identical_over_shared_prefix():
+    hkv, d, prompt, n = 8, 128, 517, 4
+    nb = 200
+    order = W.shuffled_free_order(nb, 1)
+    bm = B.BlockManager(nb, order)
+    bm.add_seq(0, prompt)
+    for c in range(1, n):
+        bm.fork(0, c)
+    kp = W.normal_values((nb, hkv, 16, d), "f16", 11, "cuda")
+    vp = W.normal_values((nb, hkv, 16, d), "f16", 12, "cuda")
+    slots, pairs = bm.append_slots(range(n))
+    assert pairs.shape == (n - 1, 2)
+    k_before = W.to_numpy_storage(kp, "f16")
+    B.copy_blocks(kp, vp, torch.from_numpy(pairs).to("cuda"))
+    knew = W.normal_values((n, hkv, d), "f16", 13, "cuda")
+    B.reshape_and_cache(knew, knew, kp, vp, torch.from_numpy(slots).to("cuda"))
+    torch.cuda.synchronize()
+    k_after = W.to_numpy_storage(kp, "f16")
+    for src, dst in pairs.tolist():
+        assert np.array_equal(k_after[dst, :, :prompt % 16], k_before[src, :, :prompt % 16])
+    tables, lens = bm.block_tables(range(n), 40)
+    q = W.normal_values((1, hkv, d), "f16", 14, "cuda").expand(n, hkv, d).contiguous()
+    shared = H.DecodeCase(q, kp, vp, torch.from_numpy(tables).cuda(),
+                          torch.full((n,), prompt, dtype=torch.int32, device="cuda"), d ** -0.5, "f16")
+    out = _run(shared)
+    for s in range(1, n):
+        assert torch.equal(out[s], out[0])
+    grown = H.DecodeCase(q, kp, vp, torch.from_numpy(tables).cuda(), torch.from_numpy(lens).cuda(),
+                         d ** -0.5, "f16")
+    H.assert_attention_close(H.to_f64(_run(grown)), H.oracle_full(grown), "siblings after append")
+
+
+# ---------------------------------------------------------------------------
+# device-side index checks: flagged, never faulting
+# ---------------------------------------------------------------------------
+def test_bad_device_indices_are_flagged():
+    case = H.make_case([40, 20], 4, 4, 64, "f16", seed=7)
+    B.device_status(clear=True)
+    bad = case.tables.clone()
+    bad[0, 1] = case.k_pool.shape[0] + 5        # outside the pool
+    B.paged_attention_decode(case.new_out(), case.q, case.k_pool, case.v_pool, bad, case.lens, case.scale)
+    assert B.device_status(clear=True) & 0x1
+    lens = case.lens.clone()
+    lens[1] = 10_000                              # longer than the table allows
+    B.paged_attention_decode(case.new_out(), case.q, case.k_pool, case.v_pool, case.tables, lens, case.scale)
+    assert B.device_status(clear=True) & 0x2
+    out = _run(case)                              # a clean call raises nothing
+    assert B.device_status(clear=True) == 0
+    H.assert_attention_close(H.to_f64(out), H.oracle_full(case), "after flags")
+
+
+# ---------------------------------------------------------------------------
+# full-size workloads, sampled outputs, automatic partitioning (bench config)
+# ---------------------------------------------------------------------------
+def _sample_pairs(rng, S, hq, k):
+    pairs = {(0, 0), (S - 1, hq - 1)}
+    while len(pairs) < k:
+        pairs.add((int(rng.integers(S)), int(rng.integers(hq))))
+    return sorted(pairs)
+
+
+def _check_sampled(case, out, k, seed):
+    rng = np.random.default_rng(seed)
+    pairs = _sample_pairs(rng, case.q.shape[0], case.q.shape[1], k)
+    want = H.oracle_sampled(case, pairs)
+    got = H.to_f64(out)
+    for (s, h), w in want.items():
+        H.assert_attention_close(got[s, h], w, f"seq {s} head {h}")
+    assert torch.isfinite(out).all()
+
+
+@pytest.mark.parametrize("name", ["llama13b", "llama3_8b", "opt175b_long"])
+def test_full_size_decode_sampled(name):
+    shape = W.CONFIGS[name](0)
+    case = H.make_case(shape.context_lens, shape.num_q_heads, shape.num_kv_heads, shape.head_dim,
+                       shape.dtype, seed=0)
+    out = _run(case)
+    _check_sampled(case, out, 12 if name == "opt175b_long" else 40, seed=1)
+    del case, out
+    torch.cuda.empty_cache()
+
+
+def test_full_size_parallel_sampling():
+    trace = W.opt66b_parallel_sampling(0)
+    nb = trace.block_budget()
+    bm = B.BlockManager(nb, W.shuffled_free_order(nb, 0))
+    plan = W.drive_parallel_sampling(trace, bm)
+    dev = "cuda"
+    kp = W.normal_values((nb, 72, 16, 128), "f16", 21, dev)
+    vp = W.normal_values((nb, 72, 16, 128), "f16", 22, dev)
+    k_host_blocks = {}
+    for src, dst in plan.pairs:
+        k_host_blocks[src] = kp[src].clone()
+    B.check_copy_pairs(plan.pairs, nb)
+    B.copy_blocks(kp, vp, torch.tensor(plan.pairs, dtype=torch.int64, device=dev).reshape(-1, 2))
+    for src, dst in plan.pairs:
+        assert torch.equal(kp[dst], k_host_blocks[src])
+    all_slots = np.concatenate([sl for _, sl in plan.step_slots]) if plan.step_slots else np.zeros(0, np.int64)
+    knew = W.normal_values((all_slots.size, 72, 128), "f16", 23, dev)
+    vnew = W.normal_values((all_slots.size, 72, 128), "f16", 24, dev)
+    B.reshape_and_cache(knew, vnew, kp, vp, torch.from_numpy(all_slots).to(dev))
+    tables, lens = bm.block_tables(plan.seq_ids, max(-(-L // 16) for L in plan.final_lens.values()))
+    assert lens.tolist() == [plan.final_lens[s] for s in plan.seq_ids]
+    q = W.normal_values((len(plan.seq_ids), 72, 128), "f16", 25, dev)
+    case = H.DecodeCase(q, kp, vp, torch.from_numpy(tables).to(dev), torch.from_numpy(lens).to(dev),
+                        128 ** -0.5, "f16")
+    out = _run(case)
+    _check_sampled(case, out, 24, seed=2)
+    # a sibling's shared prompt blocks are the very same physical blocks
+    n = trace.n
+    t = tables
+    for i in range(trace.prompt_lens.shape[0]):
+        full = int(trace.prompt_lens[i]) // 16
+        for c in range(1, n):
+            assert np.array_equal(t[i * n + c, :full], t[i * n, :full])

@@ -345,12 +345,13 @@ paged_decode_kernel(const DecodeArgs a) {
     }
   }
 
-  // Publish the warp's (m, l, acc) in its own ring (all its copies have landed).
+  // Publish the warp's (acc, m, l) in its own ring (all its copies have landed):
+  // acc[G][D] first so its float4 stores stay 16-byte aligned, then m[G], l[G].
   float* wsm = reinterpret_cast<float*>(ring);
   if (r == 0) {
 #pragma unroll
     for (int h = 0; h < G; ++h) {
-      float4* dst = reinterpret_cast<float4*>(wsm + 2 * G + h * D + sub * 8);
+      float4* dst = reinterpret_cast<float4*>(wsm + h * D + sub * 8);
       dst[0] = make_float4(acc[h][0], acc[h][1], acc[h][2], acc[h][3]);
       dst[1] = make_float4(acc[h][4], acc[h][5], acc[h][6], acc[h][7]);
     }
@@ -358,8 +359,8 @@ paged_decode_kernel(const DecodeArgs a) {
   if (lane == 0) {
 #pragma unroll
     for (int h = 0; h < G; ++h) {
-      wsm[h] = mrun[h];
-      wsm[G + h] = lsum[h];
+      wsm[G * D + h] = mrun[h];
+      wsm[G * D + G + h] = lsum[h];
     }
   }
   __syncthreads();
@@ -372,18 +373,18 @@ paged_decode_kernel(const DecodeArgs a) {
     float M = -INFINITY;
 #pragma unroll
     for (int w = 0; w < NW; ++w)
-      M = fmaxf(M, reinterpret_cast<const float*>(smem + size_t(w) * STAGES * C::STAGE_BYTES)[h]);
+      M = fmaxf(M, reinterpret_cast<const float*>(smem + size_t(w) * STAGES * C::STAGE_BYTES)[G * D + h]);
     float den = 0.f, num[8];
 #pragma unroll
     for (int c = 0; c < 8; ++c) num[c] = 0.f;
 #pragma unroll
     for (int w = 0; w < NW; ++w) {
       const float* ws = reinterpret_cast<const float*>(smem + size_t(w) * STAGES * C::STAGE_BYTES);
-      const float mw = ws[h];
+      const float mw = ws[G * D + h];
       if (mw == -INFINITY) continue;
       const float wt = fast_exp2(mw - M);
-      den = fmaf(wt, ws[G + h], den);
-      const float4* src = reinterpret_cast<const float4*>(ws + 2 * G + h * D + c8 * 8);
+      den = fmaf(wt, ws[G * D + G + h], den);
+      const float4* src = reinterpret_cast<const float4*>(ws + h * D + c8 * 8);
       const float4 x0 = src[0], x1 = src[1];
       num[0] = fmaf(wt, x0.x, num[0]);
       num[1] = fmaf(wt, x0.y, num[1]);

@@ -153,6 +153,37 @@ size_t pkv_paged_attention_workspace_size(
 int pkv_paged_attention_partition(
     int num_seqs, int num_kv_heads, int max_blocks_per_seq, int partition_size);
 
+/*
+ * Decode attention that allocates nothing (the pages have no counterpart;
+ * this is a deployment convenience of this library).
+ *
+ * Same arguments, semantics and results as pkv_paged_attention_decode,
+ * without the workspace. For callers that cannot allocate device memory when
+ * they decode -- e.g. a serving engine that reserves nearly all HBM for its
+ * KV-cache pool, or host code that must not call cudaMalloc/cudaFree on its
+ * critical path because they can synchronise the device -- split-K scratch
+ * comes from a fixed array in the library's module memory of
+ * PKV_NOALLOC_SCRATCH_BYTES, which every GPU that loads the library holds
+ * until the process exits. Sizes whose split-K scratch
+ * (pkv_paged_attention_workspace_size) exceeds it return PKV_ERR_UNSUPPORTED
+ * and launch nothing; a larger partition_size or -1 (one pass) needs less.
+ *
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture. Every call on a device shares the one array, which keeps the last
+ * call's contents; nothing in it needs to start at zero. Calls that overlap
+ * on the GPU (different streams, or different host threads) race on it.
+ * No cudaMalloc, cudaFree or other allocating routine is called.
+ */
+#define PKV_NOALLOC_SCRATCH_BYTES (32u << 20) /* 32 MiB */
+
+pkv_status_t pkv_paged_attention_decode_noalloc(
+    void* out, const void* q, const void* k_pool, const void* v_pool,
+    const int32_t* block_tables, const int32_t* context_lens,
+    int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+    int max_blocks_per_seq, int num_blocks, float scale, pkv_dtype_t dtype,
+    int partition_size, pkv_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* Cache writes and copy-on-write                                            */
 /* ------------------------------------------------------------------------ */

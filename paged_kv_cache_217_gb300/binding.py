@@ -22,6 +22,7 @@ STATUS = {0: "PKV_OK", 1: "PKV_ERR_INVALID_ARG", 2: "PKV_ERR_UNSUPPORTED",
           3: "PKV_ERR_OUT_OF_BLOCKS", 4: "PKV_ERR_CUDA", 5: "PKV_ERR_WORKSPACE"}
 PKV_F16, PKV_BF16 = 0, 1
 BLOCK_SIZE = 16
+NOALLOC_SCRATCH_BYTES = 32 << 20   # PKV_NOALLOC_SCRATCH_BYTES
 
 DEV_FLAGS = {0x1: "BAD_BLOCK_ID", 0x2: "BAD_CONTEXT_LEN", 0x4: "BAD_SLOT", 0x8: "BAD_PAIR",
              0x10: "WAIT_TIMEOUT"}
@@ -52,6 +53,7 @@ _SIGS = {
     "pkv_device_status": ([ctypes.POINTER(ctypes.c_uint32), _c_int], _c_int),
     "pkv_paged_attention_decode": ([_c_p] * 6 + [_c_int] * 6 + [_c_f, _c_int, _c_int, _c_p, _c_sz, _c_p],
                                    _c_int),
+    "pkv_paged_attention_decode_noalloc": ([_c_p] * 6 + [_c_int] * 6 + [_c_f, _c_int, _c_int, _c_p], _c_int),
     "pkv_paged_attention_workspace_size": ([_c_int] * 6, _c_sz),
     "pkv_paged_attention_partition": ([_c_int] * 4, _c_int),
     "pkv_reshape_and_cache": ([_c_p] * 5 + [_c_int] * 5 + [_c_p], _c_int),
@@ -194,6 +196,37 @@ def paged_attention_decode(out, q, k_pool, v_pool, block_tables, context_lens, s
         out.data_ptr(), q.data_ptr(), k_pool.data_ptr(), v_pool.data_ptr(), block_tables.data_ptr(),
         context_lens.data_ptr(), S, Hq, num_kv_heads, D, mb, nb, float(scale), dt, int(partition_size),
         ws_ptr, ws_bytes, _stream_ptr(q.device)), "paged_attention_decode")
+    return out
+
+
+def paged_attention_decode_noalloc(out, q, k_pool, v_pool, block_tables, context_lens, scale,
+                                   num_kv_heads=None, partition_size=0):
+    """paged_attention_decode for callers that cannot allocate device memory.
+
+    Split-K scratch comes from the library's fixed 32 MiB array instead of a
+    workspace; see pkv_paged_attention_decode_noalloc in include/paged_kv.h
+    (calls overlapping on the GPU race on that array).
+    """
+    import torch
+    _need_cuda(out, q, k_pool, v_pool, block_tables, context_lens)
+    dt = _dtype_code(q)
+    if out.dtype != q.dtype or k_pool.dtype != q.dtype or v_pool.dtype != q.dtype:
+        raise TypeError("q, out, k_pool and v_pool must share one dtype")
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise TypeError("block_tables and context_lens must be int32")
+    S, Hq, D = q.shape
+    nb, hkv = k_pool.shape[0], k_pool.shape[1]
+    if num_kv_heads is None:
+        num_kv_heads = hkv
+    if k_pool.shape[2:] != (BLOCK_SIZE, D) or v_pool.shape != k_pool.shape or hkv != num_kv_heads:
+        raise ValueError("pools must be [num_blocks, num_kv_heads, 16, head_dim]")
+    if tuple(out.shape) != (S, Hq, D) or block_tables.dim() != 2 or block_tables.shape[0] != S \
+            or tuple(context_lens.shape) != (S,):
+        raise ValueError("shape mismatch among out, q, block_tables and context_lens")
+    _check(lib().pkv_paged_attention_decode_noalloc(
+        out.data_ptr(), q.data_ptr(), k_pool.data_ptr(), v_pool.data_ptr(), block_tables.data_ptr(),
+        context_lens.data_ptr(), S, Hq, num_kv_heads, D, block_tables.shape[1], nb, float(scale), dt,
+        int(partition_size), _stream_ptr(q.device)), "paged_attention_decode_noalloc")
     return out
 
 

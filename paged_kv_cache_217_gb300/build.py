@@ -24,6 +24,7 @@ LIB = os.path.join(LIBDIR, "libpaged_kv.so")
 
 SOURCES = [
     "api.cu",
+    "decode_noalloc.cu",
     "decode_f16.cu",
     "decode_bf16.cu",
     "cache_ops.cu",

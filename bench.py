@@ -48,8 +48,11 @@ FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 8000.0
 L2_FLUSH_BYTES = 512 << 20
 KERNEL_SOURCES = ["paged_kv_cache_217_gb300/csrc/decode.cuh",
+                  "paged_kv_cache_217_gb300/csrc/decode_mma.cuh",
+                  "paged_kv_cache_217_gb300/csrc/decode_sk.cuh",
                   "paged_kv_cache_217_gb300/csrc/device_common.cuh",
-                  "paged_kv_cache_217_gb300/csrc/decode_launch.cuh"]
+                  "paged_kv_cache_217_gb300/csrc/decode_launch.cuh",
+                  "paged_kv_cache_217_gb300/csrc/api.cu"]
 
 
 # ---------------------------------------------------------------------------
@@ -126,20 +129,32 @@ def build_workload(name, seed, device):
 
 
 def device_inputs(wl, device):
+    """The step's inputs (q, new K/V, tables, lengths, slots) packed in one pinned
+    host buffer and one device buffer, so a step's host-to-device transfer is a
+    single copy; the device tensors are views into the device buffer."""
     import torch
-    wl.q = wl.q_h.to(device)
-    wl.knew = wl.knew_h.to(device)
-    wl.vnew = wl.vnew_h.to(device)
-    wl.tables = torch.from_numpy(wl.tables_h).to(device)
-    wl.lens = torch.from_numpy(wl.lens_h).to(device)
-    wl.slots = torch.from_numpy(wl.slots_h).to(device)
+    items = [("q", wl.q_h), ("knew", wl.knew_h), ("vnew", wl.vnew_h),
+             ("tables", torch.from_numpy(wl.tables_h)), ("lens", torch.from_numpy(wl.lens_h)),
+             ("slots", torch.from_numpy(wl.slots_h))]
+    offs, total = {}, 0
+    for name, t in items:
+        offs[name] = total
+        total += (t.numel() * t.element_size() + 255) // 256 * 256
+    wl.pack_host = torch.empty(total, dtype=torch.uint8).pin_memory()
+    wl.pack_dev = torch.empty(total, dtype=torch.uint8, device=device)
+    for name, t in items:
+        n = t.numel() * t.element_size()
+        wl.pack_host[offs[name]:offs[name] + n].copy_(t.contiguous().reshape(-1).view(torch.uint8))
+        setattr(wl, name, wl.pack_dev[offs[name]:offs[name] + n].view(t.dtype).view(t.shape))
+    wl.pack_dev.copy_(wl.pack_host)
     wl.out = torch.empty_like(wl.q)
 
 
 def step(wl, B):
     """One pass of the hot path on device-resident inputs."""
     B.reshape_and_cache(wl.knew, wl.vnew, wl.k_pool, wl.v_pool, wl.slots)
-    B.paged_attention_decode(wl.out, wl.q, wl.k_pool, wl.v_pool, wl.tables, wl.lens, wl.scale)
+    B.paged_attention_decode(wl.out, wl.q, wl.k_pool, wl.v_pool, wl.tables, wl.lens, wl.scale,
+                             partition_size=wl.partition)
 
 
 # ---------------------------------------------------------------------------
@@ -325,10 +340,13 @@ def run_ours(args):
     B.lib()
 
     wl = build_workload(args.workload, args.seed, device)
+    wl.partition = args.partition
     device_inputs(wl, device)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
-    part = B.resolved_partition(wl.num_seqs, wl.hkv, wl.tables_h.shape[1])
-    launches_per_step = 1 + 1 + (1 if part != -1 else 0)
+    # L2 eviction buffer: read (not written) between timed steps, so the next
+    # step starts with L2 full of clean, unrelated lines and pays no write-backs.
+    flush = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=device)
+    part = B.resolved_partition(wl.num_seqs, wl.hq, wl.hkv, wl.d, wl.tables_h.shape[1], args.partition)
+    launches_per_step = 2   # reshape_and_cache + decode (the split-K merge runs inside the decode kernel)
 
     for _ in range(args.warmup):
         step(wl, B)
@@ -346,12 +364,13 @@ def run_ours(args):
     torch.cuda.synchronize()
     t0 = sampler.mark()
     for k in range(K):
-        flush.fill_(k & 0xFF)                                    # evict L2 between steps
+        flush_sum = flush.sum()                                  # evict L2 with clean lines between steps
         e_start, e_mid, e_end = ev[k]
         e_start.record(stream)
         B.reshape_and_cache(wl.knew, wl.vnew, wl.k_pool, wl.v_pool, wl.slots)
         e_mid.record(stream)
-        B.paged_attention_decode(wl.out, wl.q, wl.k_pool, wl.v_pool, wl.tables, wl.lens, wl.scale)
+        B.paged_attention_decode(wl.out, wl.q, wl.k_pool, wl.v_pool, wl.tables, wl.lens, wl.scale,
+                                 partition_size=wl.partition)
         e_end.record(stream)
     torch.cuda.synchronize()
     if world > 1:
@@ -367,27 +386,17 @@ def run_ours(args):
 
     # end to end through the public API with host buffers: H2D of the step's
     # inputs from pinned memory, the calls, D2H of the output
-    pinned = {k: getattr(wl, k + "_h") for k in ("q", "knew", "vnew")}
-    pinned = {k: v.pin_memory() for k, v in pinned.items()}
-    pinned["tables"] = torch.from_numpy(wl.tables_h).pin_memory()
-    pinned["lens"] = torch.from_numpy(wl.lens_h).pin_memory()
-    pinned["slots"] = torch.from_numpy(wl.slots_h).pin_memory()
     out_h = torch.empty(wl.q_h.shape, dtype=wl.q_h.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in pinned.values())
+    h2d = wl.pack_host.numel()
     d2h = out_h.numel() * out_h.element_size()
     Ke = max(1, min(K, 200))
     e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(Ke)]
     torch.cuda.synchronize()
     for k in range(Ke):
-        flush.fill_(k & 0xFF)
+        flush_sum = flush.sum()
         s_, e_ = e2e_ev[k]
         s_.record(stream)
-        wl.q.copy_(pinned["q"], non_blocking=True)
-        wl.knew.copy_(pinned["knew"], non_blocking=True)
-        wl.vnew.copy_(pinned["vnew"], non_blocking=True)
-        wl.tables.copy_(pinned["tables"], non_blocking=True)
-        wl.lens.copy_(pinned["lens"], non_blocking=True)
-        wl.slots.copy_(pinned["slots"], non_blocking=True)
+        wl.pack_dev.copy_(wl.pack_host, non_blocking=True)   # q, new K/V, tables, lengths, slots
         step(wl, B)
         out_h.copy_(wl.out, non_blocking=True)
         e_.record(stream)
@@ -425,9 +434,10 @@ def run_ours(args):
             "workload": wl.description,
             "num_seqs": wl.num_seqs,
             "kv_bytes_per_step": wl.kv_bytes,
-            "partition_tokens": part,
+            "schedule": ("balanced persistent (equal tiles per warp)" if part == B.BALANCED else
+                         "one pass per (sequence, KV head)" if part == -1 else f"split-K, {part}-token partitions"),
             "l2": f"KV working set {wl.kv_bytes / 1e6:.0f} MB > 129 MB L2, and L2 flushed "
-                  f"({L2_FLUSH_BYTES >> 20} MB write) between timed steps outside the timed events",
+                  f"(a {L2_FLUSH_BYTES >> 20} MB read) between timed steps outside the timed events",
             "parallelism": "replicas" if world > 1 else "single GPU",
         },
         "seqs_layers_per_s": round(world * wl.num_seqs / (per_step_ms * 1e-3), 1),
@@ -515,6 +525,9 @@ def main(argv=None):
     ap.add_argument("--workload", default="llama13b",
                     choices=["llama13b", "llama3_8b", "opt66b_sampling", "opt175b_long", "tiny"])
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--partition", type=int, default=0,
+                    help="decode schedule: 0 = library choice, -1 = one CTA per (sequence, KV head), "
+                         "N = split-K partitions of N tokens")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--reference-budget", type=float, default=150.0,
                     help="seconds of oracle work for the whole reference run (split over its steps)")

@@ -119,20 +119,35 @@ pkv_status_t pkv_device_status(uint32_t* flags_out, int clear);
  * Softmax, dot products and the weighted sum run in fp32 (online maximum and
  * running sum); out is rounded once to T. L == 0 writes zeros.
  *
- * partition_size (tokens): 0 lets the library choose; -1 forces one pass per
- * (sequence, KV head); any other value must be a positive multiple of 16 and
- * splits each sequence into partitions of that many tokens, whose partial
- * (max, sum, weighted V) are merged with a log-sum-exp merge. Sequences that
- * fit one partition are written directly. The result does not depend on the
- * partitioning beyond fp32 rounding.
+ * partition_size (tokens) picks the schedule:
+ *   0   library choice: one CTA per (sequence, KV head) when there are at
+ *       least 608 such pairs (4 per SM), else split-K partitions just large
+ *       enough to reach that many CTAs (>= 256 tokens);
+ *  -1   one CTA per (sequence, KV head), no split;
+ *  -2   balanced persistent schedule: every warp streams an equal share of
+ *       the batch's 16-token tiles; items split between warps are merged by
+ *       log-sum-exp (for heavily skewed length mixes; batches of up to 2048
+ *       sequences at head_dim 128);
+ *  N>0  (multiple of 16) split-K partitions of N tokens, one CTA each, whose
+ *       partial (max, sum, weighted V) are merged by log-sum-exp.
+ * The result does not depend on the schedule beyond fp32 rounding.
  *
  * Supported: T in {fp16, bf16}; head_dim in {64, 128, 256};
  * num_q_heads % num_kv_heads == 0 with group size <= 8.
  *
  * workspace: device memory of at least
  * pkv_paged_attention_workspace_size(...) bytes for the same arguments, or
- * NULL when that size is 0. Its contents need no initialisation, and calls
- * that use one workspace must not overlap on the GPU.
+ * NULL when that size is 0. It holds fp32 partial results and one arrival
+ * counter per (sequence, KV head): the last part of a split item to finish
+ * merges the partials. The library clears the counters on `stream` before
+ * each launch that uses them, so the workspace needs no initialisation and
+ * may be reused by calls of any shape; calls that use one workspace must not
+ * overlap on the GPU.
+ *
+ * Group size 1 runs on the CUDA cores; groups of 2..8 query heads per KV head
+ * run the QK and PV products of each 16-token tile on the tensor cores (fp32
+ * accumulation; the softmax weights enter as two 16-bit terms, keeping about
+ * 16 significant bits).
  */
 pkv_status_t pkv_paged_attention_decode(
     void* out, const void* q, const void* k_pool, const void* v_pool,
@@ -148,10 +163,12 @@ size_t pkv_paged_attention_workspace_size(
     int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
     int max_blocks_per_seq, int partition_size);
 
-/* The partition size (tokens) a call with these sizes runs with: -1 for one
- * pass, else the split-K partition; resolves partition_size == 0. */
+/* The schedule a call with these sizes runs: -2 for the balanced persistent
+ * schedule, -1 for one CTA per (sequence, KV head), else the split-K
+ * partition in tokens; 0 for invalid sizes. Resolves partition_size == 0. */
 int pkv_paged_attention_partition(
-    int num_seqs, int num_kv_heads, int max_blocks_per_seq, int partition_size);
+    int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+    int max_blocks_per_seq, int partition_size);
 
 /*
  * Decode attention that allocates nothing (the pages have no counterpart;
@@ -171,7 +188,8 @@ int pkv_paged_attention_partition(
  * The first call on a device looks up the array's device address (once per
  * device, with that device current); make that first call before any stream
  * capture. Every call on a device shares the one array, which keeps the last
- * call's contents; nothing in it needs to start at zero. Calls that overlap
+ * call's contents; the only part that must start at zero (the split-K
+ * arrival counters) is cleared on `stream` by every call. Calls that overlap
  * on the GPU (different streams, or different host threads) race on it.
  * No cudaMalloc, cudaFree or other allocating routine is called.
  */

@@ -23,6 +23,7 @@ STATUS = {0: "PKV_OK", 1: "PKV_ERR_INVALID_ARG", 2: "PKV_ERR_UNSUPPORTED",
 PKV_F16, PKV_BF16 = 0, 1
 BLOCK_SIZE = 16
 NOALLOC_SCRATCH_BYTES = 32 << 20   # PKV_NOALLOC_SCRATCH_BYTES
+BALANCED = -2                      # pkv_paged_attention_partition: balanced persistent schedule
 
 DEV_FLAGS = {0x1: "BAD_BLOCK_ID", 0x2: "BAD_CONTEXT_LEN", 0x4: "BAD_SLOT", 0x8: "BAD_PAIR",
              0x10: "WAIT_TIMEOUT"}
@@ -55,7 +56,7 @@ _SIGS = {
                                    _c_int),
     "pkv_paged_attention_decode_noalloc": ([_c_p] * 6 + [_c_int] * 6 + [_c_f, _c_int, _c_int, _c_p], _c_int),
     "pkv_paged_attention_workspace_size": ([_c_int] * 6, _c_sz),
-    "pkv_paged_attention_partition": ([_c_int] * 4, _c_int),
+    "pkv_paged_attention_partition": ([_c_int] * 6, _c_int),
     "pkv_reshape_and_cache": ([_c_p] * 5 + [_c_int] * 5 + [_c_p], _c_int),
     "pkv_copy_blocks": ([_c_p] * 3 + [_c_int] * 5 + [_c_p], _c_int),
     "pkv_check_copy_pairs": ([_c_p, _c_int, _c_int], _c_int),
@@ -156,10 +157,11 @@ def workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per
                                                          max_blocks_per_seq, partition_size))
 
 
-def resolved_partition(num_seqs, num_kv_heads, max_blocks_per_seq, partition_size=0):
-    """Partition size (tokens) a call runs with; -1 means one pass."""
-    return int(lib().pkv_paged_attention_partition(num_seqs, num_kv_heads, max_blocks_per_seq,
-                                                   partition_size))
+def resolved_partition(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, partition_size=0):
+    """Schedule a call runs with: BALANCED (-2), -1 (one pass per sequence and KV
+    head) or the split-K partition size in tokens; 0 for invalid arguments."""
+    return int(lib().pkv_paged_attention_partition(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                                   max_blocks_per_seq, partition_size))
 
 
 def paged_attention_decode(out, q, k_pool, v_pool, block_tables, context_lens, scale,

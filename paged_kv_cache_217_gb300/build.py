@@ -50,8 +50,9 @@ def _headers():
     return out
 
 
-def _cmd(nvcc, src, obj, ptxas_verbose):
-    common = ["-O3", "-std=c++17", "-I", INCLUDE, "-I", CSRC, "-Xcompiler", "-fPIC"]
+def _cmd(nvcc, src, obj, ptxas_verbose, defines=()):
+    common = ["-O3", "-std=c++17", "-I", INCLUDE, "-I", CSRC, "-Xcompiler", "-fPIC"] + \
+        [f"-D{d}" for d in defines]
     if src.endswith(".cu"):
         extra = ARCH + ["-lineinfo", "--expt-relaxed-constexpr"]
         if ptxas_verbose:
@@ -60,21 +61,28 @@ def _cmd(nvcc, src, obj, ptxas_verbose):
     return [nvcc] + common + ["-x", "c++", "-c", src, "-o", obj]
 
 
-def build(force=False, verbose=False, ptxas_verbose=False):
-    """Compile every translation unit and link libpaged_kv.so; returns its path."""
-    os.makedirs(BUILD, exist_ok=True)
-    os.makedirs(LIBDIR, exist_ok=True)
+def build(force=False, verbose=False, ptxas_verbose=False, defines=(), out_dir=None):
+    """Compile every translation unit and link libpaged_kv.so; returns its path.
+
+    ``defines`` (NAME=VALUE strings) and ``out_dir`` build a variant (for
+    example another ring shape, PKV_SK_WARPS_CUDA / PKV_SK_WARPS_MMA /
+    PKV_SK_STAGES) into a directory of its own instead of the package.
+    """
+    build_dir = os.path.join(out_dir, "_build") if out_dir else BUILD
+    lib_path = os.path.join(out_dir, "libpaged_kv.so") if out_dir else LIB
+    os.makedirs(build_dir, exist_ok=True)
+    os.makedirs(os.path.dirname(lib_path), exist_ok=True)
     nvcc = _nvcc()
     newest_header = max((os.path.getmtime(h) for h in _headers()), default=0.0)
     procs, objs = [], []
     for s in SOURCES:
         src = os.path.join(CSRC, s)
-        obj = os.path.join(BUILD, s + ".o")
+        obj = os.path.join(build_dir, s + ".o")
         objs.append(obj)
         stale = force or not os.path.exists(obj) or \
             os.path.getmtime(obj) < max(os.path.getmtime(src), newest_header)
         if stale:
-            cmd = _cmd(nvcc, src, obj, ptxas_verbose)
+            cmd = _cmd(nvcc, src, obj, ptxas_verbose, defines)
             if verbose:
                 print(" ".join(cmd), flush=True)
             procs.append((s, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT,
@@ -88,15 +96,15 @@ def build(force=False, verbose=False, ptxas_verbose=False):
             failed.append(s)
     if failed:
         raise RuntimeError(f"nvcc failed for {failed}")
-    if procs or force or not os.path.exists(LIB) or \
-            os.path.getmtime(LIB) < max(os.path.getmtime(o) for o in objs):
-        tmp = LIB + ".tmp"
+    if procs or force or not os.path.exists(lib_path) or \
+            os.path.getmtime(lib_path) < max(os.path.getmtime(o) for o in objs):
+        tmp = lib_path + ".tmp"
         cmd = [nvcc, "-shared", "-o", tmp] + objs + ARCH + ["-cudart", "static"]
         if verbose:
             print(" ".join(cmd), flush=True)
         subprocess.run(cmd, check=True)
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib_path)
+    return lib_path
 
 
 def main(argv=None):
@@ -104,8 +112,11 @@ def main(argv=None):
     ap.add_argument("--force", action="store_true")
     ap.add_argument("--verbose", action="store_true")
     ap.add_argument("--ptxas-verbose", action="store_true")
+    ap.add_argument("--define", action="append", default=[], help="NAME=VALUE passed to nvcc as -D")
+    ap.add_argument("--out-dir", default=None, help="build a variant into this directory")
     args = ap.parse_args(argv)
-    print(build(force=args.force, verbose=args.verbose, ptxas_verbose=args.ptxas_verbose))
+    print(build(force=args.force, verbose=args.verbose, ptxas_verbose=args.ptxas_verbose,
+                defines=args.define, out_dir=args.out_dir))
 
 
 if __name__ == "__main__":

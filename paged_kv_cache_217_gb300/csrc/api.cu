@@ -1,6 +1,8 @@
 // C ABI entry points: host-side argument checks, partition choice, workspace
 // sizing, the device status word, and dispatch to the kernel launchers.
 // Semantics and citations of every call are in include/paged_kv.h.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -9,6 +11,7 @@
 #include <vector>
 
 #include "decode.cuh"
+#include "decode_sk.cuh"
 #include "launch.h"
 #include "paged_kv.h"
 #include "status.h"
@@ -45,18 +48,60 @@ int round_pow2_group(int g) {
   return p;
 }
 
-// The library's partition choice. A CTA handles one partition of one
-// (sequence, KV head); short contexts run in one pass, longer ones are split
-// into 512-token partitions so that no CTA streams more than 32 tiles and
-// long sequences spread over many SMs.
-int choose_partition(int num_seqs, int num_kv_heads, int max_blocks_per_seq, int requested) {
-  (void)num_seqs;
-  (void)num_kv_heads;
-  if (requested == -1) return -1;
+constexpr int kBalanced = -2;  // partition choice: balanced persistent schedule
+constexpr int64_t kLongFirstMaxCtas = 4096;  // grids up to ~9 waves start long sequences first
+
+// CTAs the one-pass grid should have to keep every SM busy: 4 per SM of a
+// 152-SM GB300 (3 are resident per SM; the fourth wave hides CTA start-up).
+constexpr int64_t kFillCtas = 4 * 152;
+
+// The library's schedule choice for partition_size == 0 (measured on GB300
+// over the LLaMA-13B, Llama-3-8B, OPT-66B and OPT-175B layer workloads):
+// one CTA per (sequence, KV head) whenever there are enough of them to fill
+// the GPU -- it needs no merge and keeps sibling sequences that share prompt
+// blocks in lockstep, so their reads hit L2. Too few (sequence, KV head)
+// pairs are split into partitions just large enough to give kFillCtas CTAs
+// (at least 256 tokens). The balanced persistent schedule (-2) is chosen
+// only on request.
+int choose_partition(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int max_blocks_per_seq,
+                     int requested) {
+  (void)num_q_heads;
+  (void)head_dim;
+  if (requested == -1 || requested == kBalanced) return requested;
   if (requested > 0) return requested;
+  const int64_t pairs = int64_t(num_seqs) * num_kv_heads;
   const int64_t max_ctx = int64_t(max_blocks_per_seq) * PKV_BLOCK_SIZE;
-  if (max_ctx <= 512) return -1;
-  return 512;
+  if (pairs >= kFillCtas || max_ctx <= 256) return -1;
+  const int64_t parts = (kFillCtas + pairs - 1) / pairs;
+  int64_t p = (max_ctx + parts - 1) / parts;
+  p = (p + PKV_BLOCK_SIZE - 1) / PKV_BLOCK_SIZE * PKV_BLOCK_SIZE;
+  if (p < 256) p = 256;
+  return p >= max_ctx ? -1 : int(p);
+}
+
+bool balanced_fits(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim) {
+  const int group = num_kv_heads > 0 ? num_q_heads / num_kv_heads : 0;
+  int gpad = 1;
+  while (gpad < group) gpad <<= 1;
+  return num_kv_heads < 512 && gpad <= 8 && num_seqs <= pkv::decode_sk_max_seqs(head_dim, gpad);
+}
+
+// Workspace of the balanced schedule: two partial slots per persistent warp
+// (acc[group][D], m[group], l[group] in fp32, 16-byte rounded), then one
+// arrival counter per (sequence, KV head).
+struct SkLayout {
+  int slot_floats;
+  size_t counter_offset, counter_bytes, total;
+};
+
+SkLayout sk_layout(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim) {
+  SkLayout l;
+  const int group = num_q_heads / num_kv_heads;
+  l.slot_floats = (group * (head_dim + 2) + 3) / 4 * 4;
+  l.counter_offset = size_t(2) * pkv::kSkMaxWarps * size_t(l.slot_floats) * sizeof(float);
+  l.counter_bytes = size_t(num_seqs) * size_t(num_kv_heads) * sizeof(unsigned int);
+  l.total = (l.counter_offset + l.counter_bytes + 15) / 16 * 16;
+  return l;
 }
 
 struct Plan {
@@ -67,6 +112,11 @@ struct Plan {
 pkv_status_t plan_decode(int max_blocks_per_seq, int partition, Plan* plan) {
   const int64_t max_ctx = int64_t(max_blocks_per_seq) * PKV_BLOCK_SIZE;
   if (max_ctx > INT32_MAX / 2) return pkv::fail(PKV_ERR_INVALID_ARG, "max_blocks_per_seq too large");
+  if (partition == kBalanced) {
+    plan->part_tokens = 0;
+    plan->max_parts = 0;
+    return PKV_OK;
+  }
   if (partition == -1) {
     plan->part_tokens = int(max_ctx);
     plan->max_parts = 1;
@@ -83,10 +133,55 @@ pkv_status_t plan_decode(int max_blocks_per_seq, int partition, Plan* plan) {
   return PKV_OK;
 }
 
-size_t split_workspace_bytes(int num_seqs, int num_q_heads, int head_dim, int max_parts) {
-  if (max_parts <= 1) return 0;
+// Split-K workspace: part_o fp32 [S][Hq][P][D] | part_ml float2 [S][Hq][P] |
+// counters u32 [S][Hkv] (partitions finished per (sequence, KV head)).
+struct SplitLayout {
+  size_t ml_offset, counter_offset, counter_bytes, total;
+};
+
+SplitLayout split_layout(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int max_parts) {
+  SplitLayout l{0, 0, 0, 0};
+  if (max_parts <= 1) return l;
   const size_t rows = size_t(num_seqs) * size_t(num_q_heads) * size_t(max_parts);
-  return rows * size_t(head_dim) * sizeof(float) + rows * sizeof(float2);
+  l.ml_offset = rows * size_t(head_dim) * sizeof(float);
+  l.counter_offset = l.ml_offset + rows * sizeof(float2);
+  l.counter_bytes = size_t(num_seqs) * size_t(num_kv_heads) * sizeof(unsigned int);
+  l.total = (l.counter_offset + l.counter_bytes + 15) / 16 * 16;
+  return l;
+}
+
+// cuTensorMapEncodeTiled from the driver, looked up once through the runtime.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// A pool [num_blocks][num_kv_heads][16][head_dim] seen as a 2-D tensor of
+// num_blocks*num_kv_heads*16 rows by head_dim columns, read in boxes of 16 rows
+// x 64 columns with the 128-byte swizzle.
+pkv_status_t pool_tensor_map(CUtensorMap* map, const void* pool, int64_t rows, int head_dim,
+                             pkv_dtype_t dtype) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return pkv::fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const cuuint64_t dims[2] = {cuuint64_t(head_dim), cuuint64_t(rows)};
+  const cuuint64_t strides[1] = {cuuint64_t(head_dim) * 2};
+  const cuuint32_t box[2] = {64, PKV_BLOCK_SIZE};
+  const cuuint32_t elem_strides[2] = {1, 1};
+  const CUresult r = enc(map, dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                         2, const_cast<void*>(pool), dims, strides, box, elem_strides,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return pkv::fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", int(r));
+  return PKV_OK;
 }
 
 pkv_status_t cuda_status(cudaError_t err, const char* what) {
@@ -119,11 +214,15 @@ pkv_status_t pkv_device_status(uint32_t* flags_out, int clear) {
   return pkv::ok();
 }
 
-int pkv_paged_attention_partition(int num_seqs, int num_kv_heads, int max_blocks_per_seq,
-                                  int partition_size) {
-  const int p = choose_partition(num_seqs, num_kv_heads, max_blocks_per_seq, partition_size);
+int pkv_paged_attention_partition(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                  int max_blocks_per_seq, int partition_size) {
+  if (num_seqs <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0 ||
+      max_blocks_per_seq <= 0)
+    return 0;
+  const int p = choose_partition(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, partition_size);
   Plan plan;
   if (plan_decode(max_blocks_per_seq, p, &plan) != PKV_OK) return 0;
+  if (p == kBalanced) return kBalanced;
   return plan.max_parts <= 1 ? -1 : plan.part_tokens;
 }
 
@@ -133,10 +232,14 @@ size_t pkv_paged_attention_workspace_size(int num_seqs, int num_q_heads, int num
   if (num_seqs <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
       max_blocks_per_seq <= 0)
     return 0;
-  const int p = choose_partition(num_seqs, num_kv_heads, max_blocks_per_seq, partition_size);
+  const int p = choose_partition(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, partition_size);
   Plan plan;
   if (plan_decode(max_blocks_per_seq, p, &plan) != PKV_OK) return 0;
-  return split_workspace_bytes(num_seqs, num_q_heads, head_dim, plan.max_parts);
+  if (p == kBalanced) {
+    if (num_q_heads % num_kv_heads != 0) return 0;
+    return sk_layout(num_seqs, num_q_heads, num_kv_heads, head_dim).total;
+  }
+  return split_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, plan.max_parts).total;
 }
 
 pkv_status_t pkv_paged_attention_decode(void* out, const void* q, const void* k_pool,
@@ -166,11 +269,19 @@ pkv_status_t pkv_paged_attention_decode(void* out, const void* q, const void* k_
   if (!aligned(block_tables, 4) || !aligned(context_lens, 4))
     return pkv::fail(PKV_ERR_INVALID_ARG, "block_tables and context_lens must be 4-byte aligned");
 
-  const int p = choose_partition(num_seqs, num_kv_heads, max_blocks_per_seq, partition_size);
+  const int p = choose_partition(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, partition_size);
   Plan plan;
   pkv_status_t st = plan_decode(max_blocks_per_seq, p, &plan);
   if (st != PKV_OK) return st;
-  const size_t need = split_workspace_bytes(num_seqs, num_q_heads, head_dim, plan.max_parts);
+  const bool balanced = p == kBalanced;
+  if (balanced && !balanced_fits(num_seqs, num_q_heads, num_kv_heads, head_dim))
+    return pkv::fail(PKV_ERR_UNSUPPORTED, "the balanced schedule takes at most %d sequences at these sizes",
+                     pkv::decode_sk_max_seqs(head_dim, round_pow2_group(group)));
+  const SplitLayout lay = split_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, plan.max_parts);
+  const SkLayout sk = sk_layout(num_seqs, num_q_heads, num_kv_heads, head_dim);
+  const size_t need = balanced ? sk.total : lay.total;
+  if (int64_t(num_blocks) * num_kv_heads * PKV_BLOCK_SIZE > INT32_MAX)
+    return pkv::fail(PKV_ERR_UNSUPPORTED, "num_blocks * num_kv_heads * 16 exceeds 2^31 rows");
   if (need > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, 16)))
     return pkv::fail(PKV_ERR_WORKSPACE, "workspace of %zu bytes (16-byte aligned) required, got %zu at %p",
                      need, workspace_bytes, workspace);
@@ -179,6 +290,43 @@ pkv_status_t pkv_paged_attention_decode(void* out, const void* q, const void* k_
   st = status_word(&status);
   if (st != PKV_OK) return st;
 
+  const int gpad = round_pow2_group(group);
+  alignas(64) CUtensorMap kmap, vmap;
+  if (gpad >= 2) {
+    const int64_t rows = int64_t(num_blocks) * num_kv_heads * PKV_BLOCK_SIZE;
+    st = pool_tensor_map(&kmap, k_pool, rows, head_dim, dtype);
+    if (st != PKV_OK) return st;
+    st = pool_tensor_map(&vmap, v_pool, rows, head_dim, dtype);
+    if (st != PKV_OK) return st;
+  }
+
+  if (balanced) {
+    pkv::SkArgs b;
+    b.out = out;
+    b.q = q;
+    b.k_pool = k_pool;
+    b.v_pool = v_pool;
+    b.block_tables = block_tables;
+    b.context_lens = context_lens;
+    b.slots = static_cast<float*>(workspace);
+    b.counters = reinterpret_cast<unsigned int*>(static_cast<char*>(workspace) + sk.counter_offset);
+    b.status = status;
+    b.num_seqs = num_seqs;
+    b.num_q_heads = num_q_heads;
+    b.num_kv_heads = num_kv_heads;
+    b.group = group;
+    b.max_blocks_per_seq = max_blocks_per_seq;
+    b.num_blocks = num_blocks;
+    b.slot_floats = sk.slot_floats;
+    b.scale_log2 = scale * 1.4426950408889634f;
+    // Arrival counters start at zero on every call; the slots need no initialisation.
+    cudaError_t err = cudaMemsetAsync(b.counters, 0, sk.counter_bytes, stream);
+    if (err != cudaSuccess) return cuda_status(err, "clear arrival counters");
+    err = dtype == PKV_F16 ? pkv::launch_decode_sk_f16(b, head_dim, gpad, &kmap, &vmap, stream)
+                           : pkv::launch_decode_sk_bf16(b, head_dim, gpad, &kmap, &vmap, stream);
+    return cuda_status(err, "paged_attention_decode launch");
+  }
+
   pkv::DecodeArgs a;
   a.out = out;
   a.q = q;
@@ -186,11 +334,10 @@ pkv_status_t pkv_paged_attention_decode(void* out, const void* q, const void* k_
   a.v_pool = v_pool;
   a.block_tables = block_tables;
   a.context_lens = context_lens;
-  a.part_o = static_cast<float*>(workspace);
-  a.part_ml = need > 0 ? reinterpret_cast<float2*>(static_cast<char*>(workspace) +
-                                                   size_t(num_seqs) * num_q_heads * plan.max_parts *
-                                                       head_dim * sizeof(float))
-                       : nullptr;
+  a.part_o = need > 0 ? static_cast<float*>(workspace) : nullptr;
+  a.part_ml = need > 0 ? reinterpret_cast<float2*>(static_cast<char*>(workspace) + lay.ml_offset) : nullptr;
+  a.counters = need > 0 ? reinterpret_cast<unsigned int*>(static_cast<char*>(workspace) + lay.counter_offset)
+                        : nullptr;
   a.status = status;
   a.num_seqs = num_seqs;
   a.num_q_heads = num_q_heads;
@@ -200,11 +347,21 @@ pkv_status_t pkv_paged_attention_decode(void* out, const void* q, const void* k_
   a.num_blocks = num_blocks;
   a.part_tokens = plan.part_tokens;
   a.max_parts = plan.max_parts;
+  // Ranking the batch costs each CTA a dependent read of all lengths (about a
+  // microsecond); it pays off only when the grid has few waves, where a long
+  // sequence started last sets the end time (measured on GB300: -9 % on the
+  // LLaMA-13B layer at 2560 CTAs, +7 % on the OPT-66B sampling batch at 9216).
+  a.long_first = int64_t(num_seqs) * num_kv_heads * plan.max_parts <= kLongFirstMaxCtas ? 1 : 0;
   a.scale_log2 = scale * 1.4426950408889634f;
 
-  const int gpad = round_pow2_group(group);
-  cudaError_t err = dtype == PKV_F16 ? pkv::launch_decode_f16(a, head_dim, gpad, stream)
-                                     : pkv::launch_decode_bf16(a, head_dim, gpad, stream);
+  cudaError_t err = cudaSuccess;
+  if (need > 0) {
+    // The partition counters start at zero on every call; the partials need no initialisation.
+    err = cudaMemsetAsync(a.counters, 0, lay.counter_bytes, stream);
+    if (err != cudaSuccess) return cuda_status(err, "clear split-K counters");
+  }
+  err = dtype == PKV_F16 ? pkv::launch_decode_f16(a, head_dim, gpad, &kmap, &vmap, stream)
+                         : pkv::launch_decode_bf16(a, head_dim, gpad, &kmap, &vmap, stream);
   return cuda_status(err, "paged_attention_decode launch");
 }
 

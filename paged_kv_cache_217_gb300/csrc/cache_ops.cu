@@ -25,6 +25,9 @@ reshape_and_cache_kernel(const uint4* __restrict__ k, const uint4* __restrict__ 
                          uint4* __restrict__ k_pool, uint4* __restrict__ v_pool,
                          const int64_t* __restrict__ slots, int64_t total, int num_kv_heads,
                          int vec_per_row, int64_t num_slots, unsigned int* status) {
+  // The decode kernel that usually follows may become resident now; it waits
+  // for this grid to finish before reading the pools.
+  asm volatile("griddepcontrol.launch_dependents;");
   const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= total) return;
   const int c = int(i % vec_per_row);

@@ -28,9 +28,10 @@
 //    l, running weighted V sum; the accumulator is rescaled only when a
 //    head's max grows.
 //  * Warps are merged through shared memory (the same max/sum rescaling).
-//  * Split-K: each partition writes (m, l, unnormalised o) in fp32; the merge
-//    kernel combines them by log-sum-exp. Sequences that fit in one partition
-//    are finished by their CTA directly.
+//  * Split-K: each partition writes (m, l, unnormalised o) in fp32; the last
+//    CTA of a (sequence, KV head) to finish -- counted by an atomic counter in
+//    the workspace, which it resets -- merges them by log-sum-exp. Sequences
+//    that fit in one partition are finished by their CTA directly.
 #pragma once
 
 #include <cmath>
@@ -50,6 +51,7 @@ struct DecodeArgs {
   const int32_t* context_lens;
   float* part_o;        // split-K: [S][Hq][max_parts][D] unnormalised sums
   float2* part_ml;      // split-K: [S][Hq][max_parts] (max, sum), log2 domain
+  unsigned int* counters; // split-K: [S][Hkv] partitions finished; zero between calls
   unsigned int* status; // device status word (PKV_DEV_* flags)
   int num_seqs;
   int num_q_heads;
@@ -59,8 +61,91 @@ struct DecodeArgs {
   int num_blocks;
   int part_tokens;      // tokens per partition (multiple of 16)
   int max_parts;        // grid.z
+  int long_first;       // start sequences of twice the mean length first (long_first_seq)
   float scale_log2;     // scale * log2(e)
 };
+
+// Waits until the kernel launched before this one in the stream has finished
+// and its writes are visible (programmatic dependent launch: the grid may
+// become resident while its predecessor still runs). Every global read of
+// the decode kernels comes after this.
+__device__ __forceinline__ void wait_for_predecessor() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+#ifndef PKV_ORDER_MAX_SEQS
+#define PKV_ORDER_MAX_SEQS 1024
+#endif
+constexpr int kOrderMaxSeqs = PKV_ORDER_MAX_SEQS;  // batches up to this size start long sequences first
+
+// Position of the k-th (0-based) set bit of m; m has more than k set bits.
+__device__ __forceinline__ int kth_set_bit(unsigned int m, int k) {
+  for (int i = 0; i < k; ++i) m &= m - 1u;
+  return __ffs(int(m)) - 1;
+}
+
+// The sequence that the CTAs of grid row `rank` process. Rows are dispatched
+// in order, and a long sequence that starts in the last wave decides when the
+// kernel ends, so sequences with at least twice the batch's mean tile count
+// take the first rows (in natural order) and all others follow (in natural
+// order, which keeps parallel samples of one prompt -- sequences that share
+// blocks -- running side by side). Every CTA derives the same mapping from
+// context_lens, so each sequence is taken exactly once.
+template <int NW>
+__device__ __forceinline__ int long_first_seq(const DecodeArgs& a, int rank) {
+  const int S = a.num_seqs;
+  if (!a.long_first || S > kOrderMaxSeqs || S <= 1) return rank;
+  __shared__ int tiles[kOrderMaxSeqs > 0 ? kOrderMaxSeqs : 1];
+  __shared__ unsigned int long_bits[kOrderMaxSeqs > 32 ? kOrderMaxSeqs / 32 : 1];
+  __shared__ int red[NW];
+  __shared__ int picked;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int max_len = a.max_blocks_per_seq * kBlock;
+  int local = 0;
+  for (int s = tid; s < S; s += NW * 32) {
+    int L = __ldg(a.context_lens + s);
+    L = L < 0 ? 0 : (L > max_len ? max_len : L);
+    tiles[s] = (L + kBlock - 1) / kBlock;
+    local += tiles[s];
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) local += __shfl_xor_sync(kFull, local, o);
+  if (lane == 0) red[warp] = local;
+  __syncthreads();
+  long long total = 0;
+#pragma unroll
+  for (int w = 0; w < NW; ++w) total += red[w];
+  const int words = (S + 31) / 32;
+  for (int i = warp; i < words; i += NW) {
+    const int s = 32 * i + lane;
+    const bool lg = s < S && (long long)tiles[s] * S >= 2 * total;
+    const unsigned int m = __ballot_sync(kFull, lg);
+    if (lane == 0) long_bits[i] = m;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    // lane i owns word i (words <= 32)
+    const unsigned int valid = lane < words ? (lane == words - 1 && (S & 31) ? (1u << (S & 31)) - 1u : kFull) : 0u;
+    const unsigned int lb = lane < words ? long_bits[lane] : 0u;
+    const int nl = __popc(lb), ns = __popc(valid & ~lb);
+    int il = nl, is = ns;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int a1 = __shfl_up_sync(kFull, il, o), a2 = __shfl_up_sync(kFull, is, o);
+      if (lane >= o) {
+        il += a1;
+        is += a2;
+      }
+    }
+    const int n_long = __shfl_sync(kFull, il, 31);
+    if (rank < n_long) {  // the rank-th long sequence
+      if (il - nl <= rank && rank < il) picked = 32 * lane + kth_set_bit(lb, rank - (il - nl));
+    } else {              // the (rank - n_long)-th other sequence
+      const int r2 = rank - n_long;
+      if (is - ns <= r2 && r2 < is) picked = 32 * lane + kth_set_bit(valid & ~lb, r2 - (is - ns));
+    }
+  }
+  __syncthreads();
+  return picked;
+}
 
 template <typename T, int D, int G, int NW, int STAGES>
 struct DecodeCfg {
@@ -199,6 +284,103 @@ __device__ __forceinline__ void decode_tile(uint32_t kt, uint32_t vt, int rows,
   }
 }
 
+// Epilogue shared by the decode kernels. On entry every warp w has published
+// its running sums for the chunk in its own shared-memory area
+// (smem + w * area_bytes): acc[G][D], then m[G], then l[G] (log2 domain), and
+// the CTA has synchronised. The warps are merged by rescaling each to the
+// common max; a sequence that fits one partition is finished here. Otherwise
+// the partition's (m, l, o) go to the workspace and the last partition of the
+// (sequence, KV head) to arrive merges all of them by log-sum-exp:
+//   M = max_p m_p,  w_p = 2^(m_p - M),  out = sum_p w_p o_p / sum_p w_p l_p.
+template <typename T, int D, int G, int NW>
+__device__ __forceinline__ void finish_chunk(const DecodeArgs& a, const unsigned char* smem,
+                                             size_t area_bytes, int s, int g, int part, int nparts) {
+  constexpr int CHUNKS = D / 8;
+  const int hq0 = g * a.group;
+  const bool direct = nparts == 1;
+  for (int it = threadIdx.x; it < a.group * CHUNKS; it += NW * 32) {
+    const int h = it / CHUNKS, c8 = it % CHUNKS;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < NW; ++w)
+      M = fmaxf(M, reinterpret_cast<const float*>(smem + size_t(w) * area_bytes)[G * D + h]);
+    float den = 0.f, num[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) num[c] = 0.f;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+      const float* ws = reinterpret_cast<const float*>(smem + size_t(w) * area_bytes);
+      const float mw = ws[G * D + h];
+      if (mw == -INFINITY) continue;
+      const float wt = fast_exp2(mw - M);
+      den = fmaf(wt, ws[G * D + G + h], den);
+      const float4* src = reinterpret_cast<const float4*>(ws + h * D + c8 * 8);
+      const float4 x0 = src[0], x1 = src[1];
+      num[0] = fmaf(wt, x0.x, num[0]);
+      num[1] = fmaf(wt, x0.y, num[1]);
+      num[2] = fmaf(wt, x0.z, num[2]);
+      num[3] = fmaf(wt, x0.w, num[3]);
+      num[4] = fmaf(wt, x1.x, num[4]);
+      num[5] = fmaf(wt, x1.y, num[5]);
+      num[6] = fmaf(wt, x1.z, num[6]);
+      num[7] = fmaf(wt, x1.w, num[7]);
+    }
+    const size_t row = size_t(s) * a.num_q_heads + hq0 + h;
+    if (direct) {
+      const float inv = 1.f / den;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) num[c] *= inv;
+      reinterpret_cast<uint4*>(static_cast<T*>(a.out) + row * D)[c8] = Vec8<T>::from_float(num);
+    } else {
+      float4* dst = reinterpret_cast<float4*>(a.part_o + (row * a.max_parts + part) * D + c8 * 8);
+      dst[0] = make_float4(num[0], num[1], num[2], num[3]);
+      dst[1] = make_float4(num[4], num[5], num[6], num[7]);
+      if (c8 == 0) a.part_ml[row * a.max_parts + part] = make_float2(M, den);
+    }
+  }
+  if (direct) return;
+
+  __shared__ unsigned int last_arrival;
+  __threadfence();
+  __syncthreads();
+  unsigned int* counter = a.counters + size_t(s) * a.num_kv_heads + g;
+  if (threadIdx.x == 0) last_arrival = atomicAdd(counter, 1u) == unsigned(nparts - 1) ? 1u : 0u;
+  __syncthreads();
+  if (!last_arrival) return;
+  __threadfence();
+  for (int it = threadIdx.x; it < a.group * CHUNKS; it += NW * 32) {
+    const int h = it / CHUNKS, c8 = it % CHUNKS;
+    const size_t row = size_t(s) * a.num_q_heads + hq0 + h;
+    const float2* ml = a.part_ml + row * a.max_parts;
+    const float* po = a.part_o + row * a.max_parts * D + c8 * 8;
+    float M = -INFINITY;
+    for (int p = 0; p < nparts; ++p) M = fmaxf(M, __ldcg(&ml[p].x));
+    float den = 0.f, num[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) num[c] = 0.f;
+    for (int p = 0; p < nparts; ++p) {
+      const float2 x = __ldcg(ml + p);
+      const float w = fast_exp2(x.x - M);
+      den = fmaf(w, x.y, den);
+      const float4* src = reinterpret_cast<const float4*>(po + size_t(p) * D);
+      const float4 x0 = __ldcg(src), x1 = __ldcg(src + 1);
+      num[0] = fmaf(w, x0.x, num[0]);
+      num[1] = fmaf(w, x0.y, num[1]);
+      num[2] = fmaf(w, x0.z, num[2]);
+      num[3] = fmaf(w, x0.w, num[3]);
+      num[4] = fmaf(w, x1.x, num[4]);
+      num[5] = fmaf(w, x1.y, num[5]);
+      num[6] = fmaf(w, x1.z, num[6]);
+      num[7] = fmaf(w, x1.w, num[7]);
+    }
+    const float inv = 1.f / den;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) num[c] *= inv;
+    reinterpret_cast<uint4*>(static_cast<T*>(a.out) + row * D)[c8] = Vec8<T>::from_float(num);
+  }
+  if (threadIdx.x == 0) *counter = 0u;  // leave the workspace ready for the next call
+}
+
 template <typename T, int D, int G, int NW, int STAGES>
 __global__ void __launch_bounds__(NW * 32)
 paged_decode_kernel(const DecodeArgs a) {
@@ -206,7 +388,8 @@ paged_decode_kernel(const DecodeArgs a) {
   constexpr int LPR = C::LPR;
   extern __shared__ __align__(1024) unsigned char smem[];
 
-  const int g = blockIdx.x, s = blockIdx.y, part = blockIdx.z;
+  wait_for_predecessor();
+  const int g = blockIdx.x, s = long_first_seq<NW>(a, blockIdx.y), part = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int sub = lane & (LPR - 1), r = lane / LPR;
   const int hq0 = g * a.group;
@@ -365,105 +548,7 @@ paged_decode_kernel(const DecodeArgs a) {
   }
   __syncthreads();
 
-  // Merge the warps: rescale each warp's sums to the common max.
-  const bool direct = nparts == 1;
-  constexpr int CHUNKS = D / 8;
-  for (int it = threadIdx.x; it < a.group * CHUNKS; it += NW * 32) {
-    const int h = it / CHUNKS, c8 = it % CHUNKS;
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < NW; ++w)
-      M = fmaxf(M, reinterpret_cast<const float*>(smem + size_t(w) * STAGES * C::STAGE_BYTES)[G * D + h]);
-    float den = 0.f, num[8];
-#pragma unroll
-    for (int c = 0; c < 8; ++c) num[c] = 0.f;
-#pragma unroll
-    for (int w = 0; w < NW; ++w) {
-      const float* ws = reinterpret_cast<const float*>(smem + size_t(w) * STAGES * C::STAGE_BYTES);
-      const float mw = ws[G * D + h];
-      if (mw == -INFINITY) continue;
-      const float wt = fast_exp2(mw - M);
-      den = fmaf(wt, ws[G * D + G + h], den);
-      const float4* src = reinterpret_cast<const float4*>(ws + h * D + c8 * 8);
-      const float4 x0 = src[0], x1 = src[1];
-      num[0] = fmaf(wt, x0.x, num[0]);
-      num[1] = fmaf(wt, x0.y, num[1]);
-      num[2] = fmaf(wt, x0.z, num[2]);
-      num[3] = fmaf(wt, x0.w, num[3]);
-      num[4] = fmaf(wt, x1.x, num[4]);
-      num[5] = fmaf(wt, x1.y, num[5]);
-      num[6] = fmaf(wt, x1.z, num[6]);
-      num[7] = fmaf(wt, x1.w, num[7]);
-    }
-    const size_t row = size_t(s) * a.num_q_heads + hq0 + h;
-    if (direct) {
-      const float inv = 1.f / den;
-#pragma unroll
-      for (int c = 0; c < 8; ++c) num[c] *= inv;
-      reinterpret_cast<uint4*>(static_cast<T*>(a.out) + row * D)[c8] = Vec8<T>::from_float(num);
-    } else {
-      float4* dst = reinterpret_cast<float4*>(a.part_o + (row * a.max_parts + part) * D + c8 * 8);
-      dst[0] = make_float4(num[0], num[1], num[2], num[3]);
-      dst[1] = make_float4(num[4], num[5], num[6], num[7]);
-      if (c8 == 0) a.part_ml[row * a.max_parts + part] = make_float2(M, den);
-    }
-  }
-}
-
-// Log-sum-exp merge of split-K partitions, one CTA (D threads) per (seq, q head):
-//   M = max_p m_p,  w_p = 2^(m_p - M),  out = sum_p w_p o_p / sum_p w_p l_p.
-template <typename T, int D>
-__global__ void __launch_bounds__(D)
-paged_decode_merge_kernel(const DecodeArgs a) {
-  extern __shared__ float wts[];  // [max_parts]
-  __shared__ float red[D / 32];
-  const int hq = blockIdx.x, s = blockIdx.y;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  int L = a.context_lens[s];
-  const int max_len = a.max_blocks_per_seq * kBlock;
-  L = L < 0 ? 0 : (L > max_len ? max_len : L);
-  const int nparts = L == 0 ? 1 : (L + a.part_tokens - 1) / a.part_tokens;
-  if (nparts <= 1) return;  // written by the decode kernel
-  const size_t row = size_t(s) * a.num_q_heads + hq;
-  const float2* ml = a.part_ml + row * a.max_parts;
-
-  float m = -INFINITY;
-  for (int p = tid; p < nparts; p += D) m = fmaxf(m, ml[p].x);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
-  if (lane == 0) red[warp] = m;
-  __syncthreads();
-  float M = red[0];
-#pragma unroll
-  for (int w = 1; w < D / 32; ++w) M = fmaxf(M, red[w]);
-  __syncthreads();
-
-  float den = 0.f;
-  for (int p = tid; p < nparts; p += D) {
-    const float2 x = ml[p];
-    const float w = fast_exp2(x.x - M);
-    wts[p] = w;
-    den = fmaf(w, x.y, den);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(kFull, den, o);
-  if (lane == 0) red[warp] = den;
-  __syncthreads();
-  float tot = 0.f;
-#pragma unroll
-  for (int w = 0; w < D / 32; ++w) tot += red[w];
-
-  const float* po = a.part_o + row * a.max_parts * D + tid;
-  float acc = 0.f;
-  for (int p = 0; p < nparts; ++p) acc = fmaf(wts[p], po[size_t(p) * D], acc);
-  const float val = acc / tot;
-  T* o = static_cast<T*>(a.out) + row * D;
-  if constexpr (sizeof(T) == 2) {
-    if constexpr (std::is_same<T, __half>::value)
-      o[tid] = __float2half_rn(val);
-    else
-      o[tid] = __float2bfloat16_rn(val);
-  }
+  finish_chunk<T, D, G, NW>(a, smem, size_t(STAGES) * C::STAGE_BYTES, s, g, part, nparts);
 }
 
 }  // namespace pkv

@@ -2,7 +2,21 @@
 #include "decode_launch.cuh"
 
 namespace pkv {
-cudaError_t launch_decode_f16(const DecodeArgs& a, int head_dim, int gpad, cudaStream_t stream) {
-  return launch_decode_t<__half>(a, head_dim, gpad, stream);
+cudaError_t launch_decode_f16(const DecodeArgs& a, int head_dim, int gpad, const CUtensorMap* kmap,
+                              const CUtensorMap* vmap, cudaStream_t stream) {
+  return launch_decode_t<__half>(a, head_dim, gpad, kmap, vmap, stream);
+}
+cudaError_t launch_decode_sk_f16(const SkArgs& a, int head_dim, int gpad, const CUtensorMap* kmap,
+                                 const CUtensorMap* vmap, cudaStream_t stream) {
+  return launch_decode_sk_t<__half>(a, head_dim, gpad, kmap, vmap, stream);
+}
+int decode_sk_max_seqs(int head_dim, int gpad) {
+  // The limit depends only on sizes, not on the element type (both are 2 bytes).
+  switch (head_dim) {
+    case 64: return sk_max_seqs_d<__half, 64>(gpad);
+    case 128: return sk_max_seqs_d<__half, 128>(gpad);
+    case 256: return sk_max_seqs_d<__half, 256>(gpad);
+    default: return 0;
+  }
 }
 }  // namespace pkv

@@ -2,52 +2,171 @@
 #pragma once
 
 #include "decode.cuh"
+#include "decode_mma.cuh"
+#include "decode_sk.cuh"
 #include "launch.h"
 
 namespace pkv {
 
-template <typename T, int D, int G>
-cudaError_t launch_decode_dg(const DecodeArgs& a, cudaStream_t stream) {
-  constexpr int NW = 4;
-  constexpr int STAGES = 2;
-  using C = DecodeCfg<T, D, G, NW, STAGES>;
-  auto kern = paged_decode_kernel<T, D, G, NW, STAGES>;
-  static bool configured[kMaxDevices] = {};
+// Raises the dynamic shared-memory limit of a kernel once per device.
+template <typename K>
+cudaError_t configure_once(K kern, size_t smem, bool (&configured)[kMaxDevices]) {
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   if (!configured[dev]) {
-    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(C::SMEM_BYTES));
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (err != cudaSuccess) return err;
     configured[dev] = true;
   }
+  return cudaSuccess;
+}
+
+// Shape of the one-CTA-per-(sequence, KV head, partition) kernels: warps per
+// CTA and stages per warp (overridable at build time for tuning).
+#ifndef PKV_GRID_WARPS
+#define PKV_GRID_WARPS 4
+#endif
+#ifndef PKV_GRID_STAGES
+#define PKV_GRID_STAGES 2
+#endif
+
+// Launch with programmatic stream serialization: the grid may become resident
+// while the previous kernel in the stream finishes (the kernels wait for it
+// with griddepcontrol.wait before touching global memory).
+#ifndef PKV_USE_PDL
+#define PKV_USE_PDL 1
+#endif
+template <typename K, typename... Args>
+cudaError_t launch_pdl(K kern, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, Args... args) {
+  if (!PKV_USE_PDL) {
+    kern<<<grid, block, smem, stream>>>(args...);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
+template <typename T, int D, int G>
+cudaError_t launch_decode_dg(const DecodeArgs& a, const CUtensorMap* kmap, const CUtensorMap* vmap,
+                             cudaStream_t stream) {
+  constexpr int NW = PKV_GRID_WARPS;
+  constexpr int STAGES = (D == 256 && PKV_GRID_WARPS * PKV_GRID_STAGES > 8) ? 2 : PKV_GRID_STAGES;
+  static bool configured[kMaxDevices] = {};
   const dim3 grid(unsigned(a.num_kv_heads), unsigned(a.num_seqs), unsigned(a.max_parts));
-  kern<<<grid, NW * 32, C::SMEM_BYTES, stream>>>(a);
-  err = cudaGetLastError();
-  if (err != cudaSuccess || a.max_parts <= 1) return err;
-  const dim3 mgrid(unsigned(a.num_q_heads), unsigned(a.num_seqs));
-  paged_decode_merge_kernel<T, D><<<mgrid, D, size_t(a.max_parts) * sizeof(float), stream>>>(a);
+  if constexpr (G == 1) {
+    using C = DecodeCfg<T, D, G, NW, STAGES>;
+    auto kern = paged_decode_kernel<T, D, G, NW, STAGES>;
+    cudaError_t err = configure_once(kern, C::SMEM_BYTES, configured);
+    if (err != cudaSuccess) return err;
+    err = launch_pdl(kern, grid, dim3(NW * 32), C::SMEM_BYTES, stream, a);
+    if (err != cudaSuccess) return err;
+  } else {
+    using C = MmaCfg<T, D, NW, STAGES>;
+    auto kern = paged_decode_mma_kernel<T, D, G, NW, STAGES>;
+    cudaError_t err = configure_once(kern, C::SMEM_BYTES, configured);
+    if (err != cudaSuccess) return err;
+    err = launch_pdl(kern, grid, dim3(NW * 32), C::SMEM_BYTES, stream, a, *kmap, *vmap);
+    if (err != cudaSuccess) return err;
+  }
   return cudaGetLastError();
 }
 
 template <typename T, int D>
-cudaError_t launch_decode_d(const DecodeArgs& a, int gpad, cudaStream_t stream) {
+cudaError_t launch_decode_d(const DecodeArgs& a, int gpad, const CUtensorMap* kmap, const CUtensorMap* vmap,
+                            cudaStream_t stream) {
   switch (gpad) {
-    case 1: return launch_decode_dg<T, D, 1>(a, stream);
-    case 2: return launch_decode_dg<T, D, 2>(a, stream);
-    case 4: return launch_decode_dg<T, D, 4>(a, stream);
-    case 8: return launch_decode_dg<T, D, 8>(a, stream);
+    case 1: return launch_decode_dg<T, D, 1>(a, kmap, vmap, stream);
+    case 2: return launch_decode_dg<T, D, 2>(a, kmap, vmap, stream);
+    case 4: return launch_decode_dg<T, D, 4>(a, kmap, vmap, stream);
+    case 8: return launch_decode_dg<T, D, 8>(a, kmap, vmap, stream);
     default: return cudaErrorInvalidValue;
   }
 }
 
 template <typename T>
-cudaError_t launch_decode_t(const DecodeArgs& a, int head_dim, int gpad, cudaStream_t stream) {
+cudaError_t launch_decode_t(const DecodeArgs& a, int head_dim, int gpad, const CUtensorMap* kmap,
+                            const CUtensorMap* vmap, cudaStream_t stream) {
   switch (head_dim) {
-    case 64: return launch_decode_d<T, 64>(a, gpad, stream);
-    case 128: return launch_decode_d<T, 128>(a, gpad, stream);
-    case 256: return launch_decode_d<T, 256>(a, gpad, stream);
+    case 64: return launch_decode_d<T, 64>(a, gpad, kmap, vmap, stream);
+    case 128: return launch_decode_d<T, 128>(a, gpad, kmap, vmap, stream);
+    case 256: return launch_decode_d<T, 256>(a, gpad, kmap, vmap, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+// ---- balanced persistent schedule -------------------------------------------
+template <typename T, int D, int G>
+cudaError_t launch_decode_sk_dg(const SkArgs& a, const CUtensorMap* kmap, const CUtensorMap* vmap,
+                                cudaStream_t stream) {
+  constexpr int NW = sk_warps<D, G>();
+  constexpr int STAGES = sk_stages<D>();
+  constexpr bool MMA = G > 1;
+  using SM = SkSmem<T, D, G, NW, STAGES, MMA>;
+  auto kern = paged_decode_sk_kernel<T, D, G, NW, STAGES, MMA>;
+  static bool configured[kMaxDevices] = {};
+  static int sm_count[kMaxDevices] = {};
+  if (a.num_seqs > SM::max_seqs()) return cudaErrorInvalidValue;
+  cudaError_t err = configure_once(kern, SM::bytes(SM::max_seqs()), configured);
+  if (err != cudaSuccess) return err;
+  int dev = 0;
+  err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (!sm_count[dev]) {
+    err = cudaDeviceGetAttribute(&sm_count[dev], cudaDevAttrMultiProcessorCount, dev);
+    if (err != cudaSuccess) return err;
+  }
+  const size_t smem = SM::bytes(a.num_seqs);
+  int per_sm = 0;
+  err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, NW * 32, smem);
+  if (err != cudaSuccess) return err;
+  int grid = sm_count[dev] * (per_sm > 0 ? per_sm : 1);
+  if (grid > kSkMaxWarps / NW) grid = kSkMaxWarps / NW;
+  err = launch_pdl(kern, dim3(grid), dim3(NW * 32), smem, stream, a, *kmap, *vmap);
+  if (err != cudaSuccess) return err;
+  return cudaGetLastError();
+}
+
+template <typename T, int D>
+int sk_max_seqs_d(int gpad) {
+  switch (gpad) {
+    case 1: return SkSmem<T, D, 1, sk_warps<D, 1>(), sk_stages<D>(), false>::max_seqs();
+    case 2: return SkSmem<T, D, 2, sk_warps<D, 2>(), sk_stages<D>(), true>::max_seqs();
+    case 4: return SkSmem<T, D, 4, sk_warps<D, 4>(), sk_stages<D>(), true>::max_seqs();
+    case 8: return SkSmem<T, D, 8, sk_warps<D, 8>(), sk_stages<D>(), true>::max_seqs();
+    default: return 0;
+  }
+}
+
+template <typename T, int D>
+cudaError_t launch_decode_sk_d(const SkArgs& a, int gpad, const CUtensorMap* kmap, const CUtensorMap* vmap,
+                               cudaStream_t stream) {
+  switch (gpad) {
+    case 1: return launch_decode_sk_dg<T, D, 1>(a, kmap, vmap, stream);
+    case 2: return launch_decode_sk_dg<T, D, 2>(a, kmap, vmap, stream);
+    case 4: return launch_decode_sk_dg<T, D, 4>(a, kmap, vmap, stream);
+    case 8: return launch_decode_sk_dg<T, D, 8>(a, kmap, vmap, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <typename T>
+cudaError_t launch_decode_sk_t(const SkArgs& a, int head_dim, int gpad, const CUtensorMap* kmap,
+                               const CUtensorMap* vmap, cudaStream_t stream) {
+  switch (head_dim) {
+    case 64: return launch_decode_sk_d<T, 64>(a, gpad, kmap, vmap, stream);
+    case 128: return launch_decode_sk_d<T, 128>(a, gpad, kmap, vmap, stream);
+    case 256: return launch_decode_sk_d<T, 256>(a, gpad, kmap, vmap, stream);
     default: return cudaErrorInvalidValue;
   }
 }

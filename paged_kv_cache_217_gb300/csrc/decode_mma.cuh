@@ -1,0 +1,340 @@
+// PagedAttention decode for GQA groups on the tensor cores (sm_103a).
+//
+// Same computation, grid, per-warp pipeline and epilogue as the CUDA-core
+// kernel in decode.cuh (see its header for what is computed and the pages it
+// follows). What changes is how one 16-token tile is contracted: with G >= 2
+// query heads per KV head, the per-tile work is a small matrix product,
+//     S[G x 16] = Q[G x D] . K^T[D x 16],   O[G x D] += P[G x 16] . V[16 x D],
+// which runs as mma.sync m16n8k16 (fp16/bf16 inputs, fp32 accumulators) with
+// the G heads on the M dimension (rows G..15 are zero padding). This cuts the
+// issued instructions per tile by about 10x against fp32 FMAs and shuffles.
+//
+// Tiles arrive by TMA tensor copies (cp.async.bulk.tensor, 128-byte swizzle):
+// the pool is seen as a 2-D tensor [num_blocks*num_kv_heads*16 rows, D cols]
+// and each tile as D/64 boxes of 16 rows x 64 columns. The swizzle makes the
+// ldmatrix reads of K rows (and the transposed reads of V rows) free of bank
+// conflicts, which rows 256 bytes apart would otherwise hit 8 ways.
+//
+// P is fed to the PV product as two fp16/bf16 terms, hi = round(P) and
+// lo = round(P - hi), so the weights keep about 16 significant bits instead
+// of the 8 (bf16) or 11 (fp16) a single rounding leaves.
+#pragma once
+
+#include <cuda.h>
+
+#include "decode.cuh"
+
+namespace pkv {
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          dst),
+      "l"(map), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+template <typename T>
+struct Mma;
+
+template <>
+struct Mma<__nv_bfloat16> {
+  // c += a (16x16, row) . b (16x8, col), fp32 accumulate
+  static __device__ __forceinline__ void run(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                             uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  }
+  // Packs two floats rounded to nearest even; returns the packed pair and
+  // writes back the values it represents.
+  static __device__ __forceinline__ uint32_t pack(float x, float y, float& xr, float& yr) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(x, y);
+    const float2 f = __bfloat1622float2(h);
+    xr = f.x;
+    yr = f.y;
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+};
+
+template <>
+struct Mma<__half> {
+  static __device__ __forceinline__ void run(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                             uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  }
+  static __device__ __forceinline__ uint32_t pack(float x, float y, float& xr, float& yr) {
+    __half2 h = __floats2half2_rn(x, y);
+    const float2 f = __half22float2(h);
+    xr = f.x;
+    yr = f.y;
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+};
+
+template <typename T, int D, int NW, int STAGES>
+struct MmaCfg {
+  static constexpr int BOXES = D / 64;               // 64-column boxes per tile
+  static constexpr int BOX_BYTES = kBlock * 128;     // 16 rows x 128 bytes
+  static constexpr int TILE_BYTES = BOXES * BOX_BYTES;
+  static constexpr int STAGE_BYTES = 2 * TILE_BYTES; // K tile then V tile
+  static constexpr int KSTEPS = D / 16;
+  static constexpr int NTILES = D / 8;
+  static constexpr size_t RING_BYTES = size_t(NW) * STAGES * STAGE_BYTES;
+  static constexpr size_t SMEM_BYTES = RING_BYTES + size_t(NW) * STAGES * 8 + 1024;  // + alignment slack
+  static_assert(D % 64 == 0 && D >= 64 && D <= 256, "head_dim must be 64, 128 or 256");
+};
+
+// Byte offset of 16-byte chunk `chunk` (0 .. D/8-1) of row `row` (0..15) in a
+// tile written by 128-byte-swizzled boxes of 16 rows x 64 columns.
+__device__ __forceinline__ uint32_t swz(int row, int chunk) {
+  return uint32_t((chunk >> 3) * (kBlock * 128) + row * 128 + (((chunk & 7) ^ (row & 7)) << 4));
+}
+
+// One 16-row tile for the G heads of this warp's lane row g = lane/4.
+template <typename T, int D, int NW, int STAGES, bool MASK>
+__device__ __forceinline__ void mma_tile(uint32_t kt, uint32_t vt, int rows, const uint32_t (&qa)[D / 16][2],
+                                         float (&o)[D / 8][4], float& mrun, float& lrun, float scale_log2,
+                                         int lane) {
+  using C = MmaCfg<T, D, NW, STAGES>;
+  const int t = lane & 3;
+  const int mi = lane >> 3, rr = lane & 7;
+
+  // S = Q . K^T for tokens 0-7 (s0) and 8-15 (s1).
+  float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+  {
+    const int tok = (mi >> 1) * 8 + rr;
+#pragma unroll
+    for (int ks = 0; ks < C::KSTEPS; ++ks) {
+      uint32_t b[4];
+      ldsm_x4(kt + swz(tok, 2 * ks + (mi & 1)), b);
+      Mma<T>::run(s0, qa[ks][0], 0u, qa[ks][1], 0u, b[0], b[1]);
+      Mma<T>::run(s1, qa[ks][0], 0u, qa[ks][1], 0u, b[2], b[3]);
+    }
+  }
+
+  // Online softmax on head g's scores for tokens 2t, 2t+1, 8+2t, 9+2t.
+  float x[4] = {s0[0] * scale_log2, s0[1] * scale_log2, s1[0] * scale_log2, s1[1] * scale_log2};
+  if (MASK) {
+    if (2 * t >= rows) x[0] = -INFINITY;
+    if (2 * t + 1 >= rows) x[1] = -INFINITY;
+    if (8 + 2 * t >= rows) x[2] = -INFINITY;
+    if (9 + 2 * t >= rows) x[3] = -INFINITY;
+  }
+  float mt = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+  mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 1));
+  mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 2));
+  const float mn = fmaxf(mrun, mt);
+  if (__any_sync(kFull, mn > mrun)) {
+    const float alpha = fast_exp2(mrun - mn);  // 1 for rows whose max did not move
+    lrun *= alpha;
+#pragma unroll
+    for (int nd = 0; nd < C::NTILES; ++nd) {
+      o[nd][0] *= alpha;
+      o[nd][1] *= alpha;
+    }
+    mrun = mn;
+  }
+  float p[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) p[i] = fast_exp2(x[i] - mn);
+  lrun += (p[0] + p[1]) + (p[2] + p[3]);
+  float r0, r1, r2, r3, d0, d1, d2, d3;
+  const uint32_t hi01 = Mma<T>::pack(p[0], p[1], r0, r1);
+  const uint32_t hi23 = Mma<T>::pack(p[2], p[3], r2, r3);
+  const uint32_t lo01 = Mma<T>::pack(p[0] - r0, p[1] - r1, d0, d1);
+  const uint32_t lo23 = Mma<T>::pack(p[2] - r2, p[3] - r3, d2, d3);
+
+  // O += P . V, two n-tiles (16 dims) per transposed ldmatrix.
+  {
+    const int tok = (mi & 1) * 8 + rr;
+#pragma unroll
+    for (int c = 0; c < C::NTILES / 2; ++c) {
+      uint32_t b[4];
+      ldsm_x4_trans(vt + swz(tok, 2 * c + (mi >> 1)), b);
+      Mma<T>::run(o[2 * c], hi01, 0u, hi23, 0u, b[0], b[1]);
+      Mma<T>::run(o[2 * c], lo01, 0u, lo23, 0u, b[0], b[1]);
+      Mma<T>::run(o[2 * c + 1], hi01, 0u, hi23, 0u, b[2], b[3]);
+      Mma<T>::run(o[2 * c + 1], lo01, 0u, lo23, 0u, b[2], b[3]);
+    }
+  }
+}
+
+// Zeroes rows [rows, 16) of a swizzled V tile so that 0 * (stale data) in the
+// PV product cannot produce NaN, then orders these generic-proxy writes before
+// the next bulk-tensor write into the same stage.
+template <int D>
+__device__ __forceinline__ void zero_tail_rows(uint32_t vt, int rows, int lane) {
+  constexpr int CH = D / 8;
+  for (int i = lane; i < (kBlock - rows) * CH; i += 32) {
+    const int row = rows + i / CH, chunk = i % CH;
+    asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(vt + swz(row, chunk)), "r"(0u) : "memory");
+  }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  __syncwarp();
+}
+
+template <typename T, int D, int G, int NW, int STAGES>
+__global__ void __launch_bounds__(NW * 32)
+paged_decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap kmap,
+                        const __grid_constant__ CUtensorMap vmap) {
+  using C = MmaCfg<T, D, NW, STAGES>;
+  static_assert(G >= 2 && G <= 8 && (G & (G - 1)) == 0, "tensor-core path is for GQA groups of 2..8");
+  extern __shared__ unsigned char smem_raw[];
+  // 128-byte-swizzled bulk-tensor destinations want 1024-byte alignment.
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+  wait_for_predecessor();
+  const int g = blockIdx.x, s = long_first_seq<NW>(a, blockIdx.y), part = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int hq0 = g * a.group;
+  const int gr = lane >> 2, t = lane & 3;   // MMA row (query head) and column pair of this lane
+
+  int L = a.context_lens[s];
+  const int max_len = a.max_blocks_per_seq * kBlock;
+  if (L < 0 || L > max_len) {
+    if (threadIdx.x == 0 && part == 0 && g == 0) flag(a.status, PKV_DEV_BAD_CONTEXT_LEN);
+    L = L < 0 ? 0 : max_len;
+  }
+  const int nparts = L == 0 ? 1 : (L + a.part_tokens - 1) / a.part_tokens;
+  if (part >= nparts) return;
+  if (L == 0) {
+    T* o = static_cast<T*>(a.out) + (size_t(s) * a.num_q_heads + hq0) * D;
+    for (int i = threadIdx.x; i < a.group * D / 8; i += NW * 32)
+      reinterpret_cast<uint4*>(o)[i] = make_uint4(0u, 0u, 0u, 0u);
+    return;
+  }
+  const int t0 = part * a.part_tokens;
+  const int ntok = min(L, t0 + a.part_tokens) - t0;
+  const int nb = (ntok + kBlock - 1) / kBlock;
+
+  unsigned char* ring = smem + size_t(warp) * STAGES * C::STAGE_BYTES;
+  const uint32_t ring_s = smem_addr(ring);
+  const uint32_t bar_s = smem_addr(smem + C::RING_BYTES) + warp * STAGES * 8;
+  if (lane == 0) {
+#pragma unroll
+    for (int st = 0; st < STAGES; ++st) mbar_init(bar_s + 8 * st, 1);
+    mbar_init_fence();
+  }
+  __syncwarp();
+
+  // Q as the A operand: row gr holds query head hq0 + gr (zero past the group).
+  uint32_t qa[C::KSTEPS][2];
+  {
+    const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
+        static_cast<const T*>(a.q) + (size_t(s) * a.num_q_heads + hq0 + gr) * D);
+#pragma unroll
+    for (int ks = 0; ks < C::KSTEPS; ++ks) {
+      qa[ks][0] = gr < a.group ? __ldg(qrow + 8 * ks + t) : 0u;
+      qa[ks][1] = gr < a.group ? __ldg(qrow + 8 * ks + 4 + t) : 0u;
+    }
+  }
+
+  const int n_my = nb > warp ? (nb - warp + NW - 1) / NW : 0;
+  const int32_t* trow = a.block_tables + size_t(s) * a.max_blocks_per_seq + t0 / kBlock;
+  auto load_ids = [&](int batch) -> int {
+    const int k = batch * 32 + lane;
+    if (k >= n_my) return 0;
+    int id = __ldg(trow + warp + k * NW);
+    if (id < 0 || id >= a.num_blocks) {
+      flag(a.status, PKV_DEV_BAD_BLOCK_ID);
+      id = 0;
+    }
+    return id;
+  };
+  int ids = load_ids(0);
+  int ids_next = n_my > 32 ? load_ids(1) : 0;
+  int id_batch = 0;
+
+  auto issue = [&](int k) {  // warp-uniform; k increases by one per call
+    if ((k >> 5) != id_batch) {
+      ids = ids_next;
+      ++id_batch;
+      ids_next = (id_batch + 1) * 32 < n_my ? load_ids(id_batch + 1) : 0;
+    }
+    const int id = __shfl_sync(kFull, ids, k & 31);
+    if (lane == 0) {
+      const int st = k % STAGES;
+      const uint32_t bar = bar_s + 8 * st;
+      const uint32_t dst = ring_s + st * C::STAGE_BYTES;
+      const int y = (id * a.num_kv_heads + g) * kBlock;
+      mbar_arrive_expect_tx(bar, C::STAGE_BYTES);
+#pragma unroll
+      for (int j = 0; j < C::BOXES; ++j) {
+        tma_load_2d(dst + j * C::BOX_BYTES, &kmap, 64 * j, y, bar);
+        tma_load_2d(dst + C::TILE_BYTES + j * C::BOX_BYTES, &vmap, 64 * j, y, bar);
+      }
+    }
+  };
+
+  float o[C::NTILES][4];
+#pragma unroll
+  for (int nd = 0; nd < C::NTILES; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
+  float mrun = -INFINITY, lrun = 0.f;
+
+  const int pre = n_my < STAGES ? n_my : STAGES;
+  for (int k = 0; k < pre; ++k) issue(k);
+
+  for (int k = 0; k < n_my; ++k) {
+    const int st = k % STAGES;
+    const uint32_t parity = (k / STAGES) & 1;
+    const bool ok = mbar_wait_bounded(bar_s + 8 * st, parity);
+    if (!__all_sync(kFull, ok)) {
+      if (lane == 0) flag(a.status, PKV_DEV_WAIT_TIMEOUT);
+      const int last = min(n_my, k + STAGES);
+      for (int kk = k; kk < last; ++kk) mbar_wait_bounded(bar_s + 8 * (kk % STAGES), (kk / STAGES) & 1);
+      break;
+    }
+    const int j = warp + k * NW;
+    const int rows = min(kBlock, ntok - j * kBlock);
+    const uint32_t kt = ring_s + st * C::STAGE_BYTES;
+    if (rows == kBlock) {
+      mma_tile<T, D, NW, STAGES, false>(kt, kt + C::TILE_BYTES, rows, qa, o, mrun, lrun, a.scale_log2, lane);
+    } else {
+      zero_tail_rows<D>(kt + C::TILE_BYTES, rows, lane);
+      mma_tile<T, D, NW, STAGES, true>(kt, kt + C::TILE_BYTES, rows, qa, o, mrun, lrun, a.scale_log2, lane);
+    }
+    __syncwarp();
+    if (k + STAGES < n_my) issue(k + STAGES);
+  }
+
+  // Row sums: the four lanes of a row each summed a quarter of the tokens.
+  lrun += __shfl_xor_sync(kFull, lrun, 1);
+  lrun += __shfl_xor_sync(kFull, lrun, 2);
+
+  // Publish (acc[G][D], m[G], l[G]) in this warp's ring for the shared epilogue.
+  float* wsm = reinterpret_cast<float*>(ring);
+  if (gr < G) {
+#pragma unroll
+    for (int nd = 0; nd < C::NTILES; ++nd)
+      *reinterpret_cast<float2*>(wsm + gr * D + 8 * nd + 2 * t) = make_float2(o[nd][0], o[nd][1]);
+    if (t == 0) {
+      wsm[G * D + gr] = mrun;
+      wsm[G * D + G + gr] = lrun;
+    }
+  }
+  __syncthreads();
+  finish_chunk<T, D, G, NW>(a, smem, size_t(STAGES) * C::STAGE_BYTES, s, g, part, nparts);
+}
+
+}  // namespace pkv

@@ -1,19 +1,35 @@
 // Host-side launchers of the CUDA kernels (internal to the library).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cstdint>
 
 namespace pkv {
 
 struct DecodeArgs;
+struct SkArgs;
 
 constexpr int kMaxParts = 8192;   // split-K partitions per sequence (merge smem bound)
 constexpr int kMaxDevices = 64;
 
-// Decode (+ merge when a.max_parts > 1). head_dim in {64,128,256}; gpad in {1,2,4,8}.
-cudaError_t launch_decode_f16(const DecodeArgs& a, int head_dim, int gpad, cudaStream_t stream);
-cudaError_t launch_decode_bf16(const DecodeArgs& a, int head_dim, int gpad, cudaStream_t stream);
+// Decode. head_dim in {64,128,256}; gpad in {1,2,4,8}. gpad 1 runs the CUDA-core
+// kernel; gpad >= 2 runs the tensor-core kernel, which reads the pools through
+// the tensor maps kmap/vmap (128-byte swizzle, boxes of 16 rows x 64 columns).
+cudaError_t launch_decode_f16(const DecodeArgs& a, int head_dim, int gpad, const CUtensorMap* kmap,
+                              const CUtensorMap* vmap, cudaStream_t stream);
+cudaError_t launch_decode_bf16(const DecodeArgs& a, int head_dim, int gpad, const CUtensorMap* kmap,
+                               const CUtensorMap* vmap, cudaStream_t stream);
+
+// Decode with the balanced persistent schedule (decode_sk.cuh); same gpad rules.
+cudaError_t launch_decode_sk_f16(const SkArgs& a, int head_dim, int gpad, const CUtensorMap* kmap,
+                                 const CUtensorMap* vmap, cudaStream_t stream);
+cudaError_t launch_decode_sk_bf16(const SkArgs& a, int head_dim, int gpad, const CUtensorMap* kmap,
+                                  const CUtensorMap* vmap, cudaStream_t stream);
+
+// Largest batch the balanced schedule takes for these sizes (its prefix sums
+// share the CTA's shared memory with the rings); 0 for unsupported sizes.
+int decode_sk_max_seqs(int head_dim, int gpad);
 
 // Bit copies; element size is 2 bytes for both supported dtypes.
 cudaError_t launch_reshape_and_cache(const void* k, const void* v, void* k_pool, void* v_pool,

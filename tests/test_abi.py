@@ -36,24 +36,47 @@ def test_library_exports_every_declared_function():
     assert B.version().startswith("paged_kv")
 
 
+def _round16(x):
+    return (x + 15) // 16 * 16
+
+
+def _split_bytes(S, hq, hkv, d, parts):
+    """Fixed partitions: fp32 partials [S][Hq][P][D], (max, sum) [S][Hq][P], counters [S][Hkv]."""
+    return _round16(S * hq * parts * (d * 4 + 8) + S * hkv * 4)
+
+
+def _balanced_bytes(S, hq, hkv, d):
+    """Balanced schedule: two slots per persistent warp (2048 warps max), counters [S][Hkv]."""
+    slot_floats = ((hq // hkv) * (d + 2) + 3) // 4 * 4
+    return _round16(2 * 2048 * slot_floats * 4 + S * hkv * 4)
+
+
 def test_workspace_and_partition_choice():
-    # short contexts run in one pass and need no workspace
-    assert B.resolved_partition(64, 40, 32) == -1
+    # automatic choice: one CTA per (sequence, KV head) with at least 608 pairs
+    assert B.resolved_partition(64, 40, 40, 128, 32) == -1          # 2560 pairs
     assert B.workspace_size(64, 40, 40, 128, 32) == 0
-    # longer contexts split into 512-token partitions by default
-    assert B.resolved_partition(64, 40, 128) == 512
-    parts = 128 * 16 // 512
-    assert B.workspace_size(64, 40, 40, 128, 128) == 64 * 40 * parts * (128 * 4 + 8)
+    assert B.resolved_partition(256, 32, 8, 128, 64) == -1          # 2048 pairs
+    assert B.resolved_partition(8, 96, 96, 128, 2048) == -1         # 768 pairs
+    # fewer pairs: partitions just large enough for 608 CTAs, at least 256 tokens
+    assert B.resolved_partition(2, 8, 8, 128, 2048) == 864          # 16 pairs x 38 parts
+    assert B.workspace_size(2, 8, 8, 128, 2048) == _split_bytes(2, 8, 8, 128, 38)
+    assert B.resolved_partition(4, 4, 4, 64, 100) == 256            # 16 pairs, 1600 tokens
+    assert B.resolved_partition(4, 4, 4, 64, 16) == -1              # 256 tokens: one pass
+    # the balanced persistent schedule, on request
+    assert B.resolved_partition(64, 40, 40, 128, 32, -2) == B.BALANCED
+    assert B.workspace_size(64, 40, 40, 128, 32, -2) == _balanced_bytes(64, 40, 40, 128)
+    assert B.workspace_size(256, 32, 8, 128, 64, -2) == _balanced_bytes(256, 32, 8, 128)
     # explicit choices
-    assert B.resolved_partition(8, 96, 2048, -1) == -1
-    assert B.resolved_partition(8, 96, 2048, 256) == 256
+    assert B.resolved_partition(8, 96, 96, 128, 2048, -1) == -1
+    assert B.resolved_partition(8, 96, 96, 128, 2048, 256) == 256
     assert B.workspace_size(8, 96, 96, 128, 2048, -1) == 0
-    assert B.workspace_size(8, 96, 96, 128, 2048, 512) == 8 * 96 * 64 * (128 * 4 + 8)
+    assert B.workspace_size(8, 96, 96, 128, 2048, 512) == _split_bytes(8, 96, 96, 128, 64)
+    assert B.workspace_size(3, 6, 2, 64, 10, 16) == _split_bytes(3, 6, 2, 64, 10)
     # a partition that covers the whole context is one pass
-    assert B.resolved_partition(4, 4, 4, 64) == -1
+    assert B.resolved_partition(4, 4, 4, 64, 4, 64) == -1
     assert B.workspace_size(4, 4, 4, 64, 4, 64) == 0
     # invalid partition sizes
-    assert B.resolved_partition(4, 4, 4, 24) == 0
+    assert B.resolved_partition(4, 4, 4, 64, 4, 24) == 0
     assert B.workspace_size(0, 4, 4, 64, 4) == 0
 
 
@@ -84,6 +107,8 @@ def _decode(**kw):
     (dict(part=24), 1),               # not a multiple of 16
     (dict(MB=64, part=16), 5),        # split needs a workspace
     (dict(MB=64, part=16, ws=FAKE, wsb=100), 5),
+    (dict(part=-2), 5),               # the balanced schedule needs one too
+    (dict(part=-2, S=4000, MB=4), 2),  # beyond the balanced schedule's batch limit
 ])
 def test_decode_rejects_bad_arguments_before_launch(kw, status):
     st, msg = _decode(**kw)

@@ -92,7 +92,7 @@ RAGGED = [1, 15, 16, 17, 31, 33, 100, 0, 255, 257, 700]
 def test_decode_matches_oracle(dtype, d, hq, hkv):
     case = H.make_case(RAGGED, hq, hkv, d, dtype, seed=d + hq + hkv, extra_cols=3)
     want = H.oracle_full(case)
-    for part in (0, -1, 64, 512):
+    for part in (0, -1, -2, 64, 512):
         H.assert_attention_close(H.to_f64(_run(case, part)), want, f"{dtype} d={d} {hq}/{hkv} part={part}")
 
 
@@ -110,6 +110,57 @@ def test_scores_large_and_scale_extremes():
     case.k_pool.mul_(2)
     H.assert_attention_close(H.to_f64(_run(case)), H.oracle_full(case), "large logits")
     H.assert_attention_close(H.to_f64(_run(case, 16)), H.oracle_full(case), "large logits split 16")
+
+
+def test_split_calls_with_different_shapes_share_one_workspace():
+    # The binding reuses one workspace; a later call's partition counters may sit
+    # where an earlier call left partials, so every split call must start clean.
+    small = H.make_case([700, 40], 8, 2, 128, "bf16", seed=41)
+    large = H.make_case([600 + 37 * i for i in range(40)], 8, 8, 128, "bf16", seed=42)
+    want_small, want_large = H.oracle_full(small), H.oracle_full(large)
+    ws = torch.zeros(64 << 20, dtype=torch.uint8, device="cuda")
+    for case, want in ((small, want_small), (large, want_large), (small, want_small), (large, want_large)):
+        out = case.new_out()
+        B.paged_attention_decode(out, case.q, case.k_pool, case.v_pool, case.tables, case.lens, case.scale,
+                                 partition_size=32, workspace=ws)
+        torch.cuda.synchronize()
+        H.assert_attention_close(H.to_f64(out), want, "shared workspace")
+        ws[: 32 << 20].fill_(0x7f)   # stale garbage everywhere the next call may look
+
+
+@pytest.mark.parametrize("lens,hq,hkv,d,dtype", [
+    ([30000], 4, 1, 128, "bf16"),                        # one item spread over hundreds of warps
+    ([3] * 500 + [1, 16, 17, 0], 8, 8, 64, "f16"),       # hundreds of tiny items
+    ([900, 901, 17], 32, 8, 128, "f16"),                 # GQA, few long items
+    ([5, 0, 0, 33], 16, 2, 256, "bf16"),                 # group 8, head_dim 256, empty sequences
+])
+def test_balanced_schedule_matches_oracle(lens, hq, hkv, d, dtype):
+    case = H.make_case(lens, hq, hkv, d, dtype, seed=len(lens) + d)
+    assert B.resolved_partition(len(lens), hq, hkv, d, case.tables.shape[1], -2) == B.BALANCED
+    want = H.oracle_full(case)
+    H.assert_attention_close(H.to_f64(_run(case, -2)), want, f"balanced {lens[:3]}")
+    H.assert_attention_close(H.to_f64(_run(case)), want, f"auto {lens[:3]}")
+
+
+@pytest.mark.parametrize("S", [2048, 2049])
+def test_batch_size_limit_of_the_balanced_schedule(S):
+    # The balanced schedule keeps its prefix sums in shared memory: 2048 sequences
+    # fit, 2049 are refused (nothing launched); the automatic choice runs both.
+    rng = np.random.default_rng(S)
+    lens = rng.integers(0, 300, size=S).astype(np.int32)
+    case = H.make_case(lens, 8, 2, 128, "bf16", seed=S)
+    if S <= 2048:
+        out = _run(case, -2)
+        _check_sampled(case, out, 24, seed=S)
+    else:
+        with pytest.raises(B.PagedKVError) as exc:
+            _run(case, -2)
+        assert exc.value.status == 2
+    out = _run(case)
+    _check_sampled(case, out, 24, seed=S + 1)
+    zero = np.flatnonzero(lens == 0)
+    if zero.size:
+        assert torch.all(out[torch.from_numpy(zero).cuda()] == 0)
 
 
 # ---------------------------------------------------------------------------

@@ -292,7 +292,7 @@ pkv_status_t pkv_paged_attention_decode(void* out, const void* q, const void* k_
 
   const int gpad = round_pow2_group(group);
   alignas(64) CUtensorMap kmap, vmap;
-  if (gpad >= 2) {
+  if (gpad >= 2 || PKV_MMA_FOR_MHA) {
     const int64_t rows = int64_t(num_blocks) * num_kv_heads * PKV_BLOCK_SIZE;
     st = pool_tensor_map(&kmap, k_pool, rows, head_dim, dtype);
     if (st != PKV_OK) return st;

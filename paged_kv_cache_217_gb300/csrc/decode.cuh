@@ -71,6 +71,25 @@ struct DecodeArgs {
 // the decode kernels comes after this.
 __device__ __forceinline__ void wait_for_predecessor() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// Grid layout of the one-CTA-per-(sequence, KV head) kernels: 0 = KV heads
+// vary fastest in launch order (blockIdx.x = head), 1 = sequences do.
+#ifndef PKV_GRID_SEQ_FASTEST
+#define PKV_GRID_SEQ_FASTEST 0
+#endif
+constexpr bool kSeqFastest = PKV_GRID_SEQ_FASTEST != 0;
+
+// Route group size 1 (MHA) to the tensor-core tile as well (measurement knob;
+// CUDA cores by default).
+#ifndef PKV_MMA_FOR_MHA
+#define PKV_MMA_FOR_MHA 0
+#endif
+
+// Packed fp32 FMAs (fma.rn.f32x2) in the CUDA-core tile math.
+#ifndef PKV_PACKED_FMA
+#define PKV_PACKED_FMA 0
+#endif
+constexpr bool kPackedFma = PKV_PACKED_FMA != 0;
+
 #ifndef PKV_ORDER_MAX_SEQS
 #define PKV_ORDER_MAX_SEQS 1024
 #endif
@@ -216,12 +235,18 @@ __device__ __forceinline__ void decode_tile(uint32_t kt, uint32_t vt, int rows,
     for (int h = 0; h < G; ++h) {
       float d0 = qf[h][0] * kf[0];
       float d1 = qf[h][1] * kf[1];
-      d0 = fmaf(qf[h][2], kf[2], d0);
-      d1 = fmaf(qf[h][3], kf[3], d1);
-      d0 = fmaf(qf[h][4], kf[4], d0);
-      d1 = fmaf(qf[h][5], kf[5], d1);
-      d0 = fmaf(qf[h][6], kf[6], d0);
-      d1 = fmaf(qf[h][7], kf[7], d1);
+      if constexpr (kPackedFma) {
+        ffma2(d0, d1, qf[h][2], qf[h][3], kf[2], kf[3], d0, d1);
+        ffma2(d0, d1, qf[h][4], qf[h][5], kf[4], kf[5], d0, d1);
+        ffma2(d0, d1, qf[h][6], qf[h][7], kf[6], kf[7], d0, d1);
+      } else {
+        d0 = fmaf(qf[h][2], kf[2], d0);
+        d1 = fmaf(qf[h][3], kf[3], d1);
+        d0 = fmaf(qf[h][4], kf[4], d0);
+        d1 = fmaf(qf[h][5], kf[5], d1);
+        d0 = fmaf(qf[h][6], kf[6], d0);
+        d1 = fmaf(qf[h][7], kf[7], d1);
+      }
       sc[h * NPASS + i] = d0 + d1;
     }
   }
@@ -278,8 +303,13 @@ __device__ __forceinline__ void decode_tile(uint32_t kt, uint32_t vt, int rows,
       const int src = r * LPR + ((v >> (C::LOGV - C::NH)) << (C::LOGL - C::NH));
       const float pp = __shfl_sync(kFull, p[v & (NF - 1)], src);
       lsum[h] += pp;
+      if constexpr (kPackedFma) {
 #pragma unroll
-      for (int c = 0; c < 8; ++c) acc[h][c] = fmaf(pp, vf[c], acc[h][c]);
+        for (int c = 0; c < 8; c += 2) ffma2(acc[h][c], acc[h][c + 1], pp, pp, vf[c], vf[c + 1], acc[h][c], acc[h][c + 1]);
+      } else {
+#pragma unroll
+        for (int c = 0; c < 8; ++c) acc[h][c] = fmaf(pp, vf[c], acc[h][c]);
+      }
     }
   }
 }
@@ -389,11 +419,19 @@ paged_decode_kernel(const DecodeArgs a) {
   extern __shared__ __align__(1024) unsigned char smem[];
 
   wait_for_predecessor();
-  const int g = blockIdx.x, s = long_first_seq<NW>(a, blockIdx.y), part = blockIdx.z;
+  const int g = kSeqFastest ? blockIdx.y : blockIdx.x;
+  const int s = long_first_seq<NW>(a, kSeqFastest ? blockIdx.x : blockIdx.y), part = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int sub = lane & (LPR - 1), r = lane / LPR;
   const int hq0 = g * a.group;
 
+  // The first 32 block ids of this warp's tiles do not depend on the length:
+  // read them together with it (entries past the sequence are never used).
+  int ids_early = 0;
+  {
+    const int j0 = (blockIdx.z * a.part_tokens) / kBlock + warp + lane * NW;
+    if (j0 < a.max_blocks_per_seq) ids_early = __ldg(a.block_tables + size_t(s) * a.max_blocks_per_seq + j0);
+  }
   int L = a.context_lens[s];
   const int max_len = a.max_blocks_per_seq * kBlock;
   if (L < 0 || L > max_len) {
@@ -454,7 +492,14 @@ paged_decode_kernel(const DecodeArgs a) {
     }
     return id;
   };
-  int ids = load_ids(0);
+  int ids = 0;
+  if (lane < n_my) {
+    ids = ids_early;
+    if (ids < 0 || ids >= a.num_blocks) {
+      flag(a.status, PKV_DEV_BAD_BLOCK_ID);
+      ids = 0;
+    }
+  }
   int ids_next = n_my > 32 ? load_ids(1) : 0;
   int id_batch = 0;
 

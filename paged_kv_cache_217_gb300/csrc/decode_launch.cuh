@@ -63,8 +63,9 @@ cudaError_t launch_decode_dg(const DecodeArgs& a, const CUtensorMap* kmap, const
   constexpr int NW = PKV_GRID_WARPS;
   constexpr int STAGES = (D == 256 && PKV_GRID_WARPS * PKV_GRID_STAGES > 8) ? 2 : PKV_GRID_STAGES;
   static bool configured[kMaxDevices] = {};
-  const dim3 grid(unsigned(a.num_kv_heads), unsigned(a.num_seqs), unsigned(a.max_parts));
-  if constexpr (G == 1) {
+  const dim3 grid(kSeqFastest ? unsigned(a.num_seqs) : unsigned(a.num_kv_heads),
+                  kSeqFastest ? unsigned(a.num_kv_heads) : unsigned(a.num_seqs), unsigned(a.max_parts));
+  if constexpr (G == 1 && !PKV_MMA_FOR_MHA) {
     using C = DecodeCfg<T, D, G, NW, STAGES>;
     auto kern = paged_decode_kernel<T, D, G, NW, STAGES>;
     cudaError_t err = configure_once(kern, C::SMEM_BYTES, configured);

@@ -91,6 +91,12 @@ struct Mma<__half> {
   }
 };
 
+// Split the QK accumulation of each 8-token half into two chains.
+#ifndef PKV_SPLIT_QK
+#define PKV_SPLIT_QK 0
+#endif
+constexpr bool kSplitQk = PKV_SPLIT_QK != 0;
+
 template <typename T, int D, int NW, int STAGES>
 struct MmaCfg {
   static constexpr int BOXES = D / 64;               // 64-column boxes per tile
@@ -119,16 +125,30 @@ __device__ __forceinline__ void mma_tile(uint32_t kt, uint32_t vt, int rows, con
   const int t = lane & 3;
   const int mi = lane >> 3, rr = lane & 7;
 
-  // S = Q . K^T for tokens 0-7 (s0) and 8-15 (s1).
+  // S = Q . K^T for tokens 0-7 (s0) and 8-15 (s1); with kSplitQk the k-steps
+  // alternate between two accumulators per half (shorter dependency chains).
   float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
   {
+    float s0b[4] = {0.f, 0.f, 0.f, 0.f}, s1b[4] = {0.f, 0.f, 0.f, 0.f};
     const int tok = (mi >> 1) * 8 + rr;
 #pragma unroll
     for (int ks = 0; ks < C::KSTEPS; ++ks) {
       uint32_t b[4];
       ldsm_x4(kt + swz(tok, 2 * ks + (mi & 1)), b);
-      Mma<T>::run(s0, qa[ks][0], 0u, qa[ks][1], 0u, b[0], b[1]);
-      Mma<T>::run(s1, qa[ks][0], 0u, qa[ks][1], 0u, b[2], b[3]);
+      if (kSplitQk && (ks & 1)) {
+        Mma<T>::run(s0b, qa[ks][0], 0u, qa[ks][1], 0u, b[0], b[1]);
+        Mma<T>::run(s1b, qa[ks][0], 0u, qa[ks][1], 0u, b[2], b[3]);
+      } else {
+        Mma<T>::run(s0, qa[ks][0], 0u, qa[ks][1], 0u, b[0], b[1]);
+        Mma<T>::run(s1, qa[ks][0], 0u, qa[ks][1], 0u, b[2], b[3]);
+      }
+    }
+    if (kSplitQk) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        s0[i] += s0b[i];
+        s1[i] += s1b[i];
+      }
     }
   }
 
@@ -198,18 +218,26 @@ __global__ void __launch_bounds__(NW * 32)
 paged_decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap) {
   using C = MmaCfg<T, D, NW, STAGES>;
-  static_assert(G >= 2 && G <= 8 && (G & (G - 1)) == 0, "tensor-core path is for GQA groups of 2..8");
+  static_assert(G >= 1 && G <= 8 && (G & (G - 1)) == 0, "tensor-core path takes groups of 1..8");
   extern __shared__ unsigned char smem_raw[];
   // 128-byte-swizzled bulk-tensor destinations want 1024-byte alignment.
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
   wait_for_predecessor();
-  const int g = blockIdx.x, s = long_first_seq<NW>(a, blockIdx.y), part = blockIdx.z;
+  const int g = kSeqFastest ? blockIdx.y : blockIdx.x;
+  const int s = long_first_seq<NW>(a, kSeqFastest ? blockIdx.x : blockIdx.y), part = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int hq0 = g * a.group;
   const int gr = lane >> 2, t = lane & 3;   // MMA row (query head) and column pair of this lane
 
+  // The first 32 block ids of this warp's tiles do not depend on the length:
+  // read them together with it (entries past the sequence are never used).
+  int ids_early = 0;
+  {
+    const int j0 = (blockIdx.z * a.part_tokens) / kBlock + warp + lane * NW;
+    if (j0 < a.max_blocks_per_seq) ids_early = __ldg(a.block_tables + size_t(s) * a.max_blocks_per_seq + j0);
+  }
   int L = a.context_lens[s];
   const int max_len = a.max_blocks_per_seq * kBlock;
   if (L < 0 || L > max_len) {
@@ -262,7 +290,14 @@ paged_decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap 
     }
     return id;
   };
-  int ids = load_ids(0);
+  int ids = 0;
+  if (lane < n_my) {
+    ids = ids_early;
+    if (ids < 0 || ids >= a.num_blocks) {
+      flag(a.status, PKV_DEV_BAD_BLOCK_ID);
+      ids = 0;
+    }
+  }
   int ids_next = n_my > 32 ? load_ids(1) : 0;
   int id_batch = 0;
 

@@ -221,6 +221,24 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def max_over_ranks(values, device="cpu"):
+    """Element-wise maximum of `values` over all ranks of the default process
+    group (the slowest rank's times); the values themselves on one rank."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def whole_job_gbs(bytes_per_rank_step, ms_per_step, world):
+    """Whole-job throughput: every rank moves bytes_per_rank_step per step and a
+    step takes ms_per_step on the slowest rank."""
+    return world * bytes_per_rank_step / (ms_per_step * 1e-3) / 1e9
+
+
 def measured_peak():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -403,17 +421,13 @@ def run_ours(args):
     torch.cuda.synchronize()
     e2e_ms = sum(s_.elapsed_time(e_) for s_, e_ in e2e_ev) / Ke
 
-    per_step_ms = total_ms / K
-    if world > 1:
-        t = torch.tensor([per_step_ms, e2e_ms], dtype=torch.float64, device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        per_step_ms, e2e_ms = float(t[0]), float(t[1])
+    per_step_ms, e2e_ms = max_over_ranks([total_ms / K, e2e_ms], device)
     if rank != 0:
         dist.destroy_process_group()
         return
 
     peak, peak_kind = measured_peak()
-    value = world * wl.kv_bytes / (per_step_ms * 1e-3) / 1e9
+    value = whole_job_gbs(wl.kv_bytes, per_step_ms, world)
     dec_ms = statistics.mean(decode_ms)
     achieved = wl.kv_bytes / (dec_ms * 1e-3) / 1e9
     traffic = recorded_traffic(args.workload)
@@ -458,7 +472,7 @@ def run_ours(args):
             "decode_ms": round(dec_ms, 5),
         },
         "e2e": {
-            "value": round(world * wl.kv_bytes / (e2e_ms * 1e-3) / 1e9, 1),
+            "value": round(whole_job_gbs(wl.kv_bytes, e2e_ms, world), 1),
             "unit": "GB/s",
             "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h,

@@ -103,6 +103,17 @@ const char* pkv_last_error_string(void);
  */
 pkv_status_t pkv_device_status(uint32_t* flags_out, int clear);
 
+/*
+ * Self-test of the kernels' bounded waits (no counterpart on the pages; a
+ * failure-detection check). Launches one warp on `stream` that waits on a
+ * shared-memory mbarrier for 16 bytes that no copy delivers, using the same
+ * bounded wait as the decode kernels but with a limit of `limit_us`
+ * microseconds (1..1000000). The wait runs out, the warp sets
+ * PKV_DEV_WAIT_TIMEOUT in the device status word and exits; the context stays
+ * usable. Read the flag with pkv_device_status.
+ */
+pkv_status_t pkv_selftest_bounded_wait(uint32_t limit_us, pkv_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* Decode attention                                                          */
 /* ------------------------------------------------------------------------ */

@@ -60,6 +60,7 @@ _SIGS = {
     "pkv_reshape_and_cache": ([_c_p] * 5 + [_c_int] * 5 + [_c_p], _c_int),
     "pkv_copy_blocks": ([_c_p] * 3 + [_c_int] * 5 + [_c_p], _c_int),
     "pkv_check_copy_pairs": ([_c_p, _c_int, _c_int], _c_int),
+    "pkv_selftest_bounded_wait": ([ctypes.c_uint32, _c_p], _c_int),
     "pkv_bm_create": ([_c_int, _c_int, _c_p, ctypes.POINTER(_c_p)], _c_int),
     "pkv_bm_destroy": ([_c_p], None),
     "pkv_bm_add_seq": ([_c_p, _c_i64, _c_i64], _c_int),
@@ -274,6 +275,14 @@ def device_status(clear=True):
     v = ctypes.c_uint32(0)
     _check(lib().pkv_device_status(ctypes.byref(v), 1 if clear else 0), "device_status")
     return int(v.value)
+
+
+def selftest_bounded_wait(limit_us=2000):
+    """Runs the bounded-wait self-test on the current device and stream (a wait
+    that must run out and raise PKV_DEV_WAIT_TIMEOUT); read it with device_status()."""
+    import torch
+    _check(lib().pkv_selftest_bounded_wait(int(limit_us), _stream_ptr(torch.device("cuda", torch.cuda.current_device()))),
+           "selftest_bounded_wait")
 
 
 def describe_device_flags(flags):

@@ -407,6 +407,16 @@ pkv_status_t pkv_copy_blocks(void* k_pool, void* v_pool, const int64_t* src_dst_
                      "copy_blocks launch");
 }
 
+pkv_status_t pkv_selftest_bounded_wait(uint32_t limit_us, pkv_stream_t stream) {
+  if (limit_us == 0 || limit_us > 1000000)
+    return pkv::fail(PKV_ERR_INVALID_ARG, "selftest_bounded_wait: limit_us must be in 1..1000000");
+  unsigned int* status = nullptr;
+  pkv_status_t st = status_word(&status);
+  if (st != PKV_OK) return st;
+  return cuda_status(pkv::launch_bounded_wait_selftest(1000ull * limit_us, status, stream),
+                     "bounded-wait self-test launch");
+}
+
 pkv_status_t pkv_check_copy_pairs(const int64_t* pairs, int num_pairs, int num_blocks) {
   if (num_pairs < 0 || num_blocks <= 0 || (num_pairs > 0 && !pairs))
     return pkv::fail(PKV_ERR_INVALID_ARG, "check_copy_pairs: bad argument");

@@ -84,7 +84,29 @@ copy_blocks_kernel(uint4* __restrict__ k_pool, uint4* __restrict__ v_pool,
   }
 }
 
+// Self-test of the bounded wait: arms an mbarrier for 16 bytes that no copy
+// will deliver and waits on it exactly as the decode kernels wait on a tile,
+// with a short limit. The wait runs out and the status word gets
+// PKV_DEV_WAIT_TIMEOUT; nothing is in flight, so the CTA exits cleanly.
+__global__ void bounded_wait_selftest_kernel(unsigned long long limit_ns, unsigned int* status) {
+  __shared__ __align__(8) uint64_t bar;
+  const uint32_t b = smem_addr(&bar);
+  if (threadIdx.x == 0) {
+    mbar_init(b, 1);
+    mbar_init_fence();
+    mbar_arrive_expect_tx(b, 16);
+  }
+  __syncwarp();
+  const bool ok = mbar_wait_bounded(b, 0, limit_ns);
+  if (!__all_sync(kFull, ok) && threadIdx.x == 0) flag(status, PKV_DEV_WAIT_TIMEOUT);
+}
+
 }  // namespace
+
+cudaError_t launch_bounded_wait_selftest(unsigned long long limit_ns, unsigned int* status, cudaStream_t stream) {
+  bounded_wait_selftest_kernel<<<1, 32, 0, stream>>>(limit_ns, status);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_reshape_and_cache(const void* k, const void* v, void* k_pool, void* v_pool,
                                      const int64_t* slots, int num_tokens, int num_kv_heads,

@@ -54,12 +54,14 @@ __device__ __forceinline__ unsigned long long global_timer_ns() {
 }
 
 // Waits for the phase with the given parity to complete, for at most
-// kWaitLimitNs. Returns false when the limit ran out.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+// limit_ns (kWaitLimitNs for the decode kernels). Returns false when the
+// limit ran out.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  unsigned long long limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_timer_ns();
   while (!mbar_try_wait(bar, parity)) {
-    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+    if (global_timer_ns() - t0 > limit_ns) return false;
   }
   return true;
 }

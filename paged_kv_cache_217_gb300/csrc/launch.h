@@ -31,6 +31,9 @@ cudaError_t launch_decode_sk_bf16(const SkArgs& a, int head_dim, int gpad, const
 // share the CTA's shared memory with the rings); 0 for unsupported sizes.
 int decode_sk_max_seqs(int head_dim, int gpad);
 
+// One warp that waits on an mbarrier no copy completes (bounded-wait self-test).
+cudaError_t launch_bounded_wait_selftest(unsigned long long limit_ns, unsigned int* status, cudaStream_t stream);
+
 // Bit copies; element size is 2 bytes for both supported dtypes.
 cudaError_t launch_reshape_and_cache(const void* k, const void* v, void* k_pool, void* v_pool,
                                      const int64_t* slots, int num_tokens, int num_kv_heads,

@@ -31,6 +31,8 @@ Modules:
   block_manager  -- independent model of the block manager (free list,
                     refcounts, fork, append with copy-on-write, free)
   numerics       -- exact fp16/bf16 -> fp64 conversion
+  quant          -- INT8 KV cache: per-row quantisation, quantised cache
+                    write, decode over the dequantised cache
 
 Every function here is pinned by tests in ``tests/test_oracle*.py`` against
 values and invariants that the pages and mathematics fix (hand-worked
@@ -38,4 +40,4 @@ examples under ``tests/golden/``, brute force on tiny inputs, closed forms,
 permutation invariance, copy-on-write sibling equality).
 """
 
-from . import numerics, attention, cache_ops, block_manager  # noqa: F401
+from . import numerics, attention, cache_ops, block_manager, quant  # noqa: F401

@@ -2,6 +2,7 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload llama13b|llama3_8b|opt66b_sampling|opt175b_long|tiny]
+                    [--kv native|int8]
 
 One step is one pass of the whole hot path over one batch: write each
 sequence's new K/V into its slot (reshape_and_cache), copy-on-write block
@@ -17,6 +18,10 @@ value = algorithmic KV bytes read per step (sum over sequences of
 L * num_kv_heads * head_dim * 2 (K and V) * 2 bytes) / device time per step,
 in GB/s, with inputs resident in HBM. L2 is flushed between timed steps
 (outside the timed events) and the KV working set is larger than L2.
+
+``--kv int8`` runs the same step over the INT8 KV cache (int8 codes plus one
+fp32 scale per row): the write quantises, the decode dequantises on the fly;
+its bytes per token and KV head are 2 * (head_dim + 4).
 
 Under torchrun (N > 1) every rank runs the same workload on its own GPU
 (replicas: the path has no exchange step); value = all ranks' bytes / the
@@ -70,7 +75,7 @@ def kernel_sha():
     return h.hexdigest()[:16]
 
 
-def build_workload(name, seed, device):
+def build_workload(name, seed, device, kv="native"):
     import torch
     from paged_kv_cache_217_gb300 import binding as B
     from paged_kv_cache_217_gb300 import workloads as W
@@ -123,8 +128,24 @@ def build_workload(name, seed, device):
     wl.q_h = W.normal_values((S, hq, d), dtype, seed * 11 + 4, "cpu")
     wl.knew_h = W.normal_values((S, hkv, d), dtype, seed * 11 + 5, "cpu")
     wl.vnew_h = W.normal_values((S, hkv, d), dtype, seed * 11 + 6, "cpu")
-    wl.kv_bytes = int(wl.lens_h.astype(np.int64).sum()) * hkv * d * 2 * 2
+    wl.kv = kv
     wl.num_blocks = k_pool.shape[0]
+    if kv == "int8":
+        # synthetic INT8 cache of the same pool shape: uniform codes, row scales
+        # about max|x| / 127 of N(0, 1) rows
+        del k_pool, v_pool
+        wl.k_pool = wl.v_pool = None
+        nb = wl.num_blocks
+        wl.k_cache = W.int8_codes((nb, hkv, 16, d), seed * 11 + 7, device)
+        wl.v_cache = W.int8_codes((nb, hkv, 16, d), seed * 11 + 8, device)
+        wl.k_scale = W.row_scales((nb, hkv, 16), seed * 11 + 9, device)
+        wl.v_scale = W.row_scales((nb, hkv, 16), seed * 11 + 10, device)
+        row_bytes = d + 4
+        if wl.unique_kv_bytes:
+            wl.unique_kv_bytes = wl.unique_kv_bytes // (d * 2) * row_bytes
+    else:
+        row_bytes = d * 2
+    wl.kv_bytes = int(wl.lens_h.astype(np.int64).sum()) * hkv * row_bytes * 2
     return wl
 
 
@@ -150,11 +171,26 @@ def device_inputs(wl, device):
     wl.out = torch.empty_like(wl.q)
 
 
+def cache_write(wl, B):
+    if wl.kv == "int8":
+        B.reshape_and_cache_int8(wl.knew, wl.vnew, wl.k_cache, wl.v_cache, wl.k_scale, wl.v_scale, wl.slots)
+    else:
+        B.reshape_and_cache(wl.knew, wl.vnew, wl.k_pool, wl.v_pool, wl.slots)
+
+
+def decode(wl, B):
+    if wl.kv == "int8":
+        B.paged_attention_decode_int8(wl.out, wl.q, wl.k_cache, wl.v_cache, wl.k_scale, wl.v_scale, wl.tables,
+                                      wl.lens, wl.scale, partition_size=wl.partition)
+    else:
+        B.paged_attention_decode(wl.out, wl.q, wl.k_pool, wl.v_pool, wl.tables, wl.lens, wl.scale,
+                                 partition_size=wl.partition)
+
+
 def step(wl, B):
     """One pass of the hot path on device-resident inputs."""
-    B.reshape_and_cache(wl.knew, wl.vnew, wl.k_pool, wl.v_pool, wl.slots)
-    B.paged_attention_decode(wl.out, wl.q, wl.k_pool, wl.v_pool, wl.tables, wl.lens, wl.scale,
-                             partition_size=wl.partition)
+    cache_write(wl, B)
+    decode(wl, B)
 
 
 # ---------------------------------------------------------------------------
@@ -279,17 +315,24 @@ def oracle_sample(wl, budget_s):
             break
     blocks = sorted({int(b) for s in seqs for b in wl.tables_h[s, :-(-int(wl.lens_h[s]) // 16)]})
     remap = {b: i for i, b in enumerate(blocks)}
-    idx = torch.tensor(blocks if blocks else [0], dtype=torch.int64, device=wl.k_pool.device)
-    kp = W.to_numpy_storage(wl.k_pool.index_select(0, idx), wl.dtype)
-    vp = W.to_numpy_storage(wl.v_pool.index_select(0, idx), wl.dtype)
+    if wl.kv == "int8":
+        idx = torch.tensor(blocks if blocks else [0], dtype=torch.int64, device=wl.k_cache.device)
+        kp, vp, ks, vs = [x.index_select(0, idx).cpu().numpy() for x in
+                          (wl.k_cache, wl.v_cache, wl.k_scale, wl.v_scale)]
+    else:
+        idx = torch.tensor(blocks if blocks else [0], dtype=torch.int64, device=wl.k_pool.device)
+        kp = W.to_numpy_storage(wl.k_pool.index_select(0, idx), wl.dtype)
+        vp = W.to_numpy_storage(wl.v_pool.index_select(0, idx), wl.dtype)
+        ks = vs = np.zeros(0, np.float32)
     tab = np.full((len(seqs), wl.tables_h.shape[1]), -1, np.int32)
     for i, s in enumerate(seqs):
         nb = -(-int(wl.lens_h[s]) // 16)
         tab[i, :nb] = [remap[int(b)] for b in wl.tables_h[s, :nb]]
     q = W.to_numpy_storage(wl.q_h[seqs], wl.dtype)
     lens = wl.lens_h[seqs]
-    return dict(q=q, kp=kp, vp=vp, tab=tab, lens=lens, seqs=len(seqs),
-                bytes=int(lens.astype(np.int64).sum()) * wl.hkv * wl.d * 2 * 2)
+    row_bytes = wl.d + 4 if wl.kv == "int8" else wl.d * 2
+    return dict(q=q, kp=kp, vp=vp, ks=ks, vs=vs, tab=tab, lens=lens, seqs=len(seqs),
+                bytes=int(lens.astype(np.int64).sum()) * wl.hkv * row_bytes * 2)
 
 
 # rough cost of the oracle per (token, KV head): two row gathers plus the fp64 math
@@ -302,17 +345,21 @@ def time_oracle(wl, sample, repeats):
     each run."""
     with tempfile.TemporaryDirectory() as td:
         path = os.path.join(td, "sample.npz")
-        np.savez(path, q=sample["q"], kp=sample["kp"], vp=sample["vp"], tab=sample["tab"],
-                 lens=sample["lens"])
+        np.savez(path, q=sample["q"], kp=sample["kp"], vp=sample["vp"], ks=sample["ks"], vs=sample["vs"],
+                 tab=sample["tab"], lens=sample["lens"])
+        if wl.kv == "int8":
+            names, call = "('q', 'kp', 'vp', 'ks', 'vs', 'tab', 'lens')", "OQ.paged_attention_decode_int8"
+        else:
+            names, call = "('q', 'kp', 'vp', 'tab', 'lens')", "OA.paged_attention_decode"
         code = ("import sys, time, numpy as np; sys.path.insert(0, %r)\n"
-                "import oracle.attention as OA\n"
+                "import oracle.attention as OA, oracle.quant as OQ\n"
                 "z = np.load(%r)\n"
-                "a = [z[k] for k in ('q', 'kp', 'vp', 'tab', 'lens')]\n"
+                "a = [z[k] for k in %s]\n"
                 "for _ in range(%d):\n"
                 "    t = time.perf_counter()\n"
-                "    OA.paged_attention_decode(*a, %r, %d, %r)\n"
+                "    %s(*a, %r, %d, %r)\n"
                 "    print(time.perf_counter() - t, flush=True)\n") % (
-                    ROOT, path, repeats, wl.scale, wl.hkv, wl.dtype)
+                    ROOT, path, names, repeats, call, wl.scale, wl.hkv, wl.dtype)
         env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
         res = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env,
                              timeout=3600)
@@ -357,7 +404,7 @@ def run_ours(args):
         dist.barrier()
     B.lib()
 
-    wl = build_workload(args.workload, args.seed, device)
+    wl = build_workload(args.workload, args.seed, device, args.kv)
     wl.partition = args.partition
     device_inputs(wl, device)
     # L2 eviction buffer: read (not written) between timed steps, so the next
@@ -385,10 +432,9 @@ def run_ours(args):
         flush_sum = flush.sum()                                  # evict L2 with clean lines between steps
         e_start, e_mid, e_end = ev[k]
         e_start.record(stream)
-        B.reshape_and_cache(wl.knew, wl.vnew, wl.k_pool, wl.v_pool, wl.slots)
+        cache_write(wl, B)
         e_mid.record(stream)
-        B.paged_attention_decode(wl.out, wl.q, wl.k_pool, wl.v_pool, wl.tables, wl.lens, wl.scale,
-                                 partition_size=wl.partition)
+        decode(wl, B)
         e_end.record(stream)
     torch.cuda.synchronize()
     if world > 1:
@@ -430,7 +476,7 @@ def run_ours(args):
     value = whole_job_gbs(wl.kv_bytes, per_step_ms, world)
     dec_ms = statistics.mean(decode_ms)
     achieved = wl.kv_bytes / (dec_ms * 1e-3) / 1e9
-    traffic = recorded_traffic(args.workload)
+    traffic = recorded_traffic(args.workload if args.kv == "native" else f"{args.workload}-{args.kv}")
     line = {
         "metric": METRIC,
         "value": round(value, 1),
@@ -442,10 +488,13 @@ def run_ours(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": wl.dtype,
-        "data": "synthetic (seeded N(0,1) K/V/q; shapes and length distributions of the named layer)",
+        "dtype": wl.dtype if wl.kv == "native" else "int8",
+        "data": "synthetic (seeded N(0,1) K/V/q; shapes and length distributions of the named layer)"
+                + ("; INT8 cache: uniform codes in [-127, 127], fp32 row scales U[0.01, 0.03]"
+                   if wl.kv == "int8" else ""),
         "config": {
-            "workload": wl.description,
+            "workload": wl.description + (" (INT8 KV cache)" if wl.kv == "int8" else ""),
+            "kv_cache": "int8 codes + fp32 row scales, fp32 math" if wl.kv == "int8" else f"{wl.dtype}",
             "num_seqs": wl.num_seqs,
             "kv_bytes_per_step": wl.kv_bytes,
             "schedule": ("balanced persistent (equal tiles per warp)" if part == B.BALANCED else
@@ -461,7 +510,8 @@ def run_ours(args):
         },
         "roofline": {
             "bound": "hbm",
-            "kernel": "paged_decode_kernel (+ its LSE merge when split)",
+            "kernel": ("paged_decode_kernel<KvInt8>" if wl.kv == "int8" else "paged_decode_kernel") +
+                      " (+ its LSE merge when split)",
             "achieved": round(achieved, 1),
             "peak": peak,
             "peak_kind": f"{peak_kind} (copy bandwidth, burst)",
@@ -499,7 +549,7 @@ def run_reference(args):
         return
     import torch
     device = "cuda" if torch.cuda.is_available() else "cpu"
-    wl = build_workload(args.workload, args.seed, device)
+    wl = build_workload(args.workload, args.seed, device, args.kv)
     total = args.steps + args.warmup
     budget = min(6.0, max(0.02, args.reference_budget / total))
     sample = oracle_sample(wl, budget)
@@ -519,6 +569,7 @@ def run_reference(args):
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "f64",
+        "kv_cache": "int8 codes + fp32 row scales" if wl.kv == "int8" else wl.dtype,
         "data": "synthetic (seeded N(0,1) K/V/q; shapes and length distributions of the named layer)",
         "config": {"workload": wl.description, "num_seqs": wl.num_seqs, "kv_bytes_per_step": wl.kv_bytes,
                    "sample_kv_bytes_per_step": sample["bytes"]},
@@ -539,6 +590,8 @@ def main(argv=None):
     ap.add_argument("--workload", default="llama13b",
                     choices=["llama13b", "llama3_8b", "opt66b_sampling", "opt175b_long", "tiny"])
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--kv", choices=["native", "int8"], default="native",
+                    help="KV cache storage: native (the workload's fp16/bf16) or int8 codes with row scales")
     ap.add_argument("--partition", type=int, default=0,
                     help="decode schedule: 0 = library choice, -1 = one CTA per (sequence, KV head), "
                          "N = split-K partitions of N tokens")

@@ -251,6 +251,62 @@ pkv_status_t pkv_check_copy_pairs(const int64_t* src_dst_pairs_host, int num_pai
                                   int num_blocks);
 
 /* ------------------------------------------------------------------------ */
+/* INT8 KV cache ([G] "他のKVキャッシュ最適化との組み合わせ": INT8             */
+/* quantisation of the KV cache combines with paging, halving each block)    */
+/* ------------------------------------------------------------------------ */
+/*
+ * The page names INT8 KV quantisation but gives no scheme; this library
+ * takes the symmetric per-row reading: every stored row (block, KV head,
+ * slot) of K and of V holds int8 codes and one fp32 scale,
+ *   s = max_i |x_i| / 127,  c_i = rint(x_i / s)  (ties to even),
+ * both computed in IEEE fp32 from the fp32 value of the 16-bit input, so
+ * x_i ~= c_i * s with |x_i - c_i * s| <= s / 2. A row of zeros has s = 0 and
+ * codes 0. Layouts:
+ *   k_cache, v_cache : int8[num_blocks][num_kv_heads][16][head_dim]
+ *   k_scale, v_scale : fp32[num_blocks][num_kv_heads][16]
+ * head_dim is 64, 128 or 256. All four arrays must be 16-byte aligned.
+ */
+
+/*
+ * Quantising cache write: for each t with slot = slot_mapping[t] >= 0 and
+ * every KV head g, row k[t][g][:] (T = dtype) is quantised as above into
+ * k_cache[slot/16][g][slot%16][:] and k_scale[slot/16][g][slot%16] (v
+ * likewise). Slots >= num_blocks*16 are skipped and flagged
+ * (PKV_DEV_BAD_SLOT). Codes and scales are bit-exact to the definition.
+ */
+pkv_status_t pkv_reshape_and_cache_int8(
+    const void* k, const void* v, pkv_dtype_t dtype, int8_t* k_cache,
+    int8_t* v_cache, float* k_scale, float* v_scale, const int64_t* slot_mapping,
+    int num_tokens, int num_kv_heads, int head_dim, int num_blocks,
+    pkv_stream_t stream);
+
+/*
+ * Decode over the INT8 cache: pkv_paged_attention_decode with every K row
+ * read as c_K * s_K and every V row as c_V * s_V. q and out are T = dtype.
+ * Same block tables, lengths, GQA rule, partition_size values (except -2,
+ * the balanced schedule, which returns PKV_ERR_UNSUPPORTED), workspace
+ * (pkv_paged_attention_workspace_size with the same arguments) and error
+ * behaviour. Internally the scores are q . c_K scaled by s_K, and s_V is
+ * folded into each softmax weight.
+ */
+pkv_status_t pkv_paged_attention_decode_int8(
+    void* out, const void* q, const int8_t* k_cache, const int8_t* v_cache,
+    const float* k_scale, const float* v_scale, const int32_t* block_tables,
+    const int32_t* context_lens, int num_seqs, int num_q_heads, int num_kv_heads,
+    int head_dim, int max_blocks_per_seq, int num_blocks, float scale,
+    pkv_dtype_t dtype, int partition_size, void* workspace,
+    size_t workspace_bytes, pkv_stream_t stream);
+
+/*
+ * Copy-on-write block copies of an INT8 cache: like pkv_copy_blocks, block
+ * src of the codes and of the scales (K and V) is copied to block dst.
+ */
+pkv_status_t pkv_copy_blocks_int8(
+    int8_t* k_cache, int8_t* v_cache, float* k_scale, float* v_scale,
+    const int64_t* src_dst_pairs, int num_pairs, int num_kv_heads, int head_dim,
+    int num_blocks, pkv_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
 /* Host block manager ([S] "KV キャッシュマネージャ", [B] "OSの知恵をGPUへ")  */
 /* ------------------------------------------------------------------------ */
 /*

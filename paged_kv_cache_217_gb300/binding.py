@@ -60,6 +60,10 @@ _SIGS = {
     "pkv_reshape_and_cache": ([_c_p] * 5 + [_c_int] * 5 + [_c_p], _c_int),
     "pkv_copy_blocks": ([_c_p] * 3 + [_c_int] * 5 + [_c_p], _c_int),
     "pkv_check_copy_pairs": ([_c_p, _c_int, _c_int], _c_int),
+    "pkv_reshape_and_cache_int8": ([_c_p, _c_p, _c_int] + [_c_p] * 5 + [_c_int] * 4 + [_c_p], _c_int),
+    "pkv_paged_attention_decode_int8": ([_c_p] * 8 + [_c_int] * 6 + [_c_f, _c_int, _c_int, _c_p, _c_sz, _c_p],
+                                        _c_int),
+    "pkv_copy_blocks_int8": ([_c_p] * 5 + [_c_int] * 4 + [_c_p], _c_int),
     "pkv_selftest_bounded_wait": ([ctypes.c_uint32, _c_p], _c_int),
     "pkv_bm_create": ([_c_int, _c_int, _c_p, ctypes.POINTER(_c_p)], _c_int),
     "pkv_bm_destroy": ([_c_p], None),
@@ -262,6 +266,81 @@ def copy_blocks(k_pool, v_pool, src_dst_pairs):
     _check(lib().pkv_copy_blocks(k_pool.data_ptr(), v_pool.data_ptr(), src_dst_pairs.data_ptr(),
                                  src_dst_pairs.shape[0], hkv, D, nb, dt, _stream_ptr(k_pool.device)),
            "copy_blocks")
+
+
+# ---------------------------------------------------------------------------
+# INT8 KV cache: int8 codes [num_blocks, Hkv, 16, D], fp32 scales [num_blocks, Hkv, 16]
+# ---------------------------------------------------------------------------
+def _check_int8_cache(k_cache, v_cache, k_scale, v_scale):
+    import torch
+    if k_cache.dtype != torch.int8 or v_cache.dtype != torch.int8:
+        raise TypeError("k_cache and v_cache must be int8")
+    if k_scale.dtype != torch.float32 or v_scale.dtype != torch.float32:
+        raise TypeError("k_scale and v_scale must be float32")
+    if k_cache.dim() != 4 or k_cache.shape[2] != BLOCK_SIZE or v_cache.shape != k_cache.shape \
+            or tuple(k_scale.shape) != tuple(k_cache.shape[:3]) or v_scale.shape != k_scale.shape:
+        raise ValueError("caches must be [num_blocks, Hkv, 16, D] and scales [num_blocks, Hkv, 16]")
+
+
+def reshape_and_cache_int8(k, v, k_cache, v_cache, k_scale, v_scale, slot_mapping):
+    """Quantise each new K/V row (s = max|x|/127, c = rint(x/s)) into its slot of the INT8 cache."""
+    import torch
+    _need_cuda(k, v, k_cache, v_cache, k_scale, v_scale, slot_mapping)
+    dt = _dtype_code(k)
+    _check_int8_cache(k_cache, v_cache, k_scale, v_scale)
+    if slot_mapping.dtype != torch.int64:
+        raise TypeError("slot_mapping must be int64")
+    T, hkv, D = k.shape
+    if v.shape != k.shape or v.dtype != k.dtype or k_cache.shape[1:] != (hkv, BLOCK_SIZE, D) \
+            or tuple(slot_mapping.shape) != (T,):
+        raise ValueError("k, v: [T, Hkv, D]; caches: [num_blocks, Hkv, 16, D]; slot_mapping: [T]")
+    _check(lib().pkv_reshape_and_cache_int8(
+        k.data_ptr(), v.data_ptr(), dt, k_cache.data_ptr(), v_cache.data_ptr(), k_scale.data_ptr(),
+        v_scale.data_ptr(), slot_mapping.data_ptr(), T, hkv, D, k_cache.shape[0], _stream_ptr(k.device)),
+        "reshape_and_cache_int8")
+
+
+def paged_attention_decode_int8(out, q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens, scale,
+                                partition_size=0, workspace=None):
+    """paged_attention_decode over the INT8 cache (K = c_K * s_K, V = c_V * s_V per row)."""
+    import torch
+    _need_cuda(out, q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens)
+    dt = _dtype_code(q)
+    _check_int8_cache(k_cache, v_cache, k_scale, v_scale)
+    if out.dtype != q.dtype:
+        raise TypeError("q and out must share one dtype")
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise TypeError("block_tables and context_lens must be int32")
+    S, Hq, D = q.shape
+    nb, hkv = k_cache.shape[0], k_cache.shape[1]
+    if k_cache.shape[3] != D or tuple(out.shape) != (S, Hq, D) or block_tables.dim() != 2 \
+            or block_tables.shape[0] != S or tuple(context_lens.shape) != (S,):
+        raise ValueError("shape mismatch among out, q, caches, block_tables and context_lens")
+    mb = block_tables.shape[1]
+    need = workspace_size(S, Hq, hkv, D, mb, partition_size)
+    ws_ptr, ws_bytes = None, 0
+    if need:
+        ws = workspace if workspace is not None else _workspace(q.device, need)
+        ws_ptr, ws_bytes = ws.data_ptr(), ws.numel() * ws.element_size()
+    _check(lib().pkv_paged_attention_decode_int8(
+        out.data_ptr(), q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), k_scale.data_ptr(),
+        v_scale.data_ptr(), block_tables.data_ptr(), context_lens.data_ptr(), S, Hq, hkv, D, mb, nb,
+        float(scale), dt, int(partition_size), ws_ptr, ws_bytes, _stream_ptr(q.device)),
+        "paged_attention_decode_int8")
+    return out
+
+
+def copy_blocks_int8(k_cache, v_cache, k_scale, v_scale, src_dst_pairs):
+    """copy_blocks for the INT8 cache: codes and scales of block src go to block dst."""
+    import torch
+    _need_cuda(k_cache, v_cache, k_scale, v_scale, src_dst_pairs)
+    _check_int8_cache(k_cache, v_cache, k_scale, v_scale)
+    if src_dst_pairs.dtype != torch.int64 or src_dst_pairs.dim() != 2 or src_dst_pairs.shape[1] != 2:
+        raise ValueError("src_dst_pairs must be int64 [n, 2]")
+    nb, hkv, _, D = k_cache.shape
+    _check(lib().pkv_copy_blocks_int8(k_cache.data_ptr(), v_cache.data_ptr(), k_scale.data_ptr(),
+                                      v_scale.data_ptr(), src_dst_pairs.data_ptr(), src_dst_pairs.shape[0],
+                                      hkv, D, nb, _stream_ptr(k_cache.device)), "copy_blocks_int8")
 
 
 def check_copy_pairs(pairs, num_blocks):

@@ -27,6 +27,7 @@ SOURCES = [
     "decode_noalloc.cu",
     "decode_f16.cu",
     "decode_bf16.cu",
+    "decode_int8.cu",
     "cache_ops.cu",
     "block_manager.cpp",
     "status.cpp",

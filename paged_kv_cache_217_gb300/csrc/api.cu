@@ -327,7 +327,7 @@ pkv_status_t pkv_paged_attention_decode(void* out, const void* q, const void* k_
     return cuda_status(err, "paged_attention_decode launch");
   }
 
-  pkv::DecodeArgs a;
+  pkv::DecodeArgs a{};
   a.out = out;
   a.q = q;
   a.k_pool = k_pool;
@@ -363,6 +363,132 @@ pkv_status_t pkv_paged_attention_decode(void* out, const void* q, const void* k_
   err = dtype == PKV_F16 ? pkv::launch_decode_f16(a, head_dim, gpad, &kmap, &vmap, stream)
                          : pkv::launch_decode_bf16(a, head_dim, gpad, &kmap, &vmap, stream);
   return cuda_status(err, "paged_attention_decode launch");
+}
+
+pkv_status_t pkv_paged_attention_decode_int8(void* out, const void* q, const int8_t* k_cache,
+                                             const int8_t* v_cache, const float* k_scale, const float* v_scale,
+                                             const int32_t* block_tables, const int32_t* context_lens,
+                                             int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                             int max_blocks_per_seq, int num_blocks, float scale,
+                                             pkv_dtype_t dtype, int partition_size, void* workspace,
+                                             size_t workspace_bytes, pkv_stream_t stream) {
+  if (num_seqs < 0) return pkv::fail(PKV_ERR_INVALID_ARG, "num_seqs < 0");
+  if (num_seqs == 0) return pkv::ok();
+  if (num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0)
+    return pkv::fail(PKV_ERR_INVALID_ARG, "num_q_heads (%d) must be a positive multiple of num_kv_heads (%d)",
+                     num_q_heads, num_kv_heads);
+  const int group = num_q_heads / num_kv_heads;
+  if (group > 8) return pkv::fail(PKV_ERR_UNSUPPORTED, "query heads per KV head %d > 8", group);
+  if (!supported_head_dim(head_dim)) return pkv::fail(PKV_ERR_UNSUPPORTED, "head_dim %d (64, 128 or 256)", head_dim);
+  if (dtype != PKV_F16 && dtype != PKV_BF16) return pkv::fail(PKV_ERR_UNSUPPORTED, "dtype %d", int(dtype));
+  if (max_blocks_per_seq <= 0 || num_blocks <= 0)
+    return pkv::fail(PKV_ERR_INVALID_ARG, "max_blocks_per_seq and num_blocks must be > 0");
+  if (num_seqs > 65535) return pkv::fail(PKV_ERR_UNSUPPORTED, "num_seqs %d > 65535", num_seqs);
+  if (!std::isfinite(scale)) return pkv::fail(PKV_ERR_INVALID_ARG, "scale is not finite");
+  if (!out || !q || !k_cache || !v_cache || !k_scale || !v_scale || !block_tables || !context_lens)
+    return pkv::fail(PKV_ERR_INVALID_ARG, "NULL tensor pointer");
+  if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      !aligned(k_scale, 16) || !aligned(v_scale, 16))
+    return pkv::fail(PKV_ERR_INVALID_ARG, "out, q, caches and scales must be 16-byte aligned");
+  if (!aligned(block_tables, 4) || !aligned(context_lens, 4))
+    return pkv::fail(PKV_ERR_INVALID_ARG, "block_tables and context_lens must be 4-byte aligned");
+  const int p = choose_partition(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, partition_size);
+  if (p == kBalanced) return pkv::fail(PKV_ERR_UNSUPPORTED, "the INT8 cache has no balanced schedule");
+  Plan plan;
+  pkv_status_t st = plan_decode(max_blocks_per_seq, p, &plan);
+  if (st != PKV_OK) return st;
+  if (int64_t(num_blocks) * num_kv_heads * PKV_BLOCK_SIZE > INT32_MAX)
+    return pkv::fail(PKV_ERR_UNSUPPORTED, "num_blocks * num_kv_heads * 16 exceeds 2^31 rows");
+  const SplitLayout lay = split_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, plan.max_parts);
+  const size_t need = lay.total;
+  if (need > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, 16)))
+    return pkv::fail(PKV_ERR_WORKSPACE, "workspace of %zu bytes (16-byte aligned) required, got %zu at %p",
+                     need, workspace_bytes, workspace);
+  unsigned int* status = nullptr;
+  st = status_word(&status);
+  if (st != PKV_OK) return st;
+
+  pkv::DecodeArgs a{};
+  a.out = out;
+  a.q = q;
+  a.k_pool = k_cache;
+  a.v_pool = v_cache;
+  a.k_scale = k_scale;
+  a.v_scale = v_scale;
+  a.block_tables = block_tables;
+  a.context_lens = context_lens;
+  a.part_o = need > 0 ? static_cast<float*>(workspace) : nullptr;
+  a.part_ml = need > 0 ? reinterpret_cast<float2*>(static_cast<char*>(workspace) + lay.ml_offset) : nullptr;
+  a.counters = need > 0 ? reinterpret_cast<unsigned int*>(static_cast<char*>(workspace) + lay.counter_offset)
+                        : nullptr;
+  a.status = status;
+  a.num_seqs = num_seqs;
+  a.num_q_heads = num_q_heads;
+  a.num_kv_heads = num_kv_heads;
+  a.group = group;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.num_blocks = num_blocks;
+  a.part_tokens = plan.part_tokens;
+  a.max_parts = plan.max_parts;
+  a.long_first = int64_t(num_seqs) * num_kv_heads * plan.max_parts <= kLongFirstMaxCtas ? 1 : 0;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  cudaError_t err = cudaSuccess;
+  if (need > 0) {
+    err = cudaMemsetAsync(a.counters, 0, lay.counter_bytes, stream);
+    if (err != cudaSuccess) return cuda_status(err, "clear split-K counters");
+  }
+  err = pkv::launch_decode_int8(a, dtype == PKV_BF16, head_dim, round_pow2_group(group), stream);
+  return cuda_status(err, "paged_attention_decode_int8 launch");
+}
+
+pkv_status_t pkv_reshape_and_cache_int8(const void* k, const void* v, pkv_dtype_t dtype, int8_t* k_cache,
+                                        int8_t* v_cache, float* k_scale, float* v_scale,
+                                        const int64_t* slot_mapping, int num_tokens, int num_kv_heads,
+                                        int head_dim, int num_blocks, pkv_stream_t stream) {
+  if (num_tokens < 0) return pkv::fail(PKV_ERR_INVALID_ARG, "num_tokens < 0");
+  if (num_tokens == 0) return pkv::ok();
+  if (num_kv_heads <= 0 || num_blocks <= 0) return pkv::fail(PKV_ERR_INVALID_ARG, "num_kv_heads and num_blocks must be > 0");
+  if (!supported_head_dim(head_dim)) return pkv::fail(PKV_ERR_UNSUPPORTED, "head_dim %d (64, 128 or 256)", head_dim);
+  if (dtype != PKV_F16 && dtype != PKV_BF16) return pkv::fail(PKV_ERR_UNSUPPORTED, "dtype %d", int(dtype));
+  if (!k || !v || !k_cache || !v_cache || !k_scale || !v_scale || !slot_mapping)
+    return pkv::fail(PKV_ERR_INVALID_ARG, "NULL pointer");
+  if (!aligned(k, 16) || !aligned(v, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      !aligned(k_scale, 16) || !aligned(v_scale, 16) || !aligned(slot_mapping, 8))
+    return pkv::fail(PKV_ERR_INVALID_ARG, "k, v, caches and scales must be 16-byte aligned, slot_mapping 8-byte aligned");
+  if (int64_t(num_tokens) * num_kv_heads > int64_t(UINT32_MAX) * 8)
+    return pkv::fail(PKV_ERR_UNSUPPORTED, "too many tokens for one launch");
+  unsigned int* status = nullptr;
+  pkv_status_t st = status_word(&status);
+  if (st != PKV_OK) return st;
+  return cuda_status(pkv::launch_reshape_and_cache_int8(k, v, dtype == PKV_BF16, k_cache, v_cache, k_scale, v_scale,
+                                                        slot_mapping, num_tokens, num_kv_heads, head_dim,
+                                                        num_blocks, status, stream),
+                     "reshape_and_cache_int8 launch");
+}
+
+pkv_status_t pkv_copy_blocks_int8(int8_t* k_cache, int8_t* v_cache, float* k_scale, float* v_scale,
+                                  const int64_t* src_dst_pairs, int num_pairs, int num_kv_heads, int head_dim,
+                                  int num_blocks, pkv_stream_t stream) {
+  if (num_pairs < 0) return pkv::fail(PKV_ERR_INVALID_ARG, "num_pairs < 0");
+  if (num_pairs == 0) return pkv::ok();
+  if (num_pairs > 65535) return pkv::fail(PKV_ERR_UNSUPPORTED, "num_pairs %d > 65535", num_pairs);
+  if (num_kv_heads <= 0 || num_blocks <= 0) return pkv::fail(PKV_ERR_INVALID_ARG, "num_kv_heads and num_blocks must be > 0");
+  if (!supported_head_dim(head_dim)) return pkv::fail(PKV_ERR_UNSUPPORTED, "head_dim %d (64, 128 or 256)", head_dim);
+  if (!k_cache || !v_cache || !k_scale || !v_scale || !src_dst_pairs) return pkv::fail(PKV_ERR_INVALID_ARG, "NULL pointer");
+  if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(k_scale, 16) || !aligned(v_scale, 16) ||
+      !aligned(src_dst_pairs, 8))
+    return pkv::fail(PKV_ERR_INVALID_ARG, "caches and scales must be 16-byte aligned, pairs 8-byte aligned");
+  unsigned int* status = nullptr;
+  pkv_status_t st = status_word(&status);
+  if (st != PKV_OK) return st;
+  cudaError_t err = pkv::launch_copy_blocks_bytes(k_cache, v_cache, src_dst_pairs, num_pairs,
+                                                  int64_t(num_kv_heads) * PKV_BLOCK_SIZE * head_dim, num_blocks,
+                                                  status, stream);
+  if (err != cudaSuccess) return cuda_status(err, "copy_blocks_int8 launch (codes)");
+  return cuda_status(pkv::launch_copy_blocks_bytes(k_scale, v_scale, src_dst_pairs, num_pairs,
+                                                   int64_t(num_kv_heads) * PKV_BLOCK_SIZE * 4, num_blocks, status,
+                                                   stream),
+                     "copy_blocks_int8 launch (scales)");
 }
 
 pkv_status_t pkv_reshape_and_cache(const void* k, const void* v, void* k_pool, void* v_pool,

@@ -1,4 +1,5 @@
-// reshape_and_cache and copy_blocks: bit copies with 16-byte vectors.
+// reshape_and_cache and copy_blocks: bit copies with 16-byte vectors; the
+// INT8 cache write, which quantises each row on its way into the pool.
 //
 // reshape_and_cache writes each decode step's new K/V row into its slot, the
 // "fill the last block" step of the KV cache manager (abeam.tech summary of
@@ -44,6 +45,101 @@ reshape_and_cache_kernel(const uint4* __restrict__ k, const uint4* __restrict__ 
   const int64_t dst = ((blk * num_kv_heads + gh) * kBlock + off) * vec_per_row + c;
   k_pool[dst] = __ldg(k + i);
   v_pool[dst] = __ldg(v + i);
+}
+
+// ---- INT8 cache write ---------------------------------------------------
+// One warp per (token, KV head) row of K and of V: each lane holds D/32
+// consecutive elements; the warp's max |x| gives the row scale
+// s = max|x| / 127 and the codes rint(x / s) (IEEE division, ties to even),
+// both decisions taken in fp32 exactly as the definition states.
+template <typename T>
+__device__ __forceinline__ float elem_to_float(T x);
+template <>
+__device__ __forceinline__ float elem_to_float<__half>(__half x) { return __half2float(x); }
+template <>
+__device__ __forceinline__ float elem_to_float<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <int BYTES>
+struct Chunk;  // a register chunk of BYTES bytes
+template <> struct Chunk<2> { using type = unsigned short; };
+template <> struct Chunk<4> { using type = uint32_t; };
+template <> struct Chunk<8> { using type = uint2; };
+template <> struct Chunk<16> { using type = uint4; };
+
+template <typename T, int D>
+__device__ __forceinline__ void quantize_row(const T* __restrict__ src, int8_t* __restrict__ codes,
+                                             float* __restrict__ scale, int lane) {
+  constexpr int E = D / 32;  // elements per lane
+  using In = typename Chunk<E * 2>::type;
+  using Out = typename Chunk<E>::type;
+  const In raw = __ldg(reinterpret_cast<const In*>(src) + lane);
+  const T* xs = reinterpret_cast<const T*>(&raw);
+  float x[E];
+  float m = 0.f;
+#pragma unroll
+  for (int i = 0; i < E; ++i) {
+    x[i] = elem_to_float(xs[i]);
+    m = fmaxf(m, fabsf(x[i]));
+  }
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
+  const float s = __fdiv_rn(m, 127.f);
+  Out packed;
+  unsigned char* pb = reinterpret_cast<unsigned char*>(&packed);
+#pragma unroll
+  for (int i = 0; i < E; ++i) {
+    int c = 0;
+    if (s > 0.f) c = min(127, max(-127, __float2int_rn(__fdiv_rn(x[i], s))));
+    pb[i] = static_cast<unsigned char>(c & 0xff);
+  }
+  reinterpret_cast<Out*>(codes)[lane] = packed;
+  if (lane == 0) *scale = s;
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(256)
+reshape_and_cache_int8_kernel(const T* __restrict__ k, const T* __restrict__ v, int8_t* __restrict__ k_codes,
+                              int8_t* __restrict__ v_codes, float* __restrict__ k_scale,
+                              float* __restrict__ v_scale, const int64_t* __restrict__ slots, int64_t rows,
+                              int num_kv_heads, int64_t num_slots, unsigned int* status) {
+  asm volatile("griddepcontrol.launch_dependents;");
+  const int64_t row = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;  // warp-uniform
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  const int gh = int(row % num_kv_heads);
+  const int64_t t = row / num_kv_heads;
+  const int64_t slot = __ldg(slots + t);
+  if (slot < 0) return;
+  if (slot >= num_slots) {
+    if (gh == 0 && lane == 0) flag(status, PKV_DEV_BAD_SLOT);
+    return;
+  }
+  const int64_t dst = ((slot / kBlock) * num_kv_heads + gh) * kBlock + slot % kBlock;  // pool row
+  quantize_row<T, D>(k + row * D, k_codes + dst * D, k_scale + dst, lane);
+  quantize_row<T, D>(v + row * D, v_codes + dst * D, v_scale + dst, lane);
+}
+
+template <typename T, int D>
+cudaError_t launch_int8_write(const void* k, const void* v, int8_t* kc, int8_t* vc, float* ks, float* vs,
+                              const int64_t* slots, int64_t rows, int num_kv_heads, int64_t num_slots,
+                              unsigned int* status, cudaStream_t stream) {
+  const int64_t nblk = (rows + 7) / 8;  // 8 warps (rows) per CTA
+  reshape_and_cache_int8_kernel<T, D><<<unsigned(nblk), 256, 0, stream>>>(
+      static_cast<const T*>(k), static_cast<const T*>(v), kc, vc, ks, vs, slots, rows, num_kv_heads, num_slots,
+      status);
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_int8_write_t(const void* k, const void* v, int8_t* kc, int8_t* vc, float* ks, float* vs,
+                                const int64_t* slots, int64_t rows, int num_kv_heads, int head_dim,
+                                int64_t num_slots, unsigned int* status, cudaStream_t stream) {
+  switch (head_dim) {
+    case 64: return launch_int8_write<T, 64>(k, v, kc, vc, ks, vs, slots, rows, num_kv_heads, num_slots, status, stream);
+    case 128: return launch_int8_write<T, 128>(k, v, kc, vc, ks, vs, slots, rows, num_kv_heads, num_slots, status, stream);
+    case 256: return launch_int8_write<T, 256>(k, v, kc, vc, ks, vs, slots, rows, num_kv_heads, num_slots, status, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 constexpr int kCopyThreads = 256;
@@ -123,11 +219,31 @@ cudaError_t launch_reshape_and_cache(const void* k, const void* v, void* k_pool,
   return cudaGetLastError();
 }
 
+cudaError_t launch_reshape_and_cache_int8(const void* k, const void* v, bool bf16, int8_t* k_codes,
+                                          int8_t* v_codes, float* k_scale, float* v_scale, const int64_t* slots,
+                                          int num_tokens, int num_kv_heads, int head_dim, int num_blocks,
+                                          unsigned int* status, cudaStream_t stream) {
+  const int64_t rows = int64_t(num_tokens) * num_kv_heads;
+  if (rows == 0) return cudaSuccess;
+  const int64_t num_slots = int64_t(num_blocks) * kBlock;
+  return bf16 ? launch_int8_write_t<__nv_bfloat16>(k, v, k_codes, v_codes, k_scale, v_scale, slots, rows,
+                                                   num_kv_heads, head_dim, num_slots, status, stream)
+              : launch_int8_write_t<__half>(k, v, k_codes, v_codes, k_scale, v_scale, slots, rows, num_kv_heads,
+                                            head_dim, num_slots, status, stream);
+}
+
 cudaError_t launch_copy_blocks(void* k_pool, void* v_pool, const int64_t* pairs, int num_pairs,
                                int num_kv_heads, int head_dim, int num_blocks,
                                unsigned int* status, cudaStream_t stream) {
+  return launch_copy_blocks_bytes(k_pool, v_pool, pairs, num_pairs, int64_t(num_kv_heads) * kBlock * head_dim * 2,
+                                  num_blocks, status, stream);
+}
+
+cudaError_t launch_copy_blocks_bytes(void* k_pool, void* v_pool, const int64_t* pairs, int num_pairs,
+                                     int64_t bytes_per_block, int num_blocks, unsigned int* status,
+                                     cudaStream_t stream) {
   if (num_pairs == 0) return cudaSuccess;
-  const int64_t vec_per_block = int64_t(num_kv_heads) * kBlock * head_dim / 8;
+  const int64_t vec_per_block = bytes_per_block / 16;
   const int64_t per_cta = int64_t(kCopyThreads) * kCopyVecPerThread;
   const dim3 grid(unsigned((vec_per_block + per_cta - 1) / per_cta), unsigned(num_pairs));
   copy_blocks_kernel<<<grid, kCopyThreads, 0, stream>>>(static_cast<uint4*>(k_pool),

@@ -49,6 +49,8 @@ struct DecodeArgs {
   const void* v_pool;
   const int32_t* block_tables;
   const int32_t* context_lens;
+  const float* k_scale; // INT8 cache: per-row scales [num_blocks][Hkv][16] (else unused)
+  const float* v_scale;
   float* part_o;        // split-K: [S][Hq][max_parts][D] unnormalised sums
   float2* part_ml;      // split-K: [S][Hq][max_parts] (max, sum), log2 domain
   unsigned int* counters; // split-K: [S][Hkv] partitions finished; zero between calls
@@ -166,14 +168,33 @@ __device__ __forceinline__ int long_first_seq(const DecodeArgs& a, int rank) {
   return picked;
 }
 
-template <typename T, int D, int G, int NW, int STAGES>
+// Storage formats of the KV pools for the CUDA-core tile math: eight
+// elements per lane per row, loaded from shared memory as floats.
+template <typename T>
+struct KvHalf {  // fp16 / bf16 elements
+  static constexpr int ELEM = 2;
+  static constexpr bool SCALED = false;
+  static __device__ __forceinline__ void load8(uint32_t addr, float (&f)[8]) {
+    Vec8<T>::to_float(lds128(addr), f);
+  }
+};
+
+struct KvInt8 {  // int8 codes, one fp32 scale per row (16 per tile, after the codes)
+  static constexpr int ELEM = 1;
+  static constexpr bool SCALED = true;
+  static __device__ __forceinline__ void load8(uint32_t addr, float (&f)[8]) { int8x8_to_float(lds64(addr), f); }
+};
+
+template <typename T, int D, int G, int NW, int STAGES, typename KV = KvHalf<T>>
 struct DecodeCfg {
   static constexpr int LPR = D / 8;                  // lanes per row
   static constexpr int RPP = 32 / LPR;               // rows per pass
   static constexpr int NPASS = kBlock / RPP;         // passes per tile
-  static constexpr int ROW_BYTES = D * int(sizeof(T));
+  static constexpr int ROW_BYTES = D * KV::ELEM;
   static constexpr int TILE_BYTES = kBlock * ROW_BYTES;
-  static constexpr int STAGE_BYTES = 2 * TILE_BYTES; // K tile then V tile
+  static constexpr int SCALE_BYTES = KV::SCALED ? kBlock * 4 : 0;
+  // K tile, V tile, then (INT8) the 16 K scales and the 16 V scales
+  static constexpr int STAGE_BYTES = 2 * TILE_BYTES + 2 * SCALE_BYTES;
   static constexpr int V = NPASS * G;                // scores per lane before the reduction
   static constexpr int LOGV = ilog2(V);
   static constexpr int LOGL = ilog2(LPR);
@@ -215,11 +236,12 @@ struct RowReduceScatter {
 
 // One 16-row tile: scores, online-softmax update, weighted V accumulation.
 // MASK: the tile holds only `rows` valid rows (the rest of the stage is stale).
-template <typename T, int D, int G, int NW, int STAGES, bool MASK>
+template <typename T, int D, int G, int NW, int STAGES, bool MASK, typename KV = KvHalf<T>>
 __device__ __forceinline__ void decode_tile(uint32_t kt, uint32_t vt, int rows,
                                             const float (&qf)[G][8], float (&acc)[G][8],
-                                            float (&lsum)[G], float (&mrun)[G], int lane) {
-  using C = DecodeCfg<T, D, G, NW, STAGES>;
+                                            float (&lsum)[G], float (&mrun)[G], int lane,
+                                            uint32_t ksc = 0, uint32_t vsc = 0) {
+  using C = DecodeCfg<T, D, G, NW, STAGES, KV>;
   constexpr int LPR = C::LPR, RPP = C::RPP, NPASS = C::NPASS, NF = C::NF;
   const int sub = lane & (LPR - 1);
   const int r = lane / LPR;
@@ -228,9 +250,8 @@ __device__ __forceinline__ void decode_tile(uint32_t kt, uint32_t vt, int rows,
   float sc[C::V];
 #pragma unroll
   for (int i = 0; i < NPASS; ++i) {
-    const uint4 u = lds128(kt + (i * RPP + r) * C::ROW_BYTES + sub * 16);
     float kf[8];
-    Vec8<T>::to_float(u, kf);
+    KV::load8(kt + (i * RPP + r) * C::ROW_BYTES + sub * 8 * KV::ELEM, kf);
 #pragma unroll
     for (int h = 0; h < G; ++h) {
       float d0 = qf[h][0] * kf[0];
@@ -259,6 +280,7 @@ __device__ __forceinline__ void decode_tile(uint32_t kt, uint32_t vt, int rows,
   float mloc = -INFINITY;
 #pragma unroll
   for (int e = 0; e < NF; ++e) {
+    if constexpr (KV::SCALED) sc[e] *= lds_f32(ksc + ((i0 + e) * RPP + r) * 4);  // dequantise K
     if (MASK && (i0 + e) * RPP + r >= rows) sc[e] = -INFINITY;
     mloc = fmaxf(mloc, sc[e]);
   }
@@ -293,16 +315,24 @@ __device__ __forceinline__ void decode_tile(uint32_t kt, uint32_t vt, int rows,
 #pragma unroll
   for (int i = 0; i < NPASS; ++i) {
     const int row = i * RPP + r;
-    uint4 u = lds128(vt + row * C::ROW_BYTES + sub * 16);
-    if (MASK && row >= rows) u = make_uint4(0u, 0u, 0u, 0u);
     float vf[8];
-    Vec8<T>::to_float(u, vf);
+    KV::load8(vt + row * C::ROW_BYTES + sub * 8 * KV::ELEM, vf);
+    // rows past the tile's valid ones hold stale data: their weight is 0 and
+    // their values must not reach the sums (0 * NaN)
+    const bool live = !MASK || row < rows;
+    if (MASK && !live) {
+#pragma unroll
+      for (int c = 0; c < 8; ++c) vf[c] = 0.f;
+    }
+    float vscale = 1.f;
+    if constexpr (KV::SCALED) vscale = live ? lds_f32(vsc + row * 4) : 0.f;  // dequantise V via the weight
 #pragma unroll
     for (int h = 0; h < G; ++h) {
       const int v = h * NPASS + i;
       const int src = r * LPR + ((v >> (C::LOGV - C::NH)) << (C::LOGL - C::NH));
-      const float pp = __shfl_sync(kFull, p[v & (NF - 1)], src);
-      lsum[h] += pp;
+      const float p_raw = __shfl_sync(kFull, p[v & (NF - 1)], src);
+      lsum[h] += p_raw;
+      const float pp = KV::SCALED ? p_raw * vscale : p_raw;
       if constexpr (kPackedFma) {
 #pragma unroll
         for (int c = 0; c < 8; c += 2) ffma2(acc[h][c], acc[h][c + 1], pp, pp, vf[c], vf[c + 1], acc[h][c], acc[h][c + 1]);
@@ -411,10 +441,10 @@ __device__ __forceinline__ void finish_chunk(const DecodeArgs& a, const unsigned
   if (threadIdx.x == 0) *counter = 0u;  // leave the workspace ready for the next call
 }
 
-template <typename T, int D, int G, int NW, int STAGES>
+template <typename T, int D, int G, int NW, int STAGES, typename KV = KvHalf<T>>
 __global__ void __launch_bounds__(NW * 32)
 paged_decode_kernel(const DecodeArgs a) {
-  using C = DecodeCfg<T, D, G, NW, STAGES>;
+  using C = DecodeCfg<T, D, G, NW, STAGES, KV>;
   constexpr int LPR = C::LPR;
   extern __shared__ __align__(1024) unsigned char smem[];
 
@@ -506,6 +536,9 @@ paged_decode_kernel(const DecodeArgs a) {
   const char* kbase = static_cast<const char*>(a.k_pool) + size_t(g) * C::TILE_BYTES;
   const char* vbase = static_cast<const char*>(a.v_pool) + size_t(g) * C::TILE_BYTES;
   const size_t blk_stride = size_t(a.num_kv_heads) * C::TILE_BYTES;
+  // INT8: the 16 scales of tile (block, g) are 64 contiguous bytes
+  const float* kscale_base = KV::SCALED ? a.k_scale + size_t(g) * kBlock : nullptr;
+  const float* vscale_base = KV::SCALED ? a.v_scale + size_t(g) * kBlock : nullptr;
 
   auto issue = [&](int k) {  // warp-uniform; k increases by one per call
     if ((k >> 5) != id_batch) {
@@ -521,9 +554,14 @@ paged_decode_kernel(const DecodeArgs a) {
       const int st = k % STAGES;
       const uint32_t bar = bar_s + 8 * st;
       const uint32_t dst = ring_s + st * C::STAGE_BYTES;
-      mbar_arrive_expect_tx(bar, 2 * bytes);
+      mbar_arrive_expect_tx(bar, 2 * bytes + 2 * C::SCALE_BYTES);
       bulk_g2s(dst, kbase + size_t(id) * blk_stride, bytes, bar);
       bulk_g2s(dst + C::TILE_BYTES, vbase + size_t(id) * blk_stride, bytes, bar);
+      if constexpr (KV::SCALED) {
+        const size_t so = size_t(id) * a.num_kv_heads * kBlock;
+        bulk_g2s(dst + 2 * C::TILE_BYTES, kscale_base + so, C::SCALE_BYTES, bar);
+        bulk_g2s(dst + 2 * C::TILE_BYTES + C::SCALE_BYTES, vscale_base + so, C::SCALE_BYTES, bar);
+      }
     }
   };
 
@@ -554,10 +592,11 @@ paged_decode_kernel(const DecodeArgs a) {
     const int j = warp + k * NW;
     const int rows = min(kBlock, ntok - j * kBlock);
     const uint32_t kt = ring_s + st * C::STAGE_BYTES;
+    const uint32_t ks = kt + 2 * C::TILE_BYTES, vs = ks + C::SCALE_BYTES;
     if (rows == kBlock)
-      decode_tile<T, D, G, NW, STAGES, false>(kt, kt + C::TILE_BYTES, rows, qf, acc, lsum, mrun, lane);
+      decode_tile<T, D, G, NW, STAGES, false, KV>(kt, kt + C::TILE_BYTES, rows, qf, acc, lsum, mrun, lane, ks, vs);
     else
-      decode_tile<T, D, G, NW, STAGES, true>(kt, kt + C::TILE_BYTES, rows, qf, acc, lsum, mrun, lane);
+      decode_tile<T, D, G, NW, STAGES, true, KV>(kt, kt + C::TILE_BYTES, rows, qf, acc, lsum, mrun, lane, ks, vs);
     __syncwarp();
     if (k + STAGES < n_my) issue(k + STAGES);
   }

@@ -91,6 +91,12 @@ struct Mma<__half> {
   }
 };
 
+// Measurement knob: feed P to the PV product as one rounded term only.
+#ifndef PKV_PV_HI_ONLY
+#define PKV_PV_HI_ONLY 0
+#endif
+constexpr bool kPvHiOnly = PKV_PV_HI_ONLY != 0;
+
 // Split the QK accumulation of each 8-token half into two chains.
 #ifndef PKV_SPLIT_QK
 #define PKV_SPLIT_QK 0
@@ -192,9 +198,9 @@ __device__ __forceinline__ void mma_tile(uint32_t kt, uint32_t vt, int rows, con
       uint32_t b[4];
       ldsm_x4_trans(vt + swz(tok, 2 * c + (mi >> 1)), b);
       Mma<T>::run(o[2 * c], hi01, 0u, hi23, 0u, b[0], b[1]);
-      Mma<T>::run(o[2 * c], lo01, 0u, lo23, 0u, b[0], b[1]);
+      if (!kPvHiOnly) Mma<T>::run(o[2 * c], lo01, 0u, lo23, 0u, b[0], b[1]);
       Mma<T>::run(o[2 * c + 1], hi01, 0u, hi23, 0u, b[2], b[3]);
-      Mma<T>::run(o[2 * c + 1], lo01, 0u, lo23, 0u, b[2], b[3]);
+      if (!kPvHiOnly) Mma<T>::run(o[2 * c + 1], lo01, 0u, lo23, 0u, b[2], b[3]);
     }
   }
 }

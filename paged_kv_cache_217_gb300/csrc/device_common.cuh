@@ -86,6 +86,32 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   return v;
 }
 
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ float lds_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+  return v;
+}
+
+// Eight signed bytes -> eight floats, exactly. Each byte b is biased to
+// b + 128 (xor 0x80) and placed in the low mantissa byte of 2^23
+// (0x4B000000), which is the float 2^23 + b + 128; subtracting 2^23 + 128
+// leaves b.
+__device__ __forceinline__ void int8x8_to_float(const uint2& u, float (&f)[8]) {
+  const uint32_t w[2] = {u.x ^ 0x80808080u, u.y ^ 0x80808080u};
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+#pragma unroll
+    for (int b = 0; b < 4; ++b)
+      f[4 * i + b] = __uint_as_float(__byte_perm(w[i], 0x4B000000u, 0x7440u + b)) - 8388736.f;
+  }
+}
+
 // 2^x on the SFU (PTX ex2.approx; +0 for x = -inf).
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;

@@ -42,5 +42,17 @@ cudaError_t launch_reshape_and_cache(const void* k, const void* v, void* k_pool,
 cudaError_t launch_copy_blocks(void* k_pool, void* v_pool, const int64_t* pairs, int num_pairs,
                                int num_kv_heads, int head_dim, int num_blocks,
                                unsigned int* status, cudaStream_t stream);
+// Block copy of two pools whose blocks are bytes_per_block bytes (a multiple of 16).
+cudaError_t launch_copy_blocks_bytes(void* k_pool, void* v_pool, const int64_t* pairs, int num_pairs,
+                                     int64_t bytes_per_block, int num_blocks, unsigned int* status,
+                                     cudaStream_t stream);
+
+// INT8 KV cache: quantising cache write (head_dim 64, 128 or 256) and decode
+// over int8 codes with per-row fp32 scales (CUDA-core kernel, every gpad).
+cudaError_t launch_reshape_and_cache_int8(const void* k, const void* v, bool bf16, int8_t* k_codes,
+                                          int8_t* v_codes, float* k_scale, float* v_scale, const int64_t* slots,
+                                          int num_tokens, int num_kv_heads, int head_dim, int num_blocks,
+                                          unsigned int* status, cudaStream_t stream);
+cudaError_t launch_decode_int8(const DecodeArgs& a, bool bf16, int head_dim, int gpad, cudaStream_t stream);
 
 }  // namespace pkv

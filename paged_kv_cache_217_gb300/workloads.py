@@ -179,6 +179,26 @@ def normal_values(shape, dtype, seed, device="cpu"):
     return x.to(tdt)
 
 
+def int8_codes(shape, seed, device="cpu"):
+    """A torch int8 tensor of codes drawn uniformly from [-127, 127] with a
+    seeded generator on ``device`` (the synthetic content of an INT8 cache)."""
+    import torch
+    gen = torch.Generator(device=device)
+    gen.manual_seed(int(seed))
+    return torch.randint(-127, 128, shape, generator=gen, dtype=torch.int8, device=device)
+
+
+def row_scales(shape, seed, device="cpu", lo=0.01, hi=0.03):
+    """A torch float32 tensor of per-row scales drawn uniformly from [lo, hi]
+    (about max|x| / 127 for rows of N(0, 1) values), seeded on ``device``."""
+    import torch
+    gen = torch.Generator(device=device)
+    gen.manual_seed(int(seed))
+    x = torch.empty(shape, dtype=torch.float32, device=device)
+    x.uniform_(lo, hi, generator=gen)
+    return x
+
+
 def to_numpy_storage(t, dtype):
     """Host NumPy view of a 16-bit tensor: float16 for fp16, uint16 bits for bf16."""
     import torch

@@ -1,0 +1,207 @@
+"""GPU parity of the INT8 KV cache (through the C ABI) against the oracle:
+quantising cache write and block copies bit-exact (codes and scales), decode
+over the INT8 cache within the attention tolerance."""
+
+import numpy as np
+import pytest
+import torch
+
+import helpers as H
+import oracle.cache_ops as OC
+import oracle.quant as OQ
+from paged_kv_cache_217_gb300 import binding as B
+from paged_kv_cache_217_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    H.ensure_built()
+    B.device_status(clear=True)
+    yield
+
+
+def _np(t):
+    return t.detach().cpu().contiguous().numpy()
+
+
+def _int8_cache(nb, hkv, d, seed, device="cuda"):
+    kc = W.int8_codes((nb, hkv, 16, d), seed * 5 + 1, device)
+    vc = W.int8_codes((nb, hkv, 16, d), seed * 5 + 2, device)
+    ks = W.row_scales((nb, hkv, 16), seed * 5 + 3, device)
+    vs = W.row_scales((nb, hkv, 16), seed * 5 + 4, device)
+    return kc, vc, ks, vs
+
+
+# ---- quantising cache write ---------------------------------------------------
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("hkv,d", [(4, 64), (8, 128), (2, 256), (40, 128)])
+def test_reshape_int8_bit_exact(dtype, hkv, d):
+    nb, T = 30, 101
+    rng = np.random.default_rng(hkv * 1000 + d)
+    slots = rng.choice(nb * 16, size=T, replace=False).astype(np.int64)
+    slots[::9] = -1                                        # skipped tokens
+    kc, vc, ks, vs = _int8_cache(nb, hkv, d, 3)
+    k = W.normal_values((T, hkv, d), dtype, 11, "cuda")
+    v = W.normal_values((T, hkv, d), dtype, 12, "cuda")
+    k[5] = 0                                               # all-zero rows: scale 0, codes 0
+    v[6, 1 % hkv] = 0
+    before = [_np(x) for x in (kc, vc, ks, vs)]
+    B.reshape_and_cache_int8(k, v, kc, vc, ks, vs, torch.from_numpy(slots).cuda())
+    torch.cuda.synchronize()
+    want = OQ.reshape_and_cache_int8(W.to_numpy_storage(k, dtype), W.to_numpy_storage(v, dtype), dtype,
+                                     *before, slots)
+    for got, exp, name in zip((kc, vc, ks, vs), want, ("k codes", "v codes", "k scales", "v scales")):
+        g = _np(got)
+        if g.dtype == np.float32:   # scales compared as bit patterns
+            g, exp = g.view(np.uint32), np.asarray(exp, np.float32).view(np.uint32)
+        assert np.array_equal(g, exp), f"{name} differ at {np.argwhere(g != exp)[:5].tolist()}"
+    assert B.device_status(clear=True) == 0
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_reshape_int8_ties_round_to_even(dtype):
+    # max |x| = 127 gives s = 1 exactly, so x / s = x: halves are ties
+    d, hkv = 64, 1
+    row = np.zeros(d, np.float32)
+    row[:8] = [127.0, 2.5, -3.5, 0.5, -0.5, 1.5, 126.5, -125.5]
+    k = torch.from_numpy(np.stack([row])[:, None, :]).to(H.torch_dtype(dtype)).cuda()
+    v = (-k).contiguous()
+    kc, vc, ks, vs = _int8_cache(2, hkv, d, 4)
+    B.reshape_and_cache_int8(k, v, kc, vc, ks, vs, torch.tensor([17], dtype=torch.int64, device="cuda"))
+    torch.cuda.synchronize()
+    assert float(ks[1, 0, 1]) == 1.0 and float(vs[1, 0, 1]) == 1.0
+    assert _np(kc[1, 0, 1, :8]).tolist() == [127, 2, -4, 0, 0, 2, 126, -126]
+    assert _np(vc[1, 0, 1, :8]).tolist() == [-127, -2, 4, 0, 0, -2, -126, 126]
+
+
+def test_reshape_int8_bad_slot_flagged():
+    d, hkv, nb = 128, 2, 4
+    kc, vc, ks, vs = _int8_cache(nb, hkv, d, 5)
+    before = [_np(x) for x in (kc, vc, ks, vs)]
+    k = W.normal_values((2, hkv, d), "bf16", 1, "cuda")
+    B.reshape_and_cache_int8(k, k.clone(), kc, vc, ks, vs,
+                             torch.tensor([nb * 16, nb * 16 + 5], dtype=torch.int64, device="cuda"))
+    torch.cuda.synchronize()
+    assert B.device_status(clear=True) & 0x4
+    for got, exp in zip((kc, vc, ks, vs), before):
+        assert np.array_equal(_np(got), exp)
+
+
+# ---- block copies ----------------------------------------------------------------
+def test_copy_blocks_int8_bit_exact():
+    nb, hkv, d = 24, 8, 128
+    kc, vc, ks, vs = _int8_cache(nb, hkv, d, 6)
+    pairs = np.array([[0, 5], [3, 7], [3, 9], [20, 1]], np.int64)
+    B.check_copy_pairs(pairs, nb)
+    before = [_np(x) for x in (kc, vc, ks, vs)]
+    B.copy_blocks_int8(kc, vc, ks, vs, torch.from_numpy(pairs).cuda())
+    torch.cuda.synchronize()
+    ekc, evc = OC.copy_blocks(before[0], before[1], pairs)
+    eks, evs = OC.copy_blocks(before[2], before[3], pairs)
+    for got, exp in zip((kc, vc, ks, vs), (ekc, evc, eks, evs)):
+        assert np.array_equal(_np(got), exp)
+    assert B.device_status(clear=True) == 0
+
+
+# ---- decode over the INT8 cache ---------------------------------------------------
+class Int8Case:
+    def __init__(self, lens, hq, hkv, d, dtype, seed, extra_cols=0):
+        lens = np.asarray(lens, np.int32)
+        nb = W.pool_size(lens, 1.2) + 1
+        tables, _ = W.scattered_tables(lens, nb, seed, extra_cols=extra_cols)
+        self.kc, self.vc, self.ks, self.vs = _int8_cache(nb, hkv, d, seed)
+        self.q = W.normal_values((len(lens), hq, d), dtype, seed * 5 + 7, "cuda")
+        self.tables = torch.from_numpy(tables).cuda()
+        self.lens = torch.from_numpy(lens).cuda()
+        self.scale = d ** -0.5
+        self.dtype, self.hkv = dtype, hkv
+
+    def run(self, partition_size=0):
+        out = torch.full_like(self.q, float("nan"))
+        B.paged_attention_decode_int8(out, self.q, self.kc, self.vc, self.ks, self.vs, self.tables, self.lens,
+                                      self.scale, partition_size=partition_size)
+        torch.cuda.synchronize()
+        return out
+
+    def oracle(self):
+        return OQ.paged_attention_decode_int8(
+            W.to_numpy_storage(self.q, self.dtype), _np(self.kc), _np(self.vc), _np(self.ks), _np(self.vs),
+            _np(self.tables), _np(self.lens), self.scale, self.hkv, self.dtype)
+
+    def oracle_rows(self, pairs):
+        """Oracle rows for a few (seq, q head) pairs, each over a sub-pool of
+        the blocks its sequence uses (relabelled ids)."""
+        group = self.q.shape[1] // self.hkv
+        lens, tables = _np(self.lens), _np(self.tables)
+        rows = {}
+        for s, h in pairs:
+            g, L = h // group, int(lens[s])
+            nb = -(-L // 16)
+            ids = torch.from_numpy(tables[s, :max(nb, 1)].astype(np.int64)).cuda()
+            sub = [x[:, g].index_select(0, ids).unsqueeze(1) for x in (self.kc, self.vc, self.ks, self.vs)]
+            out = OQ.paged_attention_decode_int8(
+                W.to_numpy_storage(self.q[s, h].reshape(1, 1, -1), self.dtype), *[_np(x) for x in sub],
+                np.arange(max(nb, 1), dtype=np.int32).reshape(1, -1), np.array([L], np.int32), self.scale, 1,
+                self.dtype)
+            rows[(s, h)] = out[0, 0]
+        return rows
+
+
+RAGGED = [0, 1, 15, 16, 17, 33, 100, 257, 530]
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("hq,hkv,d", [(4, 4, 64), (8, 8, 128), (2, 2, 256), (8, 4, 128), (16, 4, 64),
+                                      (16, 2, 128), (8, 1, 256), (12, 2, 128)])
+@pytest.mark.parametrize("partition", [0, -1, 64])
+def test_decode_int8_parity(dtype, hq, hkv, d, partition):
+    case = Int8Case(RAGGED, hq, hkv, d, dtype, seed=hq + d, extra_cols=2)
+    got = H.to_f64(case.run(partition))
+    H.assert_attention_close(got, case.oracle(), f"int8 {dtype} hq={hq} hkv={hkv} d={d} p={partition}")
+    assert np.all(got[0] == 0.0)                            # empty sequence gives zeros
+    assert B.device_status(clear=True) == 0
+
+
+def test_decode_int8_split_partitions_long():
+    # several partitions per sequence, the last one ragged, with the default schedule and explicit ones
+    case = Int8Case([3000, 2049, 17, 4096], 16, 8, 128, "bf16", seed=21)
+    want = case.oracle()
+    for p in (0, 256, 512, -1):
+        H.assert_attention_close(H.to_f64(case.run(p)), want, f"partition {p}")
+    assert B.device_status(clear=True) == 0
+
+
+def test_decode_int8_zero_scale_rows():
+    # rows stored as all-zero (scale 0) take part in the softmax with score 0
+    case = Int8Case([40, 64], 4, 4, 64, "f16", seed=3)
+    case.ks[:, :, 3] = 0
+    case.vs[:, :, 5] = 0
+    H.assert_attention_close(H.to_f64(case.run()), case.oracle(), "zero-scale rows")
+
+
+def test_decode_int8_balanced_rejected():
+    case = Int8Case([20, 30], 8, 8, 128, "bf16", seed=4)
+    with pytest.raises(B.PagedKVError) as ei:
+        case.run(B.BALANCED)
+    assert ei.value.status == 2
+
+
+@pytest.mark.parametrize("name", ["llama13b", "llama3_8b"])
+def test_decode_int8_full_size_sampled(name):
+    shape = {"llama13b": W.llama13b_mha_decode, "llama3_8b": W.llama3_8b_gqa_decode}[name](0)
+    case = Int8Case(shape.context_lens, shape.num_q_heads, shape.num_kv_heads, shape.head_dim, shape.dtype,
+                    seed=1)
+    got = case.run()
+    S, Hq = case.q.shape[0], case.q.shape[1]
+    rng = np.random.default_rng(7)
+    pairs = [(int(s), int(h)) for s, h in zip(rng.integers(0, S, 12), rng.integers(0, Hq, 12))]
+    pairs.append((int(np.argmax(shape.context_lens)), Hq - 1))
+    rows = case.oracle_rows(pairs)
+    for (s, h), want in rows.items():
+        H.assert_attention_close(H.to_f64(got[s, h]), want, f"{name} int8 ({s}, {h})")
+    assert torch.isfinite(got.float()).all()
+    assert B.device_status(clear=True) == 0

@@ -33,6 +33,8 @@ Modules:
   numerics       -- exact fp16/bf16 -> fp64 conversion
   quant          -- INT8 KV cache: per-row quantisation, quantised cache
                     write, decode over the dequantised cache
+  memsim         -- memory-utilisation replay: paged blocks against
+                    contiguous pre-allocation (slot-by-slot arena)
 
 Every function here is pinned by tests in ``tests/test_oracle*.py`` against
 values and invariants that the pages and mathematics fix (hand-worked
@@ -40,4 +42,4 @@ examples under ``tests/golden/``, brute force on tiny inputs, closed forms,
 permutation invariance, copy-on-write sibling equality).
 """
 
-from . import numerics, attention, cache_ops, block_manager, quant  # noqa: F401
+from . import numerics, attention, cache_ops, block_manager, quant, memsim  # noqa: F401

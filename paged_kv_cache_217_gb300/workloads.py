@@ -135,6 +135,23 @@ CONFIGS = {
 }
 
 
+def memsim_trace(name, num_requests, seed=0):
+    """A request-length trace for the memory-utilisation simulator: total
+    lengths L from the named layer's length distribution, each split into a
+    prompt of ceil(L / 2) tokens and an output of the rest; with the
+    distribution's upper clip as the maximum length. Returns (prompt_lens,
+    output_lens, max_len)."""
+    rng = np.random.default_rng(seed)
+    if name == "llama13b":
+        L, max_len = _lognormal_lengths(rng, num_requests, 512, 0.8, 16, 2048), 2048
+    elif name == "llama3_8b":
+        L, max_len = _lognormal_lengths(rng, num_requests, 150, 0.6, 8, 1024), 1024
+    else:
+        raise ValueError(f"unknown trace {name!r}")
+    P = (L + 1) // 2
+    return P.astype(np.int64), (L - P).astype(np.int64), max_len
+
+
 def shuffled_free_order(num_blocks, seed):
     """A seeded random permutation of the physical block ids 0..num_blocks-1."""
     return np.random.default_rng(seed + 1_000_003).permutation(num_blocks).astype(np.int32)

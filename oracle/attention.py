@@ -35,17 +35,20 @@ from .numerics import to_f64
 BLOCK_SIZE = 16
 
 
-def gather_kv(pool_f64, table_row, length, kv_head, block_size=BLOCK_SIZE):
-    """Contiguous [length, head_dim] copy of one sequence's K (or V) for one KV head.
+def gather_kv(pool_f64, table_row, length, kv_head, block_size=BLOCK_SIZE, start=0):
+    """Contiguous [length - start, head_dim] copy of positions start .. length-1
+    of one sequence's K (or V) for one KV head.
 
     Position p is read from physical block table_row[p // block_size],
     slot p % block_size.
     """
     head_dim = pool_f64.shape[-1]
-    out = np.empty((length, head_dim), dtype=np.float64)
-    for p in range(length):
+    out = np.empty((length - start, head_dim), dtype=np.float64)
+    for p in range(start, length):
         block = int(table_row[p // block_size])
-        out[p] = pool_f64[block, kv_head, p % block_size]
+        if block < 0:
+            raise ValueError(f"position {p} maps to no block (table entry {block})")
+        out[p - start] = pool_f64[block, kv_head, p % block_size]
     return out
 
 
@@ -128,3 +131,37 @@ def lse_merge(parts):
     num = sum(np.exp(m - M) * o for m, _, o in parts)
     den = sum(np.exp(m - M) * l for m, l, _ in parts)
     return num / den
+
+
+def window_start(length, window):
+    """First position a query at position length-1 attends to under a sliding
+    window of `window` tokens (the query's own token included); 0 when the
+    window is 0 (no window) or covers the whole sequence."""
+    if window > 0 and length > window:
+        return length - window
+    return 0
+
+
+def paged_attention_decode_window(q, k_pool, v_pool, block_tables, context_lens, scale,
+                                  num_kv_heads, dtype, window, block_size=BLOCK_SIZE):
+    """Sliding-window decode: each sequence's query attends over its last
+    `window` tokens only, positions window_start(L, window) .. L-1 (glossary
+    entry "PagedAttention（ページドアテンション）", section
+    "他のKVキャッシュ最適化との組み合わせ": sliding-window attention combined
+    with paging). Block-table entries of blocks wholly before that range are
+    never read. float64 [num_seqs, num_q_heads, head_dim]."""
+    qf = to_f64(q, dtype)
+    num_seqs, num_q_heads, head_dim = qf.shape
+    group = num_q_heads // num_kv_heads
+    kf = to_f64(k_pool, dtype)
+    vf = to_f64(v_pool, dtype)
+    out = np.zeros((num_seqs, num_q_heads, head_dim))
+    for s in range(num_seqs):
+        L = int(context_lens[s])
+        start = window_start(L, window)
+        for g in range(num_kv_heads):
+            K = gather_kv(kf, block_tables[s], L, g, block_size, start)
+            V = gather_kv(vf, block_tables[s], L, g, block_size, start)
+            for h in range(g * group, (g + 1) * group):
+                out[s, h] = attend(qf[s, h], K, V, scale)
+    return out

@@ -33,6 +33,10 @@ Readings where the pages are silent:
   blocks are never copied, because appends only ever write the last block.
   The slot returned is table[L // 16] * 16 + L % 16 and L becomes L + 1.
 * Every failing call raises and leaves the state unchanged.
+* Sliding window (glossary entry, "他のKVキャッシュ最適化との組み合わせ"
+  names sliding-window attention alongside paging): blocks wholly before the
+  window are released (release_before); their table entries become -1 so
+  that later blocks keep their logical indices.
 """
 
 BLOCK_SIZE = 16
@@ -105,7 +109,8 @@ class OracleBlockManager:
         self.tables[child] = list(self.tables[parent])
         self.lengths[child] = self.lengths[parent]
         for b in self.tables[child]:
-            self.refcount[b] += 1
+            if b >= 0:                      # released entries (-1) are not shared
+                self.refcount[b] += 1
 
     def append_slot(self, seq_id):
         """Reserve the slot of the next token. Returns (slot, cow_src, cow_dst); -1 = no copy."""
@@ -134,10 +139,35 @@ class OracleBlockManager:
         if seq_id not in self.tables:
             raise InvalidArgument(f"unknown sequence {seq_id}")
         for b in self.tables.pop(seq_id):
+            if b < 0:
+                continue
             self.refcount[b] -= 1
             if self.refcount[b] == 0:
                 self.free.append(b)
         del self.lengths[seq_id]
+
+    def release_before(self, seq_id, first_token):
+        """Sliding window: drop the sequence's hold on every block that lies
+        wholly before position first_token (blocks j with (j+1)*16 <=
+        first_token), in table order. Their table entries become -1 (logical
+        positions keep their blocks' indices); a block whose refcount reaches
+        0 goes back on the free list. Returns the number of entries dropped."""
+        if seq_id not in self.tables:
+            raise InvalidArgument(f"unknown sequence {seq_id}")
+        if first_token < 0 or first_token > self.lengths[seq_id]:
+            raise InvalidArgument("first_token must be in [0, length]")
+        table = self.tables[seq_id]
+        dropped = 0
+        for j in range(first_token // self.block_size):
+            b = table[j]
+            if b < 0:
+                continue
+            self.refcount[b] -= 1
+            if self.refcount[b] == 0:
+                self.free.append(b)
+            table[j] = -1
+            dropped += 1
+        return dropped
 
     def padded_tables(self, seq_ids, max_blocks_per_seq):
         """([n][max_blocks_per_seq] table padded with -1, [n] lengths)."""

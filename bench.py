@@ -2,7 +2,7 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload llama13b|llama3_8b|opt66b_sampling|opt175b_long|tiny]
-                    [--kv native|int8]
+                    [--kv native|int8] [--window W]
 
 One step is one pass of the whole hot path over one batch: write each
 sequence's new K/V into its slot (reshape_and_cache), copy-on-write block
@@ -21,7 +21,9 @@ in GB/s, with inputs resident in HBM. L2 is flushed between timed steps
 
 ``--kv int8`` runs the same step over the INT8 KV cache (int8 codes plus one
 fp32 scale per row): the write quantises, the decode dequantises on the fly;
-its bytes per token and KV head are 2 * (head_dim + 4).
+its bytes per token and KV head are 2 * (head_dim + 4). ``--window W`` runs
+sliding-window decode over each sequence's last W tokens; only those tokens'
+bytes count.
 
 Under torchrun (N > 1) every rank runs the same workload on its own GPU
 (replicas: the path has no exchange step); value = all ranks' bytes / the
@@ -75,7 +77,7 @@ def kernel_sha():
     return h.hexdigest()[:16]
 
 
-def build_workload(name, seed, device, kv="native"):
+def build_workload(name, seed, device, kv="native", window=0):
     import torch
     from paged_kv_cache_217_gb300 import binding as B
     from paged_kv_cache_217_gb300 import workloads as W
@@ -145,7 +147,9 @@ def build_workload(name, seed, device, kv="native"):
             wl.unique_kv_bytes = wl.unique_kv_bytes // (d * 2) * row_bytes
     else:
         row_bytes = d * 2
-    wl.kv_bytes = int(wl.lens_h.astype(np.int64).sum()) * hkv * row_bytes * 2
+    wl.window = window
+    attended = np.minimum(wl.lens_h, window) if window > 0 else wl.lens_h
+    wl.kv_bytes = int(attended.astype(np.int64).sum()) * hkv * row_bytes * 2
     return wl
 
 
@@ -182,6 +186,9 @@ def decode(wl, B):
     if wl.kv == "int8":
         B.paged_attention_decode_int8(wl.out, wl.q, wl.k_cache, wl.v_cache, wl.k_scale, wl.v_scale, wl.tables,
                                       wl.lens, wl.scale, partition_size=wl.partition)
+    elif wl.window > 0:
+        B.paged_attention_decode_sliding(wl.out, wl.q, wl.k_pool, wl.v_pool, wl.tables, wl.lens, wl.scale,
+                                         wl.window, partition_size=wl.partition)
     else:
         B.paged_attention_decode(wl.out, wl.q, wl.k_pool, wl.v_pool, wl.tables, wl.lens, wl.scale,
                                  partition_size=wl.partition)
@@ -309,6 +316,8 @@ def oracle_sample(wl, budget_s):
     seqs, est_s = [], 0.0
     for s in range(wl.num_seqs):
         L = int(wl.lens_h[s])
+        if wl.window > 0:
+            L = min(L, wl.window)
         est_s += L * wl.hkv * ORACLE_S_PER_TOKEN_HEAD + 2e-4 * wl.hq
         seqs.append(s)
         if est_s >= budget_s:
@@ -331,8 +340,9 @@ def oracle_sample(wl, budget_s):
     q = W.to_numpy_storage(wl.q_h[seqs], wl.dtype)
     lens = wl.lens_h[seqs]
     row_bytes = wl.d + 4 if wl.kv == "int8" else wl.d * 2
+    attended = np.minimum(lens, wl.window) if wl.window > 0 else lens
     return dict(q=q, kp=kp, vp=vp, ks=ks, vs=vs, tab=tab, lens=lens, seqs=len(seqs),
-                bytes=int(lens.astype(np.int64).sum()) * wl.hkv * row_bytes * 2)
+                bytes=int(attended.astype(np.int64).sum()) * wl.hkv * row_bytes * 2)
 
 
 # rough cost of the oracle per (token, KV head): two row gathers plus the fp64 math
@@ -347,8 +357,12 @@ def time_oracle(wl, sample, repeats):
         path = os.path.join(td, "sample.npz")
         np.savez(path, q=sample["q"], kp=sample["kp"], vp=sample["vp"], ks=sample["ks"], vs=sample["vs"],
                  tab=sample["tab"], lens=sample["lens"])
+        extra = ""
         if wl.kv == "int8":
             names, call = "('q', 'kp', 'vp', 'ks', 'vs', 'tab', 'lens')", "OQ.paged_attention_decode_int8"
+        elif wl.window > 0:
+            names, call = "('q', 'kp', 'vp', 'tab', 'lens')", "OA.paged_attention_decode_window"
+            extra = f", {int(wl.window)}"
         else:
             names, call = "('q', 'kp', 'vp', 'tab', 'lens')", "OA.paged_attention_decode"
         code = ("import sys, time, numpy as np; sys.path.insert(0, %r)\n"
@@ -357,9 +371,9 @@ def time_oracle(wl, sample, repeats):
                 "a = [z[k] for k in %s]\n"
                 "for _ in range(%d):\n"
                 "    t = time.perf_counter()\n"
-                "    %s(*a, %r, %d, %r)\n"
+                "    %s(*a, %r, %d, %r%s)\n"
                 "    print(time.perf_counter() - t, flush=True)\n") % (
-                    ROOT, path, names, repeats, call, wl.scale, wl.hkv, wl.dtype)
+                    ROOT, path, names, repeats, call, wl.scale, wl.hkv, wl.dtype, extra)
         env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
         res = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env,
                              timeout=3600)
@@ -404,7 +418,9 @@ def run_ours(args):
         dist.barrier()
     B.lib()
 
-    wl = build_workload(args.workload, args.seed, device, args.kv)
+    if args.window > 0 and args.kv != "native":
+        raise SystemExit("--window runs on the native cache only")
+    wl = build_workload(args.workload, args.seed, device, args.kv, args.window)
     wl.partition = args.partition
     device_inputs(wl, device)
     # L2 eviction buffer: read (not written) between timed steps, so the next
@@ -476,7 +492,8 @@ def run_ours(args):
     value = whole_job_gbs(wl.kv_bytes, per_step_ms, world)
     dec_ms = statistics.mean(decode_ms)
     achieved = wl.kv_bytes / (dec_ms * 1e-3) / 1e9
-    traffic = recorded_traffic(args.workload if args.kv == "native" else f"{args.workload}-{args.kv}")
+    traffic = recorded_traffic(args.workload + ("" if args.kv == "native" else f"-{args.kv}")
+                               + (f"-w{args.window}" if args.window > 0 else ""))
     line = {
         "metric": METRIC,
         "value": round(value, 1),
@@ -493,7 +510,8 @@ def run_ours(args):
                 + ("; INT8 cache: uniform codes in [-127, 127], fp32 row scales U[0.01, 0.03]"
                    if wl.kv == "int8" else ""),
         "config": {
-            "workload": wl.description + (" (INT8 KV cache)" if wl.kv == "int8" else ""),
+            "workload": wl.description + (" (INT8 KV cache)" if wl.kv == "int8" else "")
+                        + (f" (sliding window {wl.window})" if wl.window > 0 else ""),
             "kv_cache": "int8 codes + fp32 row scales, fp32 math" if wl.kv == "int8" else f"{wl.dtype}",
             "num_seqs": wl.num_seqs,
             "kv_bytes_per_step": wl.kv_bytes,
@@ -549,7 +567,7 @@ def run_reference(args):
         return
     import torch
     device = "cuda" if torch.cuda.is_available() else "cpu"
-    wl = build_workload(args.workload, args.seed, device, args.kv)
+    wl = build_workload(args.workload, args.seed, device, args.kv, args.window)
     total = args.steps + args.warmup
     budget = min(6.0, max(0.02, args.reference_budget / total))
     sample = oracle_sample(wl, budget)
@@ -590,6 +608,8 @@ def main(argv=None):
     ap.add_argument("--workload", default="llama13b",
                     choices=["llama13b", "llama3_8b", "opt66b_sampling", "opt175b_long", "tiny"])
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--window", type=int, default=0,
+                    help="sliding-window decode over the last W tokens of each sequence (0 = full attention)")
     ap.add_argument("--kv", choices=["native", "int8"], default="native",
                     help="KV cache storage: native (the workload's fp16/bf16) or int8 codes with row scales")
     ap.add_argument("--partition", type=int, default=0,

@@ -213,6 +213,34 @@ pkv_status_t pkv_paged_attention_decode_noalloc(
     int max_blocks_per_seq, int num_blocks, float scale, pkv_dtype_t dtype,
     int partition_size, pkv_stream_t stream);
 
+/*
+ * Sliding-window decode ([G] "他のKVキャッシュ最適化との組み合わせ" names
+ * sliding-window attention as a companion of paging; the page gives no
+ * formula, so this library takes the usual one): the query of sequence s
+ * attends over its last sliding_window tokens only,
+ *   positions [max(0, L - W), L),  W = sliding_window,
+ * and otherwise computes exactly what pkv_paged_attention_decode computes.
+ * Block-table entries of blocks wholly before that range are never read (the
+ * block manager may have released them, see pkv_bm_release_before).
+ * sliding_window <= 0 means no window. partition_size as for
+ * pkv_paged_attention_decode except -2 (balanced), which returns
+ * PKV_ERR_UNSUPPORTED; the split covers the window, not the whole length.
+ * The workspace must hold pkv_paged_attention_sliding_workspace_size bytes.
+ */
+pkv_status_t pkv_paged_attention_decode_sliding(
+    void* out, const void* q, const void* k_pool, const void* v_pool,
+    const int32_t* block_tables, const int32_t* context_lens,
+    int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+    int max_blocks_per_seq, int num_blocks, float scale, pkv_dtype_t dtype,
+    int sliding_window, int partition_size, void* workspace,
+    size_t workspace_bytes, pkv_stream_t stream);
+
+size_t pkv_paged_attention_sliding_workspace_size(int num_seqs, int num_q_heads,
+                                                  int num_kv_heads, int head_dim,
+                                                  int max_blocks_per_seq,
+                                                  int sliding_window,
+                                                  int partition_size);
+
 /* ------------------------------------------------------------------------ */
 /* Cache writes and copy-on-write                                            */
 /* ------------------------------------------------------------------------ */
@@ -354,6 +382,21 @@ pkv_status_t pkv_bm_append_slots(pkv_bm_t* bm, const int64_t* seq_ids, int n,
 
 /* Drop the sequence; blocks whose refcount reaches 0 return to the free list. */
 pkv_status_t pkv_bm_free_seq(pkv_bm_t* bm, int64_t seq_id);
+
+/*
+ * Sliding window ([G] "他のKVキャッシュ最適化との組み合わせ": sliding-window
+ * attention combined with paging): drops the sequence's hold on every block
+ * wholly before position first_token (table entries j with
+ * (j+1)*16 <= first_token), in table order. Those entries become -1, so later
+ * blocks keep their logical indices; a block whose refcount reaches 0 returns
+ * to the free list. With window W, first_token = max(0, L - W) releases
+ * exactly the blocks pkv_paged_attention_decode_sliding never reads.
+ * first_token must lie in [0, length]. *released_out (may be NULL) receives
+ * the number of entries dropped; released entries are skipped by fork and
+ * free_seq.
+ */
+pkv_status_t pkv_bm_release_before(pkv_bm_t* bm, int64_t seq_id, int64_t first_token,
+                                   int* released_out);
 
 /* Padded block tables and lengths of n sequences (host buffers):
  * table_out[n][max_blocks_per_seq] (-1 padded), lens_out[n]. */

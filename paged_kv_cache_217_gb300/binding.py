@@ -56,6 +56,9 @@ _SIGS = {
                                    _c_int),
     "pkv_paged_attention_decode_noalloc": ([_c_p] * 6 + [_c_int] * 6 + [_c_f, _c_int, _c_int, _c_p], _c_int),
     "pkv_paged_attention_workspace_size": ([_c_int] * 6, _c_sz),
+    "pkv_paged_attention_decode_sliding": ([_c_p] * 6 + [_c_int] * 6 + [_c_f, _c_int, _c_int, _c_int, _c_p, _c_sz,
+                                                                       _c_p], _c_int),
+    "pkv_paged_attention_sliding_workspace_size": ([_c_int] * 7, _c_sz),
     "pkv_paged_attention_partition": ([_c_int] * 6, _c_int),
     "pkv_reshape_and_cache": ([_c_p] * 5 + [_c_int] * 5 + [_c_p], _c_int),
     "pkv_copy_blocks": ([_c_p] * 3 + [_c_int] * 5 + [_c_p], _c_int),
@@ -72,6 +75,7 @@ _SIGS = {
     "pkv_bm_append_slot": ([_c_p, _c_i64, _c_p, _c_p, _c_p], _c_int),
     "pkv_bm_append_slots": ([_c_p, _c_p, _c_int, _c_p, _c_p, _c_p], _c_int),
     "pkv_bm_free_seq": ([_c_p, _c_i64], _c_int),
+    "pkv_bm_release_before": ([_c_p, _c_i64, _c_i64, _c_p], _c_int),
     "pkv_bm_block_tables": ([_c_p, _c_p, _c_int, _c_int, _c_p, _c_p], _c_int),
     "pkv_bm_refcount": ([_c_p, _c_int, _c_p], _c_int),
     "pkv_bm_seq_len": ([_c_p, _c_i64, _c_p], _c_int),
@@ -203,6 +207,43 @@ def paged_attention_decode(out, q, k_pool, v_pool, block_tables, context_lens, s
         out.data_ptr(), q.data_ptr(), k_pool.data_ptr(), v_pool.data_ptr(), block_tables.data_ptr(),
         context_lens.data_ptr(), S, Hq, num_kv_heads, D, mb, nb, float(scale), dt, int(partition_size),
         ws_ptr, ws_bytes, _stream_ptr(q.device)), "paged_attention_decode")
+    return out
+
+
+def sliding_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, sliding_window,
+                           partition_size=0):
+    return int(lib().pkv_paged_attention_sliding_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                                                max_blocks_per_seq, sliding_window, partition_size))
+
+
+def paged_attention_decode_sliding(out, q, k_pool, v_pool, block_tables, context_lens, scale, sliding_window,
+                                   partition_size=0, workspace=None):
+    """paged_attention_decode over each sequence's last ``sliding_window`` tokens
+    (positions max(0, L - W) .. L-1); table entries before them are never read."""
+    import torch
+    _need_cuda(out, q, k_pool, v_pool, block_tables, context_lens)
+    dt = _dtype_code(q)
+    if out.dtype != q.dtype or k_pool.dtype != q.dtype or v_pool.dtype != q.dtype:
+        raise TypeError("q, out, k_pool and v_pool must share one dtype")
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise TypeError("block_tables and context_lens must be int32")
+    S, Hq, D = q.shape
+    nb, hkv = k_pool.shape[0], k_pool.shape[1]
+    if k_pool.shape[2:] != (BLOCK_SIZE, D) or v_pool.shape != k_pool.shape:
+        raise ValueError("pools must be [num_blocks, num_kv_heads, 16, head_dim]")
+    if tuple(out.shape) != (S, Hq, D) or block_tables.dim() != 2 or block_tables.shape[0] != S \
+            or tuple(context_lens.shape) != (S,):
+        raise ValueError("shape mismatch among out, q, block_tables and context_lens")
+    mb = block_tables.shape[1]
+    need = sliding_workspace_size(S, Hq, hkv, D, mb, int(sliding_window), partition_size)
+    ws_ptr, ws_bytes = None, 0
+    if need:
+        ws = workspace if workspace is not None else _workspace(q.device, need)
+        ws_ptr, ws_bytes = ws.data_ptr(), ws.numel() * ws.element_size()
+    _check(lib().pkv_paged_attention_decode_sliding(
+        out.data_ptr(), q.data_ptr(), k_pool.data_ptr(), v_pool.data_ptr(), block_tables.data_ptr(),
+        context_lens.data_ptr(), S, Hq, hkv, D, mb, nb, float(scale), dt, int(sliding_window),
+        int(partition_size), ws_ptr, ws_bytes, _stream_ptr(q.device)), "paged_attention_decode_sliding")
     return out
 
 
@@ -427,6 +468,14 @@ class BlockManager:
 
     def free_seq(self, seq_id):
         _check(lib().pkv_bm_free_seq(self._h, int(seq_id)), "bm_free_seq")
+
+    def release_before(self, seq_id, first_token):
+        """Drops the sequence's hold on blocks wholly before position first_token
+        (their table entries become -1); returns how many entries were dropped."""
+        n = ctypes.c_int()
+        _check(lib().pkv_bm_release_before(self._h, int(seq_id), int(first_token), ctypes.byref(n)),
+               "bm_release_before")
+        return n.value
 
     def block_tables(self, seq_ids, max_blocks_per_seq):
         ids = np.ascontiguousarray(np.asarray(seq_ids, dtype=np.int64))

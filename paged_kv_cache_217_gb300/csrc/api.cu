@@ -242,13 +242,23 @@ size_t pkv_paged_attention_workspace_size(int num_seqs, int num_q_heads, int num
   return split_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, plan.max_parts).total;
 }
 
-pkv_status_t pkv_paged_attention_decode(void* out, const void* q, const void* k_pool,
-                                        const void* v_pool, const int32_t* block_tables,
-                                        const int32_t* context_lens, int num_seqs,
-                                        int num_q_heads, int num_kv_heads, int head_dim,
-                                        int max_blocks_per_seq, int num_blocks, float scale,
-                                        pkv_dtype_t dtype, int partition_size, void* workspace,
-                                        size_t workspace_bytes, pkv_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Blocks a sliding window of `window` tokens can touch (it may start inside a
+// block), capped by the table width; the whole table without a window.
+int window_blocks(int max_blocks_per_seq, int window) {
+  if (window <= 0) return max_blocks_per_seq;
+  const int64_t wb = (int64_t(window) + PKV_BLOCK_SIZE - 1) / PKV_BLOCK_SIZE + 1;
+  return wb < max_blocks_per_seq ? int(wb) : max_blocks_per_seq;
+}
+
+pkv_status_t decode_impl(void* out, const void* q, const void* k_pool, const void* v_pool,
+                         const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
+                         int num_q_heads, int num_kv_heads, int head_dim, int max_blocks_per_seq,
+                         int num_blocks, float scale, pkv_dtype_t dtype, int window, int partition_size,
+                         void* workspace, size_t workspace_bytes, pkv_stream_t stream) {
   if (num_seqs < 0) return pkv::fail(PKV_ERR_INVALID_ARG, "num_seqs < 0");
   if (num_seqs == 0) return pkv::ok();
   if (num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0)
@@ -269,11 +279,15 @@ pkv_status_t pkv_paged_attention_decode(void* out, const void* q, const void* k_
   if (!aligned(block_tables, 4) || !aligned(context_lens, 4))
     return pkv::fail(PKV_ERR_INVALID_ARG, "block_tables and context_lens must be 4-byte aligned");
 
-  const int p = choose_partition(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, partition_size);
+  // With a sliding window the partitions cover the window, not the table.
+  const int plan_blocks = window_blocks(max_blocks_per_seq, window);
+  const int p = choose_partition(num_seqs, num_q_heads, num_kv_heads, head_dim, plan_blocks, partition_size);
   Plan plan;
-  pkv_status_t st = plan_decode(max_blocks_per_seq, p, &plan);
+  pkv_status_t st = plan_decode(plan_blocks, p, &plan);
   if (st != PKV_OK) return st;
   const bool balanced = p == kBalanced;
+  if (balanced && window > 0)
+    return pkv::fail(PKV_ERR_UNSUPPORTED, "the balanced schedule takes no sliding window");
   if (balanced && !balanced_fits(num_seqs, num_q_heads, num_kv_heads, head_dim))
     return pkv::fail(PKV_ERR_UNSUPPORTED, "the balanced schedule takes at most %d sequences at these sizes",
                      pkv::decode_sk_max_seqs(head_dim, round_pow2_group(group)));
@@ -352,6 +366,7 @@ pkv_status_t pkv_paged_attention_decode(void* out, const void* q, const void* k_
   // sequence started last sets the end time (measured on GB300: -9 % on the
   // LLaMA-13B layer at 2560 CTAs, +7 % on the OPT-66B sampling batch at 9216).
   a.long_first = int64_t(num_seqs) * num_kv_heads * plan.max_parts <= kLongFirstMaxCtas ? 1 : 0;
+  a.window = window > 0 ? window : 0;
   a.scale_log2 = scale * 1.4426950408889634f;
 
   cudaError_t err = cudaSuccess;
@@ -363,6 +378,41 @@ pkv_status_t pkv_paged_attention_decode(void* out, const void* q, const void* k_
   err = dtype == PKV_F16 ? pkv::launch_decode_f16(a, head_dim, gpad, &kmap, &vmap, stream)
                          : pkv::launch_decode_bf16(a, head_dim, gpad, &kmap, &vmap, stream);
   return cuda_status(err, "paged_attention_decode launch");
+}
+
+}  // namespace
+
+extern "C" {
+
+pkv_status_t pkv_paged_attention_decode(void* out, const void* q, const void* k_pool,
+                                        const void* v_pool, const int32_t* block_tables,
+                                        const int32_t* context_lens, int num_seqs,
+                                        int num_q_heads, int num_kv_heads, int head_dim,
+                                        int max_blocks_per_seq, int num_blocks, float scale,
+                                        pkv_dtype_t dtype, int partition_size, void* workspace,
+                                        size_t workspace_bytes, pkv_stream_t stream) {
+  return decode_impl(out, q, k_pool, v_pool, block_tables, context_lens, num_seqs, num_q_heads, num_kv_heads,
+                     head_dim, max_blocks_per_seq, num_blocks, scale, dtype, 0, partition_size, workspace,
+                     workspace_bytes, stream);
+}
+
+pkv_status_t pkv_paged_attention_decode_sliding(void* out, const void* q, const void* k_pool, const void* v_pool,
+                                                const int32_t* block_tables, const int32_t* context_lens,
+                                                int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                                int max_blocks_per_seq, int num_blocks, float scale,
+                                                pkv_dtype_t dtype, int sliding_window, int partition_size,
+                                                void* workspace, size_t workspace_bytes, pkv_stream_t stream) {
+  return decode_impl(out, q, k_pool, v_pool, block_tables, context_lens, num_seqs, num_q_heads, num_kv_heads,
+                     head_dim, max_blocks_per_seq, num_blocks, scale, dtype, sliding_window > 0 ? sliding_window : 0,
+                     partition_size, workspace, workspace_bytes, stream);
+}
+
+size_t pkv_paged_attention_sliding_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                                  int max_blocks_per_seq, int sliding_window, int partition_size) {
+  if (max_blocks_per_seq <= 0) return 0;
+  if (sliding_window > 0 && partition_size == kBalanced) return 0;
+  return pkv_paged_attention_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                            window_blocks(max_blocks_per_seq, sliding_window), partition_size);
 }
 
 pkv_status_t pkv_paged_attention_decode_int8(void* out, const void* q, const int8_t* k_cache,

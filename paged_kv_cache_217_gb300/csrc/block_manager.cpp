@@ -153,7 +153,8 @@ pkv_status_t pkv_bm_fork(pkv_bm_t* bm, int64_t parent, int64_t child) {
   if (it == bm->seqs.end()) return pkv::fail(PKV_ERR_INVALID_ARG, "bm_fork: unknown parent %lld", (long long)parent);
   if (bm->seqs.count(child)) return pkv::fail(PKV_ERR_INVALID_ARG, "bm_fork: sequence %lld exists", (long long)child);
   pkv_bm::Seq c = it->second;  // copy before emplace (rehash may move it)
-  for (int32_t b : c.table) bm->refcount[b] += 1;
+  for (int32_t b : c.table)
+    if (b >= 0) bm->refcount[b] += 1;  // released entries (-1) are not shared
   bm->seqs.emplace(child, std::move(c));
   return pkv::ok();
 }
@@ -202,8 +203,31 @@ pkv_status_t pkv_bm_free_seq(pkv_bm_t* bm, int64_t seq_id) {
   if (!bm) return pkv::fail(PKV_ERR_INVALID_ARG, "bm_free_seq: NULL handle");
   auto it = bm->seqs.find(seq_id);
   if (it == bm->seqs.end()) return pkv::fail(PKV_ERR_INVALID_ARG, "bm_free_seq: unknown sequence %lld", (long long)seq_id);
-  for (int32_t b : it->second.table) bm->release(b);
+  for (int32_t b : it->second.table)
+    if (b >= 0) bm->release(b);
   bm->seqs.erase(it);
+  return pkv::ok();
+}
+
+pkv_status_t pkv_bm_release_before(pkv_bm_t* bm, int64_t seq_id, int64_t first_token, int* released_out) {
+  if (!bm) return pkv::fail(PKV_ERR_INVALID_ARG, "bm_release_before: NULL handle");
+  auto it = bm->seqs.find(seq_id);
+  if (it == bm->seqs.end())
+    return pkv::fail(PKV_ERR_INVALID_ARG, "bm_release_before: unknown sequence %lld", (long long)seq_id);
+  auto& s = it->second;
+  if (first_token < 0 || first_token > s.len)
+    return pkv::fail(PKV_ERR_INVALID_ARG, "bm_release_before: first_token %lld outside [0, %lld]",
+                     (long long)first_token, (long long)s.len);
+  int released = 0;
+  const int64_t whole = first_token / PKV_BLOCK_SIZE;  // blocks wholly before first_token
+  for (int64_t j = 0; j < whole; ++j) {
+    int32_t& b = s.table[size_t(j)];
+    if (b < 0) continue;
+    bm->release(b);
+    b = -1;
+    ++released;
+  }
+  if (released_out) *released_out = released;
   return pkv::ok();
 }
 

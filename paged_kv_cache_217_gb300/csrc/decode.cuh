@@ -64,8 +64,23 @@ struct DecodeArgs {
   int part_tokens;      // tokens per partition (multiple of 16)
   int max_parts;        // grid.z
   int long_first;       // start sequences of twice the mean length first (long_first_seq)
+  int window;           // sliding window: attend over the last `window` tokens (0 = all)
   float scale_log2;     // scale * log2(e)
 };
+
+// Token range a sequence of length L attends over: [first, L), with
+// first = L - window for a sliding window shorter than L, else 0. The tiles
+// start at the block boundary `aligned` <= first; rows before `first` in the
+// first tile are masked.
+struct TokenRange {
+  int first, aligned;
+};
+__device__ __forceinline__ TokenRange token_range(int L, int window) {
+  TokenRange r;
+  r.first = (window > 0 && L > window) ? L - window : 0;
+  r.aligned = r.first & ~(kBlock - 1);
+  return r;
+}
 
 // Waits until the kernel launched before this one in the stream has finished
 // and its writes are visible (programmatic dependent launch: the grid may
@@ -124,6 +139,7 @@ __device__ __forceinline__ int long_first_seq(const DecodeArgs& a, int rank) {
   for (int s = tid; s < S; s += NW * 32) {
     int L = __ldg(a.context_lens + s);
     L = L < 0 ? 0 : (L > max_len ? max_len : L);
+    if (a.window > 0 && L > a.window) L = a.window;
     tiles[s] = (L + kBlock - 1) / kBlock;
     local += tiles[s];
   }
@@ -235,9 +251,10 @@ struct RowReduceScatter {
 };
 
 // One 16-row tile: scores, online-softmax update, weighted V accumulation.
-// MASK: the tile holds only `rows` valid rows (the rest of the stage is stale).
+// MASK: only rows [lo, rows) of the tile are valid (the rest of the stage is
+// stale or outside a sliding window).
 template <typename T, int D, int G, int NW, int STAGES, bool MASK, typename KV = KvHalf<T>>
-__device__ __forceinline__ void decode_tile(uint32_t kt, uint32_t vt, int rows,
+__device__ __forceinline__ void decode_tile(uint32_t kt, uint32_t vt, int lo, int rows,
                                             const float (&qf)[G][8], float (&acc)[G][8],
                                             float (&lsum)[G], float (&mrun)[G], int lane,
                                             uint32_t ksc = 0, uint32_t vsc = 0) {
@@ -281,7 +298,7 @@ __device__ __forceinline__ void decode_tile(uint32_t kt, uint32_t vt, int rows,
 #pragma unroll
   for (int e = 0; e < NF; ++e) {
     if constexpr (KV::SCALED) sc[e] *= lds_f32(ksc + ((i0 + e) * RPP + r) * 4);  // dequantise K
-    if (MASK && (i0 + e) * RPP + r >= rows) sc[e] = -INFINITY;
+    if (MASK && ((i0 + e) * RPP + r < lo || (i0 + e) * RPP + r >= rows)) sc[e] = -INFINITY;
     mloc = fmaxf(mloc, sc[e]);
   }
   // Tile max of head hl: lanes that own head hl differ in the low sub bits and in r.
@@ -319,7 +336,7 @@ __device__ __forceinline__ void decode_tile(uint32_t kt, uint32_t vt, int rows,
     KV::load8(vt + row * C::ROW_BYTES + sub * 8 * KV::ELEM, vf);
     // rows past the tile's valid ones hold stale data: their weight is 0 and
     // their values must not reach the sums (0 * NaN)
-    const bool live = !MASK || row < rows;
+    const bool live = !MASK || (row >= lo && row < rows);
     if (MASK && !live) {
 #pragma unroll
       for (int c = 0; c < 8; ++c) vf[c] = 0.f;
@@ -455,10 +472,11 @@ paged_decode_kernel(const DecodeArgs a) {
   const int sub = lane & (LPR - 1), r = lane / LPR;
   const int hq0 = g * a.group;
 
-  // The first 32 block ids of this warp's tiles do not depend on the length:
-  // read them together with it (entries past the sequence are never used).
+  // Without a sliding window the first 32 block ids of this warp's tiles do
+  // not depend on the length: read them together with it (entries past the
+  // sequence are never used).
   int ids_early = 0;
-  {
+  if (a.window == 0) {
     const int j0 = (blockIdx.z * a.part_tokens) / kBlock + warp + lane * NW;
     if (j0 < a.max_blocks_per_seq) ids_early = __ldg(a.block_tables + size_t(s) * a.max_blocks_per_seq + j0);
   }
@@ -468,7 +486,8 @@ paged_decode_kernel(const DecodeArgs a) {
     if (threadIdx.x == 0 && part == 0 && g == 0) flag(a.status, PKV_DEV_BAD_CONTEXT_LEN);
     L = L < 0 ? 0 : max_len;
   }
-  const int nparts = L == 0 ? 1 : (L + a.part_tokens - 1) / a.part_tokens;
+  const TokenRange tr = token_range(L, a.window);
+  const int nparts = L == 0 ? 1 : (L - tr.aligned + a.part_tokens - 1) / a.part_tokens;
   if (part >= nparts) return;
 
   if (L == 0) {  // empty sequence: zeros
@@ -478,9 +497,10 @@ paged_decode_kernel(const DecodeArgs a) {
     return;
   }
 
-  const int t0 = part * a.part_tokens;
+  const int t0 = tr.aligned + part * a.part_tokens;
   const int ntok = min(L, t0 + a.part_tokens) - t0;
   const int nb = (ntok + kBlock - 1) / kBlock;
+  const int head = part == 0 ? tr.first - tr.aligned : 0;  // rows before the window in tile 0
 
   unsigned char* ring = smem + size_t(warp) * STAGES * C::STAGE_BYTES;
   const uint32_t ring_s = smem_addr(ring);
@@ -524,7 +544,7 @@ paged_decode_kernel(const DecodeArgs a) {
   };
   int ids = 0;
   if (lane < n_my) {
-    ids = ids_early;
+    ids = a.window == 0 ? ids_early : __ldg(trow + warp + lane * NW);
     if (ids < 0 || ids >= a.num_blocks) {
       flag(a.status, PKV_DEV_BAD_BLOCK_ID);
       ids = 0;
@@ -550,13 +570,15 @@ paged_decode_kernel(const DecodeArgs a) {
     if (lane == 0) {
       const int j = warp + k * NW;
       const int rows = min(kBlock, ntok - j * kBlock);
-      const uint32_t bytes = uint32_t(rows) * C::ROW_BYTES;
+      const int lo = j == 0 ? head : 0;  // rows before the window are not copied
+      const uint32_t bytes = uint32_t(rows - lo) * C::ROW_BYTES;
+      const uint32_t off = uint32_t(lo) * C::ROW_BYTES;
       const int st = k % STAGES;
       const uint32_t bar = bar_s + 8 * st;
       const uint32_t dst = ring_s + st * C::STAGE_BYTES;
       mbar_arrive_expect_tx(bar, 2 * bytes + 2 * C::SCALE_BYTES);
-      bulk_g2s(dst, kbase + size_t(id) * blk_stride, bytes, bar);
-      bulk_g2s(dst + C::TILE_BYTES, vbase + size_t(id) * blk_stride, bytes, bar);
+      bulk_g2s(dst + off, kbase + size_t(id) * blk_stride + off, bytes, bar);
+      bulk_g2s(dst + C::TILE_BYTES + off, vbase + size_t(id) * blk_stride + off, bytes, bar);
       if constexpr (KV::SCALED) {
         const size_t so = size_t(id) * a.num_kv_heads * kBlock;
         bulk_g2s(dst + 2 * C::TILE_BYTES, kscale_base + so, C::SCALE_BYTES, bar);
@@ -591,12 +613,13 @@ paged_decode_kernel(const DecodeArgs a) {
     }
     const int j = warp + k * NW;
     const int rows = min(kBlock, ntok - j * kBlock);
+    const int lo = j == 0 ? head : 0;
     const uint32_t kt = ring_s + st * C::STAGE_BYTES;
     const uint32_t ks = kt + 2 * C::TILE_BYTES, vs = ks + C::SCALE_BYTES;
-    if (rows == kBlock)
-      decode_tile<T, D, G, NW, STAGES, false, KV>(kt, kt + C::TILE_BYTES, rows, qf, acc, lsum, mrun, lane, ks, vs);
+    if (rows == kBlock && lo == 0)
+      decode_tile<T, D, G, NW, STAGES, false, KV>(kt, kt + C::TILE_BYTES, 0, rows, qf, acc, lsum, mrun, lane, ks, vs);
     else
-      decode_tile<T, D, G, NW, STAGES, true, KV>(kt, kt + C::TILE_BYTES, rows, qf, acc, lsum, mrun, lane, ks, vs);
+      decode_tile<T, D, G, NW, STAGES, true, KV>(kt, kt + C::TILE_BYTES, lo, rows, qf, acc, lsum, mrun, lane, ks, vs);
     __syncwarp();
     if (k + STAGES < n_my) issue(k + STAGES);
   }

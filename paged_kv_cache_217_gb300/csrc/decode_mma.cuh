@@ -124,7 +124,7 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
 
 // One 16-row tile for the G heads of this warp's lane row g = lane/4.
 template <typename T, int D, int NW, int STAGES, bool MASK>
-__device__ __forceinline__ void mma_tile(uint32_t kt, uint32_t vt, int rows, const uint32_t (&qa)[D / 16][2],
+__device__ __forceinline__ void mma_tile(uint32_t kt, uint32_t vt, int lo, int rows, const uint32_t (&qa)[D / 16][2],
                                          float (&o)[D / 8][4], float& mrun, float& lrun, float scale_log2,
                                          int lane) {
   using C = MmaCfg<T, D, NW, STAGES>;
@@ -160,11 +160,11 @@ __device__ __forceinline__ void mma_tile(uint32_t kt, uint32_t vt, int rows, con
 
   // Online softmax on head g's scores for tokens 2t, 2t+1, 8+2t, 9+2t.
   float x[4] = {s0[0] * scale_log2, s0[1] * scale_log2, s1[0] * scale_log2, s1[1] * scale_log2};
-  if (MASK) {
-    if (2 * t >= rows) x[0] = -INFINITY;
-    if (2 * t + 1 >= rows) x[1] = -INFINITY;
-    if (8 + 2 * t >= rows) x[2] = -INFINITY;
-    if (9 + 2 * t >= rows) x[3] = -INFINITY;
+  if (MASK) {  // only tokens [lo, rows) of the tile are valid
+    if (2 * t < lo || 2 * t >= rows) x[0] = -INFINITY;
+    if (2 * t + 1 < lo || 2 * t + 1 >= rows) x[1] = -INFINITY;
+    if (8 + 2 * t < lo || 8 + 2 * t >= rows) x[2] = -INFINITY;
+    if (9 + 2 * t < lo || 9 + 2 * t >= rows) x[3] = -INFINITY;
   }
   float mt = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
   mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 1));
@@ -205,14 +205,16 @@ __device__ __forceinline__ void mma_tile(uint32_t kt, uint32_t vt, int rows, con
   }
 }
 
-// Zeroes rows [rows, 16) of a swizzled V tile so that 0 * (stale data) in the
-// PV product cannot produce NaN, then orders these generic-proxy writes before
-// the next bulk-tensor write into the same stage.
+// Zeroes the rows outside [lo, rows) of a swizzled V tile so that 0 * (stale
+// data) in the PV product cannot produce NaN, then orders these generic-proxy
+// writes before the next bulk-tensor write into the same stage.
 template <int D>
-__device__ __forceinline__ void zero_tail_rows(uint32_t vt, int rows, int lane) {
+__device__ __forceinline__ void zero_rows_outside(uint32_t vt, int lo, int rows, int lane) {
   constexpr int CH = D / 8;
-  for (int i = lane; i < (kBlock - rows) * CH; i += 32) {
-    const int row = rows + i / CH, chunk = i % CH;
+  const int n_out = lo + (kBlock - rows);
+  for (int i = lane; i < n_out * CH; i += 32) {
+    const int k = i / CH, chunk = i % CH;
+    const int row = k < lo ? k : rows + (k - lo);
     asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(vt + swz(row, chunk)), "r"(0u) : "memory");
   }
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -237,10 +239,11 @@ paged_decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap 
   const int hq0 = g * a.group;
   const int gr = lane >> 2, t = lane & 3;   // MMA row (query head) and column pair of this lane
 
-  // The first 32 block ids of this warp's tiles do not depend on the length:
-  // read them together with it (entries past the sequence are never used).
+  // Without a sliding window the first 32 block ids of this warp's tiles do
+  // not depend on the length: read them together with it (entries past the
+  // sequence are never used).
   int ids_early = 0;
-  {
+  if (a.window == 0) {
     const int j0 = (blockIdx.z * a.part_tokens) / kBlock + warp + lane * NW;
     if (j0 < a.max_blocks_per_seq) ids_early = __ldg(a.block_tables + size_t(s) * a.max_blocks_per_seq + j0);
   }
@@ -250,7 +253,8 @@ paged_decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap 
     if (threadIdx.x == 0 && part == 0 && g == 0) flag(a.status, PKV_DEV_BAD_CONTEXT_LEN);
     L = L < 0 ? 0 : max_len;
   }
-  const int nparts = L == 0 ? 1 : (L + a.part_tokens - 1) / a.part_tokens;
+  const TokenRange tr = token_range(L, a.window);
+  const int nparts = L == 0 ? 1 : (L - tr.aligned + a.part_tokens - 1) / a.part_tokens;
   if (part >= nparts) return;
   if (L == 0) {
     T* o = static_cast<T*>(a.out) + (size_t(s) * a.num_q_heads + hq0) * D;
@@ -258,9 +262,10 @@ paged_decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap 
       reinterpret_cast<uint4*>(o)[i] = make_uint4(0u, 0u, 0u, 0u);
     return;
   }
-  const int t0 = part * a.part_tokens;
+  const int t0 = tr.aligned + part * a.part_tokens;
   const int ntok = min(L, t0 + a.part_tokens) - t0;
   const int nb = (ntok + kBlock - 1) / kBlock;
+  const int head = part == 0 ? tr.first - tr.aligned : 0;  // rows before the window in tile 0
 
   unsigned char* ring = smem + size_t(warp) * STAGES * C::STAGE_BYTES;
   const uint32_t ring_s = smem_addr(ring);
@@ -298,7 +303,7 @@ paged_decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap 
   };
   int ids = 0;
   if (lane < n_my) {
-    ids = ids_early;
+    ids = a.window == 0 ? ids_early : __ldg(trow + warp + lane * NW);
     if (ids < 0 || ids >= a.num_blocks) {
       flag(a.status, PKV_DEV_BAD_BLOCK_ID);
       ids = 0;
@@ -348,12 +353,13 @@ paged_decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap 
     }
     const int j = warp + k * NW;
     const int rows = min(kBlock, ntok - j * kBlock);
+    const int lo = j == 0 ? head : 0;
     const uint32_t kt = ring_s + st * C::STAGE_BYTES;
-    if (rows == kBlock) {
-      mma_tile<T, D, NW, STAGES, false>(kt, kt + C::TILE_BYTES, rows, qa, o, mrun, lrun, a.scale_log2, lane);
+    if (rows == kBlock && lo == 0) {
+      mma_tile<T, D, NW, STAGES, false>(kt, kt + C::TILE_BYTES, 0, rows, qa, o, mrun, lrun, a.scale_log2, lane);
     } else {
-      zero_tail_rows<D>(kt + C::TILE_BYTES, rows, lane);
-      mma_tile<T, D, NW, STAGES, true>(kt, kt + C::TILE_BYTES, rows, qa, o, mrun, lrun, a.scale_log2, lane);
+      zero_rows_outside<D>(kt + C::TILE_BYTES, lo, rows, lane);
+      mma_tile<T, D, NW, STAGES, true>(kt, kt + C::TILE_BYTES, lo, rows, qa, o, mrun, lrun, a.scale_log2, lane);
     }
     __syncwarp();
     if (k + STAGES < n_my) issue(k + STAGES);

@@ -399,16 +399,16 @@ paged_decode_sk_kernel(const SkArgs a, const __grid_constant__ CUtensorMap kmap,
 
     if constexpr (MMA) {
       if (tm.rows == kBlock) {
-        mma_tile<T, D, NW, STAGES, false>(kt, vt, tm.rows, qa, o, mr1, lr1, a.scale_log2, lane);
+        mma_tile<T, D, NW, STAGES, false>(kt, vt, 0, tm.rows, qa, o, mr1, lr1, a.scale_log2, lane);
       } else {
-        zero_tail_rows<D>(vt, tm.rows, lane);
-        mma_tile<T, D, NW, STAGES, true>(kt, vt, tm.rows, qa, o, mr1, lr1, a.scale_log2, lane);
+        zero_rows_outside<D>(vt, 0, tm.rows, lane);
+        mma_tile<T, D, NW, STAGES, true>(kt, vt, 0, tm.rows, qa, o, mr1, lr1, a.scale_log2, lane);
       }
     } else {
       if (tm.rows == kBlock)
-        decode_tile<T, D, G, NW, STAGES, false>(kt, vt, tm.rows, qf, acc, lsum, mrun, lane);
+        decode_tile<T, D, G, NW, STAGES, false>(kt, vt, 0, tm.rows, qf, acc, lsum, mrun, lane);
       else
-        decode_tile<T, D, G, NW, STAGES, true>(kt, vt, tm.rows, qf, acc, lsum, mrun, lane);
+        decode_tile<T, D, G, NW, STAGES, true>(kt, vt, 0, tm.rows, qf, acc, lsum, mrun, lane);
     }
     __syncwarp();
     if (k + STAGES < n) issue(k + STAGES);

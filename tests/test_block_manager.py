@@ -101,7 +101,12 @@ def test_random_trace_matches_oracle():
     cbm, obm = B.BlockManager(nb, order), OracleBlockManager(nb, initial_free_order=order)
     live, nxt = [], 0
     for it in range(2500):
-        op = int(rng.integers(0, 10))
+        op = int(rng.integers(0, 12))
+        if op >= 10 and live:             # sliding-window release
+            sid = live[int(rng.integers(len(live)))]
+            first = int(rng.integers(0, obm.length(sid) + 1))
+            assert cbm.release_before(sid, first) == obm.release_before(sid, first)
+            continue
         if op < 2 or not live:
             args, ops = (nxt, int(rng.integers(0, 70))), ("add_seq", "add_seq")
         elif op < 3:
@@ -183,3 +188,24 @@ def test_check_copy_pairs():
     for bad in ([[1, 2], [3, 2]], [[1, 2], [2, 3]], [[0, 6]], [[-1, 2]]):
         with pytest.raises(B.PagedKVError):
             B.check_copy_pairs(bad, 6)
+
+
+def test_release_before_matches_oracle_and_rejects_bad_positions():
+    order = list(range(12))
+    cbm, obm = B.BlockManager(12, order), OracleBlockManager(12, initial_free_order=order)
+    for bm in (cbm, obm):
+        bm.add_seq(1, 70)
+        bm.fork(1, 2)
+    assert cbm.release_before(1, 50) == obm.release_before(1, 50) == 3
+    assert cbm.release_before(2, 33) == obm.release_before(2, 33) == 2
+    _same_state(cbm, obm, [1, 2])
+    for bm in (cbm, obm):
+        bm.fork(1, 3)
+        bm.append_slot(3)
+        bm.free_seq(2)
+    _same_state(cbm, obm, [1, 3])
+    with pytest.raises(B.PagedKVError):
+        cbm.release_before(1, 71)
+    with pytest.raises(B.PagedKVError):
+        cbm.release_before(7, 0)
+    _same_state(cbm, obm, [1, 3])

@@ -33,6 +33,11 @@ Readings where the pages are silent:
   blocks are never copied, because appends only ever write the last block.
   The slot returned is table[L // 16] * 16 + L % 16 and L becomes L + 1.
 * Every failing call raises and leaves the state unchanged.
+* Beam search and shared prefixes (abeam.tech summary, "並列サンプリングや
+  ビームサーチでの共有" and the evaluation's shared-prefix workloads): a beam
+  step forks each new beam from its parent beam and drops the old beams; a
+  request whose prompt repeats another request's prefix shares the whole
+  blocks of that prefix. Both only move references, never data.
 * Sliding window (glossary entry, "他のKVキャッシュ最適化との組み合わせ"
   names sliding-window attention alongside paging): blocks wholly before the
   window are released (release_before); their table entries become -1 so
@@ -145,6 +150,57 @@ class OracleBlockManager:
             if self.refcount[b] == 0:
                 self.free.append(b)
         del self.lengths[seq_id]
+
+    def beam_reorder(self, old_ids, parents, new_ids):
+        """Beam search step: new beam i continues old beam old_ids[parents[i]]
+        (a fork: it shares that beam's blocks); afterwards every old beam is
+        dropped. Blocks no surviving beam holds go back on the free list (old
+        beams in the given order, each in table order). new_ids must be
+        distinct and may reuse ids of old beams only. Allocates nothing, so it
+        cannot run out of blocks."""
+        old_ids = [int(x) for x in old_ids]
+        parents = [int(x) for x in parents]
+        new_ids = [int(x) for x in new_ids]
+        if len(set(old_ids)) != len(old_ids) or any(o not in self.tables for o in old_ids):
+            raise InvalidArgument("old beams must be distinct live sequences")
+        if len(parents) != len(new_ids) or any(p < 0 or p >= len(old_ids) for p in parents):
+            raise InvalidArgument("one parent index into old_ids per new beam")
+        if len(set(new_ids)) != len(new_ids) or any(n in self.tables and n not in old_ids for n in new_ids):
+            raise InvalidArgument("new beam ids must be distinct and unused")
+        children = [(list(self.tables[old_ids[p]]), self.lengths[old_ids[p]]) for p in parents]
+        for table, _ in children:
+            for b in table:
+                if b >= 0:
+                    self.refcount[b] += 1
+        for o in old_ids:
+            self.free_seq(o)
+        for n, (table, length) in zip(new_ids, children):
+            self.tables[n] = table
+            self.lengths[n] = length
+
+    def add_seq_with_prefix(self, seq_id, num_tokens, donor, prefix_tokens):
+        """New sequence of num_tokens tokens whose first tokens repeat the first
+        prefix_tokens tokens of sequence `donor`: the whole blocks of that
+        common prefix are shared with the donor (refcount + 1), the rest are
+        fresh blocks. Returns the number of positions shared (a multiple of
+        16); the caller writes K/V from that position on."""
+        if seq_id in self.tables:
+            raise InvalidArgument(f"sequence {seq_id} exists")
+        if donor not in self.tables:
+            raise InvalidArgument(f"unknown sequence {donor}")
+        if num_tokens < 0 or prefix_tokens < 0:
+            raise InvalidArgument("num_tokens and prefix_tokens must be >= 0")
+        shared = min(prefix_tokens, num_tokens, self.lengths[donor]) // self.block_size
+        head = self.tables[donor][:shared]
+        if any(b < 0 for b in head):
+            raise InvalidArgument("the donor has released blocks of that prefix")
+        fresh = -(-num_tokens // self.block_size) - shared
+        self._need(fresh)
+        for b in head:
+            self.refcount[b] += 1
+        self.tables[seq_id] = list(head) + [self._pop() for _ in range(fresh)]
+        self.lengths[seq_id] = num_tokens
+        return shared * self.block_size
 
     def release_before(self, seq_id, first_token):
         """Sliding window: drop the sequence's hold on every block that lies

@@ -167,3 +167,128 @@ def test_cow_siblings_share_prefix_outputs():
         assert np.array_equal(shared[s], shared[0])
     grown = OA.paged_attention_decode(q, kp, vp, tables, np.full(n, prompt + 1, np.int32), 0.3, hkv, "f16")
     assert not np.array_equal(grown[1], grown[0])              # tails diverge after the write
+
+
+# ---- beam search and shared prefixes -------------------------------------------
+def _beam_golden(golden_dir):
+    import json as _json
+    with open(os.path.join(golden_dir, "beam_prefix_example.json")) as f:
+        return _json.load(f)
+
+
+def _check_refcounts(bm):
+    """Every block's refcount equals the number of live table entries naming it;
+    a block is free exactly when its refcount is 0."""
+    counts = [0] * bm.num_blocks
+    for t in bm.tables.values():
+        for b in t:
+            if b >= 0:
+                counts[b] += 1
+    assert counts == bm.refcount
+    assert sorted(bm.free) == [b for b in range(bm.num_blocks) if counts[b] == 0]
+
+
+def test_beam_step_golden(golden_dir):
+    ex = _beam_golden(golden_dir)
+    g = ex["beam"]
+    bm = OracleBlockManager(ex["num_blocks"])
+    bm.add_seq(0, g["prompt_tokens"])
+    bm.fork(0, 1)
+    bm.fork(0, 2)
+    res = [bm.append_slot(s) for s in (0, 1, 2)]
+    assert [r[0] for r in res] == g["first_append_slots"]
+    assert [[r[1], r[2]] for r in res if r[1] >= 0] == g["first_pairs"]
+    bm.beam_reorder(g["old_ids"], g["parents"], g["new_ids"])
+    assert {str(k): v for k, v in bm.tables.items()} == g["tables_after_reorder"]
+    for b, r in g["refcounts_after_reorder"].items():
+        assert bm.refcount[int(b)] == r
+    assert bm.free == g["free_after_reorder"]
+    res = [bm.append_slot(s) for s in g["new_ids"]]
+    assert [r[0] for r in res] == g["second_append_slots"]
+    assert [[r[1], r[2]] for r in res if r[1] >= 0] == g["second_pairs"]
+    _check_refcounts(bm)
+
+
+def test_prefix_sharing_golden(golden_dir):
+    ex = _beam_golden(golden_dir)
+    g = ex["prefix"]
+    bm = OracleBlockManager(ex["num_blocks"])
+    bm.add_seq(1, g["donor_tokens"])
+    assert bm.block_table(1) == g["donor_table"]
+    assert bm.add_seq_with_prefix(2, g["num_tokens"], 1, g["prefix_tokens"]) == g["shared_tokens"]
+    assert bm.block_table(2) == g["table"]
+    bm.free_seq(1)
+    assert bm.free == g["free_after_donor_freed"]
+    _check_refcounts(bm)
+
+
+def test_prefix_sharing_is_block_granular():
+    bm = OracleBlockManager(16)
+    bm.add_seq(1, 37)                                    # blocks 15, 14, 13
+    assert bm.add_seq_with_prefix(2, 100, 1, 31) == 16   # only one whole block in 31 tokens
+    assert bm.block_table(2)[0] == 15 and bm.refcount[14] == 1
+    assert bm.add_seq_with_prefix(3, 20, 1, 37) == 16    # capped by the new request's 20 tokens
+    assert bm.add_seq_with_prefix(4, 5, 1, 37) == 0      # shorter than a block: nothing shared
+    assert bm.add_seq_with_prefix(5, 64, 1, 64) == 32    # capped by the donor's 37 tokens
+    _check_refcounts(bm)
+    # a shared prefix block is copied on write like any shared block
+    bm.free_seq(2)
+    bm.free_seq(3)
+    bm.free_seq(4)
+    bm.free_seq(5)
+    _check_refcounts(bm)
+    assert bm.refcount[15] == 1
+
+
+def test_prefix_sharing_failures_leave_state_unchanged():
+    bm = OracleBlockManager(4)
+    bm.add_seq(1, 40)                                    # 3 blocks, 1 free
+    before = (list(bm.free), list(bm.refcount), {k: list(v) for k, v in bm.tables.items()})
+    with pytest.raises(OutOfBlocks):
+        bm.add_seq_with_prefix(2, 80, 1, 40)             # needs 5 - 2 = 3 fresh
+    with pytest.raises(InvalidArgument):
+        bm.add_seq_with_prefix(1, 10, 1, 10)             # id exists
+    with pytest.raises(InvalidArgument):
+        bm.add_seq_with_prefix(3, 10, 9, 10)             # unknown donor
+    assert (bm.free, bm.refcount, bm.tables) == before
+    bm.release_before(1, 16)
+    with pytest.raises(InvalidArgument):
+        bm.add_seq_with_prefix(3, 40, 1, 40)             # donor released its first block
+    assert 3 not in bm.tables and bm.tables[1][0] == -1
+    _check_refcounts(bm)
+
+
+def test_beam_reorder_rules():
+    bm = OracleBlockManager(32)
+    bm.add_seq(0, 33)
+    for c in (1, 2, 3):
+        bm.fork(0, c)
+    for s in range(4):
+        bm.append_slot(s)
+    # ids may be reused; beams that no one continues free their private blocks
+    bm.beam_reorder([0, 1, 2, 3], [3, 3, 0, 1], [0, 1, 2, 3])
+    assert bm.block_table(0) == bm.block_table(1)
+    _check_refcounts(bm)
+    free_before = bm.num_free()
+    with pytest.raises(InvalidArgument):
+        bm.beam_reorder([0, 1], [0, 2], [5, 6])          # parent index out of range
+    with pytest.raises(InvalidArgument):
+        bm.beam_reorder([0, 1], [0, 1], [5, 5])          # duplicate new ids
+    with pytest.raises(InvalidArgument):
+        bm.beam_reorder([0, 1], [0, 1], [2, 6])          # 2 is a live sequence outside old_ids
+    with pytest.raises(InvalidArgument):
+        bm.beam_reorder([0, 0], [0, 1], [5, 6])          # duplicate old ids
+    assert bm.num_free() == free_before
+    # multi-level: beams of beams, then everything is returned
+    for step in range(40):
+        olds = sorted(bm.tables)
+        rng = np.random.default_rng(step)
+        parents = rng.integers(0, len(olds), 4).tolist()
+        news = [100 * (step + 1) + i for i in range(4)]
+        bm.beam_reorder(olds, parents, news)
+        for n in news:
+            bm.append_slot(n)
+        _check_refcounts(bm)
+    for s in list(bm.tables):
+        bm.free_seq(s)
+    assert sorted(bm.free) == list(range(32))

@@ -1,7 +1,7 @@
 """Benchmark of the PagedAttention decode hot path on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload llama13b|llama3_8b|opt66b_sampling|opt175b_long|tiny]
+                    [--workload llama13b|llama3_8b|opt66b_sampling|opt175b_long|llama13b_beam|tiny]
                     [--kv native|int8] [--window W]
 
 One step is one pass of the whole hot path over one batch: write each
@@ -103,6 +103,29 @@ def build_workload(name, seed, device, kv="native", window=0):
         wl.description = (f"OPT-66B-shaped layer decode after parallel sampling: {trace.prompt_lens.size} prompts "
                           f"x n={trace.n} = {len(plan.seq_ids)} seqs, H=72 MHA, d=128, fp16, prompts U[512,1024], "
                           f"tails U[0,256], {len(plan.pairs)} copy-on-write pairs")
+        scale = trace.scale
+        unique_blocks = len({int(b) for b in tables.reshape(-1) if b >= 0})
+        wl.unique_kv_bytes = unique_blocks * hkv * 16 * d * 2 * 2
+    elif name == "llama13b_beam":
+        trace = W.beam_search_trace(seed)
+        nb = trace.block_budget()
+        bm = B.BlockManager(nb, W.shuffled_free_order(nb, seed))
+        W.beam_start(trace, bm)
+        hq, hkv, d, dtype = trace.num_q_heads, trace.num_kv_heads, trace.head_dim, trace.dtype
+        k_pool = W.normal_values((nb, hkv, 16, d), dtype, seed * 11 + 1, device)
+        v_pool = W.normal_values((nb, hkv, 16, d), dtype, seed * 11 + 2, device)
+        npairs = 0
+        for step in range(1, trace.steps + 1):
+            st = W.beam_step(trace, bm, step)
+            if st.pairs:
+                B.copy_blocks(k_pool, v_pool, torch.tensor(st.pairs, dtype=torch.int64, device=device))
+                npairs += len(st.pairs)
+            kt = W.normal_values((len(st.beam_ids), hkv, d), dtype, seed * 11 + 100 + step, device)
+            B.reshape_and_cache(kt, kt, k_pool, v_pool, torch.from_numpy(st.slots).to(device))
+        mb = -(-(int(trace.prompt_lens.max()) + trace.steps) // 16)
+        tables, lens = bm.block_tables(st.beam_ids, mb)
+        wl.description = (f"{trace.name}: decode over {len(st.beam_ids)} beams after {trace.steps} beam steps "
+                          f"({npairs} copy-on-write pairs)")
         scale = trace.scale
         unique_blocks = len({int(b) for b in tables.reshape(-1) if b >= 0})
         wl.unique_kv_bytes = unique_blocks * hkv * 16 * d * 2 * 2
@@ -606,7 +629,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama13b",
-                    choices=["llama13b", "llama3_8b", "opt66b_sampling", "opt175b_long", "tiny"])
+                    choices=["llama13b", "llama3_8b", "opt66b_sampling", "opt175b_long", "llama13b_beam", "tiny"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--window", type=int, default=0,
                     help="sliding-window decode over the last W tokens of each sequence (0 = full attention)")

@@ -384,6 +384,38 @@ pkv_status_t pkv_bm_append_slots(pkv_bm_t* bm, const int64_t* seq_ids, int n,
 pkv_status_t pkv_bm_free_seq(pkv_bm_t* bm, int64_t seq_id);
 
 /*
+ * Beam search step ([S] "並列サンプリングやビームサーチでの共有": beams share
+ * blocks and copy a shared block only when a write reaches it): new beam i
+ * (id new_ids[i]) continues old beam old_ids[parents[i]] -- it takes a copy of
+ * that beam's table and length, each live block's refcount + 1 -- and then
+ * every old beam is dropped (in the given order, blocks in table order;
+ * blocks whose refcount reaches 0 return to the free list). Beams of beams
+ * nest to any depth. old_ids must be distinct live sequences; new_ids
+ * distinct, each either unused or one of old_ids. Allocates nothing, so it
+ * never runs out of blocks; the next pkv_bm_append_slots emits the copies.
+ * Host memory; all-or-nothing (PKV_ERR_INVALID_ARG leaves the state as is).
+ */
+pkv_status_t pkv_bm_beam_reorder(pkv_bm_t* bm, const int64_t* old_ids, int num_old,
+                                 const int32_t* parents, const int64_t* new_ids,
+                                 int num_new);
+
+/*
+ * Block-granular prefix sharing across requests (the shared-prefix workloads
+ * of [S]; sharing by reference count, [B] "OSの知恵をGPUへ"): a new sequence
+ * of num_tokens tokens whose first prefix_tokens tokens repeat those of
+ * sequence `donor`. The whole blocks of that common prefix,
+ * n = min(prefix_tokens, num_tokens, donor length) / 16 (rounded down), are
+ * shared with the donor (refcount + 1); ceil(num_tokens/16) - n fresh blocks
+ * follow. *shared_tokens_out (may be NULL) = 16 * n: the caller writes K/V
+ * for positions from there on. PKV_ERR_OUT_OF_BLOCKS if the fresh blocks are
+ * not free; PKV_ERR_INVALID_ARG for an existing seq_id, an unknown donor or a
+ * prefix block the donor has released. All-or-nothing.
+ */
+pkv_status_t pkv_bm_add_seq_with_prefix(pkv_bm_t* bm, int64_t seq_id, int64_t num_tokens,
+                                        int64_t donor, int64_t prefix_tokens,
+                                        int64_t* shared_tokens_out);
+
+/*
  * Sliding window ([G] "他のKVキャッシュ最適化との組み合わせ": sliding-window
  * attention combined with paging): drops the sequence's hold on every block
  * wholly before position first_token (table entries j with

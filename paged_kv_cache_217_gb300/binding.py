@@ -76,6 +76,8 @@ _SIGS = {
     "pkv_bm_append_slots": ([_c_p, _c_p, _c_int, _c_p, _c_p, _c_p], _c_int),
     "pkv_bm_free_seq": ([_c_p, _c_i64], _c_int),
     "pkv_bm_release_before": ([_c_p, _c_i64, _c_i64, _c_p], _c_int),
+    "pkv_bm_beam_reorder": ([_c_p, _c_p, _c_int, _c_p, _c_p, _c_int], _c_int),
+    "pkv_bm_add_seq_with_prefix": ([_c_p, _c_i64, _c_i64, _c_i64, _c_i64, _c_p], _c_int),
     "pkv_bm_block_tables": ([_c_p, _c_p, _c_int, _c_int, _c_p, _c_p], _c_int),
     "pkv_bm_refcount": ([_c_p, _c_int, _c_p], _c_int),
     "pkv_bm_seq_len": ([_c_p, _c_i64, _c_p], _c_int),
@@ -468,6 +470,22 @@ class BlockManager:
 
     def free_seq(self, seq_id):
         _check(lib().pkv_bm_free_seq(self._h, int(seq_id)), "bm_free_seq")
+
+    def beam_reorder(self, old_ids, parents, new_ids):
+        """Beam step: new beam i continues old beam old_ids[parents[i]]; the old beams are dropped."""
+        o = np.ascontiguousarray(np.asarray(old_ids, dtype=np.int64))
+        p = np.ascontiguousarray(np.asarray(parents, dtype=np.int32))
+        n = np.ascontiguousarray(np.asarray(new_ids, dtype=np.int64))
+        _check(lib().pkv_bm_beam_reorder(self._h, o.ctypes.data, o.shape[0], p.ctypes.data, n.ctypes.data,
+                                         n.shape[0]), "bm_beam_reorder")
+
+    def add_seq_with_prefix(self, seq_id, num_tokens, donor, prefix_tokens):
+        """New sequence sharing the whole blocks of its common prefix with `donor`;
+        returns the number of shared positions (a multiple of 16)."""
+        out = ctypes.c_int64()
+        _check(lib().pkv_bm_add_seq_with_prefix(self._h, int(seq_id), int(num_tokens), int(donor),
+                                                int(prefix_tokens), ctypes.byref(out)), "bm_add_seq_with_prefix")
+        return out.value
 
     def release_before(self, seq_id, first_token):
         """Drops the sequence's hold on blocks wholly before position first_token

@@ -209,6 +209,80 @@ pkv_status_t pkv_bm_free_seq(pkv_bm_t* bm, int64_t seq_id) {
   return pkv::ok();
 }
 
+pkv_status_t pkv_bm_beam_reorder(pkv_bm_t* bm, const int64_t* old_ids, int num_old, const int32_t* parents,
+                                const int64_t* new_ids, int num_new) {
+  if (!bm || num_old < 0 || num_new < 0 || (num_old > 0 && !old_ids) || (num_new > 0 && (!parents || !new_ids)))
+    return pkv::fail(PKV_ERR_INVALID_ARG, "bm_beam_reorder: bad argument");
+  // Validate everything before touching the state.
+  std::unordered_map<int64_t, int> old_index;
+  for (int i = 0; i < num_old; ++i) {
+    if (!bm->seqs.count(old_ids[i]) || !old_index.emplace(old_ids[i], i).second)
+      return pkv::fail(PKV_ERR_INVALID_ARG, "bm_beam_reorder: old beam %lld is unknown or repeated",
+                       (long long)old_ids[i]);
+  }
+  std::unordered_map<int64_t, int> seen_new;
+  for (int i = 0; i < num_new; ++i) {
+    if (parents[i] < 0 || parents[i] >= num_old)
+      return pkv::fail(PKV_ERR_INVALID_ARG, "bm_beam_reorder: parent %d of new beam %d outside [0, %d)",
+                       int(parents[i]), i, num_old);
+    if (!seen_new.emplace(new_ids[i], i).second)
+      return pkv::fail(PKV_ERR_INVALID_ARG, "bm_beam_reorder: new beam id %lld repeated", (long long)new_ids[i]);
+    if (bm->seqs.count(new_ids[i]) && !old_index.count(new_ids[i]))
+      return pkv::fail(PKV_ERR_INVALID_ARG, "bm_beam_reorder: new beam id %lld is a live sequence",
+                       (long long)new_ids[i]);
+  }
+  // Children copy their parents' tables (references only), then the old beams go.
+  std::vector<pkv_bm::Seq> children;
+  children.reserve(size_t(num_new));
+  for (int i = 0; i < num_new; ++i) {
+    children.push_back(bm->seqs.find(old_ids[parents[i]])->second);
+    for (int32_t b : children.back().table)
+      if (b >= 0) bm->refcount[b] += 1;
+  }
+  for (int i = 0; i < num_old; ++i) {
+    auto it = bm->seqs.find(old_ids[i]);
+    for (int32_t b : it->second.table)
+      if (b >= 0) bm->release(b);
+    bm->seqs.erase(it);
+  }
+  for (int i = 0; i < num_new; ++i) bm->seqs.emplace(new_ids[i], std::move(children[size_t(i)]));
+  return pkv::ok();
+}
+
+pkv_status_t pkv_bm_add_seq_with_prefix(pkv_bm_t* bm, int64_t seq_id, int64_t num_tokens, int64_t donor,
+                                        int64_t prefix_tokens, int64_t* shared_tokens_out) {
+  if (!bm) return pkv::fail(PKV_ERR_INVALID_ARG, "bm_add_seq_with_prefix: NULL handle");
+  if (num_tokens < 0 || prefix_tokens < 0)
+    return pkv::fail(PKV_ERR_INVALID_ARG, "bm_add_seq_with_prefix: negative size");
+  if (bm->seqs.count(seq_id))
+    return pkv::fail(PKV_ERR_INVALID_ARG, "bm_add_seq_with_prefix: sequence %lld exists", (long long)seq_id);
+  auto dit = bm->seqs.find(donor);
+  if (dit == bm->seqs.end())
+    return pkv::fail(PKV_ERR_INVALID_ARG, "bm_add_seq_with_prefix: unknown donor %lld", (long long)donor);
+  const pkv_bm::Seq& d = dit->second;
+  const int64_t shared = std::min(std::min(prefix_tokens, num_tokens), d.len) / PKV_BLOCK_SIZE;
+  for (int64_t j = 0; j < shared; ++j)
+    if (d.table[size_t(j)] < 0)
+      return pkv::fail(PKV_ERR_INVALID_ARG, "bm_add_seq_with_prefix: the donor released block %lld of the prefix",
+                       (long long)j);
+  const int64_t fresh = (num_tokens + PKV_BLOCK_SIZE - 1) / PKV_BLOCK_SIZE - shared;
+  if (fresh > int64_t(bm->free_stack.size()))
+    return pkv::fail(PKV_ERR_OUT_OF_BLOCKS, "bm_add_seq_with_prefix: need %lld fresh blocks, %zu free",
+                     (long long)fresh, bm->free_stack.size());
+  pkv_bm::Seq s;
+  s.table.reserve(size_t(shared + fresh) + 1);
+  for (int64_t j = 0; j < shared; ++j) {
+    const int32_t b = d.table[size_t(j)];
+    bm->refcount[b] += 1;
+    s.table.push_back(b);
+  }
+  for (int64_t j = 0; j < fresh; ++j) s.table.push_back(bm->pop());
+  s.len = num_tokens;
+  bm->seqs.emplace(seq_id, std::move(s));  // d is not used after this point (rehash)
+  if (shared_tokens_out) *shared_tokens_out = shared * PKV_BLOCK_SIZE;
+  return pkv::ok();
+}
+
 pkv_status_t pkv_bm_release_before(pkv_bm_t* bm, int64_t seq_id, int64_t first_token, int* released_out) {
   if (!bm) return pkv::fail(PKV_ERR_INVALID_ARG, "bm_release_before: NULL handle");
   auto it = bm->seqs.find(seq_id);

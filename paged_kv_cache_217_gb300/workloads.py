@@ -266,3 +266,93 @@ def drive_parallel_sampling(trace, bm):
         steps.append((active, slots))
     final = {sid: int(trace.prompt_lens[sid // n]) + tails[sid] for sid in seq_ids}
     return SamplingPlan(seq_ids, prompt_of, steps, pairs, final)
+
+
+@dataclass
+class BeamSearchTrace:
+    """Beam search: prompts, a beam width, and per step the parent beam of
+    every new beam (a seeded, skewed choice: a few strong beams tend to
+    survive, as in beam search)."""
+    name: str
+    dtype: str
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    prompt_lens: np.ndarray    # int32 [num_prompts]
+    parents: np.ndarray        # int32 [steps, num_prompts, width]
+    scale: float = field(default=None)
+
+    def __post_init__(self):
+        if self.scale is None:
+            self.scale = 1.0 / math.sqrt(self.head_dim)
+
+    @property
+    def width(self):
+        return int(self.parents.shape[2])
+
+    @property
+    def steps(self):
+        return int(self.parents.shape[0])
+
+    def block_budget(self, block_size=BLOCK_SIZE):
+        """An upper bound on the blocks the trace can hold at once: every beam
+        private from the prompt's last block on, plus the prompt."""
+        per_beam = -(-(self.steps + block_size) // block_size) + 1
+        return int((-(-self.prompt_lens // block_size)).sum() + self.prompt_lens.size * self.width * per_beam)
+
+
+def beam_search_trace(seed=0, num_prompts=16, width=4, steps=64, prompt_range=(512, 1024),
+                      num_heads=40, head_dim=128, dtype="bf16"):
+    """LLaMA-13B-shaped layer (40 heads MHA, head_dim 128, bf16): 16 prompts of
+    U[512, 1024] tokens, beam width 4, 64 beam steps."""
+    rng = np.random.default_rng(seed)
+    prompts = rng.integers(prompt_range[0], prompt_range[1], size=num_prompts, endpoint=True).astype(np.int32)
+    weights = np.array([2.0 ** -i for i in range(width)])
+    weights /= weights.sum()
+    parents = np.sort(rng.choice(width, size=(steps, num_prompts, width), p=weights), axis=2).astype(np.int32)
+    return BeamSearchTrace(f"LLaMA-13B layer beam search: {num_prompts} prompts x width {width}, {steps} steps, "
+                           f"H=40, d=128, bf16, prompts U[{prompt_range[0]},{prompt_range[1]}]", dtype,
+                           num_heads, num_heads, head_dim, prompts, parents)
+
+
+@dataclass
+class BeamStep:
+    beam_ids: list             # beams after the step's reorder, prompt-major
+    slots: np.ndarray          # int64 slot of each beam's new token
+    pairs: list                # copy-on-write (src, dst) pairs of the step's appends
+
+
+def beam_ids(trace, step):
+    """Beam ids alive after `step` reorders (step 0 = the initial fork)."""
+    return [(i * (trace.steps + 1) + step) * trace.width + j for i in range(trace.prompt_lens.size)
+            for j in range(trace.width)]
+
+
+def beam_start(trace, bm):
+    """Adds every prompt and forks it into `width` beams (any block manager with
+    add_seq / fork / free_seq). Returns the initial beam ids."""
+    ids = beam_ids(trace, 0)
+    for i, plen in enumerate(trace.prompt_lens.tolist()):
+        root = ids[i * trace.width]
+        bm.add_seq(root, plen)
+        for j in range(1, trace.width):
+            bm.fork(root, ids[i * trace.width + j])
+    return ids
+
+
+def beam_step(trace, bm, step):
+    """Step `step` (1-based) of the script: each prompt's beams are reordered by
+    the trace's parents, then every beam appends one token (append_slot, in
+    beam order). Returns a BeamStep."""
+    old, new = beam_ids(trace, step - 1), beam_ids(trace, step)
+    w = trace.width
+    for i in range(trace.prompt_lens.size):
+        bm.beam_reorder(old[i * w:(i + 1) * w], trace.parents[step - 1, i].tolist(), new[i * w:(i + 1) * w])
+    slots = np.empty(len(new), dtype=np.int64)
+    pairs = []
+    for k, sid in enumerate(new):
+        slot, src, dst = bm.append_slot(sid)
+        slots[k] = slot
+        if src >= 0:
+            pairs.append((src, dst))
+    return BeamStep(new, slots, pairs)

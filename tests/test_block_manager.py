@@ -209,3 +209,96 @@ def test_release_before_matches_oracle_and_rejects_bad_positions():
     with pytest.raises(B.PagedKVError):
         cbm.release_before(7, 0)
     _same_state(cbm, obm, [1, 3])
+
+
+def test_beam_and_prefix_golden(golden_dir):
+    with open(os.path.join(golden_dir, "beam_prefix_example.json")) as f:
+        ex = json.load(f)
+    g = ex["beam"]
+    bm = B.BlockManager(ex["num_blocks"])
+    bm.add_seq(0, g["prompt_tokens"])
+    bm.fork(0, 1)
+    bm.fork(0, 2)
+    slots, pairs = bm.append_slots([0, 1, 2])
+    assert slots.tolist() == g["first_append_slots"] and pairs.tolist() == g["first_pairs"]
+    bm.beam_reorder(g["old_ids"], g["parents"], g["new_ids"])
+    for s, t in g["tables_after_reorder"].items():
+        assert bm.block_table(int(s)) == t
+    for b, r in g["refcounts_after_reorder"].items():
+        assert bm.refcount(int(b)) == r
+    assert bm.free_stack() == g["free_after_reorder"]
+    slots, pairs = bm.append_slots(g["new_ids"])
+    assert slots.tolist() == g["second_append_slots"] and pairs.tolist() == g["second_pairs"]
+
+    p = ex["prefix"]
+    bm = B.BlockManager(ex["num_blocks"])
+    bm.add_seq(1, p["donor_tokens"])
+    assert bm.add_seq_with_prefix(2, p["num_tokens"], 1, p["prefix_tokens"]) == p["shared_tokens"]
+    assert bm.block_table(2) == p["table"]
+    bm.free_seq(1)
+    assert bm.free_stack() == p["free_after_donor_freed"]
+
+
+def test_beam_and_prefix_random_trace_matches_oracle():
+    rng = np.random.default_rng(21)
+    nb = 200
+    order = rng.permutation(nb)
+    cbm, obm = B.BlockManager(nb, order), OracleBlockManager(nb, initial_free_order=order)
+    live, nxt = [], 0
+    for it in range(1500):
+        op = int(rng.integers(0, 10))
+        c_exc = o_exc = None
+        if op < 2 or not live:
+            donor = live[int(rng.integers(len(live)))] if live and op == 1 else None
+            n, pre = int(rng.integers(0, 90)), int(rng.integers(0, 90))
+            calls = (("add_seq_with_prefix", (nxt, n, donor, pre)) if donor is not None
+                     else ("add_seq", (nxt, n)))
+        elif op < 4:
+            k = int(rng.integers(1, min(len(live), 4) + 1))
+            olds = [live[i] for i in rng.choice(len(live), k, replace=False)]
+            width = int(rng.integers(1, 5))
+            parents = rng.integers(0, k, width).tolist()
+            news = [nxt + i for i in range(width)]
+            calls = ("beam_reorder", (olds, parents, news))
+        elif op < 5:
+            calls = ("free_seq", (live[int(rng.integers(len(live)))],))
+        else:
+            calls = ("append_slot", (live[int(rng.integers(len(live)))],))
+        name, args = calls
+        try:
+            cres = getattr(cbm, name)(*args)
+        except B.OutOfBlocks as e:
+            c_exc = e
+        try:
+            ores = getattr(obm, name)(*args)
+        except OracleOOB as e:
+            o_exc = e
+        assert (c_exc is None) == (o_exc is None), f"step {it}: {name}{args}"
+        if c_exc is None:
+            assert cres == ores, f"step {it}: {name}{args}"
+            if name in ("add_seq", "add_seq_with_prefix"):
+                live.append(nxt)
+                nxt += 1
+            elif name == "beam_reorder":
+                for o in args[0]:
+                    live.remove(o)
+                live.extend(args[2])
+                nxt += len(args[2])
+            elif name == "free_seq":
+                live.remove(args[0])
+        if it % 25 == 0:
+            _same_state(cbm, obm, live)
+    _same_state(cbm, obm, live)
+
+
+def test_beam_reorder_rejects_bad_arguments_atomically():
+    bm = B.BlockManager(16)
+    bm.add_seq(0, 20)
+    bm.fork(0, 1)
+    before = (bm.free_stack(), [bm.refcount(b) for b in range(16)])
+    for olds, parents, news in (([0, 1], [2], [5]), ([0, 1], [0, 1], [7, 7]), ([0, 0], [0], [5]),
+                                ([0, 9], [0], [5]), ([0], [0], [1])):
+        with pytest.raises(B.PagedKVError):
+            bm.beam_reorder(olds, parents, news)
+    assert (bm.free_stack(), [bm.refcount(b) for b in range(16)]) == before
+    assert bm.num_seqs() == 2

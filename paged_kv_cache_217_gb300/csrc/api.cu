@@ -184,6 +184,24 @@ pkv_status_t pool_tensor_map(CUtensorMap* map, const void* pool, int64_t rows, i
   return PKV_OK;
 }
 
+// An INT8 code pool seen as a 2-D uint8 tensor of num_blocks*num_kv_heads*16
+// rows by head_dim columns, read in boxes of 16 rows x min(head_dim, 128)
+// bytes with the 128-byte swizzle (the 64-byte one for 64-byte rows).
+pkv_status_t code_tensor_map(CUtensorMap* map, const void* pool, int64_t rows, int head_dim) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return pkv::fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const cuuint64_t dims[2] = {cuuint64_t(head_dim), cuuint64_t(rows)};
+  const cuuint64_t strides[1] = {cuuint64_t(head_dim)};
+  const cuuint32_t box[2] = {cuuint32_t(head_dim < 128 ? head_dim : 128), PKV_BLOCK_SIZE};
+  const cuuint32_t elem_strides[2] = {1, 1};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(pool), dims, strides, box,
+                         elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         head_dim < 128 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return pkv::fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled (uint8) failed (CUresult %d)", int(r));
+  return PKV_OK;
+}
+
 pkv_status_t cuda_status(cudaError_t err, const char* what) {
   if (err == cudaSuccess) return pkv::ok();
   return pkv::fail(PKV_ERR_CUDA, "%s: %s", what, cudaGetErrorString(err));
@@ -482,12 +500,20 @@ pkv_status_t pkv_paged_attention_decode_int8(void* out, const void* q, const int
   a.max_parts = plan.max_parts;
   a.long_first = int64_t(num_seqs) * num_kv_heads * plan.max_parts <= kLongFirstMaxCtas ? 1 : 0;
   a.scale_log2 = scale * 1.4426950408889634f;
+  alignas(64) CUtensorMap kmap, vmap;
+  if (pkv::decode_int8_uses_tensor_maps()) {
+    const int64_t rows = int64_t(num_blocks) * num_kv_heads * PKV_BLOCK_SIZE;
+    st = code_tensor_map(&kmap, k_cache, rows, head_dim);
+    if (st != PKV_OK) return st;
+    st = code_tensor_map(&vmap, v_cache, rows, head_dim);
+    if (st != PKV_OK) return st;
+  }
   cudaError_t err = cudaSuccess;
   if (need > 0) {
     err = cudaMemsetAsync(a.counters, 0, lay.counter_bytes, stream);
     if (err != cudaSuccess) return cuda_status(err, "clear split-K counters");
   }
-  err = pkv::launch_decode_int8(a, dtype == PKV_BF16, head_dim, round_pow2_group(group), stream);
+  err = pkv::launch_decode_int8(a, dtype == PKV_BF16, head_dim, round_pow2_group(group), &kmap, &vmap, stream);
   return cuda_status(err, "paged_attention_decode_int8 launch");
 }
 

@@ -48,11 +48,16 @@ cudaError_t launch_copy_blocks_bytes(void* k_pool, void* v_pool, const int64_t* 
                                      cudaStream_t stream);
 
 // INT8 KV cache: quantising cache write (head_dim 64, 128 or 256) and decode
-// over int8 codes with per-row fp32 scales (CUDA-core kernel, every gpad).
+// over int8 codes with per-row fp32 scales. The tensor-core kernel reads the
+// code pools through uint8 tensor maps (boxes of 16 rows x min(D, 128) bytes,
+// 128-byte swizzle, 64-byte at D = 64); decode_int8_uses_tensor_maps() says
+// whether the build needs them.
 cudaError_t launch_reshape_and_cache_int8(const void* k, const void* v, bool bf16, int8_t* k_codes,
                                           int8_t* v_codes, float* k_scale, float* v_scale, const int64_t* slots,
                                           int num_tokens, int num_kv_heads, int head_dim, int num_blocks,
                                           unsigned int* status, cudaStream_t stream);
-cudaError_t launch_decode_int8(const DecodeArgs& a, bool bf16, int head_dim, int gpad, cudaStream_t stream);
+bool decode_int8_uses_tensor_maps();
+cudaError_t launch_decode_int8(const DecodeArgs& a, bool bf16, int head_dim, int gpad, const CUtensorMap* kmap,
+                               const CUtensorMap* vmap, cudaStream_t stream);
 
 }  // namespace pkv

@@ -59,6 +59,8 @@ KERNEL_SOURCES = ["paged_kv_cache_217_gb300/csrc/decode.cuh",
                   "paged_kv_cache_217_gb300/csrc/decode_sk.cuh",
                   "paged_kv_cache_217_gb300/csrc/device_common.cuh",
                   "paged_kv_cache_217_gb300/csrc/decode_launch.cuh",
+                  "paged_kv_cache_217_gb300/csrc/decode_mma_int8.cuh",
+                  "paged_kv_cache_217_gb300/csrc/decode_int8.cu",
                   "paged_kv_cache_217_gb300/csrc/api.cu"]
 
 

@@ -57,6 +57,28 @@ cudaError_t launch_pdl(K kern, dim3 grid, dim3 block, size_t smem, cudaStream_t 
   return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
+// Ring shape of the CUDA-core kernel for wide grids: with at least
+// kWideGridCtas CTAs (13+ waves; the OPT-66B parallel-sampling batch has
+// 9216) six warps with one stage each -- 4 CTAs, 24 warps per SM instead of
+// 3 CTAs of 4 warps x 2 stages -- hide latency better: measured on GB300,
+// 341 -> 299 us on that batch, whose sibling samples share prompt blocks
+// through L2, against 1-1.4 % slower on the LLaMA-13B and OPT-175B layers,
+// which keep the two-stage ring.
+#ifndef PKV_WIDE_GRID_WARPS
+#define PKV_WIDE_GRID_WARPS 6
+#endif
+constexpr int64_t kWideGridCtas = 8192;
+
+template <typename T, int D, int G, int NW, int STAGES>
+cudaError_t launch_cuda_core_grid(const DecodeArgs& a, dim3 grid, cudaStream_t stream) {
+  using C = DecodeCfg<T, D, G, NW, STAGES>;
+  auto kern = paged_decode_kernel<T, D, G, NW, STAGES>;
+  static bool configured[kMaxDevices] = {};
+  cudaError_t err = configure_once(kern, C::SMEM_BYTES, configured);
+  if (err != cudaSuccess) return err;
+  return launch_pdl(kern, grid, dim3(NW * 32), C::SMEM_BYTES, stream, a);
+}
+
 template <typename T, int D, int G>
 cudaError_t launch_decode_dg(const DecodeArgs& a, const CUtensorMap* kmap, const CUtensorMap* vmap,
                              cudaStream_t stream) {
@@ -66,11 +88,11 @@ cudaError_t launch_decode_dg(const DecodeArgs& a, const CUtensorMap* kmap, const
   const dim3 grid(kSeqFastest ? unsigned(a.num_seqs) : unsigned(a.num_kv_heads),
                   kSeqFastest ? unsigned(a.num_kv_heads) : unsigned(a.num_seqs), unsigned(a.max_parts));
   if constexpr (G == 1 && !PKV_MMA_FOR_MHA) {
-    using C = DecodeCfg<T, D, G, NW, STAGES>;
-    auto kern = paged_decode_kernel<T, D, G, NW, STAGES>;
-    cudaError_t err = configure_once(kern, C::SMEM_BYTES, configured);
-    if (err != cudaSuccess) return err;
-    err = launch_pdl(kern, grid, dim3(NW * 32), C::SMEM_BYTES, stream, a);
+    const int64_t ctas = int64_t(a.num_seqs) * a.num_kv_heads * a.max_parts;
+    cudaError_t err = (PKV_WIDE_GRID_WARPS > 0 && ctas >= kWideGridCtas)
+                          ? launch_cuda_core_grid<T, D, G, (PKV_WIDE_GRID_WARPS > 0 ? PKV_WIDE_GRID_WARPS : 1), 1>(
+                                a, grid, stream)
+                          : launch_cuda_core_grid<T, D, G, NW, STAGES>(a, grid, stream);
     if (err != cudaSuccess) return err;
   } else {
     using C = MmaCfg<T, D, NW, STAGES>;

@@ -305,3 +305,16 @@ def test_full_size_parallel_sampling():
         full = int(trace.prompt_lens[i]) // 16
         for c in range(1, n):
             assert np.array_equal(t[i * n + c, :full], t[i * n, :full])
+
+
+@pytest.mark.parametrize("dtype,d", [("f16", 64), ("bf16", 128)])
+@pytest.mark.parametrize("partition", [0, 32])
+def test_wide_grid_ring_shape(dtype, d, partition):
+    # 256 sequences x 40 KV heads = 10240 CTAs: the CUDA-core kernel runs its
+    # six-warp, one-stage ring (with 32-token partitions the split grid is wider still)
+    rng = np.random.default_rng(5)
+    lens = rng.integers(1, 120, 256).astype(np.int32)
+    case = H.make_case(lens, 40, 40, d, dtype, seed=31)
+    out = _run(case, partition)
+    _check_sampled(case, out, 40, seed=6)
+    assert B.device_status(clear=True) == 0

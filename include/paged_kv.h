@@ -155,6 +155,16 @@ pkv_status_t pkv_selftest_bounded_wait(uint32_t limit_us, pkv_stream_t stream);
  * may be reused by calls of any shape; calls that use one workspace must not
  * overlap on the GPU.
  *
+ * Launch order: grids of at most 4096 CTAs start the sequences of at least
+ * twice the batch's mean length first. For batches of 128 to 1024 sequences
+ * that order is computed once, by a one-CTA kernel launched on `stream`
+ * ahead of the decode, into num_seqs int32 at the end of the workspace.
+ * That kernel reads context_lens without waiting for the previous kernel on
+ * the stream to finish when that kernel allows programmatic early launch
+ * (the library's cache writes do, and never touch context_lens): a kernel
+ * that writes context_lens and allows early launch must not directly
+ * precede this call.
+ *
  * Group size 1 runs on the CUDA cores; groups of 2..8 query heads per KV head
  * run the QK and PV products of each 16-token tile on the tensor cores (fp32
  * accumulation; the softmax weights enter as two 16-bit terms, keeping about
@@ -168,8 +178,10 @@ pkv_status_t pkv_paged_attention_decode(
     int partition_size, void* workspace, size_t workspace_bytes,
     pkv_stream_t stream);
 
-/* Bytes of workspace pkv_paged_attention_decode needs for these sizes
- * (0 when the call runs in one pass). Returns 0 for invalid sizes as well. */
+/* Bytes of workspace pkv_paged_attention_decode needs for these sizes: the
+ * split-K partials and counters, plus the launch order of batches of 128 to
+ * 1024 sequences (see above); 0 for one-pass calls without either. Returns 0
+ * for invalid sizes as well. */
 size_t pkv_paged_attention_workspace_size(
     int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
     int max_blocks_per_seq, int partition_size);

@@ -79,6 +79,27 @@ int choose_partition(int num_seqs, int num_q_heads, int num_kv_heads, int head_d
   return p >= max_ctx ? -1 : int(p);
 }
 
+// For batches of at least kOrderKernelMinSeqs sequences the long-first order
+// (grid row -> sequence) is computed once by a one-CTA kernel into the
+// workspace instead of by every CTA, which costs each CTA a read of all the
+// lengths and a CTA-wide ranking. Measured on GB300: Llama-3-8B layer (256
+// sequences) 44.5 -> 43.4 us, its INT8 cache 43.2 -> 41.3 us; on the 64-
+// sequence LLaMA-13B layer the extra launch cost 0.9 %, so small batches keep
+// ranking in each CTA.
+#ifndef PKV_ORDER_KERNEL
+#define PKV_ORDER_KERNEL 1
+#endif
+constexpr int kOrderKernelMinSeqs = 128;
+bool long_first_grid(int num_seqs, int num_kv_heads, int max_parts) {
+  return int64_t(num_seqs) * num_kv_heads * max_parts <= kLongFirstMaxCtas;
+}
+size_t order_bytes(int num_seqs, int num_kv_heads, int max_parts) {
+  if (!PKV_ORDER_KERNEL || num_seqs < kOrderKernelMinSeqs || num_seqs > pkv::kOrderMaxSeqs ||
+      !long_first_grid(num_seqs, num_kv_heads, max_parts))
+    return 0;
+  return (size_t(num_seqs) * sizeof(int32_t) + 15) / 16 * 16;
+}
+
 bool balanced_fits(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim) {
   const int group = num_kv_heads > 0 ? num_q_heads / num_kv_heads : 0;
   int gpad = 1;
@@ -257,7 +278,8 @@ size_t pkv_paged_attention_workspace_size(int num_seqs, int num_q_heads, int num
     if (num_q_heads % num_kv_heads != 0) return 0;
     return sk_layout(num_seqs, num_q_heads, num_kv_heads, head_dim).total;
   }
-  return split_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, plan.max_parts).total;
+  return split_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, plan.max_parts).total +
+         order_bytes(num_seqs, num_kv_heads, plan.max_parts);
 }
 
 }  // extern "C"
@@ -311,7 +333,8 @@ pkv_status_t decode_impl(void* out, const void* q, const void* k_pool, const voi
                      pkv::decode_sk_max_seqs(head_dim, round_pow2_group(group)));
   const SplitLayout lay = split_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, plan.max_parts);
   const SkLayout sk = sk_layout(num_seqs, num_q_heads, num_kv_heads, head_dim);
-  const size_t need = balanced ? sk.total : lay.total;
+  const size_t ord = balanced ? 0 : order_bytes(num_seqs, num_kv_heads, plan.max_parts);
+  const size_t need = balanced ? sk.total : lay.total + ord;
   if (int64_t(num_blocks) * num_kv_heads * PKV_BLOCK_SIZE > INT32_MAX)
     return pkv::fail(PKV_ERR_UNSUPPORTED, "num_blocks * num_kv_heads * 16 exceeds 2^31 rows");
   if (need > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, 16)))
@@ -366,10 +389,12 @@ pkv_status_t decode_impl(void* out, const void* q, const void* k_pool, const voi
   a.v_pool = v_pool;
   a.block_tables = block_tables;
   a.context_lens = context_lens;
-  a.part_o = need > 0 ? static_cast<float*>(workspace) : nullptr;
-  a.part_ml = need > 0 ? reinterpret_cast<float2*>(static_cast<char*>(workspace) + lay.ml_offset) : nullptr;
-  a.counters = need > 0 ? reinterpret_cast<unsigned int*>(static_cast<char*>(workspace) + lay.counter_offset)
-                        : nullptr;
+  a.part_o = lay.total > 0 ? static_cast<float*>(workspace) : nullptr;
+  a.part_ml = lay.total > 0 ? reinterpret_cast<float2*>(static_cast<char*>(workspace) + lay.ml_offset) : nullptr;
+  a.counters = lay.total > 0 ? reinterpret_cast<unsigned int*>(static_cast<char*>(workspace) + lay.counter_offset)
+                             : nullptr;
+  int32_t* order = ord > 0 ? reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + lay.total) : nullptr;
+  a.order = order;
   a.status = status;
   a.num_seqs = num_seqs;
   a.num_q_heads = num_q_heads;
@@ -383,15 +408,20 @@ pkv_status_t decode_impl(void* out, const void* q, const void* k_pool, const voi
   // microsecond); it pays off only when the grid has few waves, where a long
   // sequence started last sets the end time (measured on GB300: -9 % on the
   // LLaMA-13B layer at 2560 CTAs, +7 % on the OPT-66B sampling batch at 9216).
-  a.long_first = int64_t(num_seqs) * num_kv_heads * plan.max_parts <= kLongFirstMaxCtas ? 1 : 0;
+  a.long_first = long_first_grid(num_seqs, num_kv_heads, plan.max_parts) ? 1 : 0;
   a.window = window > 0 ? window : 0;
   a.scale_log2 = scale * 1.4426950408889634f;
 
   cudaError_t err = cudaSuccess;
-  if (need > 0) {
+  if (lay.total > 0) {
     // The partition counters start at zero on every call; the partials need no initialisation.
     err = cudaMemsetAsync(a.counters, 0, lay.counter_bytes, stream);
     if (err != cudaSuccess) return cuda_status(err, "clear split-K counters");
+  }
+  if (order) {
+    err = pkv::launch_seq_order(context_lens, num_seqs, max_blocks_per_seq * PKV_BLOCK_SIZE, a.window, order,
+                                stream);
+    if (err != cudaSuccess) return cuda_status(err, "sequence order launch");
   }
   err = dtype == PKV_F16 ? pkv::launch_decode_f16(a, head_dim, gpad, &kmap, &vmap, stream)
                          : pkv::launch_decode_bf16(a, head_dim, gpad, &kmap, &vmap, stream);
@@ -468,7 +498,8 @@ pkv_status_t pkv_paged_attention_decode_int8(void* out, const void* q, const int
   if (int64_t(num_blocks) * num_kv_heads * PKV_BLOCK_SIZE > INT32_MAX)
     return pkv::fail(PKV_ERR_UNSUPPORTED, "num_blocks * num_kv_heads * 16 exceeds 2^31 rows");
   const SplitLayout lay = split_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, plan.max_parts);
-  const size_t need = lay.total;
+  const size_t ord = order_bytes(num_seqs, num_kv_heads, plan.max_parts);
+  const size_t need = lay.total + ord;
   if (need > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, 16)))
     return pkv::fail(PKV_ERR_WORKSPACE, "workspace of %zu bytes (16-byte aligned) required, got %zu at %p",
                      need, workspace_bytes, workspace);
@@ -485,10 +516,12 @@ pkv_status_t pkv_paged_attention_decode_int8(void* out, const void* q, const int
   a.v_scale = v_scale;
   a.block_tables = block_tables;
   a.context_lens = context_lens;
-  a.part_o = need > 0 ? static_cast<float*>(workspace) : nullptr;
-  a.part_ml = need > 0 ? reinterpret_cast<float2*>(static_cast<char*>(workspace) + lay.ml_offset) : nullptr;
-  a.counters = need > 0 ? reinterpret_cast<unsigned int*>(static_cast<char*>(workspace) + lay.counter_offset)
-                        : nullptr;
+  a.part_o = lay.total > 0 ? static_cast<float*>(workspace) : nullptr;
+  a.part_ml = lay.total > 0 ? reinterpret_cast<float2*>(static_cast<char*>(workspace) + lay.ml_offset) : nullptr;
+  a.counters = lay.total > 0 ? reinterpret_cast<unsigned int*>(static_cast<char*>(workspace) + lay.counter_offset)
+                             : nullptr;
+  int32_t* order = ord > 0 ? reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + lay.total) : nullptr;
+  a.order = order;
   a.status = status;
   a.num_seqs = num_seqs;
   a.num_q_heads = num_q_heads;
@@ -498,7 +531,7 @@ pkv_status_t pkv_paged_attention_decode_int8(void* out, const void* q, const int
   a.num_blocks = num_blocks;
   a.part_tokens = plan.part_tokens;
   a.max_parts = plan.max_parts;
-  a.long_first = int64_t(num_seqs) * num_kv_heads * plan.max_parts <= kLongFirstMaxCtas ? 1 : 0;
+  a.long_first = long_first_grid(num_seqs, num_kv_heads, plan.max_parts) ? 1 : 0;
   a.scale_log2 = scale * 1.4426950408889634f;
   alignas(64) CUtensorMap kmap, vmap;
   if (pkv::decode_int8_uses_tensor_maps()) {
@@ -509,9 +542,13 @@ pkv_status_t pkv_paged_attention_decode_int8(void* out, const void* q, const int
     if (st != PKV_OK) return st;
   }
   cudaError_t err = cudaSuccess;
-  if (need > 0) {
+  if (lay.total > 0) {
     err = cudaMemsetAsync(a.counters, 0, lay.counter_bytes, stream);
     if (err != cudaSuccess) return cuda_status(err, "clear split-K counters");
+  }
+  if (order) {
+    err = pkv::launch_seq_order(context_lens, num_seqs, max_blocks_per_seq * PKV_BLOCK_SIZE, 0, order, stream);
+    if (err != cudaSuccess) return cuda_status(err, "sequence order launch");
   }
   err = pkv::launch_decode_int8(a, dtype == PKV_BF16, head_dim, round_pow2_group(group), &kmap, &vmap, stream);
   return cuda_status(err, "paged_attention_decode_int8 launch");

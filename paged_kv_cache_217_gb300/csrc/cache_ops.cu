@@ -197,7 +197,71 @@ __global__ void bounded_wait_selftest_kernel(unsigned long long limit_ns, unsign
   if (!__all_sync(kFull, ok) && threadIdx.x == 0) flag(status, PKV_DEV_WAIT_TIMEOUT);
 }
 
+// The long-first order of a batch, computed once for the whole decode grid
+// (the same order long_first_seq derives in every CTA when it is not given):
+// sequences with at least twice the mean tile count first, in natural order,
+// then all others in natural order. One CTA, one thread per sequence (S <=
+// 1024). Launched with programmatic dependent launch ahead of the decode: it
+// lets the decode grid become resident at once, reads only the lengths (which
+// no kernel of this library writes), and waits for its own predecessor before
+// it exits, so its completion implies that predecessor's.
+__global__ void __launch_bounds__(1024)
+seq_order_kernel(const int32_t* __restrict__ lens, int S, int max_len, int window, int32_t* __restrict__ order) {
+  asm volatile("griddepcontrol.launch_dependents;");
+  __shared__ long long part_tiles[32];
+  __shared__ int part_long[32], part_short[32];
+  const int s = threadIdx.x, lane = s & 31, warp = s >> 5;
+  int tiles = 0;
+  if (s < S) {
+    int L = __ldg(lens + s);
+    L = L < 0 ? 0 : (L > max_len ? max_len : L);
+    if (window > 0 && L > window) L = window;
+    tiles = (L + kBlock - 1) / kBlock;
+  }
+  long long t = tiles;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(kFull, t, o);
+  if (lane == 0) part_tiles[warp] = t;
+  __syncthreads();
+  long long total = 0;
+  for (int w = 0; w < int(blockDim.x >> 5); ++w) total += part_tiles[w];
+  const bool is_long = s < S && (long long)tiles * S >= 2 * total;
+  const bool is_short = s < S && !is_long;
+  const unsigned lb = __ballot_sync(kFull, is_long), sb = __ballot_sync(kFull, is_short);
+  if (lane == 0) {
+    part_long[warp] = __popc(lb);
+    part_short[warp] = __popc(sb);
+  }
+  __syncthreads();
+  int long_before = __popc(lb & ((1u << lane) - 1u)), short_before = __popc(sb & ((1u << lane) - 1u));
+  int n_long = 0;
+  for (int w = 0; w < int(blockDim.x >> 5); ++w) {
+    if (w < warp) {
+      long_before += part_long[w];
+      short_before += part_short[w];
+    }
+    n_long += part_long[w];
+  }
+  if (s < S) order[is_long ? long_before : n_long + short_before] = s;
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 }  // namespace
+
+cudaError_t launch_seq_order(const int32_t* lens, int num_seqs, int max_len, int window, int32_t* order,
+                             cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3(unsigned((num_seqs + 31) / 32 * 32));
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, seq_order_kernel, lens, num_seqs, max_len, window, order);
+}
 
 cudaError_t launch_bounded_wait_selftest(unsigned long long limit_ns, unsigned int* status, cudaStream_t stream) {
   bounded_wait_selftest_kernel<<<1, 32, 0, stream>>>(limit_ns, status);

@@ -64,6 +64,7 @@ struct DecodeArgs {
   int part_tokens;      // tokens per partition (multiple of 16)
   int max_parts;        // grid.z
   int long_first;       // start sequences of twice the mean length first (long_first_seq)
+  const int32_t* order; // long_first: grid row -> sequence, computed once (seq_order_kernel), or null
   int window;           // sliding window: attend over the last `window` tokens (0 = all)
   float scale_log2;     // scale * log2(e)
 };
@@ -129,6 +130,7 @@ template <int NW>
 __device__ __forceinline__ int long_first_seq(const DecodeArgs& a, int rank) {
   const int S = a.num_seqs;
   if (!a.long_first || S > kOrderMaxSeqs || S <= 1) return rank;
+  if (a.order) return a.order[rank];  // ranked once for the whole grid
   __shared__ int tiles[kOrderMaxSeqs > 0 ? kOrderMaxSeqs : 1];
   __shared__ unsigned int long_bits[kOrderMaxSeqs > 32 ? kOrderMaxSeqs / 32 : 1];
   __shared__ int red[NW];

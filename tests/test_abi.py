@@ -56,6 +56,12 @@ def test_workspace_and_partition_choice():
     assert B.resolved_partition(64, 40, 40, 128, 32) == -1          # 2560 pairs
     assert B.workspace_size(64, 40, 40, 128, 32) == 0
     assert B.resolved_partition(256, 32, 8, 128, 64) == -1          # 2048 pairs
+    # 128..1024 sequences in a grid of at most 4096 CTAs: the launch order is
+    # computed once into num_seqs int32 of workspace (16-byte rounded)
+    assert B.workspace_size(256, 32, 8, 128, 64) == 256 * 4
+    assert B.workspace_size(130, 8, 8, 128, 64) == 528               # 130 * 4 rounded up to 16
+    assert B.workspace_size(127, 8, 8, 128, 64) == 0                 # smaller batches rank in each CTA
+    assert B.workspace_size(512, 16, 16, 128, 64) == 0               # 8192 CTAs: no long-first order
     assert B.resolved_partition(8, 96, 96, 128, 2048) == -1         # 768 pairs
     # fewer pairs: partitions just large enough for 608 CTAs, at least 256 tokens
     assert B.resolved_partition(2, 8, 8, 128, 2048) == 864          # 16 pairs x 38 parts

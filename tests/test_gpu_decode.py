@@ -318,3 +318,19 @@ def test_wide_grid_ring_shape(dtype, d, partition):
     out = _run(case, partition)
     _check_sampled(case, out, 40, seed=6)
     assert B.device_status(clear=True) == 0
+
+
+@pytest.mark.parametrize("dtype,hq,hkv,d", [("f16", 8, 4, 64), ("bf16", 4, 4, 128)])
+def test_batch_ranked_once_for_the_grid(dtype, hq, hkv, d):
+    # 150 sequences (128..1024) in a grid of at most 4096 CTAs: the long-first
+    # order comes from the one-CTA ordering kernel; a few long sequences among
+    # short ones make the order differ from the natural one
+    rng = np.random.default_rng(8)
+    lens = rng.integers(1, 60, 150).astype(np.int32)
+    lens[[7, 90, 149]] = [900, 700, 1200]
+    lens[20] = 0
+    case = H.make_case(lens, hq, hkv, d, dtype, seed=17)
+    assert B.workspace_size(150, hq, hkv, d, case.tables.shape[1]) > 0
+    out = _run(case)
+    H.assert_attention_close(H.to_f64(out), H.oracle_full(case), "ordered batch")
+    assert B.device_status(clear=True) == 0

@@ -163,3 +163,15 @@ def test_balanced_schedule_rejects_a_window():
     with pytest.raises(B.PagedKVError) as ei:
         _run(case, 16, B.BALANCED)
     assert ei.value.status == 2
+
+
+def test_sliding_window_with_batch_ranked_once():
+    # 140 sequences: the ordering kernel ranks by the windowed lengths
+    rng = np.random.default_rng(3)
+    lens = rng.integers(1, 80, 140).astype(np.int32)
+    lens[[5, 60]] = [1000, 600]
+    case = H.make_case(lens, 8, 2, 64, "bf16", seed=23)
+    for window in (16, 100):
+        want = _oracle_window(case, window)
+        H.assert_attention_close(H.to_f64(_run(case, window)), want, f"W={window}")
+    assert B.device_status(clear=True) == 0

@@ -31,6 +31,13 @@ cudaError_t configure_once(K kern, size_t smem, bool (&configured)[kMaxDevices])
 #ifndef PKV_GRID_STAGES
 #define PKV_GRID_STAGES 2
 #endif
+// Shape of the tensor-core (group size >= 2) grid kernel.
+#ifndef PKV_MMA_WARPS
+#define PKV_MMA_WARPS PKV_GRID_WARPS
+#endif
+#ifndef PKV_MMA_STAGES
+#define PKV_MMA_STAGES PKV_GRID_STAGES
+#endif
 
 // Launch with programmatic stream serialization: the grid may become resident
 // while the previous kernel in the stream finishes (the kernels wait for it
@@ -95,11 +102,12 @@ cudaError_t launch_decode_dg(const DecodeArgs& a, const CUtensorMap* kmap, const
                           : launch_cuda_core_grid<T, D, G, NW, STAGES>(a, grid, stream);
     if (err != cudaSuccess) return err;
   } else {
-    using C = MmaCfg<T, D, NW, STAGES>;
-    auto kern = paged_decode_mma_kernel<T, D, G, NW, STAGES>;
+    constexpr int MW = PKV_MMA_WARPS, MS = (D == 256 && PKV_MMA_WARPS * PKV_MMA_STAGES > 8) ? 2 : PKV_MMA_STAGES;
+    using C = MmaCfg<T, D, MW, MS>;
+    auto kern = paged_decode_mma_kernel<T, D, G, MW, MS>;
     cudaError_t err = configure_once(kern, C::SMEM_BYTES, configured);
     if (err != cudaSuccess) return err;
-    err = launch_pdl(kern, grid, dim3(NW * 32), C::SMEM_BYTES, stream, a, *kmap, *vmap);
+    err = launch_pdl(kern, grid, dim3(MW * 32), C::SMEM_BYTES, stream, a, *kmap, *vmap);
     if (err != cudaSuccess) return err;
   }
   return cudaGetLastError();

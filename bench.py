@@ -452,7 +452,12 @@ def run_ours(args):
     # step starts with L2 full of clean, unrelated lines and pays no write-backs.
     flush = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=device)
     part = B.resolved_partition(wl.num_seqs, wl.hq, wl.hkv, wl.d, wl.tables_h.shape[1], args.partition)
-    launches_per_step = 2   # reshape_and_cache + decode (the split-K merge runs inside the decode kernel)
+    # reshape_and_cache + decode (the split-K merge runs inside the decode kernel),
+    # plus the one-CTA ordering kernel that batches of 128..1024 sequences in
+    # grids of at most 4096 CTAs get (see pkv_paged_attention_decode)
+    parts = 1 if part in (-1, B.BALANCED) else -(-wl.tables_h.shape[1] * 16 // part)
+    ordered = part != B.BALANCED and 128 <= wl.num_seqs <= 1024 and wl.num_seqs * wl.hkv * parts <= 4096
+    launches_per_step = 2 + (1 if ordered else 0)
 
     for _ in range(args.warmup):
         step(wl, B)

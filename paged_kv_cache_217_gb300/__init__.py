@@ -15,8 +15,14 @@ from .binding import (  # noqa: F401
     copy_blocks,
     describe_device_flags,
     device_status,
+    copy_blocks_int8,
     paged_attention_decode,
+    paged_attention_decode_int8,
+    paged_attention_decode_noalloc,
+    paged_attention_decode_sliding,
     reshape_and_cache,
+    reshape_and_cache_int8,
+    sliding_workspace_size,
     resolved_partition,
     version,
     workspace_size,

@@ -35,8 +35,6 @@ Modules:
                     write, decode over the dequantised cache
   memsim         -- memory-utilisation replay: paged blocks against
                     contiguous pre-allocation (slot-by-slot arena)
-  cascade        -- prefix groups: consecutive sequences sharing leading
-                    full blocks, for decode over shared blocks
 
 Every function here is pinned by tests in ``tests/test_oracle*.py`` against
 values and invariants that the pages and mathematics fix (hand-worked
@@ -44,4 +42,4 @@ examples under ``tests/golden/``, brute force on tiny inputs, closed forms,
 permutation invariance, copy-on-write sibling equality).
 """
 
-from . import numerics, attention, cache_ops, block_manager, quant, memsim, cascade  # noqa: F401
+from . import numerics, attention, cache_ops, block_manager, quant, memsim  # noqa: F401

@@ -646,9 +646,15 @@ def main(argv=None):
                     help="decode schedule: 0 = library choice, -1 = one CTA per (sequence, KV head), "
                          "N = split-K partitions of N tokens")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--lib", default=None,
+                    help="load this libpaged_kv.so instead of the package's own (a variant built with "
+                         "python -m paged_kv_cache_217_gb300.build --out-dir DIR --define NAME=VALUE)")
     ap.add_argument("--reference-budget", type=float, default=150.0,
                     help="seconds of oracle work for the whole reference run (split over its steps)")
     args = ap.parse_args(argv)
+    if args.lib:
+        from paged_kv_cache_217_gb300 import binding as B
+        B.LIB_PATH = os.path.abspath(args.lib)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":

@@ -253,6 +253,24 @@ size_t pkv_paged_attention_sliding_workspace_size(int num_seqs, int num_q_heads,
                                                   int sliding_window,
                                                   int partition_size);
 
+/*
+ * Diagnostics (the pages have no counterpart). Libraries built with
+ * -DPKV_TRACE=1 (python -m paged_kv_cache_217_gb300.build --define
+ * PKV_TRACE=1 --out-dir DIR) let each CTA of the one-pass and split decode
+ * grids record eight 64-bit words into a device buffer of the caller's:
+ * %globaltimer (ns) at its start, when its sequence is known, when its
+ * length and block ids are known, when warp 0's first tile has landed, when
+ * warp 0's tile loop ends and at its end; its SM; and its sequence (low 32
+ * bits) and tile count (high 32 bits). Record i belongs to the CTA of linear
+ * index i (blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z));
+ * CTAs past `records` and CTAs of empty sequences write nothing. The buffer
+ * applies to the decode calls that follow on any thread (NULL / 0 stops);
+ * pkv_set_trace_buffer returns PKV_ERR_UNSUPPORTED in other builds, and
+ * pkv_trace_enabled tells which build is loaded (1 or 0).
+ */
+int pkv_trace_enabled(void);
+pkv_status_t pkv_set_trace_buffer(unsigned long long* device_buffer, int records);
+
 /* ------------------------------------------------------------------------ */
 /* Cache writes and copy-on-write                                            */
 /* ------------------------------------------------------------------------ */

@@ -68,6 +68,8 @@ _SIGS = {
                                         _c_int),
     "pkv_copy_blocks_int8": ([_c_p] * 5 + [_c_int] * 4 + [_c_p], _c_int),
     "pkv_selftest_bounded_wait": ([ctypes.c_uint32, _c_p], _c_int),
+    "pkv_trace_enabled": ([], _c_int),
+    "pkv_set_trace_buffer": ([_c_p, _c_int], _c_int),
     "pkv_bm_create": ([_c_int, _c_int, _c_p, ctypes.POINTER(_c_p)], _c_int),
     "pkv_bm_destroy": ([_c_p], None),
     "pkv_bm_add_seq": ([_c_p, _c_i64, _c_i64], _c_int),
@@ -405,6 +407,24 @@ def selftest_bounded_wait(limit_us=2000):
     import torch
     _check(lib().pkv_selftest_bounded_wait(int(limit_us), _stream_ptr(torch.device("cuda", torch.cuda.current_device()))),
            "selftest_bounded_wait")
+
+
+def trace_enabled():
+    """True when the loaded library was built with per-CTA tracing (PKV_TRACE=1)."""
+    return bool(lib().pkv_trace_enabled())
+
+
+def set_trace_buffer(buffer):
+    """Per-CTA phase timestamps of the following decode calls go into ``buffer``
+    (an int64 CUDA tensor of 8 * records words), or stop with None."""
+    if buffer is None:
+        _check(lib().pkv_set_trace_buffer(None, 0), "set_trace_buffer")
+        return
+    _need_cuda(buffer)
+    import torch
+    if buffer.dtype != torch.int64 or buffer.numel() % 8:
+        raise ValueError("the trace buffer is int64 with 8 words a record")
+    _check(lib().pkv_set_trace_buffer(buffer.data_ptr(), buffer.numel() // 8), "set_trace_buffer")
 
 
 def describe_device_flags(flags):

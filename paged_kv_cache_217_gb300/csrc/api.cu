@@ -230,9 +230,24 @@ pkv_status_t cuda_status(cudaError_t err, const char* what) {
 
 bool supported_head_dim(int d) { return d == 64 || d == 128 || d == 256; }
 
+// Trace buffer of PKV_TRACE builds (pkv_set_trace_buffer), per process.
+unsigned long long* g_trace_buffer = nullptr;
+int g_trace_records = 0;
+
 }  // namespace
 
 extern "C" {
+
+int pkv_trace_enabled(void) { return pkv::kTrace ? 1 : 0; }
+
+pkv_status_t pkv_set_trace_buffer(unsigned long long* device_buffer, int records) {
+  if (!pkv::kTrace) return pkv::fail(PKV_ERR_UNSUPPORTED, "this build records no traces (build with PKV_TRACE=1)");
+  if (records < 0 || (records > 0 && !device_buffer) || !aligned(device_buffer, 8))
+    return pkv::fail(PKV_ERR_INVALID_ARG, "set_trace_buffer: bad buffer");
+  g_trace_buffer = records > 0 ? device_buffer : nullptr;
+  g_trace_records = records;
+  return pkv::ok();
+}
 
 pkv_status_t pkv_device_status(uint32_t* flags_out, int clear) {
   if (!flags_out) return pkv::fail(PKV_ERR_INVALID_ARG, "device_status: flags_out is NULL");
@@ -410,6 +425,8 @@ pkv_status_t decode_impl(void* out, const void* q, const void* k_pool, const voi
   // LLaMA-13B layer at 2560 CTAs, +7 % on the OPT-66B sampling batch at 9216).
   a.long_first = long_first_grid(num_seqs, num_kv_heads, plan.max_parts) ? 1 : 0;
   a.window = window > 0 ? window : 0;
+  a.trace = g_trace_buffer;
+  a.trace_records = g_trace_records;
   a.scale_log2 = scale * 1.4426950408889634f;
 
   cudaError_t err = cudaSuccess;

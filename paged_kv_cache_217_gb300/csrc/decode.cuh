@@ -65,6 +65,8 @@ struct DecodeArgs {
   int max_parts;        // grid.z
   int long_first;       // start sequences of twice the mean length first (long_first_seq)
   const int32_t* order; // long_first: grid row -> sequence, computed once (seq_order_kernel), or null
+  unsigned long long* trace;  // PKV_TRACE builds: per-CTA phase timestamps (8 words a CTA), or null
+  int trace_records;          // CTAs the trace buffer holds
   int window;           // sliding window: attend over the last `window` tokens (0 = all)
   float scale_log2;     // scale * log2(e)
 };
@@ -81,6 +83,39 @@ __device__ __forceinline__ TokenRange token_range(int L, int window) {
   r.first = (window > 0 && L > window) ? L - window : 0;
   r.aligned = r.first & ~(kBlock - 1);
   return r;
+}
+
+// Tracing (diagnostic builds only, -DPKV_TRACE=1): each CTA of the one-pass
+// and split grid kernels records %globaltimer at its phase boundaries -- start
+// (after the predecessor), sequence known, length and ids known, first tile
+// landed (warp 0), tile loop done (warp 0), end -- plus its SM and (sequence,
+// tiles) into a caller-supplied buffer. Off by default: no code is generated.
+#ifndef PKV_TRACE
+#define PKV_TRACE 0
+#endif
+constexpr bool kTrace = PKV_TRACE != 0;
+
+struct TraceMarks {
+  unsigned long long t[5];
+};
+
+__device__ __forceinline__ void trace_mark(TraceMarks& m, int i) {
+  if constexpr (kTrace) m.t[i] = global_timer_ns();
+}
+
+__device__ __forceinline__ void trace_write(const DecodeArgs& a, const TraceMarks& m, int s, int tiles) {
+  if constexpr (kTrace) {
+    if (threadIdx.x != 0 || !a.trace) return;
+    const unsigned long long cta = blockIdx.x + (unsigned long long)gridDim.x * (blockIdx.y + (unsigned long long)gridDim.y * blockIdx.z);
+    if (cta >= (unsigned long long)a.trace_records) return;
+    unsigned int smid;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+    unsigned long long* r = a.trace + 8 * cta;
+    for (int i = 0; i < 5; ++i) r[i] = m.t[i];
+    r[5] = global_timer_ns();
+    r[6] = smid;
+    r[7] = (unsigned long long)(unsigned)s | ((unsigned long long)(unsigned)tiles << 32);
+  }
 }
 
 // Waits until the kernel launched before this one in the stream has finished
@@ -468,8 +503,11 @@ paged_decode_kernel(const DecodeArgs a) {
   extern __shared__ __align__(1024) unsigned char smem[];
 
   wait_for_predecessor();
+  TraceMarks tm{};
+  trace_mark(tm, 0);
   const int g = kSeqFastest ? blockIdx.y : blockIdx.x;
   const int s = long_first_seq<NW>(a, kSeqFastest ? blockIdx.x : blockIdx.y), part = blockIdx.z;
+  trace_mark(tm, 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int sub = lane & (LPR - 1), r = lane / LPR;
   const int hq0 = g * a.group;
@@ -491,6 +529,7 @@ paged_decode_kernel(const DecodeArgs a) {
   const TokenRange tr = token_range(L, a.window);
   const int nparts = L == 0 ? 1 : (L - tr.aligned + a.part_tokens - 1) / a.part_tokens;
   if (part >= nparts) return;
+  trace_mark(tm, 2);
 
   if (L == 0) {  // empty sequence: zeros
     T* o = static_cast<T*>(a.out) + (size_t(s) * a.num_q_heads + hq0) * D;
@@ -613,6 +652,7 @@ paged_decode_kernel(const DecodeArgs a) {
       for (int kk = k; kk < last; ++kk) mbar_wait_bounded(bar_s + 8 * (kk % STAGES), (kk / STAGES) & 1);
       break;
     }
+    if (k == 0) trace_mark(tm, 3);
     const int j = warp + k * NW;
     const int rows = min(kBlock, ntok - j * kBlock);
     const int lo = j == 0 ? head : 0;
@@ -626,6 +666,7 @@ paged_decode_kernel(const DecodeArgs a) {
     if (k + STAGES < n_my) issue(k + STAGES);
   }
 
+  trace_mark(tm, 4);
   // Sum the row groups of the warp (lanes that differ in r).
 #pragma unroll
   for (int m = LPR; m < 32; m <<= 1) {
@@ -658,6 +699,7 @@ paged_decode_kernel(const DecodeArgs a) {
   __syncthreads();
 
   finish_chunk<T, D, G, NW>(a, smem, size_t(STAGES) * C::STAGE_BYTES, s, g, part, nparts);
+  trace_write(a, tm, s, nb);
 }
 
 }  // namespace pkv

@@ -233,8 +233,11 @@ paged_decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap 
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
   wait_for_predecessor();
+  TraceMarks tm{};
+  trace_mark(tm, 0);
   const int g = kSeqFastest ? blockIdx.y : blockIdx.x;
   const int s = long_first_seq<NW>(a, kSeqFastest ? blockIdx.x : blockIdx.y), part = blockIdx.z;
+  trace_mark(tm, 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int hq0 = g * a.group;
   const int gr = lane >> 2, t = lane & 3;   // MMA row (query head) and column pair of this lane
@@ -256,6 +259,7 @@ paged_decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap 
   const TokenRange tr = token_range(L, a.window);
   const int nparts = L == 0 ? 1 : (L - tr.aligned + a.part_tokens - 1) / a.part_tokens;
   if (part >= nparts) return;
+  trace_mark(tm, 2);
   if (L == 0) {
     T* o = static_cast<T*>(a.out) + (size_t(s) * a.num_q_heads + hq0) * D;
     for (int i = threadIdx.x; i < a.group * D / 8; i += NW * 32)
@@ -351,6 +355,7 @@ paged_decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap 
       for (int kk = k; kk < last; ++kk) mbar_wait_bounded(bar_s + 8 * (kk % STAGES), (kk / STAGES) & 1);
       break;
     }
+    if (k == 0) trace_mark(tm, 3);
     const int j = warp + k * NW;
     const int rows = min(kBlock, ntok - j * kBlock);
     const int lo = j == 0 ? head : 0;
@@ -365,6 +370,7 @@ paged_decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap 
     if (k + STAGES < n_my) issue(k + STAGES);
   }
 
+  trace_mark(tm, 4);
   // Row sums: the four lanes of a row each summed a quarter of the tokens.
   lrun += __shfl_xor_sync(kFull, lrun, 1);
   lrun += __shfl_xor_sync(kFull, lrun, 2);
@@ -382,6 +388,7 @@ paged_decode_mma_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap 
   }
   __syncthreads();
   finish_chunk<T, D, G, NW>(a, smem, size_t(STAGES) * C::STAGE_BYTES, s, g, part, nparts);
+  trace_write(a, tm, s, nb);
 }
 
 }  // namespace pkv

@@ -1,0 +1,87 @@
+"""Per-CTA phase timeline of one decode call (diagnostic).
+
+    python -m paged_kv_cache_217_gb300.build --define PKV_TRACE=1 --out-dir DIR
+    python -m paged_kv_cache_217_gb300.trace --lib DIR/libpaged_kv.so --workload llama3_8b
+
+Runs the named layer's decode (seeded synthetic inputs, blocks scattered
+through a shuffled pool, L2 evicted between calls) with a trace buffer set
+(pkv_set_trace_buffer) and summarises the last call's records: the mean,
+median, p90 and max of each phase of a CTA's life, CTAs resident per
+microsecond, and the phases by tile count. Needs a library built with
+PKV_TRACE=1; timings of traced calls are not benchmark numbers.
+"""
+
+import argparse
+import os
+
+import numpy as np
+
+PHASES = ["order (sequence known)", "length and block ids", "first tile landed", "tile loop", "merge and exit"]
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--lib", required=True, help="a libpaged_kv.so built with PKV_TRACE=1")
+    ap.add_argument("--workload", default="llama3_8b", choices=["tiny", "llama13b", "llama3_8b", "opt175b_long"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--calls", type=int, default=20)
+    args = ap.parse_args(argv)
+
+    import torch
+    from . import binding as B
+    from . import workloads as W
+    B.LIB_PATH = os.path.abspath(args.lib)
+    if not B.trace_enabled():
+        raise SystemExit(f"{args.lib} was not built with PKV_TRACE=1")
+
+    dev = torch.device("cuda", 0)
+    shape = W.CONFIGS[args.workload](args.seed)
+    lens = shape.context_lens
+    nb = W.pool_size(lens, shape.pool_factor)
+    tables, _ = W.scattered_tables(lens, nb, args.seed)
+    hq, hkv, d = shape.num_q_heads, shape.num_kv_heads, shape.head_dim
+    k_pool = W.normal_values((nb, hkv, 16, d), shape.dtype, args.seed * 11 + 1, dev)
+    v_pool = W.normal_values((nb, hkv, 16, d), shape.dtype, args.seed * 11 + 2, dev)
+    q = W.normal_values((lens.size, hq, d), shape.dtype, args.seed * 11 + 4, dev)
+    out = torch.empty_like(q)
+    t_d = torch.from_numpy(tables).to(dev)
+    l_d = torch.from_numpy(lens).to(dev)
+    records = 1 << 17
+    buf = torch.zeros(8 * records, dtype=torch.int64, device=dev)
+    flush = torch.ones((512 << 20) // 4, dtype=torch.int32, device=dev)
+    B.set_trace_buffer(buf)
+    try:
+        for _ in range(args.calls):
+            buf.zero_()
+            flush.sum()
+            B.paged_attention_decode(out, q, k_pool, v_pool, t_d, l_d, shape.scale)
+        torch.cuda.synchronize()
+    finally:
+        B.set_trace_buffer(None)
+    r = buf.view(-1, 8).cpu().numpy()
+    r = r[r[:, 0] > 0]
+    t0 = r[:, 0].min()
+    st = (r[:, :6] - t0) / 1000.0
+    tiles = r[:, 7] >> 32
+    d_ph = np.diff(st, axis=1)
+    life = st[:, 5] - st[:, 0]
+    print(f"{shape.name}: {len(r)} CTAs traced, span {st[:, 5].max():.1f} us")
+    for i, name in enumerate(PHASES):
+        x = d_ph[:, i]
+        print(f"  {name:24s} mean {x.mean():6.2f} us  median {np.median(x):6.2f}  p90 {np.percentile(x, 90):6.2f}"
+              f"  max {x.max():6.2f}")
+    print(f"  {'lifetime':24s} mean {life.mean():6.2f} us  median {np.median(life):6.2f}"
+          f"  p90 {np.percentile(life, 90):6.2f}  max {life.max():6.2f}")
+    print(f"  tiles per CTA: mean {tiles.mean():.1f}, max {tiles.max()}")
+    grid = np.arange(0.0, st[:, 5].max(), 1.0)
+    resident = [int(np.sum((st[:, 0] <= t) & (st[:, 5] > t))) for t in grid]
+    print("  CTAs resident per us:", " ".join(map(str, resident)))
+    for lo, hi in [(1, 4), (4, 8), (8, 16), (16, 32), (32, 64), (64, 1 << 30)]:
+        m = (tiles >= lo) & (tiles < hi)
+        if m.any():
+            print(f"  tiles [{lo}, {hi if hi < 1 << 30 else 'inf'}): {m.sum():5d} CTAs, life {life[m].mean():6.2f} us,"
+                  f" first tile {d_ph[m, 2].mean():5.2f}, loop {d_ph[m, 3].mean():6.2f}, merge {d_ph[m, 4].mean():5.2f}")
+
+
+if __name__ == "__main__":
+    main()

@@ -149,3 +149,8 @@ def test_missing_library_fails_loudly(monkeypatch):
     monkeypatch.setattr(B, "LIB_PATH", "/nonexistent/libpaged_kv.so")
     with pytest.raises(B.LibraryNotBuilt):
         B.lib()
+
+
+def test_tracing_is_off_in_the_default_build():
+    assert B.trace_enabled() is False
+    assert B.lib().pkv_set_trace_buffer(None, 0) == 2          # PKV_ERR_UNSUPPORTED

@@ -32,6 +32,10 @@
 //    CTA of a (sequence, KV head) to finish -- counted by an atomic counter in
 //    the workspace, which it resets -- merges them by log-sum-exp. Sequences
 //    that fit in one partition are finished by their CTA directly.
+//  * The KV storage format is a policy of the tile math: 16-bit elements
+//    (KvHalf) or int8 codes with one fp32 scale per row (KvInt8).
+//  * A sliding window of W tokens starts the tiles at the block holding
+//    position L - W and masks the rows before it (token_range).
 #pragma once
 
 #include <cmath>

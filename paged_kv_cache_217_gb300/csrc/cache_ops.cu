@@ -14,6 +14,7 @@
 
 #include <cstdint>
 
+#include "decode.cuh"
 #include "device_common.cuh"
 #include "launch.h"
 
@@ -225,7 +226,7 @@ seq_order_kernel(const int32_t* __restrict__ lens, int S, int max_len, int windo
   __syncthreads();
   long long total = 0;
   for (int w = 0; w < int(blockDim.x >> 5); ++w) total += part_tiles[w];
-  const bool is_long = s < S && (long long)tiles * S >= 2 * total;
+  const bool is_long = s < S && 2 * (long long)tiles * S >= kLongFirstX2 * total;
   const bool is_short = s < S && !is_long;
   const unsigned lb = __ballot_sync(kFull, is_long), sb = __ballot_sync(kFull, is_short);
   if (lane == 0) {

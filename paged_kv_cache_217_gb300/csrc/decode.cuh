@@ -151,6 +151,12 @@ constexpr bool kPackedFma = PKV_PACKED_FMA != 0;
 #define PKV_ORDER_MAX_SEQS 1024
 #endif
 constexpr int kOrderMaxSeqs = PKV_ORDER_MAX_SEQS;  // batches up to this size start long sequences first
+// A sequence is "long" when its tile count is at least PKV_LONG_FIRST_X2 / 2
+// times the batch mean (2x by default).
+#ifndef PKV_LONG_FIRST_X2
+#define PKV_LONG_FIRST_X2 4
+#endif
+constexpr long long kLongFirstX2 = PKV_LONG_FIRST_X2;
 
 // Position of the k-th (0-based) set bit of m; m has more than k set bits.
 __device__ __forceinline__ int kth_set_bit(unsigned int m, int k) {
@@ -194,7 +200,7 @@ __device__ __forceinline__ int long_first_seq(const DecodeArgs& a, int rank) {
   const int words = (S + 31) / 32;
   for (int i = warp; i < words; i += NW) {
     const int s = 32 * i + lane;
-    const bool lg = s < S && (long long)tiles[s] * S >= 2 * total;
+    const bool lg = s < S && 2 * (long long)tiles[s] * S >= kLongFirstX2 * total;
     const unsigned int m = __ballot_sync(kFull, lg);
     if (lane == 0) long_bits[i] = m;
   }

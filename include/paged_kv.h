@@ -270,6 +270,15 @@ size_t pkv_paged_attention_sliding_workspace_size(int num_seqs, int num_q_heads,
  */
 int pkv_trace_enabled(void);
 pkv_status_t pkv_set_trace_buffer(unsigned long long* device_buffer, int records);
+/*
+ * pkv_trace_stamp (every build) enqueues on `stream` a one-thread kernel that
+ * writes %globaltimer (ns, the clock of the trace records) to the device word
+ * `device_word` (8-byte aligned, caller-owned) when the stream reaches it:
+ * stamps before and after a decode call place the call's CTAs within it.
+ * The stamp is itself a launch, so the interval up to a stamp includes that
+ * launch's latency. PKV_ERR_INVALID_ARG for a NULL or misaligned word.
+ */
+pkv_status_t pkv_trace_stamp(unsigned long long* device_word, void* stream);
 
 /* ------------------------------------------------------------------------ */
 /* Cache writes and copy-on-write                                            */

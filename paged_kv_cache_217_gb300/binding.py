@@ -70,6 +70,7 @@ _SIGS = {
     "pkv_selftest_bounded_wait": ([ctypes.c_uint32, _c_p], _c_int),
     "pkv_trace_enabled": ([], _c_int),
     "pkv_set_trace_buffer": ([_c_p, _c_int], _c_int),
+    "pkv_trace_stamp": ([_c_p, _c_p], _c_int),
     "pkv_bm_create": ([_c_int, _c_int, _c_p, ctypes.POINTER(_c_p)], _c_int),
     "pkv_bm_destroy": ([_c_p], None),
     "pkv_bm_add_seq": ([_c_p, _c_i64, _c_i64], _c_int),
@@ -425,6 +426,17 @@ def set_trace_buffer(buffer):
     if buffer.dtype != torch.int64 or buffer.numel() % 8:
         raise ValueError("the trace buffer is int64 with 8 words a record")
     _check(lib().pkv_set_trace_buffer(buffer.data_ptr(), buffer.numel() // 8), "set_trace_buffer")
+
+
+def trace_stamp(words, index):
+    """Enqueues on the current stream a write of the GPU clock (%globaltimer,
+    ns) into ``words[index]`` (an int64 CUDA tensor) when the stream gets there."""
+    _need_cuda(words)
+    import torch
+    if words.dtype != torch.int64 or not 0 <= index < words.numel() or not words.is_contiguous():
+        raise ValueError("trace_stamp takes a contiguous int64 tensor and an index into it")
+    ptr = words.data_ptr() + 8 * int(index)
+    _check(lib().pkv_trace_stamp(ptr, _stream_ptr(words.device)), "trace_stamp")
 
 
 def describe_device_flags(flags):

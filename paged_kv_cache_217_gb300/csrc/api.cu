@@ -249,6 +249,11 @@ pkv_status_t pkv_set_trace_buffer(unsigned long long* device_buffer, int records
   return pkv::ok();
 }
 
+pkv_status_t pkv_trace_stamp(unsigned long long* device_word, void* stream) {
+  if (!device_word || !aligned(device_word, 8)) return pkv::fail(PKV_ERR_INVALID_ARG, "trace_stamp: bad word");
+  return cuda_status(pkv::launch_trace_stamp(device_word, static_cast<cudaStream_t>(stream)), "trace_stamp launch");
+}
+
 pkv_status_t pkv_device_status(uint32_t* flags_out, int clear) {
   if (!flags_out) return pkv::fail(PKV_ERR_INVALID_ARG, "device_status: flags_out is NULL");
   unsigned int* addr = nullptr;

@@ -264,6 +264,15 @@ cudaError_t launch_seq_order(const int32_t* lens, int num_seqs, int max_len, int
   return cudaLaunchKernelEx(&cfg, seq_order_kernel, lens, num_seqs, max_len, window, order);
 }
 
+namespace {
+__global__ void trace_stamp_kernel(unsigned long long* dst) { *dst = global_timer_ns(); }
+}  // namespace
+
+cudaError_t launch_trace_stamp(unsigned long long* dst, cudaStream_t stream) {
+  trace_stamp_kernel<<<1, 1, 0, stream>>>(dst);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_bounded_wait_selftest(unsigned long long limit_ns, unsigned int* status, cudaStream_t stream) {
   bounded_wait_selftest_kernel<<<1, 32, 0, stream>>>(limit_ns, status);
   return cudaGetLastError();

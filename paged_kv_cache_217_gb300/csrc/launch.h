@@ -38,6 +38,7 @@ cudaError_t launch_seq_order(const int32_t* lens, int num_seqs, int max_len, int
 
 // One warp that waits on an mbarrier no copy completes (bounded-wait self-test).
 cudaError_t launch_bounded_wait_selftest(unsigned long long limit_ns, unsigned int* status, cudaStream_t stream);
+cudaError_t launch_trace_stamp(unsigned long long* dst, cudaStream_t stream);
 
 // Bit copies; element size is 2 bytes for both supported dtypes.
 cudaError_t launch_reshape_and_cache(const void* k, const void* v, void* k_pool, void* v_pool,

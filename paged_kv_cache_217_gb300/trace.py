@@ -5,8 +5,11 @@
 
 Runs the named layer's decode (seeded synthetic inputs, blocks scattered
 through a shuffled pool, L2 evicted between calls) with a trace buffer set
-(pkv_set_trace_buffer) and summarises the last call's records: the mean,
-median, p90 and max of each phase of a CTA's life, CTAs resident per
+(pkv_set_trace_buffer) and GPU clock stamps (pkv_trace_stamp) before and
+after each call, and summarises: where a call's time goes (stamp to first
+CTA start, first CTA start to last CTA end, last CTA end to the next stamp;
+means over the calls after two warm-up calls), then for the last call the
+mean, median, p90 and max of each phase of a CTA's life, CTAs resident per
 microsecond, and the phases by tile count. Needs a library built with
 PKV_TRACE=1; timings of traced calls are not benchmark numbers.
 """
@@ -49,17 +52,29 @@ def main(argv=None):
     records = 1 << 17
     buf = torch.zeros(8 * records, dtype=torch.int64, device=dev)
     flush = torch.ones((512 << 20) // 4, dtype=torch.int32, device=dev)
+    stamps = torch.zeros(2, dtype=torch.int64, device=dev)
+    anatomy = []
     B.set_trace_buffer(buf)
     try:
-        for _ in range(args.calls):
+        for i in range(args.calls):
             buf.zero_()
             flush.sum()
+            B.trace_stamp(stamps, 0)
             B.paged_attention_decode(out, q, k_pool, v_pool, t_d, l_d, shape.scale)
-        torch.cuda.synchronize()
+            B.trace_stamp(stamps, 1)
+            torch.cuda.synchronize()
+            r = buf.view(-1, 8).cpu().numpy()
+            r = r[r[:, 0] > 0]
+            s0, s1 = stamps.cpu().numpy()
+            if i >= 2:
+                anatomy.append(((r[:, 0].min() - s0) / 1e3, (r[:, 5].max() - r[:, 0].min()) / 1e3,
+                                (s1 - r[:, 5].max()) / 1e3))
     finally:
         B.set_trace_buffer(None)
-    r = buf.view(-1, 8).cpu().numpy()
-    r = r[r[:, 0] > 0]
+    if anatomy:
+        pre, span, post = np.mean(anatomy, axis=0)
+        print(f"{shape.name}: stamp -> first CTA {pre:.2f} us, CTA span {span:.2f} us, "
+              f"last CTA -> stamp {post:.2f} us (means of {len(anatomy)} calls)")
     t0 = r[:, 0].min()
     st = (r[:, :6] - t0) / 1000.0
     tiles = r[:, 7] >> 32

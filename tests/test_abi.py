@@ -154,3 +154,6 @@ def test_missing_library_fails_loudly(monkeypatch):
 def test_tracing_is_off_in_the_default_build():
     assert B.trace_enabled() is False
     assert B.lib().pkv_set_trace_buffer(None, 0) == 2          # PKV_ERR_UNSUPPORTED
+    # the clock stamp exists in every build and checks its word on the host
+    assert B.lib().pkv_trace_stamp(None, None) == 1             # PKV_ERR_INVALID_ARG
+    assert B.lib().pkv_trace_stamp(ctypes.c_void_p(12), None) == 1

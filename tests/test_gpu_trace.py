@@ -2,6 +2,7 @@
 separate process on a small and a full-size layer."""
 
 import os
+import re
 import subprocess
 import sys
 
@@ -29,8 +30,34 @@ def test_timeline_of_one_decode(trace_lib, workload, ctas):
                          cwd=ROOT, capture_output=True, text=True, timeout=600)
     assert res.returncode == 0, res.stderr[-2000:]
     lines = res.stdout.splitlines()
-    assert f"{ctas} CTAs traced" in lines[0], res.stdout
+    # where the call's time goes: three positive intervals between the stamps
+    anatomy = lines[0]
+    assert "stamp -> first CTA" in anatomy, res.stdout
+    parts = [float(x) for x in re.findall(r"(-?[0-9.]+) us", anatomy.split("stamp -> first CTA")[1])[:3]]
+    assert len(parts) == 3, anatomy
+    assert all(p > 0.0 for p in parts), anatomy
+    assert f"{ctas} CTAs traced" in lines[1], res.stdout
     # every phase line is present and the mean lifetime is positive
     assert sum(1 for ln in lines if " us  median " in ln) == 6
     life = [ln for ln in lines if ln.strip().startswith("lifetime")][0]
     assert float(life.split("mean")[1].split("us")[0]) > 0.0
+
+
+def test_stamps_follow_the_stream():
+    """pkv_trace_stamp writes the GPU clock when the stream reaches it: two
+    stamps around a ~1 ms device sleep are at least 0.1 ms apart, in order."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from paged_kv_cache_217_gb300 import binding as B
+    words = torch.zeros(4, dtype=torch.int64, device="cuda")
+    B.trace_stamp(words, 1)
+    torch.cuda._sleep(2_000_000)
+    B.trace_stamp(words, 3)
+    torch.cuda.synchronize()
+    w = words.cpu().tolist()
+    assert w[0] == 0 and w[2] == 0
+    assert w[3] - w[1] >= 100_000, w
+    with pytest.raises(ValueError):
+        B.trace_stamp(words.to(torch.int32), 0)
+    with pytest.raises(ValueError):
+        B.trace_stamp(words, 4)

@@ -198,10 +198,10 @@ __global__ void bounded_wait_selftest_kernel(unsigned long long limit_ns, unsign
   if (!__all_sync(kFull, ok) && threadIdx.x == 0) flag(status, PKV_DEV_WAIT_TIMEOUT);
 }
 
-// The long-first order of a batch, computed once for the whole decode grid
-// (the same order long_first_seq derives in every CTA when it is not given):
-// sequences with at least twice the mean tile count first, in natural order,
-// then all others in natural order. One CTA, one thread per sequence (S <=
+// The long-first order of a batch, computed once for the whole decode grid:
+// the buckets of order_bucket -- long sequences, the rest, short sequences --
+// each in natural order (long_first_seq, ranking in every CTA, uses the first
+// two only). One CTA, one thread per sequence (S <=
 // 1024). Launched with programmatic dependent launch ahead of the decode: it
 // lets the decode grid become resident at once, reads only the lengths (which
 // no kernel of this library writes), and waits for its own predecessor before
@@ -210,7 +210,7 @@ __global__ void __launch_bounds__(1024)
 seq_order_kernel(const int32_t* __restrict__ lens, int S, int max_len, int window, int32_t* __restrict__ order) {
   asm volatile("griddepcontrol.launch_dependents;");
   __shared__ long long part_tiles[32];
-  __shared__ int part_long[32], part_short[32];
+  __shared__ int part_long[32], part_rest[32], part_short[32];
   const int s = threadIdx.x, lane = s & 31, warp = s >> 5;
   int tiles = 0;
   if (s < S) {
@@ -226,24 +226,28 @@ seq_order_kernel(const int32_t* __restrict__ lens, int S, int max_len, int windo
   __syncthreads();
   long long total = 0;
   for (int w = 0; w < int(blockDim.x >> 5); ++w) total += part_tiles[w];
-  const bool is_long = s < S && 2 * (long long)tiles * S >= kLongFirstX2 * total;
-  const bool is_short = s < S && !is_long;
-  const unsigned lb = __ballot_sync(kFull, is_long), sb = __ballot_sync(kFull, is_short);
+  const int b = s < S ? order_bucket(tiles, S, total, true) : -1;
+  const unsigned lb = __ballot_sync(kFull, b == 0), rb = __ballot_sync(kFull, b == 1),
+                 sb = __ballot_sync(kFull, b == 2);
   if (lane == 0) {
     part_long[warp] = __popc(lb);
+    part_rest[warp] = __popc(rb);
     part_short[warp] = __popc(sb);
   }
   __syncthreads();
-  int long_before = __popc(lb & ((1u << lane) - 1u)), short_before = __popc(sb & ((1u << lane) - 1u));
-  int n_long = 0;
+  const unsigned below = (1u << lane) - 1u;
+  int long_before = __popc(lb & below), rest_before = __popc(rb & below), short_before = __popc(sb & below);
+  int n_long = 0, n_rest = 0;
   for (int w = 0; w < int(blockDim.x >> 5); ++w) {
     if (w < warp) {
       long_before += part_long[w];
+      rest_before += part_rest[w];
       short_before += part_short[w];
     }
     n_long += part_long[w];
+    n_rest += part_rest[w];
   }
-  if (s < S) order[is_long ? long_before : n_long + short_before] = s;
+  if (s < S) order[b == 0 ? long_before : (b == 1 ? n_long + rest_before : n_long + n_rest + short_before)] = s;
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 

@@ -157,6 +157,26 @@ constexpr int kOrderMaxSeqs = PKV_ORDER_MAX_SEQS;  // batches up to this size st
 #define PKV_LONG_FIRST_X2 4
 #endif
 constexpr long long kLongFirstX2 = PKV_LONG_FIRST_X2;
+// In batches ranked by the one-CTA ordering kernel (128..1024 sequences), a
+// sequence that is not long is "short", and goes after all others, when its
+// tile count is at most PKV_SHORT_LAST_X8 / 8 times the batch mean (0: no
+// short bucket). Measured on GB300, Llama-3-8B-shaped layer (256 sequences):
+// 0 -> 42.9 us, 3 -> 42.2, 4 -> 41.6, 5 -> 41.3, 6 -> 41.5, 8 -> 43.2; the
+// same bucket in smaller batches (the LLaMA-13B layer, the beam batch) cost
+// 0.5-1.8 %, so the per-CTA ranking keeps two buckets.
+#ifndef PKV_SHORT_LAST_X8
+#define PKV_SHORT_LAST_X8 5
+#endif
+constexpr long long kShortLastX8 = PKV_SHORT_LAST_X8;
+
+// Bucket of a sequence with `tiles` tiles in a batch of S sequences holding
+// `total` tiles: 0 long (first), 1 the rest, 2 short (last; only with
+// short_last).
+__device__ __forceinline__ int order_bucket(long long tiles, int S, long long total, bool short_last) {
+  if (2 * tiles * S >= kLongFirstX2 * total) return 0;
+  if (short_last && kShortLastX8 > 0 && 8 * tiles * S <= kShortLastX8 * total) return 2;
+  return 1;
+}
 
 // Position of the k-th (0-based) set bit of m; m has more than k set bits.
 __device__ __forceinline__ int kth_set_bit(unsigned int m, int k) {
@@ -170,7 +190,8 @@ __device__ __forceinline__ int kth_set_bit(unsigned int m, int k) {
 // take the first rows (in natural order) and all others follow (in natural
 // order, which keeps parallel samples of one prompt -- sequences that share
 // blocks -- running side by side). Every CTA derives the same mapping from
-// context_lens, so each sequence is taken exactly once.
+// context_lens, so each sequence is taken exactly once. (Batches that the
+// ordering kernel ranks also put their shortest sequences last.)
 template <int NW>
 __device__ __forceinline__ int long_first_seq(const DecodeArgs& a, int rank) {
   const int S = a.num_seqs;
@@ -200,7 +221,7 @@ __device__ __forceinline__ int long_first_seq(const DecodeArgs& a, int rank) {
   const int words = (S + 31) / 32;
   for (int i = warp; i < words; i += NW) {
     const int s = 32 * i + lane;
-    const bool lg = s < S && 2 * (long long)tiles[s] * S >= kLongFirstX2 * total;
+    const bool lg = s < S && order_bucket(tiles[s], S, total, false) == 0;
     const unsigned int m = __ballot_sync(kFull, lg);
     if (lane == 0) long_bits[i] = m;
   }

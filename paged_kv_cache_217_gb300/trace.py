@@ -12,6 +12,12 @@ means over the calls after two warm-up calls), then for the last call the
 mean, median, p90 and max of each phase of a CTA's life, CTAs resident per
 microsecond, and the phases by tile count. Needs a library built with
 PKV_TRACE=1; timings of traced calls are not benchmark numbers.
+
+--replay also fits the traced CTA lifetimes as a + b * tiles and replays
+the layer's CTAs through as many slots as were resident, rows dispatched in
+order, for several row orders (natural; long first; long first and short
+last; descending), printing each order's modelled span: a model of the
+dispatch only, in which a CTA's life does not depend on its neighbours.
 """
 
 import argparse
@@ -28,6 +34,7 @@ def main(argv=None):
     ap.add_argument("--workload", default="llama3_8b", choices=["tiny", "llama13b", "llama3_8b", "opt175b_long"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--calls", type=int, default=20)
+    ap.add_argument("--replay", action="store_true", help="replay the CTA lifetimes under other row orders")
     args = ap.parse_args(argv)
 
     import torch
@@ -97,6 +104,41 @@ def main(argv=None):
             print(f"  tiles [{lo}, {hi if hi < 1 << 30 else 'inf'}): {m.sum():5d} CTAs, life {life[m].mean():6.2f} us,"
                   f" first tile {d_ph[m, 2].mean():5.2f}, loop {d_ph[m, 3].mean():6.2f}, merge {d_ph[m, 4].mean():5.2f}")
 
+    if args.replay:
+        replay(tiles, life, lens, shape.num_kv_heads, max(resident) if resident else 1)
+
+
+def modelled_span(order, seq_tiles, heads, slots, a, b):
+    """End time of CTAs dispatched row by row (all heads of a row's sequence)
+    into `slots` slots, each living a + b * tiles."""
+    import heapq
+    free = [0.0] * slots
+    end = 0.0
+    for s in order:
+        for _ in range(heads):
+            t = heapq.heappop(free)
+            e = t + a + b * float(seq_tiles[s])
+            end = max(end, e)
+            heapq.heappush(free, e)
+    return end
+
+
+def replay(tiles, life, lens, heads, slots):
+    """Modelled span of the layer under several row orders (the thresholds of
+    the library's buckets: long >= 2x the mean tile count, short <= 5/8)."""
+    b, a = np.polyfit(tiles.astype(float), life, 1)
+    t = (lens.astype(np.int64) + 15) // 16
+    S, total = t.size, int(t.sum())
+    bucket = [0 if 2 * t[s] * S >= 4 * total else (2 if 8 * t[s] * S <= 5 * total else 1) for s in range(S)]
+    nat = list(range(S))
+    orders = [("natural", nat),
+              ("long first", [s for s in nat if bucket[s] == 0] + [s for s in nat if bucket[s] != 0]),
+              ("long first, short last", [s for k in (0, 1, 2) for s in nat if bucket[s] == k]),
+              ("descending", sorted(nat, key=lambda s: -t[s]))]
+    print(f"  replay: life = {a:.2f} + {b:.3f} x tiles us, {slots} slots, {heads} CTAs a sequence")
+    for name, order in orders:
+        print(f"    {name:28s} modelled span {modelled_span(order, t, heads, slots, a, b):6.2f} us")
+    print(f"    {'all slots busy to the end':28s} {(a * S + b * total) * heads / slots:6.2f} us")
 
 if __name__ == "__main__":
     main()

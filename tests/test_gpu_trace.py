@@ -26,7 +26,7 @@ def trace_lib(tmp_path_factory):
 @pytest.mark.parametrize("workload,ctas", [("tiny", 16), ("llama3_8b", 2048)])
 def test_timeline_of_one_decode(trace_lib, workload, ctas):
     res = subprocess.run([sys.executable, "-m", "paged_kv_cache_217_gb300.trace", "--lib", trace_lib,
-                          "--workload", workload, "--calls", "3"],
+                          "--workload", workload, "--calls", "3", "--replay"],
                          cwd=ROOT, capture_output=True, text=True, timeout=600)
     assert res.returncode == 0, res.stderr[-2000:]
     lines = res.stdout.splitlines()
@@ -39,6 +39,7 @@ def test_timeline_of_one_decode(trace_lib, workload, ctas):
     assert f"{ctas} CTAs traced" in lines[1], res.stdout
     # every phase line is present and the mean lifetime is positive
     assert sum(1 for ln in lines if " us  median " in ln) == 6
+    assert sum(1 for ln in lines if "modelled span" in ln) == 4, res.stdout
     life = [ln for ln in lines if ln.strip().startswith("lifetime")][0]
     assert float(life.split("mean")[1].split("us")[0]) > 0.0
 

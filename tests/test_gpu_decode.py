@@ -320,6 +320,46 @@ def test_wide_grid_ring_shape(dtype, d, partition):
     assert B.device_status(clear=True) == 0
 
 
+def _dispatch_order(lens, max_len):
+    """The row order the ordering kernel promises, restated on the host: tiles
+    t = ceil(min(max(L, 0), max_len) / 16), mean over the batch; sequences with
+    t >= 2 x mean first, then those above 5/8 of the mean, then the rest, each
+    in natural order."""
+    t = [(min(max(int(L), 0), max_len) + 15) // 16 for L in lens]
+    S, total = len(t), sum(t)
+    longs = [s for s in range(S) if 2 * t[s] * S >= 4 * total]
+    shorts = [s for s in range(S) if s not in set(longs) and 8 * t[s] * S <= 5 * total]
+    rest = [s for s in range(S) if s not in set(longs) and s not in set(shorts)]
+    return longs + rest + shorts
+
+
+@pytest.mark.parametrize("S,hkv,seed", [(128, 8, 0), (150, 4, 1), (256, 8, 2), (1024, 4, 3)])
+def test_ordering_kernel_writes_the_promised_order(S, hkv, seed):
+    # the order array (int32[S], the last 16-byte-rounded bytes of the
+    # workspace, after any split-K scratch) is index work: it must equal the
+    # host restatement exactly
+    rng = np.random.default_rng(40 + seed)
+    lens = np.clip(np.round(150 * np.exp(0.6 * rng.standard_normal(S))), 8, 1024).astype(np.int32)
+    lens[rng.integers(0, S, 3)] = 0
+    lens[rng.integers(0, S, 2)] = 1024
+    case = H.make_case(lens, 2 * hkv, hkv, 64, "f16", seed=50 + seed)
+    mb = case.tables.shape[1]
+    need = B.workspace_size(S, 2 * hkv, hkv, 64, mb)
+    at = need - (4 * S + 15) // 16 * 16
+    assert at >= 0 and at % 16 == 0
+    ws = torch.full((need,), 0xFF, dtype=torch.uint8, device="cuda")
+    out = torch.empty_like(case.q)
+    B.paged_attention_decode(out, case.q, case.k_pool, case.v_pool, case.tables, case.lens, case.scale,
+                             workspace=ws)
+    torch.cuda.synchronize()
+    got = ws[at:at + 4 * S].view(torch.int32).cpu().tolist()
+    want = _dispatch_order(lens.tolist(), mb * 16)
+    assert got == want
+    assert sorted(got) == list(range(S))
+    _check_sampled(case, out, 16, seed=seed)
+    assert B.device_status(clear=True) == 0
+
+
 @pytest.mark.parametrize("dtype,hq,hkv,d", [("f16", 8, 4, 64), ("bf16", 4, 4, 128)])
 def test_batch_ranked_once_for_the_grid(dtype, hq, hkv, d):
     # 150 sequences (128..1024) in a grid of at most 4096 CTAs: the long-first

@@ -36,7 +36,9 @@ reshape_and_cache_kernel(const uint4* __restrict__ k, const uint4* __restrict__ 
   const int64_t tg = i / vec_per_row;
   const int gh = int(tg % num_kv_heads);
   const int64_t t = tg / num_kv_heads;
+  // the row and its slot are independent loads: both in flight at once
   const int64_t slot = __ldg(slots + t);
+  const uint4 kx = __ldg(k + i), vx = __ldg(v + i);
   if (slot < 0) return;
   if (slot >= num_slots) {
     if (gh == 0 && c == 0) flag(status, PKV_DEV_BAD_SLOT);
@@ -44,8 +46,8 @@ reshape_and_cache_kernel(const uint4* __restrict__ k, const uint4* __restrict__ 
   }
   const int64_t blk = slot / kBlock, off = slot % kBlock;
   const int64_t dst = ((blk * num_kv_heads + gh) * kBlock + off) * vec_per_row + c;
-  k_pool[dst] = __ldg(k + i);
-  v_pool[dst] = __ldg(v + i);
+  k_pool[dst] = kx;
+  v_pool[dst] = vx;
 }
 
 // ---- INT8 cache write ---------------------------------------------------
@@ -68,12 +70,18 @@ template <> struct Chunk<8> { using type = uint2; };
 template <> struct Chunk<16> { using type = uint4; };
 
 template <typename T, int D>
-__device__ __forceinline__ void quantize_row(const T* __restrict__ src, int8_t* __restrict__ codes,
+using RowChunk = typename Chunk<D / 32 * 2>::type;  // one lane's D/32 elements of a row
+
+template <typename T, int D>
+__device__ __forceinline__ RowChunk<T, D> load_row_chunk(const T* __restrict__ src, int lane) {
+  return __ldg(reinterpret_cast<const RowChunk<T, D>*>(src) + lane);
+}
+
+template <typename T, int D>
+__device__ __forceinline__ void quantize_row(const RowChunk<T, D>& raw, int8_t* __restrict__ codes,
                                              float* __restrict__ scale, int lane) {
   constexpr int E = D / 32;  // elements per lane
-  using In = typename Chunk<E * 2>::type;
   using Out = typename Chunk<E>::type;
-  const In raw = __ldg(reinterpret_cast<const In*>(src) + lane);
   const T* xs = reinterpret_cast<const T*>(&raw);
   float x[E];
   float m = 0.f;
@@ -109,15 +117,18 @@ reshape_and_cache_int8_kernel(const T* __restrict__ k, const T* __restrict__ v, 
   if (row >= rows) return;
   const int gh = int(row % num_kv_heads);
   const int64_t t = row / num_kv_heads;
+  // the rows and their slot are independent loads: all in flight at once
   const int64_t slot = __ldg(slots + t);
+  const RowChunk<T, D> kx = load_row_chunk<T, D>(k + row * D, lane);
+  const RowChunk<T, D> vx = load_row_chunk<T, D>(v + row * D, lane);
   if (slot < 0) return;
   if (slot >= num_slots) {
     if (gh == 0 && lane == 0) flag(status, PKV_DEV_BAD_SLOT);
     return;
   }
   const int64_t dst = ((slot / kBlock) * num_kv_heads + gh) * kBlock + slot % kBlock;  // pool row
-  quantize_row<T, D>(k + row * D, k_codes + dst * D, k_scale + dst, lane);
-  quantize_row<T, D>(v + row * D, v_codes + dst * D, v_scale + dst, lane);
+  quantize_row<T, D>(kx, k_codes + dst * D, k_scale + dst, lane);
+  quantize_row<T, D>(vx, v_codes + dst * D, v_scale + dst, lane);
 }
 
 template <typename T, int D>

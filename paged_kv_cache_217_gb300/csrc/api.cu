@@ -187,15 +187,15 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 // A pool [num_blocks][num_kv_heads][16][head_dim] seen as a 2-D tensor of
-// num_blocks*num_kv_heads*16 rows by head_dim columns, read in boxes of 16 rows
-// x 64 columns with the 128-byte swizzle.
+// num_blocks*num_kv_heads*16 rows by head_dim columns, read in boxes of
+// box_rows (16, 8 or 4) rows x 64 columns with the 128-byte swizzle.
 pkv_status_t pool_tensor_map(CUtensorMap* map, const void* pool, int64_t rows, int head_dim,
-                             pkv_dtype_t dtype) {
+                             pkv_dtype_t dtype, int box_rows) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (!enc) return pkv::fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
   const cuuint64_t dims[2] = {cuuint64_t(head_dim), cuuint64_t(rows)};
   const cuuint64_t strides[1] = {cuuint64_t(head_dim) * 2};
-  const cuuint32_t box[2] = {64, PKV_BLOCK_SIZE};
+  const cuuint32_t box[2] = {64, cuuint32_t(box_rows)};
   const cuuint32_t elem_strides[2] = {1, 1};
   const CUresult r = enc(map, dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
                          2, const_cast<void*>(pool), dims, strides, box, elem_strides,
@@ -366,13 +366,17 @@ pkv_status_t decode_impl(void* out, const void* q, const void* k_pool, const voi
   if (st != PKV_OK) return st;
 
   const int gpad = round_pow2_group(group);
-  alignas(64) CUtensorMap kmap, vmap;
+  // boxes of 16, 8 and 4 rows (the tensor-core kernel copies partial last
+  // tiles in 4-row multiples; the balanced schedule uses the first pair)
+  alignas(64) CUtensorMap kmap[3], vmap[3];
   if (gpad >= 2 || PKV_MMA_FOR_MHA) {
     const int64_t rows = int64_t(num_blocks) * num_kv_heads * PKV_BLOCK_SIZE;
-    st = pool_tensor_map(&kmap, k_pool, rows, head_dim, dtype);
-    if (st != PKV_OK) return st;
-    st = pool_tensor_map(&vmap, v_pool, rows, head_dim, dtype);
-    if (st != PKV_OK) return st;
+    for (int i = 0; i < 3; ++i) {
+      st = pool_tensor_map(&kmap[i], k_pool, rows, head_dim, dtype, PKV_BLOCK_SIZE >> i);
+      if (st != PKV_OK) return st;
+      st = pool_tensor_map(&vmap[i], v_pool, rows, head_dim, dtype, PKV_BLOCK_SIZE >> i);
+      if (st != PKV_OK) return st;
+    }
   }
 
   if (balanced) {
@@ -397,8 +401,8 @@ pkv_status_t decode_impl(void* out, const void* q, const void* k_pool, const voi
     // Arrival counters start at zero on every call; the slots need no initialisation.
     cudaError_t err = cudaMemsetAsync(b.counters, 0, sk.counter_bytes, stream);
     if (err != cudaSuccess) return cuda_status(err, "clear arrival counters");
-    err = dtype == PKV_F16 ? pkv::launch_decode_sk_f16(b, head_dim, gpad, &kmap, &vmap, stream)
-                           : pkv::launch_decode_sk_bf16(b, head_dim, gpad, &kmap, &vmap, stream);
+    err = dtype == PKV_F16 ? pkv::launch_decode_sk_f16(b, head_dim, gpad, kmap, vmap, stream)
+                           : pkv::launch_decode_sk_bf16(b, head_dim, gpad, kmap, vmap, stream);
     return cuda_status(err, "paged_attention_decode launch");
   }
 
@@ -445,8 +449,8 @@ pkv_status_t decode_impl(void* out, const void* q, const void* k_pool, const voi
                                 stream);
     if (err != cudaSuccess) return cuda_status(err, "sequence order launch");
   }
-  err = dtype == PKV_F16 ? pkv::launch_decode_f16(a, head_dim, gpad, &kmap, &vmap, stream)
-                         : pkv::launch_decode_bf16(a, head_dim, gpad, &kmap, &vmap, stream);
+  err = dtype == PKV_F16 ? pkv::launch_decode_f16(a, head_dim, gpad, kmap, vmap, stream)
+                         : pkv::launch_decode_bf16(a, head_dim, gpad, kmap, vmap, stream);
   return cuda_status(err, "paged_attention_decode launch");
 }
 

@@ -107,7 +107,12 @@ cudaError_t launch_decode_dg(const DecodeArgs& a, const CUtensorMap* kmap, const
     auto kern = paged_decode_mma_kernel<T, D, G, MW, MS>;
     cudaError_t err = configure_once(kern, C::SMEM_BYTES, configured);
     if (err != cudaSuccess) return err;
-    err = launch_pdl(kern, grid, dim3(MW * 32), C::SMEM_BYTES, stream, a, *kmap, *vmap);
+    PoolMaps maps;
+    for (int i = 0; i < 3; ++i) {
+      maps.k[i] = kmap[i];
+      maps.v[i] = vmap[i];
+    }
+    err = launch_pdl(kern, grid, dim3(MW * 32), C::SMEM_BYTES, stream, a, maps);
     if (err != cudaSuccess) return err;
   }
   return cudaGetLastError();

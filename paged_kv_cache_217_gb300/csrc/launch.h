@@ -15,7 +15,8 @@ constexpr int kMaxDevices = 64;
 
 // Decode. head_dim in {64,128,256}; gpad in {1,2,4,8}. gpad 1 runs the CUDA-core
 // kernel; gpad >= 2 runs the tensor-core kernel, which reads the pools through
-// the tensor maps kmap/vmap (128-byte swizzle, boxes of 16 rows x 64 columns).
+// the tensor maps kmap/vmap: three each, 128-byte swizzle, boxes of 16, 8 and
+// 4 rows x 64 columns (the balanced schedule reads the first of each).
 cudaError_t launch_decode_f16(const DecodeArgs& a, int head_dim, int gpad, const CUtensorMap* kmap,
                               const CUtensorMap* vmap, cudaStream_t stream);
 cudaError_t launch_decode_bf16(const DecodeArgs& a, int head_dim, int gpad, const CUtensorMap* kmap,

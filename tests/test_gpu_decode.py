@@ -320,6 +320,18 @@ def test_wide_grid_ring_shape(dtype, d, partition):
     assert B.device_status(clear=True) == 0
 
 
+@pytest.mark.parametrize("dtype,d", [("bf16", 128), ("f16", 64), ("bf16", 256)])
+@pytest.mark.parametrize("partition", [0, 16, 48])
+def test_every_partial_tile_size_on_the_tensor_cores(dtype, d, partition):
+    # lengths 1..48: the last tile of a sequence (or of a split part) holds
+    # every count of valid rows from 1 to 16, copied as boxes of 16, 8 and 4 rows
+    lens = np.arange(1, 49, dtype=np.int32)
+    case = H.make_case(lens, 8, 2, d, dtype, seed=60 + d)
+    out = _run(case, partition)
+    H.assert_attention_close(H.to_f64(out), H.oracle_full(case), f"partial tiles d={d} p={partition}")
+    assert B.device_status(clear=True) == 0
+
+
 def _dispatch_order(lens, max_len):
     """The row order the ordering kernel promises, restated on the host: tiles
     t = ceil(min(max(L, 0), max_len) / 16), mean over the batch; sequences with

@@ -166,6 +166,18 @@ def test_decode_int8_parity(dtype, hq, hkv, d, partition):
     assert B.device_status(clear=True) == 0
 
 
+@pytest.mark.parametrize("hq,hkv,d", [(8, 2, 128), (4, 4, 64), (4, 1, 256)])
+@pytest.mark.parametrize("partition", [0, 16])
+def test_decode_int8_every_partial_tile_size(hq, hkv, d, partition):
+    # lengths 1..48: the last code tile of a sequence (or of a split part)
+    # holds every count of valid rows from 1 to 16, copied as boxes of 16, 8
+    # and 4 rows
+    case = Int8Case(np.arange(1, 49), hq, hkv, d, "bf16", seed=70 + d)
+    got = H.to_f64(case.run(partition))
+    H.assert_attention_close(got, case.oracle(), f"int8 partial tiles hq={hq} hkv={hkv} d={d} p={partition}")
+    assert B.device_status(clear=True) == 0
+
+
 def test_decode_int8_split_partitions_long():
     # several partitions per sequence, the last one ragged, with the default schedule and explicit ones
     case = Int8Case([3000, 2049, 17, 4096], 16, 8, 128, "bf16", seed=21)

@@ -31,9 +31,13 @@ cudaError_t configure_once(K kern, size_t smem, bool (&configured)[kMaxDevices])
 #ifndef PKV_GRID_STAGES
 #define PKV_GRID_STAGES 2
 #endif
-// Shape of the tensor-core (group size >= 2) grid kernel.
+// Shape of the tensor-core (group size >= 2) grid kernel: 3 warps x 2 stages
+// (48 KB of ring, 4 CTAs per SM). Measured on GB300, Llama-3-8B-shaped layer
+// with the shortest sequences last and partial-tile boxes: 41.4 us with 4 x 2,
+// 40.9-41.0 with 3 x 2 (and 40.2-40.3 with 3 x 2 without the L2 prefetch);
+// three-stage rings (4 x 3, 3 x 3) and 2 x 4 were 46-52 us.
 #ifndef PKV_MMA_WARPS
-#define PKV_MMA_WARPS PKV_GRID_WARPS
+#define PKV_MMA_WARPS 3
 #endif
 #ifndef PKV_MMA_STAGES
 #define PKV_MMA_STAGES PKV_GRID_STAGES

@@ -16,8 +16,8 @@
 // ldmatrix reads of K rows (and the transposed reads of V rows) free of bank
 // conflicts, which rows 256 bytes apart would otherwise hit 8 ways.
 //
-// Each warp also asks for the tile after its ring into L2 (bulk prefetch),
-// which shortens the CTAs of short sequences by one DRAM round trip.
+// A switch (PKV_MMA_L2_AHEAD) makes each warp also ask for the tile after its
+// ring into L2 (bulk prefetch).
 //
 // P is fed to the PV product as two fp16/bf16 terms, hi = round(P) and
 // lo = round(P - hi), so the weights keep about 16 significant bits instead
@@ -109,11 +109,11 @@ constexpr bool kSplitQk = PKV_SPLIT_QK != 0;
 
 // Tiles of a warp, beyond its ring, asked into L2 ahead of their copy into
 // shared memory (0: none), so that a warp's next round trip after its ring
-// is an L2 hit. On GB300 one tile ahead took about 0.5 us off the 43.4 us
-// call of the Llama-3-8B-shaped layer (12 tiles per CTA, 3 per warp); 2, 4,
-// 8 and 16 ahead gained less.
+// is an L2 hit. On GB300, with 4-warp rings, one tile ahead took about 0.5 us
+// off the 43.4 us call of the Llama-3-8B-shaped layer; with the 3-warp rings
+// that replaced them (4 CTAs per SM) it costs 1 us (40.3 -> 41.3), so it is off.
 #ifndef PKV_MMA_L2_AHEAD
-#define PKV_MMA_L2_AHEAD 1
+#define PKV_MMA_L2_AHEAD 0
 #endif
 constexpr int kMmaL2Ahead = PKV_MMA_L2_AHEAD;
 

@@ -156,9 +156,12 @@ pkv_status_t pkv_selftest_bounded_wait(uint32_t limit_us, pkv_stream_t stream);
  * overlap on the GPU.
  *
  * Launch order: grids of at most 4096 CTAs start the sequences of at least
- * twice the batch's mean length first. For batches of 128 to 1024 sequences
- * that order is computed once, by a one-CTA kernel launched on `stream`
- * ahead of the decode, into num_seqs int32 at the end of the workspace.
+ * twice the batch's mean length (in 16-token tiles) first. For batches of 128
+ * to 1024 sequences that order is computed once, by a one-CTA kernel launched
+ * on `stream` ahead of the decode, into num_seqs int32 at the end of the
+ * workspace; it also puts sequences of at most 5/8 of the mean length last
+ * (each group in natural order). The order changes only when the work starts,
+ * never the results.
  * That kernel reads context_lens without waiting for the previous kernel on
  * the stream to finish when that kernel allows programmatic early launch
  * (the library's cache writes do, and never touch context_lens): a kernel

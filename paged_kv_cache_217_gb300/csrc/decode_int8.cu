@@ -14,6 +14,13 @@
 #ifndef PKV_INT8_STAGES
 #define PKV_INT8_STAGES 4
 #endif
+// Warps per CTA of the INT8 tensor-core kernel for groups of 2..8 query
+// heads (group size 1 keeps PKV_GRID_WARPS). Measured on GB300: the
+// Llama-3-8B-shaped layer 39.1 us with 4 warps, 37.5 us with 3 (4 CTAs per
+// SM); 3 warps for group size 1 made the LLaMA-13B layer 104.2 -> 113.7 us.
+#ifndef PKV_INT8_GQA_WARPS
+#define PKV_INT8_GQA_WARPS 3
+#endif
 
 namespace pkv {
 namespace {
@@ -21,7 +28,7 @@ namespace {
 template <typename T, int D, int G>
 cudaError_t launch_int8_dg(const DecodeArgs& a, const CUtensorMap* kmap, const CUtensorMap* vmap,
                            cudaStream_t stream) {
-  constexpr int NW = PKV_GRID_WARPS;
+  constexpr int NW = (PKV_INT8_MMA && G >= 2) ? PKV_INT8_GQA_WARPS : PKV_GRID_WARPS;
   constexpr int STAGES = PKV_INT8_STAGES;
   static bool configured[kMaxDevices] = {};
   const dim3 grid(kSeqFastest ? unsigned(a.num_seqs) : unsigned(a.num_kv_heads),

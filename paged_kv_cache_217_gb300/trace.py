@@ -27,6 +27,12 @@ import numpy as np
 
 PHASES = ["order (sequence known)", "length and block ids", "first tile landed", "tile loop", "merge and exit"]
 
+# The library's default bucket thresholds (PKV_LONG_FIRST_X2, PKV_SHORT_LAST_X8):
+# long when 2 * tiles * S >= LONG_FIRST_X2 * total, short when
+# 8 * tiles * S <= SHORT_LAST_X8 * total.
+LONG_FIRST_X2 = 4
+SHORT_LAST_X8 = 5
+
 
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
@@ -129,7 +135,8 @@ def replay(tiles, life, lens, heads, slots):
     b, a = np.polyfit(tiles.astype(float), life, 1)
     t = (lens.astype(np.int64) + 15) // 16
     S, total = t.size, int(t.sum())
-    bucket = [0 if 2 * t[s] * S >= 4 * total else (2 if 8 * t[s] * S <= 5 * total else 1) for s in range(S)]
+    bucket = [0 if 2 * t[s] * S >= LONG_FIRST_X2 * total else (2 if 8 * t[s] * S <= SHORT_LAST_X8 * total else 1)
+              for s in range(S)]
     nat = list(range(S))
     orders = [("natural", nat),
               ("long first", [s for s in nat if bucket[s] == 0] + [s for s in nat if bucket[s] != 0]),

@@ -10,9 +10,14 @@ copies when the step has any, and paged attention decode over every sequence
 (split-K decode plus its log-sum-exp merge when the partition choice splits).
 Inputs are synthetic (seeded N(0, 1) values, log-normal/uniform lengths,
 blocks scattered through a shuffled pool) with the shapes of the named model
-layers. The headline workload is the LLaMA-13B-shaped layer (batch 64,
-40 heads, head_dim 128, bf16, lengths log-normal median 512 sigma 0.8 clipped
-to [16, 2048]).
+layers. The headline workload is the largest one-GPU configuration, the
+OPT-175B-shaped long-context layer (batch 8, 96 heads MHA, head_dim 128, fp16,
+lengths uniform in [16384, 32768], blocks scattered through a shuffled pool).
+The same run also times the decode call of the LLaMA-13B, Llama-3-8B and
+OPT-66B parallel-sampling layers and reports each against the HBM roofline
+(``per_config``); for the sampling batch, whose sibling sequences share their
+prompt blocks, the roofline figure counts each shared block once (unique
+bytes), with the per-sequence (logical) figure beside it.
 
 value = algorithmic KV bytes read per step (sum over sequences of
 L * num_kv_heads * head_dim * 2 (K and V) * 2 bytes) / device time per step,
@@ -30,7 +35,11 @@ Under torchrun (N > 1) every rank runs the same workload on its own GPU
 slowest rank's time.
 
 ``--impl reference`` times the fp64 CPU oracle on the host cores on a bounded
-sample of the same workload and reports the same metric.
+sample of the same workload and reports the same metric. The oracle is split
+over the host's cores by KV heads (and, when there are more cores than KV
+heads, by sequences): each core runs it unchanged on its share. The
+``cpu_baseline`` of this library's arm times the oracle on one sample twice,
+on one thread and on all cores.
 """
 
 import argparse
@@ -332,20 +341,24 @@ def recorded_traffic(workload):
     return None
 
 
-def oracle_sample(wl, budget_s):
+def oracle_sample(wl, budget_s, max_pool_bytes=1 << 30):
     """A bounded sample of the workload for the CPU oracle: whole sequences (all
-    heads) in workload order until about budget_s seconds of oracle work, with
-    the used blocks gathered into a small pool (table relabelled to match)."""
+    heads) in workload order until about budget_s seconds of single-thread
+    oracle work (at least one sequence, and no more once the gathered pool
+    reaches max_pool_bytes), with the used blocks gathered into a small pool
+    (table relabelled to match)."""
     import torch
     from paged_kv_cache_217_gb300 import workloads as W
-    seqs, est_s = [], 0.0
+    row_bytes = wl.d + 4 if wl.kv == "int8" else wl.d * 2
+    seqs, est_s, pool_bytes = [], 0.0, 0
     for s in range(wl.num_seqs):
         L = int(wl.lens_h[s])
         if wl.window > 0:
             L = min(L, wl.window)
         est_s += L * wl.hkv * ORACLE_S_PER_TOKEN_HEAD + 2e-4 * wl.hq
+        pool_bytes += -(-int(wl.lens_h[s]) // 16) * 16 * wl.hkv * row_bytes * 2
         seqs.append(s)
-        if est_s >= budget_s:
+        if est_s >= budget_s or pool_bytes >= max_pool_bytes:
             break
     blocks = sorted({int(b) for s in seqs for b in wl.tables_h[s, :-(-int(wl.lens_h[s]) // 16)]})
     remap = {b: i for i, b in enumerate(blocks)}
@@ -357,73 +370,243 @@ def oracle_sample(wl, budget_s):
         idx = torch.tensor(blocks if blocks else [0], dtype=torch.int64, device=wl.k_pool.device)
         kp = W.to_numpy_storage(wl.k_pool.index_select(0, idx), wl.dtype)
         vp = W.to_numpy_storage(wl.v_pool.index_select(0, idx), wl.dtype)
-        ks = vs = np.zeros(0, np.float32)
+        ks = vs = None
     tab = np.full((len(seqs), wl.tables_h.shape[1]), -1, np.int32)
     for i, s in enumerate(seqs):
         nb = -(-int(wl.lens_h[s]) // 16)
         tab[i, :nb] = [remap[int(b)] for b in wl.tables_h[s, :nb]]
     q = W.to_numpy_storage(wl.q_h[seqs], wl.dtype)
     lens = wl.lens_h[seqs]
-    row_bytes = wl.d + 4 if wl.kv == "int8" else wl.d * 2
     attended = np.minimum(lens, wl.window) if wl.window > 0 else lens
     return dict(q=q, kp=kp, vp=vp, ks=ks, vs=vs, tab=tab, lens=lens, seqs=len(seqs),
                 bytes=int(attended.astype(np.int64).sum()) * wl.hkv * row_bytes * 2)
 
 
-# rough cost of the oracle per (token, KV head): two row gathers plus the fp64 math
+# rough single-thread cost of the oracle per (token, KV head): two row gathers
+# plus the fp64 math (measured about 1.4e-6 s on the GPU machine's host; kept
+# pessimistic so a sample never overruns its budget)
 ORACLE_S_PER_TOKEN_HEAD = 4e-6
 
 
-def time_oracle(wl, sample, repeats):
-    """Runs the oracle `repeats` times on the sample in a fresh single-threaded
-    process (spawned, so no CUDA state is inherited) and returns the seconds of
-    each run."""
+def host_cores():
+    """Host cores this process may run on."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def _shares(sample, hkv, cores):
+    """Splits the sample over at most `cores` workers: KV heads into
+    min(cores, hkv) contiguous ranges, then, with cores to spare, sequences
+    into cores // that many ranges of about equal tokens. Attention of one (sequence, KV head) does not
+    depend on any other, so each share is a complete oracle problem."""
+    n_h = max(1, min(cores, hkv))
+    n_s = max(1, min(cores // n_h, sample["seqs"]))
+    h_cuts = [round(i * hkv / n_h) for i in range(n_h + 1)]
+    tok = np.cumsum(sample["lens"].astype(np.int64))
+    total = int(tok[-1]) if tok.size else 0
+    s_cuts = [0] + [int(np.searchsorted(tok, total * i / n_s, side="left")) + 1 for i in range(1, n_s)] + \
+        [sample["seqs"]]
+    s_cuts = sorted(set(min(max(c, 0), sample["seqs"]) for c in s_cuts))
+    out = []
+    for h0, h1 in zip(h_cuts[:-1], h_cuts[1:]):
+        for s0, s1 in zip(s_cuts[:-1], s_cuts[1:]):
+            if h1 > h0 and s1 > s0:
+                out.append((h0, h1, s0, s1))
+    return out
+
+
+_WORKER = r"""
+import sys, time
+import numpy as np
+sys.path.insert(0, %(root)r)
+import oracle.attention as OA, oracle.quant as OQ
+z = np.load(%(path)r)
+a = [z[k] for k in %(names)s]
+print("ready", flush=True)
+for _ in range(%(repeats)d):
+    sys.stdin.readline()
+    t0, p0 = time.time(), time.perf_counter()
+    %(call)s(*a, %(scale)r, %(hkv)d, %(dtype)r%(extra)s)
+    print(t0, time.time(), time.perf_counter() - p0, flush=True)
+"""
+
+
+def time_oracle(wl, sample, repeats, cores=1):
+    """Runs the oracle `repeats` times on the sample, split over `cores`
+    single-threaded worker processes (fresh interpreters: no CUDA state is
+    inherited), each running the oracle unchanged on its share. All workers
+    load their share first; each repeat then starts them together, and its
+    time is the wall time from the first start to the last finish. Returns
+    (seconds of each repeat, number of workers)."""
+    G = wl.hq // wl.hkv
+    shares = _shares(sample, wl.hkv, cores)
+    if wl.kv == "int8":
+        names, call = "('q', 'kp', 'vp', 'ks', 'vs', 'tab', 'lens')", "OQ.paged_attention_decode_int8"
+    else:
+        names = "('q', 'kp', 'vp', 'tab', 'lens')"
+        call = "OA.paged_attention_decode_window" if wl.window > 0 else "OA.paged_attention_decode"
+    extra = f", {int(wl.window)}" if (wl.window > 0 and wl.kv != "int8") else ""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    procs = []
     with tempfile.TemporaryDirectory() as td:
-        path = os.path.join(td, "sample.npz")
-        np.savez(path, q=sample["q"], kp=sample["kp"], vp=sample["vp"], ks=sample["ks"], vs=sample["vs"],
-                 tab=sample["tab"], lens=sample["lens"])
-        extra = ""
-        if wl.kv == "int8":
-            names, call = "('q', 'kp', 'vp', 'ks', 'vs', 'tab', 'lens')", "OQ.paged_attention_decode_int8"
-        elif wl.window > 0:
-            names, call = "('q', 'kp', 'vp', 'tab', 'lens')", "OA.paged_attention_decode_window"
-            extra = f", {int(wl.window)}"
-        else:
-            names, call = "('q', 'kp', 'vp', 'tab', 'lens')", "OA.paged_attention_decode"
-        code = ("import sys, time, numpy as np; sys.path.insert(0, %r)\n"
-                "import oracle.attention as OA, oracle.quant as OQ\n"
-                "z = np.load(%r)\n"
-                "a = [z[k] for k in %s]\n"
-                "for _ in range(%d):\n"
-                "    t = time.perf_counter()\n"
-                "    %s(*a, %r, %d, %r%s)\n"
-                "    print(time.perf_counter() - t, flush=True)\n") % (
-                    ROOT, path, names, repeats, call, wl.scale, wl.hkv, wl.dtype, extra)
-        env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
-        res = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env,
-                             timeout=3600)
-        if res.returncode != 0:
-            raise RuntimeError(f"oracle run failed: {res.stderr.strip()[-300:]}")
-        return [float(x) for x in res.stdout.split()]
+        try:
+            for i, (h0, h1, s0, s1) in enumerate(shares):
+                path = os.path.join(td, f"share{i}.npz")
+                arrs = dict(q=sample["q"][s0:s1, h0 * G:h1 * G], kp=sample["kp"][:, h0:h1],
+                            vp=sample["vp"][:, h0:h1], tab=sample["tab"][s0:s1], lens=sample["lens"][s0:s1])
+                if wl.kv == "int8":
+                    arrs.update(ks=sample["ks"][:, h0:h1], vs=sample["vs"][:, h0:h1])
+                np.savez(path, **{k: np.ascontiguousarray(v) for k, v in arrs.items()})
+                code = _WORKER % dict(root=ROOT, path=path, names=names, repeats=repeats, call=call,
+                                      scale=wl.scale, hkv=h1 - h0, dtype=wl.dtype, extra=extra)
+                procs.append(subprocess.Popen([sys.executable, "-c", code], stdin=subprocess.PIPE,
+                                              stdout=subprocess.PIPE, stderr=subprocess.PIPE, text=True,
+                                              env=env))
+            for p in procs:
+                if p.stdout.readline().strip() != "ready":
+                    raise RuntimeError(f"oracle worker failed: {p.stderr.read()[-300:]}")
+            walls = []
+            for _ in range(repeats):
+                for p in procs:
+                    p.stdin.write("go\n")
+                    p.stdin.flush()
+                marks = []
+                for p in procs:
+                    ln = p.stdout.readline().split()
+                    if len(ln) != 3:
+                        raise RuntimeError(f"oracle worker failed: {p.stderr.read()[-300:]}")
+                    marks.append((float(ln[0]), float(ln[1]), float(ln[2])))
+                if len(procs) == 1:
+                    walls.append(marks[0][2])
+                else:
+                    walls.append(max(m[1] for m in marks) - min(m[0] for m in marks))
+            for p in procs:
+                p.stdin.close()
+                p.wait(timeout=60)
+        finally:
+            for p in procs:
+                if p.poll() is None:
+                    p.kill()
+    return walls, len(shares)
 
 
-def describe_sample(wl, sample, secs):
+def describe_sample(wl, sample, secs, workers):
+    how = "1 thread" if workers == 1 else f"{workers} single-threaded processes (one per core, split by KV heads" + \
+        (" and sequences)" if workers > wl.hkv else ")")
     return (f"{sample['seqs']} of {wl.num_seqs} sequences (all {wl.hq} heads, {int(sample['lens'].sum())} "
-            f"tokens, {sample['bytes'] / 1e6:.1f} MB KV) through the fp64 NumPy oracle, 1 thread, "
-            f"{secs:.3f} s per pass")
+            f"tokens, {sample['bytes'] / 1e6:.1f} MB KV) through the fp64 NumPy oracle, {how}, "
+            f"{secs:.4g} s per pass")
 
 
 def cpu_baseline(wl, budget_s=12.0):
+    """The oracle on one bounded sample of the workload, on one thread and on
+    every host core (the same sample split by KV heads)."""
     sample = oracle_sample(wl, budget_s)
-    secs = time_oracle(wl, sample, 1)[0]
-    return {"value": round(sample["bytes"] / secs / 1e9, 5), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": describe_sample(wl, sample, secs),
+    secs = time_oracle(wl, sample, 1)[0][0]
+    cores = host_cores()
+    line = {"value": round(sample["bytes"] / secs / 1e9, 5), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": describe_sample(wl, sample, secs, 1),
             "seqs_layers_per_s": round(sample["seqs"] / secs, 3)}
+    if cores > 1:
+        walls, workers = time_oracle(wl, sample, 2, cores)
+        par = min(walls)
+        line["all_cores"] = {"value": round(sample["bytes"] / par / 1e9, 5), "unit": "GB/s", "cores": workers,
+                             "host_cores": cores, "os_cpu_count": os.cpu_count(),
+                             "sample": describe_sample(wl, sample, par, workers),
+                             "seqs_layers_per_s": round(sample["seqs"] / par, 3)}
+    return line
 
 
 # ---------------------------------------------------------------------------
 # arms
 # ---------------------------------------------------------------------------
+PER_CONFIG = ["llama13b", "llama3_8b", "opt66b_sampling", "opt175b_long"]
+
+
+def launches_per_step(wl, B):
+    """This library's kernels in one step: the cache write, the decode (its
+    split-K merge runs inside it), and the one-CTA ordering kernel that
+    batches of 128..1024 sequences in grids of at most 4096 CTAs get (see
+    pkv_paged_attention_decode)."""
+    part = B.resolved_partition(wl.num_seqs, wl.hq, wl.hkv, wl.d, wl.tables_h.shape[1], wl.partition)
+    parts = 1 if part in (-1, B.BALANCED) else -(-wl.tables_h.shape[1] * 16 // part)
+    ordered = part != B.BALANCED and 128 <= wl.num_seqs <= 1024 and wl.num_seqs * wl.hkv * parts <= 4096
+    return part, 2 + (1 if ordered else 0)
+
+
+def time_steps(wl, B, K, flush, stream):
+    """K steps on device-resident inputs, L2 evicted (a read of `flush`)
+    before each, outside the events. Returns the per-step event times (ms) of
+    the whole step and of the decode call."""
+    import torch
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for k in range(K):
+        flush.sum()                                   # evict L2 with clean lines between steps
+        e_start, e_mid, e_end = ev[k]
+        e_start.record(stream)
+        cache_write(wl, B)
+        e_mid.record(stream)
+        decode(wl, B)
+        e_end.record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(c) for a, _, c in ev], [b.elapsed_time(c) for _, b, c in ev]
+
+
+def roofline_figures(wl, dec_ms, peak):
+    """Decode-call throughput on the bytes HBM must move: every attended token's
+    K and V once, and for batches whose sequences share prompt blocks each
+    shared block once (unique bytes); the per-sequence (logical) figure, which
+    counts L2 hits of shared blocks as well, goes beside it."""
+    hbm_bytes = wl.unique_kv_bytes or wl.kv_bytes
+    achieved = hbm_bytes / (dec_ms * 1e-3) / 1e9
+    fig = {"achieved": round(achieved, 1), "frac": round(achieved / peak, 4),
+           "pct_of_nominal_8000GBs": round(100 * achieved / NOMINAL_HBM_GBS, 2),
+           "algorithmic_bytes_per_launch": hbm_bytes,
+           "bytes_counted": "unique (each shared block once)" if wl.unique_kv_bytes else "every attended token"}
+    if wl.unique_kv_bytes:
+        fig["logical_bytes_per_launch"] = wl.kv_bytes
+        fig["achieved_logical"] = round(wl.kv_bytes / (dec_ms * 1e-3) / 1e9, 1)
+    return fig
+
+
+def traffic_key(name, kv, window):
+    return name + ("" if kv == "native" else f"-{kv}") + (f"-w{window}" if window > 0 else "")
+
+
+def per_config_entry(name, args, device, B, flush, stream, peak):
+    import torch
+    wl = build_workload(name, args.seed, device, args.kv, 0)
+    wl.partition = 0
+    device_inputs(wl, device)
+    part, _ = launches_per_step(wl, B)
+    for _ in range(max(3, args.warmup)):
+        step(wl, B)
+    torch.cuda.synchronize()
+    _, dec = time_steps(wl, B, args.per_config_steps, flush, stream)
+    flags = B.device_status(clear=True)
+    if flags:
+        raise RuntimeError(f"device checks tripped on {name}: {B.describe_device_flags(flags)}")
+    dec_ms = statistics.mean(dec)
+    fig = roofline_figures(wl, dec_ms, peak)
+    entry = {"workload": wl.description, "num_seqs": wl.num_seqs, "steps": args.per_config_steps,
+             "schedule": schedule_name(part, B), "decode_us": round(dec_ms * 1e3, 2),
+             "decode_us_median": round(statistics.median(dec) * 1e3, 2), **fig,
+             "traffic": recorded_traffic(traffic_key(name, args.kv, 0)),
+             "meets_70pct_of_measured": fig["frac"] >= 0.70,
+             "meets_70pct_of_nominal": fig["pct_of_nominal_8000GBs"] >= 70.0}
+    del wl
+    torch.cuda.empty_cache()
+    return entry
+
+
+def schedule_name(part, B):
+    return ("balanced persistent (equal tiles per warp)" if part == B.BALANCED else
+            "one pass per (sequence, KV head)" if part == -1 else f"split-K, {part}-token partitions")
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -451,13 +634,7 @@ def run_ours(args):
     # L2 eviction buffer: read (not written) between timed steps, so the next
     # step starts with L2 full of clean, unrelated lines and pays no write-backs.
     flush = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=device)
-    part = B.resolved_partition(wl.num_seqs, wl.hq, wl.hkv, wl.d, wl.tables_h.shape[1], args.partition)
-    # reshape_and_cache + decode (the split-K merge runs inside the decode kernel),
-    # plus the one-CTA ordering kernel that batches of 128..1024 sequences in
-    # grids of at most 4096 CTAs get (see pkv_paged_attention_decode)
-    parts = 1 if part in (-1, B.BALANCED) else -(-wl.tables_h.shape[1] * 16 // part)
-    ordered = part != B.BALANCED and 128 <= wl.num_seqs <= 1024 and wl.num_seqs * wl.hkv * parts <= 4096
-    launches_per_step = 2 + (1 if ordered else 0)
+    part, n_launch = launches_per_step(wl, B)
 
     for _ in range(args.warmup):
         step(wl, B)
@@ -466,29 +643,17 @@ def run_ours(args):
 
     stream = torch.cuda.current_stream(device)
     K = args.steps
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-           torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     sampler = ClockSampler(local)
     sampler.start()
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     t0 = sampler.mark()
-    for k in range(K):
-        flush_sum = flush.sum()                                  # evict L2 with clean lines between steps
-        e_start, e_mid, e_end = ev[k]
-        e_start.record(stream)
-        cache_write(wl, B)
-        e_mid.record(stream)
-        decode(wl, B)
-        e_end.record(stream)
-    torch.cuda.synchronize()
+    step_ms, decode_ms = time_steps(wl, B, K, flush, stream)
     if world > 1:
         dist.barrier()
     t1 = sampler.mark()
     clocks = sampler.stop(t0, t1)
-    step_ms = [a.elapsed_time(c) for a, _, c in ev]
-    decode_ms = [b.elapsed_time(c) for _, b, c in ev]
     total_ms = float(sum(step_ms))
     flags = B.device_status(clear=True)
     if flags:
@@ -503,7 +668,7 @@ def run_ours(args):
     e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(Ke)]
     torch.cuda.synchronize()
     for k in range(Ke):
-        flush_sum = flush.sum()
+        flush.sum()
         s_, e_ = e2e_ev[k]
         s_.record(stream)
         wl.pack_dev.copy_(wl.pack_host, non_blocking=True)   # q, new K/V, tables, lengths, slots
@@ -521,9 +686,7 @@ def run_ours(args):
     peak, peak_kind = measured_peak()
     value = whole_job_gbs(wl.kv_bytes, per_step_ms, world)
     dec_ms = statistics.mean(decode_ms)
-    achieved = wl.kv_bytes / (dec_ms * 1e-3) / 1e9
-    traffic = recorded_traffic(args.workload + ("" if args.kv == "native" else f"-{args.kv}")
-                               + (f"-w{args.window}" if args.window > 0 else ""))
+    fig = roofline_figures(wl, dec_ms, peak)
     line = {
         "metric": METRIC,
         "value": round(value, 1),
@@ -545,8 +708,7 @@ def run_ours(args):
             "kv_cache": "int8 codes + fp32 row scales, fp32 math" if wl.kv == "int8" else f"{wl.dtype}",
             "num_seqs": wl.num_seqs,
             "kv_bytes_per_step": wl.kv_bytes,
-            "schedule": ("balanced persistent (equal tiles per warp)" if part == B.BALANCED else
-                         "one pass per (sequence, KV head)" if part == -1 else f"split-K, {part}-token partitions"),
+            "schedule": schedule_name(part, B),
             "l2": f"KV working set {wl.kv_bytes / 1e6:.0f} MB > 129 MB L2, and L2 flushed "
                   f"(a {L2_FLUSH_BYTES >> 20} MB read) between timed steps outside the timed events",
             "parallelism": "replicas" if world > 1 else "single GPU",
@@ -560,13 +722,13 @@ def run_ours(args):
             "bound": "hbm",
             "kernel": ("paged_decode_kernel<KvInt8>" if wl.kv == "int8" else "paged_decode_kernel") +
                       " (+ its LSE merge when split)",
-            "achieved": round(achieved, 1),
+            "achieved": fig["achieved"],
             "peak": peak,
             "peak_kind": f"{peak_kind} (copy bandwidth, burst)",
             "unit": "GB/s",
-            "frac": round(achieved / peak, 4),
-            "traffic": traffic,
-            "algorithmic_bytes_per_launch": wl.kv_bytes,
+            "frac": fig["frac"],
+            "traffic": recorded_traffic(traffic_key(args.workload, args.kv, args.window)),
+            **{k: v for k, v in fig.items() if k not in ("achieved", "frac")},
             "decode_ms": round(dec_ms, 5),
         },
         "e2e": {
@@ -576,7 +738,7 @@ def run_ours(args):
             "d2h_bytes_per_step": d2h,
             "ms_per_step": round(e2e_ms, 5),
         },
-        "gpu_launches": K * launches_per_step,
+        "gpu_launches": K * n_launch,
         "clocks": clocks,
     }
     if wl.unique_kv_bytes:
@@ -584,6 +746,26 @@ def run_ours(args):
         line["unique_bytes_gbs"] = round(world * wl.unique_kv_bytes / (per_step_ms * 1e-3) / 1e9, 1)
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(wl)
+    if not args.no_per_config and world == 1 and args.window == 0:
+        # the decode call of every target layer, timed the same way (each
+        # workload built, timed and freed in turn; the headline's own figures
+        # are reused)
+        main_entry = {"workload": wl.description, "num_seqs": wl.num_seqs, "steps": K,
+                      "schedule": schedule_name(part, B), "decode_us": round(dec_ms * 1e3, 2),
+                      "decode_us_median": round(statistics.median(decode_ms) * 1e3, 2), **fig,
+                      "traffic": line["roofline"]["traffic"],
+                      "meets_70pct_of_measured": fig["frac"] >= 0.70,
+                      "meets_70pct_of_nominal": fig["pct_of_nominal_8000GBs"] >= 70.0}
+        keep_main = args.partition == 0 and args.workload in PER_CONFIG
+        del wl
+        torch.cuda.empty_cache()
+        per = {}
+        for name in PER_CONFIG:
+            if name == args.workload and keep_main:
+                per[name] = main_entry
+            else:
+                per[name] = per_config_entry(name, args, device, B, flush, stream, peak)
+        line["per_config"] = {"peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "configs": per}
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
@@ -599,9 +781,13 @@ def run_reference(args):
     device = "cuda" if torch.cuda.is_available() else "cpu"
     wl = build_workload(args.workload, args.seed, device, args.kv, args.window)
     total = args.steps + args.warmup
+    cores = host_cores()
+    # each step is one pass over a sample sized to about `budget` seconds of
+    # wall time on all cores (single-thread estimate x cores)
     budget = min(6.0, max(0.02, args.reference_budget / total))
-    sample = oracle_sample(wl, budget)
-    secs = time_oracle(wl, sample, total)[args.warmup:]
+    sample = oracle_sample(wl, budget * cores, max_pool_bytes=512 << 20)
+    walls, workers = time_oracle(wl, sample, total, cores)
+    secs = walls[args.warmup:]
     per = statistics.mean(secs)
     gbs = sample["bytes"] / per / 1e9
     line = {
@@ -622,8 +808,8 @@ def run_reference(args):
         "config": {"workload": wl.description, "num_seqs": wl.num_seqs, "kv_bytes_per_step": wl.kv_bytes,
                    "sample_kv_bytes_per_step": sample["bytes"]},
         "seqs_layers_per_s": round(sample["seqs"] / per, 3),
-        "cpu_baseline": {"value": round(gbs, 5), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": describe_sample(wl, sample, per)},
+        "cpu_baseline": {"value": round(gbs, 5), "unit": "GB/s", "cores": workers, "kind": "oracle",
+                         "host_cores": cores, "sample": describe_sample(wl, sample, per, workers)},
         "e2e": {"value": round(gbs, 5), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -635,7 +821,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="llama13b",
+    ap.add_argument("--workload", default="opt175b_long",
                     choices=["llama13b", "llama3_8b", "opt66b_sampling", "opt175b_long", "llama13b_beam", "tiny"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--window", type=int, default=0,
@@ -646,6 +832,10 @@ def main(argv=None):
                     help="decode schedule: 0 = library choice, -1 = one CTA per (sequence, KV head), "
                          "N = split-K partitions of N tokens")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip timing the decode call of the other target layers (per_config)")
+    ap.add_argument("--per-config-steps", type=int, default=100,
+                    help="timed steps of each per_config layer")
     ap.add_argument("--lib", default=None,
                     help="load this libpaged_kv.so instead of the package's own (a variant built with "
                          "python -m paged_kv_cache_217_gb300.build --out-dir DIR --define NAME=VALUE)")

@@ -50,6 +50,11 @@
  *    arguments are checked on the host before anything is launched; on a
  *    failed check nothing is launched and the status says why
  *    (pkv_last_error_string gives the detail, per calling thread).
+ *  - Per-device state of the library (the device status word, the scratch of
+ *    pkv_paged_attention_decode_noalloc) is looked up on the current CUDA
+ *    device, once per device index, and kept for the life of the process:
+ *    make the device of the pointers and of `stream` current before a call,
+ *    and do not use the library across a cudaDeviceReset.
  *  - Device-resident indices (block ids, context lengths, slots, pairs) are
  *    checked by the kernels. A bad index never faults: the kernel records a
  *    flag in the device status word (pkv_device_status), skips the access or
@@ -211,13 +216,20 @@ int pkv_paged_attention_partition(
  * (pkv_paged_attention_workspace_size) exceeds it return PKV_ERR_UNSUPPORTED
  * and launch nothing; a larger partition_size or -1 (one pass) needs less.
  *
- * The first call on a device looks up the array's device address (once per
- * device, with that device current); make that first call before any stream
- * capture. Every call on a device shares the one array, which keeps the last
- * call's contents; the only part that must start at zero (the split-K
- * arrival counters) is cleared on `stream` by every call. Calls that overlap
- * on the GPU (different streams, or different host threads) race on it.
- * No cudaMalloc, cudaFree or other allocating routine is called.
+ * The array used is the one of the current CUDA device, which must be the
+ * device of `stream` and of every pointer argument. The first call on a
+ * device looks up the array's device address (once per device index, with
+ * that device current) and caches it for the life of the process; make that
+ * first call before any stream capture. The cached address belongs to the
+ * device's primary context: do not call this entry point again after a
+ * cudaDeviceReset (or any other teardown of that context) in the same
+ * process. Every call on a device shares the one array, which keeps the last
+ * call's contents; the parts that must start at zero (the arrival counters of
+ * the split-K and balanced schedules) are cleared on `stream` by every call,
+ * and everything else a call reads from the array it first writes itself.
+ * Calls that overlap on the GPU (different streams, or different host
+ * threads) race on it. No cudaMalloc, cudaFree or other allocating routine
+ * is called.
  */
 #define PKV_NOALLOC_SCRATCH_BYTES (32u << 20) /* 32 MiB */
 

@@ -152,6 +152,16 @@ def _stream_ptr(device):
     return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
 
 
+def _launch(device, what, fn, *args):
+    """Calls a launching entry point with ``device`` current and its current
+    torch stream as the trailing cudaStream_t: the library looks up per-device
+    state (the status word, the no-alloc scratch) on the current device, which
+    must be the device of the tensors and of the stream."""
+    import torch
+    with torch.cuda.device(device):
+        _check(fn(*args, _stream_ptr(device)), what)
+
+
 _workspaces = {}
 
 
@@ -208,10 +218,10 @@ def paged_attention_decode(out, q, k_pool, v_pool, block_tables, context_lens, s
     if need:
         ws = workspace if workspace is not None else _workspace(q.device, need)
         ws_ptr, ws_bytes = ws.data_ptr(), ws.numel() * ws.element_size()
-    _check(lib().pkv_paged_attention_decode(
-        out.data_ptr(), q.data_ptr(), k_pool.data_ptr(), v_pool.data_ptr(), block_tables.data_ptr(),
-        context_lens.data_ptr(), S, Hq, num_kv_heads, D, mb, nb, float(scale), dt, int(partition_size),
-        ws_ptr, ws_bytes, _stream_ptr(q.device)), "paged_attention_decode")
+    _launch(q.device, "paged_attention_decode", lib().pkv_paged_attention_decode,
+            out.data_ptr(), q.data_ptr(), k_pool.data_ptr(), v_pool.data_ptr(), block_tables.data_ptr(),
+            context_lens.data_ptr(), S, Hq, num_kv_heads, D, mb, nb, float(scale), dt, int(partition_size),
+            ws_ptr, ws_bytes)
     return out
 
 
@@ -245,10 +255,10 @@ def paged_attention_decode_sliding(out, q, k_pool, v_pool, block_tables, context
     if need:
         ws = workspace if workspace is not None else _workspace(q.device, need)
         ws_ptr, ws_bytes = ws.data_ptr(), ws.numel() * ws.element_size()
-    _check(lib().pkv_paged_attention_decode_sliding(
-        out.data_ptr(), q.data_ptr(), k_pool.data_ptr(), v_pool.data_ptr(), block_tables.data_ptr(),
-        context_lens.data_ptr(), S, Hq, hkv, D, mb, nb, float(scale), dt, int(sliding_window),
-        int(partition_size), ws_ptr, ws_bytes, _stream_ptr(q.device)), "paged_attention_decode_sliding")
+    _launch(q.device, "paged_attention_decode_sliding", lib().pkv_paged_attention_decode_sliding,
+            out.data_ptr(), q.data_ptr(), k_pool.data_ptr(), v_pool.data_ptr(), block_tables.data_ptr(),
+            context_lens.data_ptr(), S, Hq, hkv, D, mb, nb, float(scale), dt, int(sliding_window),
+            int(partition_size), ws_ptr, ws_bytes)
     return out
 
 
@@ -276,10 +286,10 @@ def paged_attention_decode_noalloc(out, q, k_pool, v_pool, block_tables, context
     if tuple(out.shape) != (S, Hq, D) or block_tables.dim() != 2 or block_tables.shape[0] != S \
             or tuple(context_lens.shape) != (S,):
         raise ValueError("shape mismatch among out, q, block_tables and context_lens")
-    _check(lib().pkv_paged_attention_decode_noalloc(
-        out.data_ptr(), q.data_ptr(), k_pool.data_ptr(), v_pool.data_ptr(), block_tables.data_ptr(),
-        context_lens.data_ptr(), S, Hq, num_kv_heads, D, block_tables.shape[1], nb, float(scale), dt,
-        int(partition_size), _stream_ptr(q.device)), "paged_attention_decode_noalloc")
+    _launch(q.device, "paged_attention_decode_noalloc", lib().pkv_paged_attention_decode_noalloc,
+            out.data_ptr(), q.data_ptr(), k_pool.data_ptr(), v_pool.data_ptr(), block_tables.data_ptr(),
+            context_lens.data_ptr(), S, Hq, num_kv_heads, D, block_tables.shape[1], nb, float(scale), dt,
+            int(partition_size))
     return out
 
 
@@ -296,9 +306,9 @@ def reshape_and_cache(k, v, k_pool, v_pool, slot_mapping):
         raise ValueError("k, v: [T, Hkv, D]; pools: [num_blocks, Hkv, 16, D]; slot_mapping: [T]")
     if any(x.dtype != k.dtype for x in (v, k_pool, v_pool)):
         raise TypeError("k, v and pools must share one dtype")
-    _check(lib().pkv_reshape_and_cache(k.data_ptr(), v.data_ptr(), k_pool.data_ptr(), v_pool.data_ptr(),
-                                       slot_mapping.data_ptr(), T, hkv, D, k_pool.shape[0], dt,
-                                       _stream_ptr(k.device)), "reshape_and_cache")
+    _launch(k.device, "reshape_and_cache", lib().pkv_reshape_and_cache,
+            k.data_ptr(), v.data_ptr(), k_pool.data_ptr(), v_pool.data_ptr(),
+            slot_mapping.data_ptr(), T, hkv, D, k_pool.shape[0], dt)
 
 
 def copy_blocks(k_pool, v_pool, src_dst_pairs):
@@ -309,9 +319,9 @@ def copy_blocks(k_pool, v_pool, src_dst_pairs):
     if src_dst_pairs.dtype != torch.int64 or src_dst_pairs.dim() != 2 or src_dst_pairs.shape[1] != 2:
         raise ValueError("src_dst_pairs must be int64 [n, 2]")
     nb, hkv, bs, D = k_pool.shape
-    _check(lib().pkv_copy_blocks(k_pool.data_ptr(), v_pool.data_ptr(), src_dst_pairs.data_ptr(),
-                                 src_dst_pairs.shape[0], hkv, D, nb, dt, _stream_ptr(k_pool.device)),
-           "copy_blocks")
+    _launch(k_pool.device, "copy_blocks", lib().pkv_copy_blocks,
+            k_pool.data_ptr(), v_pool.data_ptr(), src_dst_pairs.data_ptr(),
+            src_dst_pairs.shape[0], hkv, D, nb, dt)
 
 
 # ---------------------------------------------------------------------------
@@ -340,10 +350,9 @@ def reshape_and_cache_int8(k, v, k_cache, v_cache, k_scale, v_scale, slot_mappin
     if v.shape != k.shape or v.dtype != k.dtype or k_cache.shape[1:] != (hkv, BLOCK_SIZE, D) \
             or tuple(slot_mapping.shape) != (T,):
         raise ValueError("k, v: [T, Hkv, D]; caches: [num_blocks, Hkv, 16, D]; slot_mapping: [T]")
-    _check(lib().pkv_reshape_and_cache_int8(
-        k.data_ptr(), v.data_ptr(), dt, k_cache.data_ptr(), v_cache.data_ptr(), k_scale.data_ptr(),
-        v_scale.data_ptr(), slot_mapping.data_ptr(), T, hkv, D, k_cache.shape[0], _stream_ptr(k.device)),
-        "reshape_and_cache_int8")
+    _launch(k.device, "reshape_and_cache_int8", lib().pkv_reshape_and_cache_int8,
+            k.data_ptr(), v.data_ptr(), dt, k_cache.data_ptr(), v_cache.data_ptr(), k_scale.data_ptr(),
+            v_scale.data_ptr(), slot_mapping.data_ptr(), T, hkv, D, k_cache.shape[0])
 
 
 def paged_attention_decode_int8(out, q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens, scale,
@@ -368,11 +377,10 @@ def paged_attention_decode_int8(out, q, k_cache, v_cache, k_scale, v_scale, bloc
     if need:
         ws = workspace if workspace is not None else _workspace(q.device, need)
         ws_ptr, ws_bytes = ws.data_ptr(), ws.numel() * ws.element_size()
-    _check(lib().pkv_paged_attention_decode_int8(
-        out.data_ptr(), q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), k_scale.data_ptr(),
-        v_scale.data_ptr(), block_tables.data_ptr(), context_lens.data_ptr(), S, Hq, hkv, D, mb, nb,
-        float(scale), dt, int(partition_size), ws_ptr, ws_bytes, _stream_ptr(q.device)),
-        "paged_attention_decode_int8")
+    _launch(q.device, "paged_attention_decode_int8", lib().pkv_paged_attention_decode_int8,
+            out.data_ptr(), q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), k_scale.data_ptr(),
+            v_scale.data_ptr(), block_tables.data_ptr(), context_lens.data_ptr(), S, Hq, hkv, D, mb, nb,
+            float(scale), dt, int(partition_size), ws_ptr, ws_bytes)
     return out
 
 
@@ -384,9 +392,10 @@ def copy_blocks_int8(k_cache, v_cache, k_scale, v_scale, src_dst_pairs):
     if src_dst_pairs.dtype != torch.int64 or src_dst_pairs.dim() != 2 or src_dst_pairs.shape[1] != 2:
         raise ValueError("src_dst_pairs must be int64 [n, 2]")
     nb, hkv, _, D = k_cache.shape
-    _check(lib().pkv_copy_blocks_int8(k_cache.data_ptr(), v_cache.data_ptr(), k_scale.data_ptr(),
-                                      v_scale.data_ptr(), src_dst_pairs.data_ptr(), src_dst_pairs.shape[0],
-                                      hkv, D, nb, _stream_ptr(k_cache.device)), "copy_blocks_int8")
+    _launch(k_cache.device, "copy_blocks_int8", lib().pkv_copy_blocks_int8,
+            k_cache.data_ptr(), v_cache.data_ptr(), k_scale.data_ptr(),
+            v_scale.data_ptr(), src_dst_pairs.data_ptr(), src_dst_pairs.shape[0],
+            hkv, D, nb)
 
 
 def check_copy_pairs(pairs, num_blocks):
@@ -436,7 +445,7 @@ def trace_stamp(words, index):
     if words.dtype != torch.int64 or not 0 <= index < words.numel() or not words.is_contiguous():
         raise ValueError("trace_stamp takes a contiguous int64 tensor and an index into it")
     ptr = words.data_ptr() + 8 * int(index)
-    _check(lib().pkv_trace_stamp(ptr, _stream_ptr(words.device)), "trace_stamp")
+    _launch(words.device, "trace_stamp", lib().pkv_trace_stamp, ptr)
 
 
 def describe_device_flags(flags):

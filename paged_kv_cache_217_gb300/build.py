@@ -65,9 +65,9 @@ def _cmd(nvcc, src, obj, ptxas_verbose, defines=()):
 def build(force=False, verbose=False, ptxas_verbose=False, defines=(), out_dir=None):
     """Compile every translation unit and link libpaged_kv.so; returns its path.
 
-    ``defines`` (NAME=VALUE strings) and ``out_dir`` build a variant (for
-    example another ring shape, PKV_SK_WARPS_CUDA / PKV_SK_WARPS_MMA /
-    PKV_SK_STAGES) into a directory of its own instead of the package.
+    ``defines`` (NAME=VALUE strings) and ``out_dir`` build a variant (the
+    per-CTA tracing build, PKV_TRACE=1, or the CUDA-core INT8 tile,
+    PKV_INT8_MMA=0) into a directory of its own instead of the package.
     """
     build_dir = os.path.join(out_dir, "_build") if out_dir else BUILD
     lib_path = os.path.join(out_dir, "libpaged_kv.so") if out_dir else LIB

@@ -86,15 +86,12 @@ int choose_partition(int num_seqs, int num_q_heads, int num_kv_heads, int head_d
 // sequences) 44.5 -> 43.4 us, its INT8 cache 43.2 -> 41.3 us; on the 64-
 // sequence LLaMA-13B layer the extra launch cost 0.9 %, so small batches keep
 // ranking in each CTA.
-#ifndef PKV_ORDER_KERNEL
-#define PKV_ORDER_KERNEL 1
-#endif
 constexpr int kOrderKernelMinSeqs = 128;
 bool long_first_grid(int num_seqs, int num_kv_heads, int max_parts) {
   return int64_t(num_seqs) * num_kv_heads * max_parts <= kLongFirstMaxCtas;
 }
 size_t order_bytes(int num_seqs, int num_kv_heads, int max_parts) {
-  if (!PKV_ORDER_KERNEL || num_seqs < kOrderKernelMinSeqs || num_seqs > pkv::kOrderMaxSeqs ||
+  if (num_seqs < kOrderKernelMinSeqs || num_seqs > pkv::kOrderMaxSeqs ||
       !long_first_grid(num_seqs, num_kv_heads, max_parts))
     return 0;
   return (size_t(num_seqs) * sizeof(int32_t) + 15) / 16 * 16;
@@ -369,7 +366,7 @@ pkv_status_t decode_impl(void* out, const void* q, const void* k_pool, const voi
   // boxes of 16, 8 and 4 rows (the tensor-core kernel copies partial last
   // tiles in 4-row multiples; the balanced schedule uses the first pair)
   alignas(64) CUtensorMap kmap[3], vmap[3];
-  if (gpad >= 2 || PKV_MMA_FOR_MHA) {
+  if (gpad >= 2) {
     const int64_t rows = int64_t(num_blocks) * num_kv_heads * PKV_BLOCK_SIZE;
     for (int i = 0; i < 3; ++i) {
       st = pool_tensor_map(&kmap[i], k_pool, rows, head_dim, dtype, PKV_BLOCK_SIZE >> i);

@@ -128,46 +128,26 @@ __device__ __forceinline__ void trace_write(const DecodeArgs& a, const TraceMark
 // the decode kernels comes after this.
 __device__ __forceinline__ void wait_for_predecessor() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
-// Grid layout of the one-CTA-per-(sequence, KV head) kernels: 0 = KV heads
-// vary fastest in launch order (blockIdx.x = head), 1 = sequences do.
-#ifndef PKV_GRID_SEQ_FASTEST
-#define PKV_GRID_SEQ_FASTEST 0
-#endif
-constexpr bool kSeqFastest = PKV_GRID_SEQ_FASTEST != 0;
+// Grid of the one-CTA-per-(sequence, KV head) kernels: blockIdx.x is the KV
+// head (fastest in launch order, so the heads of one sequence run side by
+// side), blockIdx.y the sequence's rank in the launch order, blockIdx.z the
+// split-K partition.
 
-// Route group size 1 (MHA) to the tensor-core tile as well (measurement knob;
-// CUDA cores by default).
-#ifndef PKV_MMA_FOR_MHA
-#define PKV_MMA_FOR_MHA 0
-#endif
-
-// Packed fp32 FMAs (fma.rn.f32x2) in the CUDA-core tile math.
-#ifndef PKV_PACKED_FMA
-#define PKV_PACKED_FMA 0
-#endif
-constexpr bool kPackedFma = PKV_PACKED_FMA != 0;
-
-#ifndef PKV_ORDER_MAX_SEQS
-#define PKV_ORDER_MAX_SEQS 1024
-#endif
-constexpr int kOrderMaxSeqs = PKV_ORDER_MAX_SEQS;  // batches up to this size start long sequences first
-// A sequence is "long" when its tile count is at least PKV_LONG_FIRST_X2 / 2
-// times the batch mean (2x by default).
-#ifndef PKV_LONG_FIRST_X2
-#define PKV_LONG_FIRST_X2 4
-#endif
-constexpr long long kLongFirstX2 = PKV_LONG_FIRST_X2;
+// Batches of up to this many sequences start long sequences first.
+constexpr int kOrderMaxSeqs = 1024;
+// A sequence is "long" when its tile count is at least kLongFirstX2 / 2 times
+// the batch mean (2x). Measured on GB300 (threshold x mean -> decode call µs):
+// Llama-3-8B-shaped layer 1.5 -> 43.7, 2 -> 43.4, 2.5 -> 43.6, 4 -> 46.7;
+// LLaMA-13B-shaped layer 2 -> 133.2, 2.5 -> 132.8, 3 -> 148.3.
+constexpr long long kLongFirstX2 = 4;
 // In batches ranked by the one-CTA ordering kernel (128..1024 sequences), a
 // sequence that is not long is "short", and goes after all others, when its
-// tile count is at most PKV_SHORT_LAST_X8 / 8 times the batch mean (0: no
-// short bucket). Measured on GB300, Llama-3-8B-shaped layer (256 sequences):
-// 0 -> 42.9 us, 3 -> 42.2, 4 -> 41.6, 5 -> 41.3, 6 -> 41.5, 8 -> 43.2; the
-// same bucket in smaller batches (the LLaMA-13B layer, the beam batch) cost
+// tile count is at most kShortLastX8 / 8 times the batch mean. Measured on
+// GB300, Llama-3-8B-shaped layer (256 sequences): 0 (no short bucket) ->
+// 42.9 us, 3 -> 42.2, 4 -> 41.6, 5 -> 41.3, 6 -> 41.5, 8 -> 43.2; the same
+// bucket in smaller batches (the LLaMA-13B layer, the beam batch) cost
 // 0.5-1.8 %, so the per-CTA ranking keeps two buckets.
-#ifndef PKV_SHORT_LAST_X8
-#define PKV_SHORT_LAST_X8 5
-#endif
-constexpr long long kShortLastX8 = PKV_SHORT_LAST_X8;
+constexpr long long kShortLastX8 = 5;
 
 // Bucket of a sequence with `tiles` tiles in a batch of S sequences holding
 // `total` tiles: 0 long (first), 1 the rest, 2 short (last; only with
@@ -341,18 +321,12 @@ __device__ __forceinline__ void decode_tile(uint32_t kt, uint32_t vt, int lo, in
     for (int h = 0; h < G; ++h) {
       float d0 = qf[h][0] * kf[0];
       float d1 = qf[h][1] * kf[1];
-      if constexpr (kPackedFma) {
-        ffma2(d0, d1, qf[h][2], qf[h][3], kf[2], kf[3], d0, d1);
-        ffma2(d0, d1, qf[h][4], qf[h][5], kf[4], kf[5], d0, d1);
-        ffma2(d0, d1, qf[h][6], qf[h][7], kf[6], kf[7], d0, d1);
-      } else {
-        d0 = fmaf(qf[h][2], kf[2], d0);
-        d1 = fmaf(qf[h][3], kf[3], d1);
-        d0 = fmaf(qf[h][4], kf[4], d0);
-        d1 = fmaf(qf[h][5], kf[5], d1);
-        d0 = fmaf(qf[h][6], kf[6], d0);
-        d1 = fmaf(qf[h][7], kf[7], d1);
-      }
+      d0 = fmaf(qf[h][2], kf[2], d0);
+      d1 = fmaf(qf[h][3], kf[3], d1);
+      d0 = fmaf(qf[h][4], kf[4], d0);
+      d1 = fmaf(qf[h][5], kf[5], d1);
+      d0 = fmaf(qf[h][6], kf[6], d0);
+      d1 = fmaf(qf[h][7], kf[7], d1);
       sc[h * NPASS + i] = d0 + d1;
     }
   }
@@ -418,13 +392,8 @@ __device__ __forceinline__ void decode_tile(uint32_t kt, uint32_t vt, int lo, in
       const float p_raw = __shfl_sync(kFull, p[v & (NF - 1)], src);
       lsum[h] += p_raw;
       const float pp = KV::SCALED ? p_raw * vscale : p_raw;
-      if constexpr (kPackedFma) {
 #pragma unroll
-        for (int c = 0; c < 8; c += 2) ffma2(acc[h][c], acc[h][c + 1], pp, pp, vf[c], vf[c + 1], acc[h][c], acc[h][c + 1]);
-      } else {
-#pragma unroll
-        for (int c = 0; c < 8; ++c) acc[h][c] = fmaf(pp, vf[c], acc[h][c]);
-      }
+      for (int c = 0; c < 8; ++c) acc[h][c] = fmaf(pp, vf[c], acc[h][c]);
     }
   }
 }
@@ -536,8 +505,8 @@ paged_decode_kernel(const DecodeArgs a) {
   wait_for_predecessor();
   TraceMarks tm{};
   trace_mark(tm, 0);
-  const int g = kSeqFastest ? blockIdx.y : blockIdx.x;
-  const int s = long_first_seq<NW>(a, kSeqFastest ? blockIdx.x : blockIdx.y), part = blockIdx.z;
+  const int g = blockIdx.x;
+  const int s = long_first_seq<NW>(a, blockIdx.y), part = blockIdx.z;
   trace_mark(tm, 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int sub = lane & (LPR - 1), r = lane / LPR;

@@ -9,30 +9,25 @@
 #define PKV_INT8_MMA 1
 #endif
 
-// Stages per warp of the INT8 kernels (an int8 stage is half the size of a
-// 16-bit one).
-#ifndef PKV_INT8_STAGES
-#define PKV_INT8_STAGES 4
-#endif
-// Warps per CTA of the INT8 tensor-core kernel for groups of 2..8 query
-// heads (group size 1 keeps PKV_GRID_WARPS). Measured on GB300: the
-// Llama-3-8B-shaped layer 39.1 us with 4 warps, 37.5 us with 3 (4 CTAs per
-// SM); 3 warps for group size 1 made the LLaMA-13B layer 104.2 -> 113.7 us.
-#ifndef PKV_INT8_GQA_WARPS
-#define PKV_INT8_GQA_WARPS 3
-#endif
-
 namespace pkv {
 namespace {
+
+// Stages per warp of the INT8 kernels (an int8 stage is half the size of a
+// 16-bit one).
+constexpr int kInt8Stages = 4;
+// Warps per CTA of the INT8 tensor-core kernel for groups of 2..8 query
+// heads (group size 1 keeps kGridWarps). Measured on GB300: the
+// Llama-3-8B-shaped layer 39.1 us with 4 warps, 37.5 us with 3 (4 CTAs per
+// SM); 3 warps for group size 1 made the LLaMA-13B layer 104.2 -> 113.7 us.
+constexpr int kInt8GqaWarps = 3;
 
 template <typename T, int D, int G>
 cudaError_t launch_int8_dg(const DecodeArgs& a, const CUtensorMap* kmap, const CUtensorMap* vmap,
                            cudaStream_t stream) {
-  constexpr int NW = (PKV_INT8_MMA && G >= 2) ? PKV_INT8_GQA_WARPS : PKV_GRID_WARPS;
-  constexpr int STAGES = PKV_INT8_STAGES;
+  constexpr int NW = (PKV_INT8_MMA && G >= 2) ? kInt8GqaWarps : kGridWarps;
+  constexpr int STAGES = kInt8Stages;
   static bool configured[kMaxDevices] = {};
-  const dim3 grid(kSeqFastest ? unsigned(a.num_seqs) : unsigned(a.num_kv_heads),
-                  kSeqFastest ? unsigned(a.num_kv_heads) : unsigned(a.num_seqs), unsigned(a.max_parts));
+  const dim3 grid(unsigned(a.num_kv_heads), unsigned(a.num_seqs), unsigned(a.max_parts));
   cudaError_t err = cudaSuccess;
   if constexpr (PKV_INT8_MMA) {
     using C = I8Cfg<D, NW, STAGES>;

@@ -24,37 +24,21 @@ cudaError_t configure_once(K kern, size_t smem, bool (&configured)[kMaxDevices])
 }
 
 // Shape of the one-CTA-per-(sequence, KV head, partition) kernels: warps per
-// CTA and stages per warp (overridable at build time for tuning).
-#ifndef PKV_GRID_WARPS
-#define PKV_GRID_WARPS 4
-#endif
-#ifndef PKV_GRID_STAGES
-#define PKV_GRID_STAGES 2
-#endif
-// Shape of the tensor-core (group size >= 2) grid kernel: 3 warps x 2 stages
-// (48 KB of ring, 4 CTAs per SM). Measured on GB300, Llama-3-8B-shaped layer
-// with the shortest sequences last and partial-tile boxes: 41.4 us with 4 x 2,
-// 40.9-41.0 with 3 x 2 (and 40.2-40.3 with 3 x 2 without the L2 prefetch);
-// three-stage rings (4 x 3, 3 x 3) and 2 x 4 were 46-52 us.
-#ifndef PKV_MMA_WARPS
-#define PKV_MMA_WARPS 3
-#endif
-#ifndef PKV_MMA_STAGES
-#define PKV_MMA_STAGES PKV_GRID_STAGES
-#endif
+// CTA and stages per warp. The CUDA-core kernel takes 4 warps x 2 stages.
+// The tensor-core (group size >= 2) kernel takes 3 warps x 2 stages (48 KB of
+// ring, 4 CTAs per SM). Measured on GB300, Llama-3-8B-shaped layer with the
+// shortest sequences last and partial-tile boxes: 41.4 us with 4 x 2, 40.2-40.3
+// with 3 x 2; three-stage rings (4 x 3, 3 x 3) and 2 x 4 were 46-52 us.
+constexpr int kGridWarps = 4;
+constexpr int kGridStages = 2;
+constexpr int kMmaWarps = 3;
+constexpr int kMmaStages = 2;
 
 // Launch with programmatic stream serialization: the grid may become resident
 // while the previous kernel in the stream finishes (the kernels wait for it
 // with griddepcontrol.wait before touching global memory).
-#ifndef PKV_USE_PDL
-#define PKV_USE_PDL 1
-#endif
 template <typename K, typename... Args>
 cudaError_t launch_pdl(K kern, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, Args... args) {
-  if (!PKV_USE_PDL) {
-    kern<<<grid, block, smem, stream>>>(args...);
-    return cudaGetLastError();
-  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
@@ -75,9 +59,7 @@ cudaError_t launch_pdl(K kern, dim3 grid, dim3 block, size_t smem, cudaStream_t 
 // 341 -> 299 us on that batch, whose sibling samples share prompt blocks
 // through L2, against 1-1.4 % slower on the LLaMA-13B and OPT-175B layers,
 // which keep the two-stage ring.
-#ifndef PKV_WIDE_GRID_WARPS
-#define PKV_WIDE_GRID_WARPS 6
-#endif
+constexpr int kWideGridWarps = 6;
 constexpr int64_t kWideGridCtas = 8192;
 
 template <typename T, int D, int G, int NW, int STAGES>
@@ -93,20 +75,17 @@ cudaError_t launch_cuda_core_grid(const DecodeArgs& a, dim3 grid, cudaStream_t s
 template <typename T, int D, int G>
 cudaError_t launch_decode_dg(const DecodeArgs& a, const CUtensorMap* kmap, const CUtensorMap* vmap,
                              cudaStream_t stream) {
-  constexpr int NW = PKV_GRID_WARPS;
-  constexpr int STAGES = (D == 256 && PKV_GRID_WARPS * PKV_GRID_STAGES > 8) ? 2 : PKV_GRID_STAGES;
+  constexpr int NW = kGridWarps;
+  constexpr int STAGES = kGridStages;
   static bool configured[kMaxDevices] = {};
-  const dim3 grid(kSeqFastest ? unsigned(a.num_seqs) : unsigned(a.num_kv_heads),
-                  kSeqFastest ? unsigned(a.num_kv_heads) : unsigned(a.num_seqs), unsigned(a.max_parts));
-  if constexpr (G == 1 && !PKV_MMA_FOR_MHA) {
+  const dim3 grid(unsigned(a.num_kv_heads), unsigned(a.num_seqs), unsigned(a.max_parts));
+  if constexpr (G == 1) {
     const int64_t ctas = int64_t(a.num_seqs) * a.num_kv_heads * a.max_parts;
-    cudaError_t err = (PKV_WIDE_GRID_WARPS > 0 && ctas >= kWideGridCtas)
-                          ? launch_cuda_core_grid<T, D, G, (PKV_WIDE_GRID_WARPS > 0 ? PKV_WIDE_GRID_WARPS : 1), 1>(
-                                a, grid, stream)
-                          : launch_cuda_core_grid<T, D, G, NW, STAGES>(a, grid, stream);
+    cudaError_t err = ctas >= kWideGridCtas ? launch_cuda_core_grid<T, D, G, kWideGridWarps, 1>(a, grid, stream)
+                                            : launch_cuda_core_grid<T, D, G, NW, STAGES>(a, grid, stream);
     if (err != cudaSuccess) return err;
   } else {
-    constexpr int MW = PKV_MMA_WARPS, MS = (D == 256 && PKV_MMA_WARPS * PKV_MMA_STAGES > 8) ? 2 : PKV_MMA_STAGES;
+    constexpr int MW = kMmaWarps, MS = kMmaStages;
     using C = MmaCfg<T, D, MW, MS>;
     auto kern = paged_decode_mma_kernel<T, D, G, MW, MS>;
     cudaError_t err = configure_once(kern, C::SMEM_BYTES, configured);

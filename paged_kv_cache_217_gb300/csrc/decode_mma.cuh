@@ -16,9 +16,6 @@
 // ldmatrix reads of K rows (and the transposed reads of V rows) free of bank
 // conflicts, which rows 256 bytes apart would otherwise hit 8 ways.
 //
-// A switch (PKV_MMA_L2_AHEAD) makes each warp also ask for the tile after its
-// ring into L2 (bulk prefetch).
-//
 // P is fed to the PV product as two fp16/bf16 terms, hi = round(P) and
 // lo = round(P - hi), so the weights keep about 16 significant bits instead
 // of the 8 (bf16) or 11 (fp16) a single rounding leaves.
@@ -95,28 +92,6 @@ struct Mma<__half> {
   }
 };
 
-// Measurement knob: feed P to the PV product as one rounded term only.
-#ifndef PKV_PV_HI_ONLY
-#define PKV_PV_HI_ONLY 0
-#endif
-constexpr bool kPvHiOnly = PKV_PV_HI_ONLY != 0;
-
-// Split the QK accumulation of each 8-token half into two chains.
-#ifndef PKV_SPLIT_QK
-#define PKV_SPLIT_QK 0
-#endif
-constexpr bool kSplitQk = PKV_SPLIT_QK != 0;
-
-// Tiles of a warp, beyond its ring, asked into L2 ahead of their copy into
-// shared memory (0: none), so that a warp's next round trip after its ring
-// is an L2 hit. On GB300, with 4-warp rings, one tile ahead took about 0.5 us
-// off the 43.4 us call of the Llama-3-8B-shaped layer; with the 3-warp rings
-// that replaced them (4 CTAs per SM) it costs 1 us (40.3 -> 41.3), so it is off.
-#ifndef PKV_MMA_L2_AHEAD
-#define PKV_MMA_L2_AHEAD 0
-#endif
-constexpr int kMmaL2Ahead = PKV_MMA_L2_AHEAD;
-
 // The pool as TMA tensor maps with boxes of 16, 8 and 4 rows (index 0, 1, 2)
 // x 64 columns. Full tiles are copied as 16-row boxes; a partial last tile
 // with r valid rows as 4-row multiples (an 8-row box, a 4-row box, or both),
@@ -125,15 +100,6 @@ constexpr int kMmaL2Ahead = PKV_MMA_L2_AHEAD;
 struct PoolMaps {
   CUtensorMap k[3], v[3];
 };
-
-// 1: partial last tiles are copied (and prefetched) in 4-row multiples
-// (PoolMaps); 0: as whole 16-row boxes. On the Llama-3-8B-shaped layer (mean
-// 185 tokens) this reads 196 instead of 199 MB for 189 MB of KV; the call
-// time is unchanged (41.5 us).
-#ifndef PKV_MMA_PARTIAL_BOXES
-#define PKV_MMA_PARTIAL_BOXES 1
-#endif
-constexpr bool kMmaPartialBoxes = PKV_MMA_PARTIAL_BOXES != 0;
 
 template <typename T, int D, int NW, int STAGES>
 struct MmaCfg {
@@ -146,7 +112,6 @@ struct MmaCfg {
   static constexpr size_t RING_BYTES = size_t(NW) * STAGES * STAGE_BYTES;
   static constexpr size_t SMEM_BYTES = RING_BYTES + size_t(NW) * STAGES * 8 + 1024;  // + alignment slack
   static_assert(D % 64 == 0 && D >= 64 && D <= 256, "head_dim must be 64, 128 or 256");
-  static_assert(STAGES + kMmaL2Ahead <= 32, "prefetch distance must stay within the next id batch");
 };
 
 // Byte offset of 16-byte chunk `chunk` (0 .. D/8-1) of row `row` (0..15) in a
@@ -164,30 +129,16 @@ __device__ __forceinline__ void mma_tile(uint32_t kt, uint32_t vt, int lo, int r
   const int t = lane & 3;
   const int mi = lane >> 3, rr = lane & 7;
 
-  // S = Q . K^T for tokens 0-7 (s0) and 8-15 (s1); with kSplitQk the k-steps
-  // alternate between two accumulators per half (shorter dependency chains).
+  // S = Q . K^T for tokens 0-7 (s0) and 8-15 (s1).
   float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
   {
-    float s0b[4] = {0.f, 0.f, 0.f, 0.f}, s1b[4] = {0.f, 0.f, 0.f, 0.f};
     const int tok = (mi >> 1) * 8 + rr;
 #pragma unroll
     for (int ks = 0; ks < C::KSTEPS; ++ks) {
       uint32_t b[4];
       ldsm_x4(kt + swz(tok, 2 * ks + (mi & 1)), b);
-      if (kSplitQk && (ks & 1)) {
-        Mma<T>::run(s0b, qa[ks][0], 0u, qa[ks][1], 0u, b[0], b[1]);
-        Mma<T>::run(s1b, qa[ks][0], 0u, qa[ks][1], 0u, b[2], b[3]);
-      } else {
-        Mma<T>::run(s0, qa[ks][0], 0u, qa[ks][1], 0u, b[0], b[1]);
-        Mma<T>::run(s1, qa[ks][0], 0u, qa[ks][1], 0u, b[2], b[3]);
-      }
-    }
-    if (kSplitQk) {
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        s0[i] += s0b[i];
-        s1[i] += s1b[i];
-      }
+      Mma<T>::run(s0, qa[ks][0], 0u, qa[ks][1], 0u, b[0], b[1]);
+      Mma<T>::run(s1, qa[ks][0], 0u, qa[ks][1], 0u, b[2], b[3]);
     }
   }
 
@@ -231,9 +182,9 @@ __device__ __forceinline__ void mma_tile(uint32_t kt, uint32_t vt, int lo, int r
       uint32_t b[4];
       ldsm_x4_trans(vt + swz(tok, 2 * c + (mi >> 1)), b);
       Mma<T>::run(o[2 * c], hi01, 0u, hi23, 0u, b[0], b[1]);
-      if (!kPvHiOnly) Mma<T>::run(o[2 * c], lo01, 0u, lo23, 0u, b[0], b[1]);
+      Mma<T>::run(o[2 * c], lo01, 0u, lo23, 0u, b[0], b[1]);
       Mma<T>::run(o[2 * c + 1], hi01, 0u, hi23, 0u, b[2], b[3]);
-      if (!kPvHiOnly) Mma<T>::run(o[2 * c + 1], lo01, 0u, lo23, 0u, b[2], b[3]);
+      Mma<T>::run(o[2 * c + 1], lo01, 0u, lo23, 0u, b[2], b[3]);
     }
   }
 }
@@ -267,8 +218,8 @@ paged_decode_mma_kernel(const DecodeArgs a, const __grid_constant__ PoolMaps map
   wait_for_predecessor();
   TraceMarks tm{};
   trace_mark(tm, 0);
-  const int g = kSeqFastest ? blockIdx.y : blockIdx.x;
-  const int s = long_first_seq<NW>(a, kSeqFastest ? blockIdx.x : blockIdx.y), part = blockIdx.z;
+  const int g = blockIdx.x;
+  const int s = long_first_seq<NW>(a, blockIdx.y), part = blockIdx.z;
   trace_mark(tm, 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int hq0 = g * a.group;
@@ -361,7 +312,7 @@ paged_decode_mma_kernel(const DecodeArgs a, const __grid_constant__ PoolMaps map
       const uint32_t dst = ring_s + st * C::STAGE_BYTES;
       const int y = (id * a.num_kv_heads + g) * kBlock;
       // rows copied: all 16, or the valid rows rounded up to a multiple of 4
-      const int cover = kMmaPartialBoxes ? min(kBlock, (ntok - (warp + k * NW) * kBlock + 3) & ~3) : kBlock;
+      const int cover = min(kBlock, (ntok - (warp + k * NW) * kBlock + 3) & ~3);
       mbar_arrive_expect_tx(bar, uint32_t(cover) * (C::STAGE_BYTES / kBlock));
       if (cover == kBlock) {
 #pragma unroll
@@ -389,25 +340,6 @@ paged_decode_mma_kernel(const DecodeArgs a, const __grid_constant__ PoolMaps map
     }
   };
 
-  // L2 prefetch of this warp's tile k (warp-uniform; k at most 32 past the
-  // current id batch, whose successor is already in ids_next).
-  const char* kpool = static_cast<const char*>(a.k_pool);
-  const char* vpool = static_cast<const char*>(a.v_pool);
-  // Bytes of this warp's tile k that its copy will read (the rows it covers).
-  auto tile_bytes = [&](int k) -> uint32_t {
-    const int cover = kMmaPartialBoxes ? min(kBlock, (ntok - (warp + k * NW) * kBlock + 3) & ~3) : kBlock;
-    return uint32_t(cover) * (C::TILE_BYTES / kBlock);
-  };
-  auto prefetch = [&](int k) {
-    const int src = (k >> 5) == id_batch ? ids : ids_next;
-    const int id = __shfl_sync(kFull, src, k & 31);
-    if (lane == 0) {
-      const size_t off = (size_t(id) * a.num_kv_heads + g) * C::TILE_BYTES;
-      bulk_prefetch_l2(kpool + off, tile_bytes(k));
-      bulk_prefetch_l2(vpool + off, tile_bytes(k));
-    }
-  };
-
   float o[C::NTILES][4];
 #pragma unroll
   for (int nd = 0; nd < C::NTILES; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
@@ -415,12 +347,6 @@ paged_decode_mma_kernel(const DecodeArgs a, const __grid_constant__ PoolMaps map
 
   const int pre = n_my < STAGES ? n_my : STAGES;
   for (int k = 0; k < pre; ++k) issue(k);
-  if (kMmaL2Ahead > 0 && lane >= STAGES && lane < STAGES + kMmaL2Ahead && lane < n_my) {
-    // the first batch of ids is spread one per lane: each lane asks for its own tile
-    const size_t off = (size_t(ids) * a.num_kv_heads + g) * C::TILE_BYTES;
-    bulk_prefetch_l2(kpool + off, tile_bytes(lane));
-    bulk_prefetch_l2(vpool + off, tile_bytes(lane));
-  }
 
   for (int k = 0; k < n_my; ++k) {
     const int st = k % STAGES;
@@ -445,7 +371,6 @@ paged_decode_mma_kernel(const DecodeArgs a, const __grid_constant__ PoolMaps map
     }
     __syncwarp();
     if (k + STAGES < n_my) issue(k + STAGES);
-    if (kMmaL2Ahead > 0 && k + STAGES + kMmaL2Ahead < n_my) prefetch(k + STAGES + kMmaL2Ahead);
   }
 
   trace_mark(tm, 4);

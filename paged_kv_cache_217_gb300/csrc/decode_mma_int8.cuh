@@ -201,8 +201,8 @@ paged_decode_mma_int8_kernel(const DecodeArgs a, const __grid_constant__ CUtenso
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
   wait_for_predecessor();
-  const int g = kSeqFastest ? blockIdx.y : blockIdx.x;
-  const int s = long_first_seq<NW>(a, kSeqFastest ? blockIdx.x : blockIdx.y), part = blockIdx.z;
+  const int g = blockIdx.x;
+  const int s = long_first_seq<NW>(a, blockIdx.y), part = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int hq0 = g * a.group;
   const int gr = lane >> 2, t = lane & 3;

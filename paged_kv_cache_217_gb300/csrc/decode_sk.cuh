@@ -31,17 +31,11 @@
 
 namespace pkv {
 
-// Ring shape of the head_dim-128 configurations (the common case), overridable
-// at build time for tuning: warps per CTA and stages per warp.
-#ifndef PKV_SK_WARPS_CUDA
-#define PKV_SK_WARPS_CUDA 6
-#endif
-#ifndef PKV_SK_WARPS_MMA
-#define PKV_SK_WARPS_MMA 5
-#endif
-#ifndef PKV_SK_STAGES
-#define PKV_SK_STAGES 2
-#endif
+// Ring shape of the head_dim-128 configurations (the common case): warps per
+// CTA (CUDA-core and tensor-core tiles) and stages per warp.
+constexpr int kSkWarpsCuda = 6;
+constexpr int kSkWarpsMma = 5;
+constexpr int kSkStages = 2;
 
 constexpr int kSkMaxSeqs = 2048;      // batch limit of the schedule (prefix sums in shared memory)
 constexpr int kSkMaxWarps = 2048;     // partial slots: two per persistent warp
@@ -82,12 +76,12 @@ struct SkCfg {
 // that two CTAs (with their prefix sums and alignment slack) share an SM.
 template <int D>
 constexpr int sk_stages() {
-  return D == 128 ? PKV_SK_STAGES : 2;
+  return D == 128 ? kSkStages : 2;
 }
 template <int D, int G>
 constexpr int sk_warps() {
-  constexpr int want = G == 1 ? (D == 256 ? 3 : (D == 128 ? PKV_SK_WARPS_CUDA : 6))
-                              : (D == 64 ? 6 : (D == 128 ? PKV_SK_WARPS_MMA : 2));
+  constexpr int want = G == 1 ? (D == 256 ? 3 : (D == 128 ? kSkWarpsCuda : 6))
+                              : (D == 64 ? 6 : (D == 128 ? kSkWarpsMma : 2));
   // at most what fits with room for 256 sequences of prefix sums
   constexpr int fit = int((kSmemPerCta - 1024 - 257 * sizeof(int)) /
                           (size_t(sk_stages<D>()) * (SkCfg<__half, D, G, (G > 1)>::STAGE_BYTES + 8)));

@@ -78,12 +78,6 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst_smem, const void* src, uin
       : "memory");
 }
 
-// Asks for `bytes` (multiple of 16, address 16-byte aligned) of global memory
-// to be brought into L2; nothing is written and nothing is waited for.
-__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
-
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   uint4 v;
   asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
@@ -123,20 +117,6 @@ __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
-}
-
-// d = a * b + c on a pair of fp32 values with one packed instruction
-// (fma.rn.f32x2, sm_100 and later); same rounding as two fmaf calls.
-__device__ __forceinline__ void ffma2(float& d0, float& d1, float a0, float a1, float b0, float b1, float c0,
-                                      float c1) {
-  asm("{\n\t.reg .b64 pa, pb, pc, pd;\n\t"
-      "mov.b64 pa, {%2, %3};\n\t"
-      "mov.b64 pb, {%4, %5};\n\t"
-      "mov.b64 pc, {%6, %7};\n\t"
-      "fma.rn.f32x2 pd, pa, pb, pc;\n\t"
-      "mov.b64 {%0, %1}, pd;\n\t}"
-      : "=f"(d0), "=f"(d1)
-      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
 }
 
 __device__ __forceinline__ void flag(unsigned int* status, unsigned int bits) {

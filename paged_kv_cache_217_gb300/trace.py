@@ -27,7 +27,7 @@ import numpy as np
 
 PHASES = ["order (sequence known)", "length and block ids", "first tile landed", "tile loop", "merge and exit"]
 
-# The library's default bucket thresholds (PKV_LONG_FIRST_X2, PKV_SHORT_LAST_X8):
+# The library's bucket thresholds (kLongFirstX2, kShortLastX8 in csrc/decode.cuh):
 # long when 2 * tiles * S >= LONG_FIRST_X2 * total, short when
 # 8 * tiles * S <= SHORT_LAST_X8 * total.
 LONG_FIRST_X2 = 4

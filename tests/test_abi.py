@@ -157,3 +157,12 @@ def test_tracing_is_off_in_the_default_build():
     # the clock stamp exists in every build and checks its word on the host
     assert B.lib().pkv_trace_stamp(None, None) == 1             # PKV_ERR_INVALID_ARG
     assert B.lib().pkv_trace_stamp(ctypes.c_void_p(12), None) == 1
+
+
+def test_binding_scratch_size_matches_the_header():
+    # the binding restates PKV_NOALLOC_SCRATCH_BYTES; both must change together
+    with open(os.path.join(ROOT, "include", "paged_kv.h")) as f:
+        text = f.read()
+    m = re.search(r"#define\s+PKV_NOALLOC_SCRATCH_BYTES\s+\((\d+)u\s*<<\s*(\d+)\)", text)
+    assert m, "PKV_NOALLOC_SCRATCH_BYTES not found in include/paged_kv.h"
+    assert int(m.group(1)) << int(m.group(2)) == B.NOALLOC_SCRATCH_BYTES

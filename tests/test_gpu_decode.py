@@ -244,8 +244,16 @@ def test_bad_device_indices_are_flagged():
 # ---------------------------------------------------------------------------
 # full-size workloads, sampled outputs, automatic partitioning (bench config)
 # ---------------------------------------------------------------------------
-def _sample_pairs(rng, S, hq, k):
+def _sample_pairs(rng, S, hq, k, lens=None):
+    """(sequence, query head) pairs to check: one random head of every
+    sequence, the first and last head of the longest sequence (and of the
+    first and last sequence), plus random pairs up to k in all."""
     pairs = {(0, 0), (S - 1, hq - 1)}
+    for s in range(S):
+        pairs.add((s, int(rng.integers(hq))))
+    if lens is not None and S > 0:
+        longest = int(np.argmax(lens))
+        pairs |= {(longest, 0), (longest, hq - 1)}
     while len(pairs) < k:
         pairs.add((int(rng.integers(S)), int(rng.integers(hq))))
     return sorted(pairs)
@@ -253,7 +261,9 @@ def _sample_pairs(rng, S, hq, k):
 
 def _check_sampled(case, out, k, seed):
     rng = np.random.default_rng(seed)
-    pairs = _sample_pairs(rng, case.q.shape[0], case.q.shape[1], k)
+    lens = case.lens.cpu().numpy()
+    pairs = _sample_pairs(rng, case.q.shape[0], case.q.shape[1], k, lens)
+    assert {s for s, _ in pairs} == set(range(case.q.shape[0]))
     want = H.oracle_sampled(case, pairs)
     got = H.to_f64(out)
     for (s, h), w in want.items():
@@ -267,8 +277,24 @@ def test_full_size_decode_sampled(name):
     case = H.make_case(shape.context_lens, shape.num_q_heads, shape.num_kv_heads, shape.head_dim,
                        shape.dtype, seed=0)
     out = _run(case)
-    _check_sampled(case, out, 12 if name == "opt175b_long" else 40, seed=1)
+    _check_sampled(case, out, 24 if name == "opt175b_long" else 40, seed=1)
     del case, out
+    torch.cuda.empty_cache()
+
+
+def test_full_size_long_context_split_512():
+    # the long-context layer with its own stated schedule: split-K partitions of
+    # 512 tokens (up to 64 per sequence) merged by log-sum-exp in the kernel
+    shape = W.CONFIGS["opt175b_long"](0)
+    case = H.make_case(shape.context_lens, shape.num_q_heads, shape.num_kv_heads, shape.head_dim,
+                       shape.dtype, seed=0)
+    assert B.resolved_partition(8, 96, 96, 128, case.tables.shape[1], 512) == 512
+    out = _run(case, 512)
+    _check_sampled(case, out, 24, seed=3)
+    # the split result agrees with the one-pass result to fp32 rounding
+    one = _run(case, -1)
+    H.assert_attention_close(H.to_f64(out), H.to_f64(one), "split 512 against one pass")
+    del case, out, one
     torch.cuda.empty_cache()
 
 

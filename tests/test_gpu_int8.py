@@ -217,3 +217,45 @@ def test_decode_int8_full_size_sampled(name):
         H.assert_attention_close(H.to_f64(got[s, h]), want, f"{name} int8 ({s}, {h})")
     assert torch.isfinite(got.float()).all()
     assert B.device_status(clear=True) == 0
+
+
+# ---- the CUDA-core INT8 tile (a build with PKV_INT8_MMA=0) -------------------------
+@pytest.fixture(scope="module")
+def cuda_core_int8_lib(tmp_path_factory):
+    """The library built with the CUDA-core INT8 tile (codes to fp32 exactly, the
+    K scale on the reduced score, the V scale folded into the softmax weight),
+    loaded in place of the default build for the tests that take it."""
+    from paged_kv_cache_217_gb300 import build
+    path = build.build(out_dir=str(tmp_path_factory.mktemp("int8_cuda_core")), defines=["PKV_INT8_MMA=0"])
+    saved = (B.LIB_PATH, B._lib)
+    B.LIB_PATH, B._lib = path, None
+    try:
+        B.lib()
+        yield path
+    finally:
+        B.LIB_PATH, B._lib = saved
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("hq,hkv,d", [(4, 4, 64), (8, 8, 128), (8, 2, 128), (8, 1, 256)])
+@pytest.mark.parametrize("partition", [0, -1, 64])
+def test_cuda_core_int8_tile_parity(cuda_core_int8_lib, dtype, hq, hkv, d, partition):
+    case = Int8Case(RAGGED, hq, hkv, d, dtype, seed=hq + d + 1, extra_cols=2)
+    got = H.to_f64(case.run(partition))
+    H.assert_attention_close(got, case.oracle(), f"cuda-core int8 {dtype} hq={hq} hkv={hkv} d={d} p={partition}")
+    assert np.all(got[0] == 0.0)
+    assert B.device_status(clear=True) == 0
+
+
+def test_cuda_core_int8_tile_partial_tiles_and_large_rows(cuda_core_int8_lib):
+    case = Int8Case(np.arange(1, 49), 8, 2, 128, "bf16", seed=90)
+    H.assert_attention_close(H.to_f64(case.run(16)), case.oracle(), "cuda-core int8 partial tiles")
+    # V rows whose dequantised values exceed the fp16 range (possible for bf16
+    # inputs): the CUDA-core tile keeps them in fp32
+    big = Int8Case([40, 300, 17], 4, 4, 128, "bf16", seed=91)
+    big.vc.fill_(100)
+    big.vs.mul_(65536.0)
+    want = big.oracle()
+    assert np.abs(want).max() > 65504.0
+    H.assert_attention_close(H.to_f64(big.run()), want, "cuda-core int8 large V rows")
+    assert B.device_status(clear=True) == 0

@@ -39,9 +39,9 @@ def test_replay_and_order_test_use_the_library_thresholds():
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
     with open(os.path.join(root, "paged_kv_cache_217_gb300", "csrc", "decode.cuh")) as f:
         src = f.read()
-    defaults = dict(re.findall(r"#define (PKV_LONG_FIRST_X2|PKV_SHORT_LAST_X8) (\d+)", src))
-    assert int(defaults["PKV_LONG_FIRST_X2"]) == T.LONG_FIRST_X2
-    assert int(defaults["PKV_SHORT_LAST_X8"]) == T.SHORT_LAST_X8
+    defaults = dict(re.findall(r"constexpr long long (kLongFirstX2|kShortLastX8) = (\d+);", src))
+    assert int(defaults["kLongFirstX2"]) == T.LONG_FIRST_X2
+    assert int(defaults["kShortLastX8"]) == T.SHORT_LAST_X8
     with open(os.path.join(root, "tests", "test_gpu_decode.py")) as f:
         gpu_test = f.read()
     assert f"2 * t[s] * S >= {T.LONG_FIRST_X2} * total" in gpu_test

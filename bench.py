@@ -5,9 +5,13 @@
                     [--kv native|int8] [--window W]
 
 One step is one pass of the whole hot path over one batch: write each
-sequence's new K/V into its slot (reshape_and_cache), copy-on-write block
-copies when the step has any, and paged attention decode over every sequence
-(split-K decode plus its log-sum-exp merge when the partition choice splits).
+sequence's new K/V into its slot (reshape_and_cache), the step's launch plan
+(pkv_paged_attention_plan: the order in which the decode grid takes the
+sequences, made once per step for every layer of the step), and paged
+attention decode over every sequence with that plan (split-K decode plus its
+log-sum-exp merge when the partition choice splits). The decode figures
+(``roofline``, ``per_config``) time the decode call alone; the step figures
+(``value``) include the cache write and the plan.
 Inputs are synthetic (seeded N(0, 1) values, log-normal/uniform lengths,
 blocks scattered through a shuffled pool) with the shapes of the named model
 layers. The headline workload is the largest one-GPU configuration, the
@@ -216,6 +220,13 @@ def cache_write(wl, B):
         B.reshape_and_cache(wl.knew, wl.vnew, wl.k_pool, wl.v_pool, wl.slots)
 
 
+def plan(wl, B):
+    """The decode step's launch plan (pkv_paged_attention_plan): made once per
+    step, it serves the decode of every layer of that step."""
+    if wl.planned:
+        B.paged_attention_plan(wl.lens, wl.hq, wl.hkv, wl.d, wl.tables_h.shape[1], partition_size=wl.partition)
+
+
 def decode(wl, B):
     if wl.kv == "int8":
         B.paged_attention_decode_int8(wl.out, wl.q, wl.k_cache, wl.v_cache, wl.k_scale, wl.v_scale, wl.tables,
@@ -225,12 +236,13 @@ def decode(wl, B):
                                          wl.window, partition_size=wl.partition)
     else:
         B.paged_attention_decode(wl.out, wl.q, wl.k_pool, wl.v_pool, wl.tables, wl.lens, wl.scale,
-                                 partition_size=wl.partition)
+                                 partition_size=wl.partition, planned=wl.planned)
 
 
 def step(wl, B):
     """One pass of the hot path on device-resident inputs."""
     cache_write(wl, B)
+    plan(wl, B)
     decode(wl, B)
 
 
@@ -527,12 +539,17 @@ PER_CONFIG = ["llama13b", "llama3_8b", "opt66b_sampling", "opt175b_long"]
 
 def launches_per_step(wl, B):
     """This library's kernels in one step: the cache write, the decode (its
-    split-K merge runs inside it), and the one-CTA ordering kernel that
-    batches of 128..1024 sequences in grids of at most 4096 CTAs get (see
-    pkv_paged_attention_decode)."""
+    split-K merge runs inside it), and the one-CTA kernel that orders the
+    batch -- the step's launch plan (native cache, full attention; batches of
+    2..1024 sequences in grids of at most 4096 CTAs), or, for the INT8 cache
+    and sliding windows, the ordering that the decode call itself launches for
+    batches of 128..1024 sequences (see pkv_paged_attention_decode). Sets
+    wl.planned."""
     part = B.resolved_partition(wl.num_seqs, wl.hq, wl.hkv, wl.d, wl.tables_h.shape[1], wl.partition)
     parts = 1 if part in (-1, B.BALANCED) else -(-wl.tables_h.shape[1] * 16 // part)
-    ordered = part != B.BALANCED and 128 <= wl.num_seqs <= 1024 and wl.num_seqs * wl.hkv * parts <= 4096
+    fits = part != B.BALANCED and wl.num_seqs <= 1024 and wl.num_seqs * wl.hkv * parts <= 4096
+    wl.planned = wl.kv == "native" and wl.window == 0 and fits and wl.num_seqs >= 2
+    ordered = wl.planned or (fits and wl.num_seqs >= 128)
     return part, 2 + (1 if ordered else 0)
 
 
@@ -548,6 +565,7 @@ def time_steps(wl, B, K, flush, stream):
         e_start, e_mid, e_end = ev[k]
         e_start.record(stream)
         cache_write(wl, B)
+        plan(wl, B)
         e_mid.record(stream)
         decode(wl, B)
         e_end.record(stream)
@@ -709,6 +727,9 @@ def run_ours(args):
             "num_seqs": wl.num_seqs,
             "kv_bytes_per_step": wl.kv_bytes,
             "schedule": schedule_name(part, B),
+            "launch_plan": ("made once per step by pkv_paged_attention_plan (inside the step's events, outside "
+                            "the decode call's), used by pkv_paged_attention_decode_planned") if wl.planned else
+                           "none (or made inside the decode call)",
             "l2": f"KV working set {wl.kv_bytes / 1e6:.0f} MB > 129 MB L2, and L2 flushed "
                   f"(a {L2_FLUSH_BYTES >> 20} MB read) between timed steps outside the timed events",
             "parallelism": "replicas" if world > 1 else "single GPU",

@@ -92,6 +92,7 @@ typedef enum { PKV_F16 = 0, PKV_BF16 = 1 } pkv_dtype_t;
 #define PKV_DEV_BAD_SLOT        0x4u  /* slot_mapping entry >= num_blocks*16 */
 #define PKV_DEV_BAD_PAIR        0x8u  /* copy pair with src or dst outside the pool */
 #define PKV_DEV_WAIT_TIMEOUT    0x10u /* a bounded wait on a copy gave up */
+#define PKV_DEV_BAD_PLAN        0x20u /* a planned decode found no plan of its batch size */
 
 typedef struct CUstream_st* pkv_stream_t; /* same type as cudaStream_t */
 
@@ -163,9 +164,10 @@ pkv_status_t pkv_selftest_bounded_wait(uint32_t limit_us, pkv_stream_t stream);
  * Launch order: grids of at most 4096 CTAs start the sequences of at least
  * twice the batch's mean length (in 16-token tiles) first. For batches of 128
  * to 1024 sequences that order is computed once, by a one-CTA kernel launched
- * on `stream` ahead of the decode, into num_seqs int32 at the end of the
- * workspace; it also puts sequences of at most 5/8 of the mean length last
- * (each group in natural order). The order changes only when the work starts,
+ * on `stream` ahead of the decode, into the plan region at the end of the
+ * workspace (see pkv_paged_attention_plan); it also puts sequences of at most
+ * 5/8 of the mean length last (each group in natural order). Smaller batches
+ * are ranked in every CTA. The order changes only when the work starts,
  * never the results.
  * That kernel reads context_lens without waiting for the previous kernel on
  * the stream to finish when that kernel allows programmatic early launch
@@ -186,13 +188,54 @@ pkv_status_t pkv_paged_attention_decode(
     int partition_size, void* workspace, size_t workspace_bytes,
     pkv_stream_t stream);
 
-/* Bytes of workspace pkv_paged_attention_decode needs for these sizes: the
- * split-K partials and counters, plus the launch order of batches of 128 to
- * 1024 sequences (see above); 0 for one-pass calls without either. Returns 0
- * for invalid sizes as well. */
+/* Bytes of workspace pkv_paged_attention_decode (and _decode_planned) needs
+ * for these sizes: the split-K partials and counters, then the launch plan
+ * (a 16-byte header and int32[num_seqs]) of batches of 2 to 1024 sequences in
+ * grids of at most 4096 CTAs (see above); 0 for calls without either.
+ * Returns 0 for invalid sizes as well. */
 size_t pkv_paged_attention_workspace_size(
     int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
     int max_blocks_per_seq, int partition_size);
+
+/*
+ * Launch plan of a decode step (the pages have no counterpart; a scheduling
+ * convenience of this library). The order in which the decode grid takes the
+ * sequences depends only on the batch (lengths and sizes), which every layer
+ * of a decode step shares: this call computes it once -- the long-first order
+ * described under pkv_paged_attention_decode (with the shortest sequences
+ * last for batches of 128 or more), behind a 16-byte header -- into the plan
+ * region of `workspace` (the bytes after the split-K scratch, see
+ * pkv_paged_attention_workspace_size), and pkv_paged_attention_decode_planned
+ * then uses it in every layer instead of ranking the batch itself.
+ * Arguments as for pkv_paged_attention_decode; context_lens is read on
+ * `stream` (device memory, the same lengths the decode calls will see). Does
+ * nothing when the sizes need no plan (one sequence, more than 1024, grids of
+ * more than 4096 CTAs, the balanced schedule).
+ */
+pkv_status_t pkv_paged_attention_plan(const int32_t* context_lens, int num_seqs, int num_q_heads,
+                                      int num_kv_heads, int head_dim, int max_blocks_per_seq,
+                                      int partition_size, void* workspace, size_t workspace_bytes,
+                                      pkv_stream_t stream);
+
+/*
+ * pkv_paged_attention_decode with the launch plan that pkv_paged_attention_plan
+ * left in `workspace` for the same sizes: one kernel, no ranking. Same
+ * arguments, semantics and results as pkv_paged_attention_decode (the plan
+ * decides only when each sequence starts, never a result). A plan made from
+ * other lengths of a batch of the same size is still correct (only the start
+ * order is off). If the workspace holds no plan of this batch size, the
+ * kernels flag PKV_DEV_BAD_PLAN and take the sequences in natural order,
+ * still computing every output. The plan region must not be overwritten
+ * between the plan and the decode calls that use it (a call with other sizes
+ * on the same workspace can overwrite it).
+ */
+pkv_status_t pkv_paged_attention_decode_planned(
+    void* out, const void* q, const void* k_pool, const void* v_pool,
+    const int32_t* block_tables, const int32_t* context_lens,
+    int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+    int max_blocks_per_seq, int num_blocks, float scale, pkv_dtype_t dtype,
+    int partition_size, void* workspace, size_t workspace_bytes,
+    pkv_stream_t stream);
 
 /* The schedule a call with these sizes runs: -2 for the balanced persistent
  * schedule, -1 for one CTA per (sequence, KV head), else the split-K

@@ -20,6 +20,7 @@ from .binding import (  # noqa: F401
     paged_attention_decode_int8,
     paged_attention_decode_noalloc,
     paged_attention_decode_sliding,
+    paged_attention_plan,
     reshape_and_cache,
     reshape_and_cache_int8,
     sliding_workspace_size,

@@ -26,7 +26,7 @@ NOALLOC_SCRATCH_BYTES = 32 << 20   # PKV_NOALLOC_SCRATCH_BYTES
 BALANCED = -2                      # pkv_paged_attention_partition: balanced persistent schedule
 
 DEV_FLAGS = {0x1: "BAD_BLOCK_ID", 0x2: "BAD_CONTEXT_LEN", 0x4: "BAD_SLOT", 0x8: "BAD_PAIR",
-             0x10: "WAIT_TIMEOUT"}
+             0x10: "WAIT_TIMEOUT", 0x20: "BAD_PLAN"}
 
 
 class LibraryNotBuilt(RuntimeError):
@@ -55,6 +55,9 @@ _SIGS = {
     "pkv_paged_attention_decode": ([_c_p] * 6 + [_c_int] * 6 + [_c_f, _c_int, _c_int, _c_p, _c_sz, _c_p],
                                    _c_int),
     "pkv_paged_attention_decode_noalloc": ([_c_p] * 6 + [_c_int] * 6 + [_c_f, _c_int, _c_int, _c_p], _c_int),
+    "pkv_paged_attention_decode_planned": ([_c_p] * 6 + [_c_int] * 6 + [_c_f, _c_int, _c_int, _c_p, _c_sz, _c_p],
+                                           _c_int),
+    "pkv_paged_attention_plan": ([_c_p] + [_c_int] * 6 + [_c_p, _c_sz, _c_p], _c_int),
     "pkv_paged_attention_workspace_size": ([_c_int] * 6, _c_sz),
     "pkv_paged_attention_decode_sliding": ([_c_p] * 6 + [_c_int] * 6 + [_c_f, _c_int, _c_int, _c_int, _c_p, _c_sz,
                                                                        _c_p], _c_int),
@@ -189,12 +192,14 @@ def resolved_partition(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks
 
 
 def paged_attention_decode(out, q, k_pool, v_pool, block_tables, context_lens, scale,
-                           num_kv_heads=None, partition_size=0, workspace=None):
+                           num_kv_heads=None, partition_size=0, workspace=None, planned=False):
     """out[s, h] = softmax(scale * K_s q[s, h]) V_s over the paged cache (in place in ``out``).
 
     q, out: [S, Hq, D]; k_pool, v_pool: [num_blocks, Hkv, 16, D]; block_tables:
     int32 [S, max_blocks]; context_lens: int32 [S]. ``workspace`` (uint8 CUDA
-    tensor) overrides the binding's own split-K workspace.
+    tensor) overrides the binding's own workspace. ``planned`` runs
+    pkv_paged_attention_decode_planned, which uses the launch plan that
+    paged_attention_plan left in the same workspace.
     """
     import torch
     _need_cuda(out, q, k_pool, v_pool, block_tables, context_lens)
@@ -218,11 +223,32 @@ def paged_attention_decode(out, q, k_pool, v_pool, block_tables, context_lens, s
     if need:
         ws = workspace if workspace is not None else _workspace(q.device, need)
         ws_ptr, ws_bytes = ws.data_ptr(), ws.numel() * ws.element_size()
-    _launch(q.device, "paged_attention_decode", lib().pkv_paged_attention_decode,
+    fn = lib().pkv_paged_attention_decode_planned if planned else lib().pkv_paged_attention_decode
+    _launch(q.device, "paged_attention_decode_planned" if planned else "paged_attention_decode", fn,
             out.data_ptr(), q.data_ptr(), k_pool.data_ptr(), v_pool.data_ptr(), block_tables.data_ptr(),
             context_lens.data_ptr(), S, Hq, num_kv_heads, D, mb, nb, float(scale), dt, int(partition_size),
             ws_ptr, ws_bytes)
     return out
+
+
+def paged_attention_plan(context_lens, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
+                         partition_size=0, workspace=None):
+    """The decode step's launch plan (pkv_paged_attention_plan) into ``workspace``
+    (default: the binding's own workspace of the current stream, which
+    paged_attention_decode(planned=True) then reads)."""
+    import torch
+    _need_cuda(context_lens)
+    if context_lens.dtype != torch.int32 or context_lens.dim() != 1:
+        raise TypeError("context_lens must be int32 [S]")
+    S = context_lens.shape[0]
+    need = workspace_size(S, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, partition_size)
+    ws_ptr, ws_bytes = None, 0
+    if need:
+        ws = workspace if workspace is not None else _workspace(context_lens.device, need)
+        ws_ptr, ws_bytes = ws.data_ptr(), ws.numel() * ws.element_size()
+    _launch(context_lens.device, "paged_attention_plan", lib().pkv_paged_attention_plan,
+            context_lens.data_ptr(), S, int(num_q_heads), int(num_kv_heads), int(head_dim),
+            int(max_blocks_per_seq), int(partition_size), ws_ptr, ws_bytes)
 
 
 def sliding_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, sliding_window,

@@ -79,22 +79,23 @@ int choose_partition(int num_seqs, int num_q_heads, int num_kv_heads, int head_d
   return p >= max_ctx ? -1 : int(p);
 }
 
-// For batches of at least kOrderKernelMinSeqs sequences the long-first order
-// (grid row -> sequence) is computed once by a one-CTA kernel into the
-// workspace instead of by every CTA, which costs each CTA a read of all the
-// lengths and a CTA-wide ranking. Measured on GB300: Llama-3-8B layer (256
-// sequences) 44.5 -> 43.4 us, its INT8 cache 43.2 -> 41.3 us; on the 64-
-// sequence LLaMA-13B layer the extra launch cost 0.9 %, so small batches keep
-// ranking in each CTA.
-constexpr int kOrderKernelMinSeqs = 128;
+// The long-first order (grid row -> sequence) of a batch is its launch plan.
+// Batches of at least kOrderKernelMinSeqs sequences get it from a one-CTA
+// kernel (seq_order_kernel) into the workspace instead of ranking the batch in
+// every CTA, which costs each CTA a read of all the lengths and a CTA-wide
+// ranking. Measured on GB300: Llama-3-8B layer (256 sequences) 44.5 -> 43.4 us,
+// its INT8 cache 43.2 -> 41.3 us; on the 64-sequence LLaMA-13B layer the
+// extra launch cost 0.9 %, so smaller batches rank in each CTA -- unless the
+// caller made the plan beforehand (pkv_paged_attention_plan, once per decode
+// step for all layers), which any batch of 2..1024 sequences can use.
+constexpr int kOrderKernelMinSeqs = pkv::kRankInCtaMaxSeqs + 1;
 bool long_first_grid(int num_seqs, int num_kv_heads, int max_parts) {
   return int64_t(num_seqs) * num_kv_heads * max_parts <= kLongFirstMaxCtas;
 }
-size_t order_bytes(int num_seqs, int num_kv_heads, int max_parts) {
-  if (num_seqs < kOrderKernelMinSeqs || num_seqs > pkv::kOrderMaxSeqs ||
-      !long_first_grid(num_seqs, num_kv_heads, max_parts))
-    return 0;
-  return (size_t(num_seqs) * sizeof(int32_t) + 15) / 16 * 16;
+// Plan region of the workspace: a 16-byte header, then int32[num_seqs].
+size_t plan_bytes(int num_seqs, int num_kv_heads, int max_parts) {
+  if (num_seqs < 2 || num_seqs > pkv::kOrderMaxSeqs || !long_first_grid(num_seqs, num_kv_heads, max_parts)) return 0;
+  return 16 + (size_t(num_seqs) * sizeof(int32_t) + 15) / 16 * 16;
 }
 
 bool balanced_fits(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim) {
@@ -296,7 +297,7 @@ size_t pkv_paged_attention_workspace_size(int num_seqs, int num_q_heads, int num
     return sk_layout(num_seqs, num_q_heads, num_kv_heads, head_dim).total;
   }
   return split_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, plan.max_parts).total +
-         order_bytes(num_seqs, num_kv_heads, plan.max_parts);
+         plan_bytes(num_seqs, num_kv_heads, plan.max_parts);
 }
 
 }  // extern "C"
@@ -315,7 +316,7 @@ pkv_status_t decode_impl(void* out, const void* q, const void* k_pool, const voi
                          const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
                          int num_q_heads, int num_kv_heads, int head_dim, int max_blocks_per_seq,
                          int num_blocks, float scale, pkv_dtype_t dtype, int window, int partition_size,
-                         void* workspace, size_t workspace_bytes, pkv_stream_t stream) {
+                         void* workspace, size_t workspace_bytes, bool planned, pkv_stream_t stream) {
   if (num_seqs < 0) return pkv::fail(PKV_ERR_INVALID_ARG, "num_seqs < 0");
   if (num_seqs == 0) return pkv::ok();
   if (num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0)
@@ -350,7 +351,7 @@ pkv_status_t decode_impl(void* out, const void* q, const void* k_pool, const voi
                      pkv::decode_sk_max_seqs(head_dim, round_pow2_group(group)));
   const SplitLayout lay = split_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, plan.max_parts);
   const SkLayout sk = sk_layout(num_seqs, num_q_heads, num_kv_heads, head_dim);
-  const size_t ord = balanced ? 0 : order_bytes(num_seqs, num_kv_heads, plan.max_parts);
+  const size_t ord = balanced ? 0 : plan_bytes(num_seqs, num_kv_heads, plan.max_parts);
   const size_t need = balanced ? sk.total : lay.total + ord;
   if (int64_t(num_blocks) * num_kv_heads * PKV_BLOCK_SIZE > INT32_MAX)
     return pkv::fail(PKV_ERR_UNSUPPORTED, "num_blocks * num_kv_heads * 16 exceeds 2^31 rows");
@@ -414,8 +415,14 @@ pkv_status_t decode_impl(void* out, const void* q, const void* k_pool, const voi
   a.part_ml = lay.total > 0 ? reinterpret_cast<float2*>(static_cast<char*>(workspace) + lay.ml_offset) : nullptr;
   a.counters = lay.total > 0 ? reinterpret_cast<unsigned int*>(static_cast<char*>(workspace) + lay.counter_offset)
                              : nullptr;
-  int32_t* order = ord > 0 ? reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + lay.total) : nullptr;
-  a.order = order;
+  // The launch plan: made here for batches of at least kOrderKernelMinSeqs
+  // sequences, read as the caller made it for a planned call, else (smaller
+  // batches) ranked in every CTA.
+  int4* plan_hdr = ord > 0 ? reinterpret_cast<int4*>(static_cast<char*>(workspace) + lay.total) : nullptr;
+  const bool make_plan = plan_hdr && !planned && num_seqs >= kOrderKernelMinSeqs;
+  const bool use_plan = plan_hdr && (planned || make_plan);
+  a.order = use_plan ? reinterpret_cast<const int32_t*>(plan_hdr + 1) : nullptr;
+  a.plan = use_plan ? plan_hdr : nullptr;
   a.status = status;
   a.num_seqs = num_seqs;
   a.num_q_heads = num_q_heads;
@@ -441,10 +448,10 @@ pkv_status_t decode_impl(void* out, const void* q, const void* k_pool, const voi
     err = cudaMemsetAsync(a.counters, 0, lay.counter_bytes, stream);
     if (err != cudaSuccess) return cuda_status(err, "clear split-K counters");
   }
-  if (order) {
-    err = pkv::launch_seq_order(context_lens, num_seqs, max_blocks_per_seq * PKV_BLOCK_SIZE, a.window, order,
+  if (make_plan) {
+    err = pkv::launch_seq_order(context_lens, num_seqs, max_blocks_per_seq * PKV_BLOCK_SIZE, a.window, true, plan_hdr,
                                 stream);
-    if (err != cudaSuccess) return cuda_status(err, "sequence order launch");
+    if (err != cudaSuccess) return cuda_status(err, "launch plan");
   }
   err = dtype == PKV_F16 ? pkv::launch_decode_f16(a, head_dim, gpad, kmap, vmap, stream)
                          : pkv::launch_decode_bf16(a, head_dim, gpad, kmap, vmap, stream);
@@ -464,7 +471,46 @@ pkv_status_t pkv_paged_attention_decode(void* out, const void* q, const void* k_
                                         size_t workspace_bytes, pkv_stream_t stream) {
   return decode_impl(out, q, k_pool, v_pool, block_tables, context_lens, num_seqs, num_q_heads, num_kv_heads,
                      head_dim, max_blocks_per_seq, num_blocks, scale, dtype, 0, partition_size, workspace,
-                     workspace_bytes, stream);
+                     workspace_bytes, false, stream);
+}
+
+pkv_status_t pkv_paged_attention_decode_planned(void* out, const void* q, const void* k_pool, const void* v_pool,
+                                                const int32_t* block_tables, const int32_t* context_lens,
+                                                int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                                int max_blocks_per_seq, int num_blocks, float scale,
+                                                pkv_dtype_t dtype, int partition_size, void* workspace,
+                                                size_t workspace_bytes, pkv_stream_t stream) {
+  return decode_impl(out, q, k_pool, v_pool, block_tables, context_lens, num_seqs, num_q_heads, num_kv_heads,
+                     head_dim, max_blocks_per_seq, num_blocks, scale, dtype, 0, partition_size, workspace,
+                     workspace_bytes, true, stream);
+}
+
+pkv_status_t pkv_paged_attention_plan(const int32_t* context_lens, int num_seqs, int num_q_heads, int num_kv_heads,
+                                      int head_dim, int max_blocks_per_seq, int partition_size, void* workspace,
+                                      size_t workspace_bytes, pkv_stream_t stream) {
+  if (num_seqs < 0) return pkv::fail(PKV_ERR_INVALID_ARG, "num_seqs < 0");
+  if (num_seqs == 0) return pkv::ok();
+  if (num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0)
+    return pkv::fail(PKV_ERR_INVALID_ARG, "num_q_heads (%d) must be a positive multiple of num_kv_heads (%d)",
+                     num_q_heads, num_kv_heads);
+  if (max_blocks_per_seq <= 0) return pkv::fail(PKV_ERR_INVALID_ARG, "max_blocks_per_seq must be > 0");
+  if (!context_lens || !aligned(context_lens, 4))
+    return pkv::fail(PKV_ERR_INVALID_ARG, "context_lens must be a 4-byte aligned pointer");
+  const int p = choose_partition(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, partition_size);
+  Plan plan;
+  pkv_status_t st = plan_decode(max_blocks_per_seq, p, &plan);
+  if (st != PKV_OK) return st;
+  if (p == kBalanced) return pkv::ok();  // the balanced schedule takes no plan
+  const SplitLayout lay = split_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, plan.max_parts);
+  const size_t ord = plan_bytes(num_seqs, num_kv_heads, plan.max_parts);
+  if (ord == 0) return pkv::ok();        // nothing to plan: natural order
+  if (!workspace || workspace_bytes < lay.total + ord || !aligned(workspace, 16))
+    return pkv::fail(PKV_ERR_WORKSPACE, "workspace of %zu bytes (16-byte aligned) required, got %zu at %p",
+                     lay.total + ord, workspace_bytes, workspace);
+  int4* plan_hdr = reinterpret_cast<int4*>(static_cast<char*>(workspace) + lay.total);
+  return cuda_status(pkv::launch_seq_order(context_lens, num_seqs, max_blocks_per_seq * PKV_BLOCK_SIZE, 0,
+                                           num_seqs >= kOrderKernelMinSeqs, plan_hdr, stream),
+                     "launch plan");
 }
 
 pkv_status_t pkv_paged_attention_decode_sliding(void* out, const void* q, const void* k_pool, const void* v_pool,
@@ -475,7 +521,7 @@ pkv_status_t pkv_paged_attention_decode_sliding(void* out, const void* q, const 
                                                 void* workspace, size_t workspace_bytes, pkv_stream_t stream) {
   return decode_impl(out, q, k_pool, v_pool, block_tables, context_lens, num_seqs, num_q_heads, num_kv_heads,
                      head_dim, max_blocks_per_seq, num_blocks, scale, dtype, sliding_window > 0 ? sliding_window : 0,
-                     partition_size, workspace, workspace_bytes, stream);
+                     partition_size, workspace, workspace_bytes, false, stream);
 }
 
 size_t pkv_paged_attention_sliding_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
@@ -521,7 +567,7 @@ pkv_status_t pkv_paged_attention_decode_int8(void* out, const void* q, const int
   if (int64_t(num_blocks) * num_kv_heads * PKV_BLOCK_SIZE > INT32_MAX)
     return pkv::fail(PKV_ERR_UNSUPPORTED, "num_blocks * num_kv_heads * 16 exceeds 2^31 rows");
   const SplitLayout lay = split_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, plan.max_parts);
-  const size_t ord = order_bytes(num_seqs, num_kv_heads, plan.max_parts);
+  const size_t ord = plan_bytes(num_seqs, num_kv_heads, plan.max_parts);
   const size_t need = lay.total + ord;
   if (need > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, 16)))
     return pkv::fail(PKV_ERR_WORKSPACE, "workspace of %zu bytes (16-byte aligned) required, got %zu at %p",
@@ -543,8 +589,11 @@ pkv_status_t pkv_paged_attention_decode_int8(void* out, const void* q, const int
   a.part_ml = lay.total > 0 ? reinterpret_cast<float2*>(static_cast<char*>(workspace) + lay.ml_offset) : nullptr;
   a.counters = lay.total > 0 ? reinterpret_cast<unsigned int*>(static_cast<char*>(workspace) + lay.counter_offset)
                              : nullptr;
-  int32_t* order = ord > 0 ? reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + lay.total) : nullptr;
-  a.order = order;
+  int4* plan_hdr =
+      ord > 0 && num_seqs >= kOrderKernelMinSeqs ? reinterpret_cast<int4*>(static_cast<char*>(workspace) + lay.total)
+                                                 : nullptr;
+  a.order = plan_hdr ? reinterpret_cast<const int32_t*>(plan_hdr + 1) : nullptr;
+  a.plan = plan_hdr;
   a.status = status;
   a.num_seqs = num_seqs;
   a.num_q_heads = num_q_heads;
@@ -569,9 +618,9 @@ pkv_status_t pkv_paged_attention_decode_int8(void* out, const void* q, const int
     err = cudaMemsetAsync(a.counters, 0, lay.counter_bytes, stream);
     if (err != cudaSuccess) return cuda_status(err, "clear split-K counters");
   }
-  if (order) {
-    err = pkv::launch_seq_order(context_lens, num_seqs, max_blocks_per_seq * PKV_BLOCK_SIZE, 0, order, stream);
-    if (err != cudaSuccess) return cuda_status(err, "sequence order launch");
+  if (plan_hdr) {
+    err = pkv::launch_seq_order(context_lens, num_seqs, max_blocks_per_seq * PKV_BLOCK_SIZE, 0, true, plan_hdr, stream);
+    if (err != cudaSuccess) return cuda_status(err, "launch plan");
   }
   err = pkv::launch_decode_int8(a, dtype == PKV_BF16, head_dim, round_pow2_group(group), &kmap, &vmap, stream);
   return cuda_status(err, "paged_attention_decode_int8 launch");

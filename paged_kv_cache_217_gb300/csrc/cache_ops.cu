@@ -209,16 +209,19 @@ __global__ void bounded_wait_selftest_kernel(unsigned long long limit_ns, unsign
   if (!__all_sync(kFull, ok) && threadIdx.x == 0) flag(status, PKV_DEV_WAIT_TIMEOUT);
 }
 
-// The long-first order of a batch, computed once for the whole decode grid:
-// the buckets of order_bucket -- long sequences, the rest, short sequences --
-// each in natural order (long_first_seq, ranking in every CTA, uses the first
-// two only). One CTA, one thread per sequence (S <=
-// 1024). Launched with programmatic dependent launch ahead of the decode: it
-// lets the decode grid become resident at once, reads only the lengths (which
-// no kernel of this library writes), and waits for its own predecessor before
-// it exits, so its completion implies that predecessor's.
+// The launch plan of a batch: its long-first order (grid row -> sequence),
+// computed once for every decode grid that takes it. The buckets of
+// order_bucket -- long sequences, the rest and, with short_last, short
+// sequences -- each in natural order, into order[S], then the plan's header
+// {kPlanMagic, S, 0, 0}, which the decode kernels check before they use the
+// order. One CTA, one thread per sequence (S <= 1024). Launched with
+// programmatic dependent launch: it lets a decode grid that follows become
+// resident at once, reads only the lengths (which no kernel of this library
+// writes), and waits for its own predecessor before it exits, so its
+// completion implies that predecessor's.
 __global__ void __launch_bounds__(1024)
-seq_order_kernel(const int32_t* __restrict__ lens, int S, int max_len, int window, int32_t* __restrict__ order) {
+seq_order_kernel(const int32_t* __restrict__ lens, int S, int max_len, int window, int short_last,
+                 int32_t* __restrict__ order, int4* __restrict__ header) {
   asm volatile("griddepcontrol.launch_dependents;");
   __shared__ long long part_tiles[32];
   __shared__ int part_long[32], part_rest[32], part_short[32];
@@ -237,7 +240,7 @@ seq_order_kernel(const int32_t* __restrict__ lens, int S, int max_len, int windo
   __syncthreads();
   long long total = 0;
   for (int w = 0; w < int(blockDim.x >> 5); ++w) total += part_tiles[w];
-  const int b = s < S ? order_bucket(tiles, S, total, true) : -1;
+  const int b = s < S ? order_bucket(tiles, S, total, short_last != 0) : -1;
   const unsigned lb = __ballot_sync(kFull, b == 0), rb = __ballot_sync(kFull, b == 1),
                  sb = __ballot_sync(kFull, b == 2);
   if (lane == 0) {
@@ -259,13 +262,14 @@ seq_order_kernel(const int32_t* __restrict__ lens, int S, int max_len, int windo
     n_rest += part_rest[w];
   }
   if (s < S) order[b == 0 ? long_before : (b == 1 ? n_long + rest_before : n_long + n_rest + short_before)] = s;
+  if (s == 0) *header = make_int4(kPlanMagic, S, 0, 0);
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 }  // namespace
 
-cudaError_t launch_seq_order(const int32_t* lens, int num_seqs, int max_len, int window, int32_t* order,
-                             cudaStream_t stream) {
+cudaError_t launch_seq_order(const int32_t* lens, int num_seqs, int max_len, int window, bool short_last,
+                             int4* plan, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(1);
   cfg.blockDim = dim3(unsigned((num_seqs + 31) / 32 * 32));
@@ -276,7 +280,8 @@ cudaError_t launch_seq_order(const int32_t* lens, int num_seqs, int max_len, int
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, seq_order_kernel, lens, num_seqs, max_len, window, order);
+  int32_t* order = reinterpret_cast<int32_t*>(plan + 1);
+  return cudaLaunchKernelEx(&cfg, seq_order_kernel, lens, num_seqs, max_len, window, short_last ? 1 : 0, order, plan);
 }
 
 namespace {

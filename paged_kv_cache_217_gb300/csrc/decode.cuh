@@ -68,7 +68,8 @@ struct DecodeArgs {
   int part_tokens;      // tokens per partition (multiple of 16)
   int max_parts;        // grid.z
   int long_first;       // start sequences of twice the mean length first (long_first_seq)
-  const int32_t* order; // long_first: grid row -> sequence, computed once (seq_order_kernel), or null
+  const int32_t* order; // long_first: grid row -> sequence from a launch plan (seq_order_kernel), or null
+  const int4* plan;     // the plan's header {kPlanMagic, num_seqs, 0, 0}, checked before `order` is used
   unsigned long long* trace;  // PKV_TRACE builds: per-CTA phase timestamps (8 words a CTA), or null
   int trace_records;          // CTAs the trace buffer holds
   int window;           // sliding window: attend over the last `window` tokens (0 = all)
@@ -135,18 +136,24 @@ __device__ __forceinline__ void wait_for_predecessor() { asm volatile("griddepco
 
 // Batches of up to this many sequences start long sequences first.
 constexpr int kOrderMaxSeqs = 1024;
+// Batches of up to this many are ranked in every CTA unless planned; larger
+// ones get a launch plan from a one-CTA kernel ahead of the decode grid.
+constexpr int kRankInCtaMaxSeqs = 127;
+// First word of a launch plan's header (pkv_paged_attention_plan).
+constexpr int kPlanMagic = 0x504b5631;  // "PKV1"
 // A sequence is "long" when its tile count is at least kLongFirstX2 / 2 times
 // the batch mean (2x). Measured on GB300 (threshold x mean -> decode call µs):
 // Llama-3-8B-shaped layer 1.5 -> 43.7, 2 -> 43.4, 2.5 -> 43.6, 4 -> 46.7;
 // LLaMA-13B-shaped layer 2 -> 133.2, 2.5 -> 132.8, 3 -> 148.3.
 constexpr long long kLongFirstX2 = 4;
-// In batches ranked by the one-CTA ordering kernel (128..1024 sequences), a
-// sequence that is not long is "short", and goes after all others, when its
-// tile count is at most kShortLastX8 / 8 times the batch mean. Measured on
+// In launch plans of batches of 128..1024 sequences, a sequence that is not
+// long is "short", and goes after all others, when its tile count is at most
+// kShortLastX8 / 8 times the batch mean. Measured on
 // GB300, Llama-3-8B-shaped layer (256 sequences): 0 (no short bucket) ->
 // 42.9 us, 3 -> 42.2, 4 -> 41.6, 5 -> 41.3, 6 -> 41.5, 8 -> 43.2; the same
 // bucket in smaller batches (the LLaMA-13B layer, the beam batch) cost
-// 0.5-1.8 %, so the per-CTA ranking keeps two buckets.
+// 0.5-1.8 %, so plans of smaller batches, and the per-CTA ranking, keep two
+// buckets.
 constexpr long long kShortLastX8 = 5;
 
 // Bucket of a sequence with `tiles` tiles in a batch of S sequences holding
@@ -176,9 +183,21 @@ template <int NW>
 __device__ __forceinline__ int long_first_seq(const DecodeArgs& a, int rank) {
   const int S = a.num_seqs;
   if (!a.long_first || S > kOrderMaxSeqs || S <= 1) return rank;
-  if (a.order) return a.order[rank];  // ranked once for the whole grid
-  __shared__ int tiles[kOrderMaxSeqs > 0 ? kOrderMaxSeqs : 1];
-  __shared__ unsigned int long_bits[kOrderMaxSeqs > 32 ? kOrderMaxSeqs / 32 : 1];
+  if (a.order) {  // ranked once for the whole grid, by a launch plan
+    const int4 h = __ldg(a.plan);
+    const int s = __ldg(a.order + rank);
+    if (h.x == kPlanMagic && h.y == S && s >= 0 && s < S) return s;
+    // not a plan of this batch size: every CTA sees the same header and takes
+    // its natural row, so each sequence is still processed exactly once
+    if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.z == 0) flag(a.status, PKV_DEV_BAD_PLAN);
+    return rank;
+  }
+  // Batches of kRankInCtaMaxSeqs + 1 or more sequences always come with a plan
+  // (the library makes one ahead of the grid), so the per-CTA ranking needs
+  // room for the small batches only.
+  if (S > kRankInCtaMaxSeqs) return rank;
+  __shared__ int tiles[kRankInCtaMaxSeqs];
+  __shared__ unsigned int long_bits[kRankInCtaMaxSeqs / 32 + 1];
   __shared__ int red[NW];
   __shared__ int picked;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;

@@ -32,10 +32,11 @@ cudaError_t launch_decode_sk_bf16(const SkArgs& a, int head_dim, int gpad, const
 // share the CTA's shared memory with the rings); 0 for unsupported sizes.
 int decode_sk_max_seqs(int head_dim, int gpad);
 
-// The long-first order of a batch (grid row -> sequence) into order[num_seqs]
-// (num_seqs <= 1024), launched ahead of a decode grid.
-cudaError_t launch_seq_order(const int32_t* lens, int num_seqs, int max_len, int window, int32_t* order,
-                             cudaStream_t stream);
+// The launch plan of a batch (num_seqs <= 1024) into `plan`: a 16-byte header
+// {magic, num_seqs, 0, 0}, then the long-first order int32[num_seqs] (grid row
+// -> sequence; the shortest sequences last with short_last).
+cudaError_t launch_seq_order(const int32_t* lens, int num_seqs, int max_len, int window, bool short_last,
+                             int4* plan, cudaStream_t stream);
 
 // One warp that waits on an mbarrier no copy completes (bounded-wait self-test).
 cudaError_t launch_bounded_wait_selftest(unsigned long long limit_ns, unsigned int* status, cudaStream_t stream);

@@ -3,8 +3,10 @@
     python -m paged_kv_cache_217_gb300.build --define PKV_TRACE=1 --out-dir DIR
     python -m paged_kv_cache_217_gb300.trace --lib DIR/libpaged_kv.so --workload llama3_8b
 
-Runs the named layer's decode (seeded synthetic inputs, blocks scattered
-through a shuffled pool, L2 evicted between calls) with a trace buffer set
+Runs the named layer's decode on the grid kernels (one CTA per sequence, KV
+head and partition; --partition -1 by default, or a split-K partition size),
+with seeded synthetic inputs, blocks scattered through a shuffled pool and L2
+evicted between calls, with a trace buffer set
 (pkv_set_trace_buffer) and GPU clock stamps (pkv_trace_stamp) before and
 after each call, and summarises: where a call's time goes (stamp to first
 CTA start, first CTA start to last CTA end, last CTA end to the next stamp;
@@ -40,6 +42,9 @@ def main(argv=None):
     ap.add_argument("--workload", default="llama3_8b", choices=["tiny", "llama13b", "llama3_8b", "opt175b_long"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--calls", type=int, default=20)
+    ap.add_argument("--partition", type=int, default=-1,
+                    help="-1 (one CTA per sequence and KV head) or a split-K partition size in tokens; the "
+                         "persistent schedules record no trace")
     ap.add_argument("--replay", action="store_true", help="replay the CTA lifetimes under other row orders")
     args = ap.parse_args(argv)
 
@@ -73,7 +78,7 @@ def main(argv=None):
             buf.zero_()
             flush.sum()
             B.trace_stamp(stamps, 0)
-            B.paged_attention_decode(out, q, k_pool, v_pool, t_d, l_d, shape.scale)
+            B.paged_attention_decode(out, q, k_pool, v_pool, t_d, l_d, shape.scale, partition_size=args.partition)
             B.trace_stamp(stamps, 1)
             torch.cuda.synchronize()
             r = buf.view(-1, 8).cpu().numpy()

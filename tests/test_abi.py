@@ -54,18 +54,20 @@ def _balanced_bytes(S, hq, hkv, d):
 def test_workspace_and_partition_choice():
     # automatic choice: one CTA per (sequence, KV head) with at least 608 pairs
     assert B.resolved_partition(64, 40, 40, 128, 32) == -1          # 2560 pairs
-    assert B.workspace_size(64, 40, 40, 128, 32) == 0
     assert B.resolved_partition(256, 32, 8, 128, 64) == -1          # 2048 pairs
-    # 128..1024 sequences in a grid of at most 4096 CTAs: the launch order is
-    # computed once into num_seqs int32 of workspace (16-byte rounded)
-    assert B.workspace_size(256, 32, 8, 128, 64) == 256 * 4
-    assert B.workspace_size(130, 8, 8, 128, 64) == 528               # 130 * 4 rounded up to 16
-    assert B.workspace_size(127, 8, 8, 128, 64) == 0                 # smaller batches rank in each CTA
+    # 2..1024 sequences in a grid of at most 4096 CTAs: a launch plan region, a
+    # 16-byte header and int32[num_seqs] (16-byte rounded)
+    assert B.workspace_size(64, 40, 40, 128, 32) == 16 + 256
+    assert B.workspace_size(256, 32, 8, 128, 64) == 16 + 256 * 4
+    assert B.workspace_size(130, 8, 8, 128, 64) == 16 + 528          # 130 * 4 rounded up to 16
+    assert B.workspace_size(2, 8, 8, 128, 1) == 16 + 16
+    assert B.workspace_size(1, 8, 8, 128, 1) == 0                    # one sequence: nothing to order
     assert B.workspace_size(512, 16, 16, 128, 64) == 0               # 8192 CTAs: no long-first order
+    assert B.workspace_size(1025, 1, 1, 128, 64) == 0                # beyond the plan's 1024 sequences
     assert B.resolved_partition(8, 96, 96, 128, 2048) == -1         # 768 pairs
     # fewer pairs: partitions just large enough for 608 CTAs, at least 256 tokens
     assert B.resolved_partition(2, 8, 8, 128, 2048) == 864          # 16 pairs x 38 parts
-    assert B.workspace_size(2, 8, 8, 128, 2048) == _split_bytes(2, 8, 8, 128, 38)
+    assert B.workspace_size(2, 8, 8, 128, 2048) == _split_bytes(2, 8, 8, 128, 38) + 32
     assert B.resolved_partition(4, 4, 4, 64, 100) == 256            # 16 pairs, 1600 tokens
     assert B.resolved_partition(4, 4, 4, 64, 16) == -1              # 256 tokens: one pass
     # the balanced persistent schedule, on request
@@ -75,12 +77,12 @@ def test_workspace_and_partition_choice():
     # explicit choices
     assert B.resolved_partition(8, 96, 96, 128, 2048, -1) == -1
     assert B.resolved_partition(8, 96, 96, 128, 2048, 256) == 256
-    assert B.workspace_size(8, 96, 96, 128, 2048, -1) == 0
-    assert B.workspace_size(8, 96, 96, 128, 2048, 512) == _split_bytes(8, 96, 96, 128, 64)
-    assert B.workspace_size(3, 6, 2, 64, 10, 16) == _split_bytes(3, 6, 2, 64, 10)
+    assert B.workspace_size(8, 96, 96, 128, 2048, -1) == 16 + 32       # 768 CTAs: the plan region
+    assert B.workspace_size(8, 96, 96, 128, 2048, 512) == _split_bytes(8, 96, 96, 128, 64)  # 49152 CTAs
+    assert B.workspace_size(3, 6, 2, 64, 10, 16) == _split_bytes(3, 6, 2, 64, 10) + 32
     # a partition that covers the whole context is one pass
     assert B.resolved_partition(4, 4, 4, 64, 4, 64) == -1
-    assert B.workspace_size(4, 4, 4, 64, 4, 64) == 0
+    assert B.workspace_size(4, 4, 4, 64, 4, 64) == 32
     # invalid partition sizes
     assert B.resolved_partition(4, 4, 4, 64, 4, 24) == 0
     assert B.workspace_size(0, 4, 4, 64, 4) == 0
@@ -166,3 +168,15 @@ def test_binding_scratch_size_matches_the_header():
     m = re.search(r"#define\s+PKV_NOALLOC_SCRATCH_BYTES\s+\((\d+)u\s*<<\s*(\d+)\)", text)
     assert m, "PKV_NOALLOC_SCRATCH_BYTES not found in include/paged_kv.h"
     assert int(m.group(1)) << int(m.group(2)) == B.NOALLOC_SCRATCH_BYTES
+
+
+def test_plan_rejects_bad_arguments_before_launch():
+    plan = B.lib().pkv_paged_attention_plan
+    assert plan(None, 4, 4, 4, 64, 4, 0, FAKE, 64, None) == 1          # no lengths
+    assert plan(FAKE + 2, 4, 4, 4, 64, 4, 0, FAKE, 64, None) == 1      # misaligned lengths
+    assert plan(FAKE, 4, 6, 4, 64, 4, 0, FAKE, 64, None) == 1          # not a multiple
+    assert plan(FAKE, 4, 4, 4, 64, 4, 0, None, 0, None) == 5           # needs the plan region
+    assert plan(FAKE, 4, 4, 4, 64, 4, 0, FAKE, 31, None) == 5          # 16 + 16 bytes
+    assert plan(FAKE, 4, 4, 4, 64, 4, 24, FAKE, 64, None) == 1         # bad partition
+    assert plan(FAKE, 0, 4, 4, 64, 4, 0, None, 0, None) == 0           # nothing to plan
+    assert plan(FAKE, 1, 4, 4, 64, 4, 0, None, 0, None) == 0           # one sequence: nothing to plan

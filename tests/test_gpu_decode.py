@@ -358,15 +358,18 @@ def test_every_partial_tile_size_on_the_tensor_cores(dtype, d, partition):
     assert B.device_status(clear=True) == 0
 
 
-def _dispatch_order(lens, max_len):
+PLAN_MAGIC = 0x504b5631  # the first word of a launch plan's header
+
+
+def _dispatch_order(lens, max_len, short_last=True):
     """The row order the ordering kernel promises, restated on the host: tiles
     t = ceil(min(max(L, 0), max_len) / 16), mean over the batch; sequences with
-    t >= 2 x mean first, then those above 5/8 of the mean, then the rest, each
-    in natural order."""
+    t >= 2 x mean first, then (with short_last) those above 5/8 of the mean,
+    then the rest, each in natural order."""
     t = [(min(max(int(L), 0), max_len) + 15) // 16 for L in lens]
     S, total = len(t), sum(t)
     longs = [s for s in range(S) if 2 * t[s] * S >= 4 * total]
-    shorts = [s for s in range(S) if s not in set(longs) and 8 * t[s] * S <= 5 * total]
+    shorts = [s for s in range(S) if short_last and s not in set(longs) and 8 * t[s] * S <= 5 * total]
     rest = [s for s in range(S) if s not in set(longs) and s not in set(shorts)]
     return longs + rest + shorts
 
@@ -384,7 +387,7 @@ def test_ordering_kernel_writes_the_promised_order(S, hkv, seed):
     mb = case.tables.shape[1]
     need = B.workspace_size(S, 2 * hkv, hkv, 64, mb)
     at = need - (4 * S + 15) // 16 * 16
-    assert at >= 0 and at % 16 == 0
+    assert at >= 16 and at % 16 == 0
     ws = torch.full((need,), 0xFF, dtype=torch.uint8, device="cuda")
     out = torch.empty_like(case.q)
     B.paged_attention_decode(out, case.q, case.k_pool, case.v_pool, case.tables, case.lens, case.scale,
@@ -393,6 +396,7 @@ def test_ordering_kernel_writes_the_promised_order(S, hkv, seed):
     got = ws[at:at + 4 * S].view(torch.int32).cpu().tolist()
     want = _dispatch_order(lens.tolist(), mb * 16)
     assert got == want
+    assert ws[at - 16:at].view(torch.int32).cpu().tolist() == [PLAN_MAGIC, S, 0, 0]
     assert sorted(got) == list(range(S))
     _check_sampled(case, out, 16, seed=seed)
     assert B.device_status(clear=True) == 0
@@ -412,3 +416,72 @@ def test_batch_ranked_once_for_the_grid(dtype, hq, hkv, d):
     out = _run(case)
     H.assert_attention_close(H.to_f64(out), H.oracle_full(case), "ordered batch")
     assert B.device_status(clear=True) == 0
+
+
+# ---------------------------------------------------------------------------
+# launch plans: made once per decode step, used by every layer's decode
+# ---------------------------------------------------------------------------
+def _lognormal_lens(S, seed, median=150, sigma=0.6, hi=1024):
+    rng = np.random.default_rng(seed)
+    lens = np.clip(np.round(median * np.exp(sigma * rng.standard_normal(S))), 1, hi).astype(np.int32)
+    lens[rng.integers(0, S, 2)] = hi
+    lens[rng.integers(0, S, 2)] = 0
+    return lens
+
+
+@pytest.mark.parametrize("S,hq,hkv,d,dtype,part", [(64, 40, 40, 128, "bf16", 0), (256, 32, 8, 128, "bf16", 0),
+                                                   (150, 8, 4, 64, "f16", 0), (40, 16, 8, 128, "f16", 0),
+                                                   (200, 4, 4, 64, "bf16", 256), (300, 4, 4, 64, "bf16", 128)])
+def test_planned_decode_matches_the_oracle_and_the_unplanned_call(S, hq, hkv, d, dtype, part):
+    lens = _lognormal_lens(S, seed=S + d)
+    case = H.make_case(lens, hq, hkv, d, dtype, seed=S + hq)
+    mb = case.tables.shape[1]
+    need = B.workspace_size(S, hq, hkv, d, mb, part)
+    ws = torch.full((need,), 0xAB, dtype=torch.uint8, device="cuda")
+    B.paged_attention_plan(case.lens, hq, hkv, d, mb, part, workspace=ws)
+    parts = 1 if part == 0 else -(-mb * 16 // part)
+    if S * hkv * parts <= 4096:     # a grid that starts long sequences first has a plan
+        at = need - (4 * S + 15) // 16 * 16
+        assert ws[at - 16:at].view(torch.int32).cpu().tolist() == [PLAN_MAGIC, S, 0, 0]
+        # smaller batches keep two buckets, batches of 128+ put the shortest last
+        order = ws[at:at + 4 * S].view(torch.int32).cpu().tolist()
+        assert order == _dispatch_order(lens.tolist(), mb * 16, S >= 128)
+    outs = []
+    for layer in range(2):          # two layers of one step share the plan
+        out = case.new_out()
+        B.paged_attention_decode(out, case.q, case.k_pool, case.v_pool, case.tables, case.lens, case.scale,
+                                 partition_size=part, workspace=ws, planned=True)
+        outs.append(out)
+    plain = _run(case, part)
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], plain)
+    H.assert_attention_close(H.to_f64(outs[0]), H.oracle_full(case), f"planned S={S}")
+    assert B.device_status(clear=True) == 0
+
+
+def test_planned_decode_without_a_plan_is_flagged_and_still_correct():
+    lens = _lognormal_lens(200, seed=5)
+    case = H.make_case(lens, 16, 8, 128, "bf16", seed=77)
+    mb = case.tables.shape[1]
+    ws = torch.full((B.workspace_size(200, 16, 8, 128, mb),), 0x5A, dtype=torch.uint8, device="cuda")
+    out = case.new_out()
+    B.paged_attention_decode(out, case.q, case.k_pool, case.v_pool, case.tables, case.lens, case.scale,
+                             workspace=ws, planned=True)
+    torch.cuda.synchronize()
+    assert B.device_status(clear=True) == 0x20          # BAD_PLAN: natural order instead
+    H.assert_attention_close(H.to_f64(out), H.oracle_full(case), "no plan")
+
+
+def test_a_plan_of_other_lengths_is_still_correct():
+    lens = _lognormal_lens(256, seed=6)
+    case = H.make_case(lens, 32, 8, 128, "bf16", seed=78)
+    mb = case.tables.shape[1]
+    ws = torch.empty((B.workspace_size(256, 32, 8, 128, mb),), dtype=torch.uint8, device="cuda")
+    other = torch.from_numpy(np.roll(lens, 17)).cuda()   # same batch size, other lengths
+    B.paged_attention_plan(other, 32, 8, 128, mb, workspace=ws)
+    out = case.new_out()
+    B.paged_attention_decode(out, case.q, case.k_pool, case.v_pool, case.tables, case.lens, case.scale,
+                             workspace=ws, planned=True)
+    torch.cuda.synchronize()
+    assert B.device_status(clear=True) == 0
+    H.assert_attention_close(H.to_f64(out), H.oracle_full(case), "stale plan")

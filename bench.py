@@ -224,7 +224,7 @@ def plan(wl, B):
     """The decode step's launch plan (pkv_paged_attention_plan): made once per
     step, it serves the decode of every layer of that step."""
     if wl.planned:
-        B.paged_attention_plan(wl.lens, wl.hq, wl.hkv, wl.d, wl.tables_h.shape[1], partition_size=wl.partition)
+        B.paged_attention_plan(wl.lens, wl.tables, wl.hq, wl.hkv, wl.d, partition_size=wl.partition)
 
 
 def decode(wl, B):

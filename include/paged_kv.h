@@ -207,15 +207,18 @@ size_t pkv_paged_attention_workspace_size(
  * region of `workspace` (the bytes after the split-K scratch, see
  * pkv_paged_attention_workspace_size), and pkv_paged_attention_decode_planned
  * then uses it in every layer instead of ranking the batch itself.
- * Arguments as for pkv_paged_attention_decode; context_lens is read on
- * `stream` (device memory, the same lengths the decode calls will see). Does
+ * Arguments as for pkv_paged_attention_decode; context_lens (and, for the
+ * shared-prefix schedule, block_tables; otherwise it may be NULL) are read on
+ * `stream` (device memory, the same values the decode calls will see). Does
  * nothing when the sizes need no plan (one sequence, more than 1024, grids of
- * more than 4096 CTAs, the balanced schedule).
+ * more than 4096 CTAs, the balanced schedule). For the shared-prefix schedule
+ * (partition_size -5) the plan holds the sibling groups instead; its decode
+ * calls must see the same lengths and tables.
  */
-pkv_status_t pkv_paged_attention_plan(const int32_t* context_lens, int num_seqs, int num_q_heads,
-                                      int num_kv_heads, int head_dim, int max_blocks_per_seq,
-                                      int partition_size, void* workspace, size_t workspace_bytes,
-                                      pkv_stream_t stream);
+pkv_status_t pkv_paged_attention_plan(const int32_t* context_lens, const int32_t* block_tables,
+                                      int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                      int max_blocks_per_seq, int partition_size, void* workspace,
+                                      size_t workspace_bytes, pkv_stream_t stream);
 
 /*
  * pkv_paged_attention_decode with the launch plan that pkv_paged_attention_plan

@@ -24,6 +24,7 @@ PKV_F16, PKV_BF16 = 0, 1
 BLOCK_SIZE = 16
 NOALLOC_SCRATCH_BYTES = 32 << 20   # PKV_NOALLOC_SCRATCH_BYTES
 BALANCED = -2                      # pkv_paged_attention_partition: balanced persistent schedule
+SHARED_PREFIX = -5                 # pkv_paged_attention_partition: shared-prefix schedule
 
 DEV_FLAGS = {0x1: "BAD_BLOCK_ID", 0x2: "BAD_CONTEXT_LEN", 0x4: "BAD_SLOT", 0x8: "BAD_PAIR",
              0x10: "WAIT_TIMEOUT", 0x20: "BAD_PLAN"}
@@ -57,7 +58,7 @@ _SIGS = {
     "pkv_paged_attention_decode_noalloc": ([_c_p] * 6 + [_c_int] * 6 + [_c_f, _c_int, _c_int, _c_p], _c_int),
     "pkv_paged_attention_decode_planned": ([_c_p] * 6 + [_c_int] * 6 + [_c_f, _c_int, _c_int, _c_p, _c_sz, _c_p],
                                            _c_int),
-    "pkv_paged_attention_plan": ([_c_p] + [_c_int] * 6 + [_c_p, _c_sz, _c_p], _c_int),
+    "pkv_paged_attention_plan": ([_c_p, _c_p] + [_c_int] * 6 + [_c_p, _c_sz, _c_p], _c_int),
     "pkv_paged_attention_workspace_size": ([_c_int] * 6, _c_sz),
     "pkv_paged_attention_decode_sliding": ([_c_p] * 6 + [_c_int] * 6 + [_c_f, _c_int, _c_int, _c_int, _c_p, _c_sz,
                                                                        _c_p], _c_int),
@@ -231,24 +232,26 @@ def paged_attention_decode(out, q, k_pool, v_pool, block_tables, context_lens, s
     return out
 
 
-def paged_attention_plan(context_lens, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
-                         partition_size=0, workspace=None):
+def paged_attention_plan(context_lens, block_tables, num_q_heads, num_kv_heads, head_dim, partition_size=0,
+                         workspace=None):
     """The decode step's launch plan (pkv_paged_attention_plan) into ``workspace``
     (default: the binding's own workspace of the current stream, which
-    paged_attention_decode(planned=True) then reads)."""
+    paged_attention_decode(planned=True) then reads). block_tables: int32
+    [S, max_blocks] (read by the shared-prefix schedule's plan)."""
     import torch
-    _need_cuda(context_lens)
-    if context_lens.dtype != torch.int32 or context_lens.dim() != 1:
-        raise TypeError("context_lens must be int32 [S]")
-    S = context_lens.shape[0]
-    need = workspace_size(S, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, partition_size)
+    _need_cuda(context_lens, block_tables)
+    if context_lens.dtype != torch.int32 or context_lens.dim() != 1 or block_tables.dtype != torch.int32 \
+            or block_tables.dim() != 2 or block_tables.shape[0] != context_lens.shape[0]:
+        raise TypeError("context_lens must be int32 [S], block_tables int32 [S, max_blocks]")
+    S, mb = block_tables.shape
+    need = workspace_size(S, num_q_heads, num_kv_heads, head_dim, mb, partition_size)
     ws_ptr, ws_bytes = None, 0
     if need:
         ws = workspace if workspace is not None else _workspace(context_lens.device, need)
         ws_ptr, ws_bytes = ws.data_ptr(), ws.numel() * ws.element_size()
     _launch(context_lens.device, "paged_attention_plan", lib().pkv_paged_attention_plan,
-            context_lens.data_ptr(), S, int(num_q_heads), int(num_kv_heads), int(head_dim),
-            int(max_blocks_per_seq), int(partition_size), ws_ptr, ws_bytes)
+            context_lens.data_ptr(), block_tables.data_ptr(), S, int(num_q_heads), int(num_kv_heads),
+            int(head_dim), int(mb), int(partition_size), ws_ptr, ws_bytes)
 
 
 def sliding_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, sliding_window,

@@ -49,6 +49,7 @@ int round_pow2_group(int g) {
 }
 
 constexpr int kBalanced = -2;  // partition choice: balanced persistent schedule
+constexpr int kSharedPrefix = -5;  // partition choice: shared prompt prefixes read once per group
 constexpr int64_t kLongFirstMaxCtas = 4096;  // grids up to ~9 waves start long sequences first
 
 // CTAs the one-pass grid should have to keep every SM busy: 4 per SM of a
@@ -67,7 +68,7 @@ int choose_partition(int num_seqs, int num_q_heads, int num_kv_heads, int head_d
                      int requested) {
   (void)num_q_heads;
   (void)head_dim;
-  if (requested == -1 || requested == kBalanced) return requested;
+  if (requested == -1 || requested == kBalanced || requested == kSharedPrefix) return requested;
   if (requested > 0) return requested;
   const int64_t pairs = int64_t(num_seqs) * num_kv_heads;
   const int64_t max_ctx = int64_t(max_blocks_per_seq) * PKV_BLOCK_SIZE;
@@ -96,6 +97,34 @@ bool long_first_grid(int num_seqs, int num_kv_heads, int max_parts) {
 size_t plan_bytes(int num_seqs, int num_kv_heads, int max_parts) {
   if (num_seqs < 2 || num_seqs > pkv::kOrderMaxSeqs || !long_first_grid(num_seqs, num_kv_heads, max_parts)) return 0;
   return 16 + (size_t(num_seqs) * sizeof(int32_t) + 15) / 16 * 16;
+}
+
+// Sizes the shared-prefix schedule takes: batches the plan kernel covers,
+// tables it compares, and at least two members per group (query heads per KV
+// head at most 4: a group's query rows fill at most kPrefixRows MMA rows).
+bool prefix_fits(int num_seqs, int num_q_heads, int num_kv_heads, int max_blocks_per_seq) {
+  const int group = num_kv_heads > 0 ? num_q_heads / num_kv_heads : 0;
+  return group >= 1 && group <= pkv::kPrefixRows / 2 && num_seqs >= 2 && num_seqs <= pkv::kOrderMaxSeqs &&
+         max_blocks_per_seq <= pkv::kPrefixMaxBlocks;
+}
+int prefix_max_members(int num_q_heads, int num_kv_heads) { return pkv::kPrefixRows / (num_q_heads / num_kv_heads); }
+
+// Workspace of the shared-prefix schedule: the split-K layout with two
+// partitions (shared prefix, own tokens), then the prefix plan: header int4,
+// groups int4[num_seqs / 2], shared tokens int32[num_seqs] (16-byte rounded).
+struct PrefixLayout {
+  size_t header_offset, groups_offset, tokens_offset, total;
+  int max_groups;
+};
+
+PrefixLayout prefix_layout(size_t split_total, int num_seqs) {
+  PrefixLayout l;
+  l.max_groups = num_seqs / 2 > 0 ? num_seqs / 2 : 1;
+  l.header_offset = split_total;
+  l.groups_offset = l.header_offset + 16;
+  l.tokens_offset = l.groups_offset + size_t(l.max_groups) * 16;
+  l.total = l.tokens_offset + (size_t(num_seqs) * sizeof(int32_t) + 15) / 16 * 16;
+  return l;
 }
 
 bool balanced_fits(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim) {
@@ -134,6 +163,11 @@ pkv_status_t plan_decode(int max_blocks_per_seq, int partition, Plan* plan) {
   if (partition == kBalanced) {
     plan->part_tokens = 0;
     plan->max_parts = 0;
+    return PKV_OK;
+  }
+  if (partition == kSharedPrefix) {  // two partial slots: the shared prefix and the own tokens
+    plan->part_tokens = int(max_ctx);
+    plan->max_parts = 2;
     return PKV_OK;
   }
   if (partition == -1) {
@@ -280,6 +314,8 @@ int pkv_paged_attention_partition(int num_seqs, int num_q_heads, int num_kv_head
   Plan plan;
   if (plan_decode(max_blocks_per_seq, p, &plan) != PKV_OK) return 0;
   if (p == kBalanced) return kBalanced;
+  if (p == kSharedPrefix)
+    return prefix_fits(num_seqs, num_q_heads, num_kv_heads, max_blocks_per_seq) ? kSharedPrefix : 0;
   return plan.max_parts <= 1 ? -1 : plan.part_tokens;
 }
 
@@ -295,6 +331,10 @@ size_t pkv_paged_attention_workspace_size(int num_seqs, int num_q_heads, int num
   if (p == kBalanced) {
     if (num_q_heads % num_kv_heads != 0) return 0;
     return sk_layout(num_seqs, num_q_heads, num_kv_heads, head_dim).total;
+  }
+  if (p == kSharedPrefix) {
+    if (!prefix_fits(num_seqs, num_q_heads, num_kv_heads, max_blocks_per_seq)) return 0;
+    return prefix_layout(split_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, 2).total, num_seqs).total;
   }
   return split_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, plan.max_parts).total +
          plan_bytes(num_seqs, num_kv_heads, plan.max_parts);
@@ -344,6 +384,12 @@ pkv_status_t decode_impl(void* out, const void* q, const void* k_pool, const voi
   pkv_status_t st = plan_decode(plan_blocks, p, &plan);
   if (st != PKV_OK) return st;
   const bool balanced = p == kBalanced;
+  const bool shared_prefix = p == kSharedPrefix;
+  if (shared_prefix && (window > 0 || !prefix_fits(num_seqs, num_q_heads, num_kv_heads, max_blocks_per_seq)))
+    return pkv::fail(PKV_ERR_UNSUPPORTED,
+                     "the shared-prefix schedule takes 2..%d sequences, at most 4 query heads per KV head, tables "
+                     "of at most %d blocks and no sliding window",
+                     pkv::kOrderMaxSeqs, pkv::kPrefixMaxBlocks);
   if (balanced && window > 0)
     return pkv::fail(PKV_ERR_UNSUPPORTED, "the balanced schedule takes no sliding window");
   if (balanced && !balanced_fits(num_seqs, num_q_heads, num_kv_heads, head_dim))
@@ -351,8 +397,9 @@ pkv_status_t decode_impl(void* out, const void* q, const void* k_pool, const voi
                      pkv::decode_sk_max_seqs(head_dim, round_pow2_group(group)));
   const SplitLayout lay = split_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, plan.max_parts);
   const SkLayout sk = sk_layout(num_seqs, num_q_heads, num_kv_heads, head_dim);
-  const size_t ord = balanced ? 0 : plan_bytes(num_seqs, num_kv_heads, plan.max_parts);
-  const size_t need = balanced ? sk.total : lay.total + ord;
+  const size_t ord = (balanced || shared_prefix) ? 0 : plan_bytes(num_seqs, num_kv_heads, plan.max_parts);
+  const PrefixLayout pre = prefix_layout(lay.total, num_seqs);
+  const size_t need = balanced ? sk.total : shared_prefix ? pre.total : lay.total + ord;
   if (int64_t(num_blocks) * num_kv_heads * PKV_BLOCK_SIZE > INT32_MAX)
     return pkv::fail(PKV_ERR_UNSUPPORTED, "num_blocks * num_kv_heads * 16 exceeds 2^31 rows");
   if (need > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, 16)))
@@ -367,7 +414,7 @@ pkv_status_t decode_impl(void* out, const void* q, const void* k_pool, const voi
   // boxes of 16, 8 and 4 rows (the tensor-core kernel copies partial last
   // tiles in 4-row multiples; the balanced schedule uses the first pair)
   alignas(64) CUtensorMap kmap[3], vmap[3];
-  if (gpad >= 2) {
+  if (gpad >= 2 || shared_prefix) {
     const int64_t rows = int64_t(num_blocks) * num_kv_heads * PKV_BLOCK_SIZE;
     for (int i = 0; i < 3; ++i) {
       st = pool_tensor_map(&kmap[i], k_pool, rows, head_dim, dtype, PKV_BLOCK_SIZE >> i);
@@ -443,6 +490,34 @@ pkv_status_t decode_impl(void* out, const void* q, const void* k_pool, const voi
   a.scale_log2 = scale * 1.4426950408889634f;
 
   cudaError_t err = cudaSuccess;
+  if (shared_prefix) {
+    // The prefix plan (made here, or by pkv_paged_attention_plan for a planned
+    // call) zeroes the merge counters; the prefix kernel reads shared prompt
+    // blocks once per group of siblings, the grid kernels the rest of every
+    // sequence, and the later of the two for a sequence merges them.
+    char* ws = static_cast<char*>(workspace);
+    int4* hdr = reinterpret_cast<int4*>(ws + pre.header_offset);
+    int4* groups = reinterpret_cast<int4*>(ws + pre.groups_offset);
+    int32_t* ptok = reinterpret_cast<int32_t*>(ws + pre.tokens_offset);
+    a.long_first = 0;
+    a.order = nullptr;
+    a.plan = nullptr;
+    a.prefix_tokens = ptok;
+    a.prefix_header = hdr;
+    if (!planned) {
+      err = pkv::launch_prefix_plan(context_lens, block_tables, num_seqs, max_blocks_per_seq, num_kv_heads,
+                                    prefix_max_members(num_q_heads, num_kv_heads), hdr, groups, ptok, a.counters,
+                                    stream);
+      if (err != cudaSuccess) return cuda_status(err, "prefix plan");
+    }
+    a.prefix_groups = groups;
+    a.prefix_slots = pre.max_groups;
+    // one launch of the tensor-core kernel with rows for groups of up to
+    // kPrefixRows query rows: the group CTAs first, then every sequence's own tokens
+    err = dtype == PKV_F16 ? pkv::launch_decode_f16(a, head_dim, pkv::kPrefixRows, kmap, vmap, stream)
+                           : pkv::launch_decode_bf16(a, head_dim, pkv::kPrefixRows, kmap, vmap, stream);
+    return cuda_status(err, "paged_attention_decode launch");
+  }
   if (lay.total > 0) {
     // The partition counters start at zero on every call; the partials need no initialisation.
     err = cudaMemsetAsync(a.counters, 0, lay.counter_bytes, stream);
@@ -485,9 +560,10 @@ pkv_status_t pkv_paged_attention_decode_planned(void* out, const void* q, const 
                      workspace_bytes, true, stream);
 }
 
-pkv_status_t pkv_paged_attention_plan(const int32_t* context_lens, int num_seqs, int num_q_heads, int num_kv_heads,
-                                      int head_dim, int max_blocks_per_seq, int partition_size, void* workspace,
-                                      size_t workspace_bytes, pkv_stream_t stream) {
+pkv_status_t pkv_paged_attention_plan(const int32_t* context_lens, const int32_t* block_tables, int num_seqs,
+                                      int num_q_heads, int num_kv_heads, int head_dim, int max_blocks_per_seq,
+                                      int partition_size, void* workspace, size_t workspace_bytes,
+                                      pkv_stream_t stream) {
   if (num_seqs < 0) return pkv::fail(PKV_ERR_INVALID_ARG, "num_seqs < 0");
   if (num_seqs == 0) return pkv::ok();
   if (num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0)
@@ -501,6 +577,25 @@ pkv_status_t pkv_paged_attention_plan(const int32_t* context_lens, int num_seqs,
   pkv_status_t st = plan_decode(max_blocks_per_seq, p, &plan);
   if (st != PKV_OK) return st;
   if (p == kBalanced) return pkv::ok();  // the balanced schedule takes no plan
+  if (p == kSharedPrefix) {
+    if (!prefix_fits(num_seqs, num_q_heads, num_kv_heads, max_blocks_per_seq))
+      return pkv::fail(PKV_ERR_UNSUPPORTED, "these sizes take no shared-prefix schedule");
+    if (!block_tables || !aligned(block_tables, 4))
+      return pkv::fail(PKV_ERR_INVALID_ARG, "the shared-prefix plan reads block_tables (4-byte aligned)");
+    const SplitLayout lay2 = split_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, 2);
+    const PrefixLayout pre = prefix_layout(lay2.total, num_seqs);
+    if (!workspace || workspace_bytes < pre.total || !aligned(workspace, 16))
+      return pkv::fail(PKV_ERR_WORKSPACE, "workspace of %zu bytes (16-byte aligned) required, got %zu at %p",
+                       pre.total, workspace_bytes, workspace);
+    char* ws = static_cast<char*>(workspace);
+    return cuda_status(pkv::launch_prefix_plan(context_lens, block_tables, num_seqs, max_blocks_per_seq, num_kv_heads,
+                                               prefix_max_members(num_q_heads, num_kv_heads),
+                                               reinterpret_cast<int4*>(ws + pre.header_offset),
+                                               reinterpret_cast<int4*>(ws + pre.groups_offset),
+                                               reinterpret_cast<int32_t*>(ws + pre.tokens_offset),
+                                               reinterpret_cast<unsigned int*>(ws + lay2.counter_offset), stream),
+                       "prefix plan");
+  }
   const SplitLayout lay = split_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, plan.max_parts);
   const size_t ord = plan_bytes(num_seqs, num_kv_heads, plan.max_parts);
   if (ord == 0) return pkv::ok();        // nothing to plan: natural order
@@ -527,7 +622,7 @@ pkv_status_t pkv_paged_attention_decode_sliding(void* out, const void* q, const 
 size_t pkv_paged_attention_sliding_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
                                                   int max_blocks_per_seq, int sliding_window, int partition_size) {
   if (max_blocks_per_seq <= 0) return 0;
-  if (sliding_window > 0 && partition_size == kBalanced) return 0;
+  if (sliding_window > 0 && (partition_size == kBalanced || partition_size == kSharedPrefix)) return 0;
   return pkv_paged_attention_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim,
                                             window_blocks(max_blocks_per_seq, sliding_window), partition_size);
 }
@@ -561,6 +656,7 @@ pkv_status_t pkv_paged_attention_decode_int8(void* out, const void* q, const int
     return pkv::fail(PKV_ERR_INVALID_ARG, "block_tables and context_lens must be 4-byte aligned");
   const int p = choose_partition(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, partition_size);
   if (p == kBalanced) return pkv::fail(PKV_ERR_UNSUPPORTED, "the INT8 cache has no balanced schedule");
+  if (p == kSharedPrefix) return pkv::fail(PKV_ERR_UNSUPPORTED, "the INT8 cache has no shared-prefix schedule");
   Plan plan;
   pkv_status_t st = plan_decode(max_blocks_per_seq, p, &plan);
   if (st != PKV_OK) return st;

@@ -266,6 +266,98 @@ seq_order_kernel(const int32_t* __restrict__ lens, int S, int max_len, int windo
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+// The prefix plan of a batch for the shared-prefix schedule
+// (decode_prefix.cuh). For each sequence s > 0, lcp[s] = the number of whole
+// blocks at the start of its table that hold the same physical ids as its
+// predecessor's (at most the whole blocks of either length). Sequence s
+// continues its predecessor's group when lcp[s] >= min_blocks; runs of such
+// sequences are cut into groups of at most max_members, each sharing the
+// smallest lcp of its links. Writes the groups {first, members, shared
+// blocks, 0}, each sequence's shared tokens (16 x shared blocks, 0 outside a
+// group), the header {kPlanMagicPrefix, S, groups, 0}, and zeroes the merge
+// counters [S][Hkv]. One CTA of 1024 threads, S <= 1024, tables of at most
+// kPrefixMaxBlocks blocks; launched like seq_order_kernel.
+__global__ void __launch_bounds__(1024)
+prefix_plan_kernel(const int32_t* __restrict__ lens, const int32_t* __restrict__ tables, int S, int max_blocks,
+                   int Hkv, int min_blocks, int max_members, int4* __restrict__ header, int4* __restrict__ groups,
+                   int32_t* __restrict__ prefix_tokens, unsigned int* __restrict__ counters) {
+  asm volatile("griddepcontrol.launch_dependents;");
+  __shared__ int full[kOrderMaxSeqs];
+  __shared__ int lcp[kOrderMaxSeqs];
+  __shared__ int warp_val[32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = int(blockDim.x >> 5);
+  const int max_len = max_blocks * kBlock;
+  for (int s = tid; s < S; s += blockDim.x) {
+    int L = __ldg(lens + s);
+    L = L < 0 ? 0 : (L > max_len ? max_len : L);
+    full[s] = L / kBlock;
+    prefix_tokens[s] = 0;
+  }
+  for (int i = tid; i < S * Hkv; i += blockDim.x) counters[i] = 0u;
+  __syncthreads();
+  // lcp, one warp per sequence, 32 table entries per step (all loads in flight)
+  for (int s = warp; s < S; s += nwarps) {
+    int n = 0;
+    if (s > 0) {
+      const int m = min(full[s], full[s - 1]);
+      const int32_t* ra = tables + size_t(s) * max_blocks;
+      const int32_t* rb = tables + size_t(s - 1) * max_blocks;
+      n = m;
+#pragma unroll 4
+      for (int j0 = 0; j0 < m; j0 += 32) {
+        const int j = j0 + lane;
+        const int x = j < m ? __ldg(ra + j) : 0, y = j < m ? __ldg(rb + j) : 0;
+        const unsigned d = __ballot_sync(kFull, x != y);
+        if (d && n == m) n = j0 + __ffs(int(d)) - 1;
+      }
+    }
+    if (lane == 0) lcp[s] = n;
+  }
+  __syncthreads();
+  // the start of each sequence's run: an inclusive max-scan of (s if it starts a run, else -1)
+  const int s = tid;
+  const bool in_batch = s < S;
+  const bool link = in_batch && s > 0 && lcp[s] >= min_blocks;
+  int v = (in_batch && !link) ? s : -1;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(kFull, v, o);
+    if (lane >= o) v = max(v, n);
+  }
+  if (lane == 31) warp_val[warp] = v;
+  __syncthreads();
+  int run_start = v;
+  for (int w = 0; w < warp; ++w) run_start = max(run_start, warp_val[w]);
+  // group leaders: every max_members-th sequence of a run
+  int members = 0, shared = 0;
+  if (in_batch && (s - run_start) % max_members == 0) {
+    members = 1;
+    shared = kPrefixMaxBlocks;
+    while (members < max_members && s + members < S && lcp[s + members] >= min_blocks) {
+      shared = min(shared, lcp[s + members]);
+      ++members;
+    }
+  }
+  const bool leader = members >= 2;
+  // compact the groups: index = leaders before this one
+  const unsigned lb = __ballot_sync(kFull, leader);
+  __syncthreads();
+  if (lane == 0) warp_val[warp] = __popc(lb);
+  __syncthreads();
+  int before = __popc(lb & ((1u << lane) - 1u));
+  int total = 0;
+  for (int w = 0; w < nwarps; ++w) {
+    if (w < warp) before += warp_val[w];
+    total += warp_val[w];
+  }
+  if (leader) {
+    groups[before] = make_int4(s, members, shared, 0);
+    for (int m = 0; m < members; ++m) prefix_tokens[s + m] = shared * kBlock;
+  }
+  if (tid == 0) *header = make_int4(kPlanMagicPrefix, S, total, 0);
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 }  // namespace
 
 cudaError_t launch_seq_order(const int32_t* lens, int num_seqs, int max_len, int window, bool short_last,
@@ -282,6 +374,23 @@ cudaError_t launch_seq_order(const int32_t* lens, int num_seqs, int max_len, int
   cfg.numAttrs = 1;
   int32_t* order = reinterpret_cast<int32_t*>(plan + 1);
   return cudaLaunchKernelEx(&cfg, seq_order_kernel, lens, num_seqs, max_len, window, short_last ? 1 : 0, order, plan);
+}
+
+cudaError_t launch_prefix_plan(const int32_t* lens, const int32_t* tables, int num_seqs, int max_blocks,
+                               int num_kv_heads, int max_members, int4* header, int4* groups, int32_t* prefix_tokens,
+                               unsigned int* counters, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3(1024);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, prefix_plan_kernel, lens, tables, num_seqs, max_blocks, num_kv_heads,
+                            kPrefixMinBlocks, max_members, header, groups, prefix_tokens, counters);
 }
 
 namespace {

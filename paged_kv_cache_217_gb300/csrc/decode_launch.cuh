@@ -3,6 +3,7 @@
 
 #include "decode.cuh"
 #include "decode_mma.cuh"
+#include "decode_prefix.cuh"
 #include "decode_sk.cuh"
 #include "launch.h"
 
@@ -78,9 +79,11 @@ cudaError_t launch_decode_dg(const DecodeArgs& a, const CUtensorMap* kmap, const
   constexpr int NW = kGridWarps;
   constexpr int STAGES = kGridStages;
   static bool configured[kMaxDevices] = {};
-  const dim3 grid(unsigned(a.num_kv_heads), unsigned(a.num_seqs), unsigned(a.max_parts));
+  // (the shared-prefix schedule's partials take two slots, its grid one pass)
+  const dim3 grid(unsigned(a.num_kv_heads), unsigned(a.num_seqs + (a.prefix_tokens ? a.prefix_slots : 0)),
+                  a.prefix_tokens ? 1u : unsigned(a.max_parts));
   if constexpr (G == 1) {
-    const int64_t ctas = int64_t(a.num_seqs) * a.num_kv_heads * a.max_parts;
+    const int64_t ctas = int64_t(grid.x) * grid.y * grid.z;
     cudaError_t err = ctas >= kWideGridCtas ? launch_cuda_core_grid<T, D, G, kWideGridWarps, 1>(a, grid, stream)
                                             : launch_cuda_core_grid<T, D, G, NW, STAGES>(a, grid, stream);
     if (err != cudaSuccess) return err;

@@ -205,6 +205,10 @@ __device__ __forceinline__ void zero_rows_outside(uint32_t vt, int lo, int rows,
   __syncwarp();
 }
 
+// One CTA of the shared-prefix schedule (decode_prefix.cuh, which defines it).
+template <typename T, int D, int G, int NW, int STAGES>
+__device__ __forceinline__ void prefix_cta(const DecodeArgs& a, const PoolMaps& maps, unsigned char* smem, int gi);
+
 template <typename T, int D, int G, int NW, int STAGES>
 __global__ void __launch_bounds__(NW * 32)
 paged_decode_mma_kernel(const DecodeArgs a, const __grid_constant__ PoolMaps maps) {
@@ -219,7 +223,15 @@ paged_decode_mma_kernel(const DecodeArgs a, const __grid_constant__ PoolMaps map
   TraceMarks tm{};
   trace_mark(tm, 0);
   const int g = blockIdx.x;
-  const int s = long_first_seq<NW>(a, blockIdx.y), part = blockIdx.z;
+  // shared-prefix schedule: the first grid rows are the sibling groups' CTAs
+  if constexpr (G == kPrefixRows) {
+    if (a.prefix_tokens && int(blockIdx.y) < a.prefix_slots) {
+      prefix_cta<T, D, G, NW, STAGES>(a, maps, smem, int(blockIdx.y));
+      return;
+    }
+  }
+  const int yrow = int(blockIdx.y) - (a.prefix_tokens ? a.prefix_slots : 0);
+  const int s = long_first_seq<NW>(a, yrow), part = blockIdx.z;
   trace_mark(tm, 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int hq0 = g * a.group;
@@ -229,7 +241,7 @@ paged_decode_mma_kernel(const DecodeArgs a, const __grid_constant__ PoolMaps map
   // not depend on the length: read them together with it (entries past the
   // sequence are never used).
   int ids_early = 0;
-  if (a.window == 0) {
+  if (a.window == 0 && !a.prefix_tokens) {
     const int j0 = (blockIdx.z * a.part_tokens) / kBlock + warp + lane * NW;
     if (j0 < a.max_blocks_per_seq) ids_early = __ldg(a.block_tables + size_t(s) * a.max_blocks_per_seq + j0);
   }
@@ -239,9 +251,30 @@ paged_decode_mma_kernel(const DecodeArgs a, const __grid_constant__ PoolMaps map
     if (threadIdx.x == 0 && part == 0 && g == 0) flag(a.status, PKV_DEV_BAD_CONTEXT_LEN);
     L = L < 0 ? 0 : max_len;
   }
-  const TokenRange tr = token_range(L, a.window);
-  const int nparts = L == 0 ? 1 : (L - tr.aligned + a.part_tokens - 1) / a.part_tokens;
+  TokenRange tr = token_range(L, a.window);
+  int nparts = L == 0 ? 1 : (L - tr.aligned + a.part_tokens - 1) / a.part_tokens;
   if (part >= nparts) return;
+  int pslot = part;  // partition slot of this CTA's partial in the workspace
+  if (a.prefix_tokens) {
+    // Shared-prefix schedule: the first prefix_tokens[s] tokens (whole blocks)
+    // are shared with sibling sequences and done by the prefix kernel, whose
+    // partial takes slot 0; this CTA takes the rest (one pass) as slot 1.
+    // Without a prefix plan of this batch every CTA takes its whole sequence.
+    const int4 ph = __ldg(a.prefix_header);
+    const bool planned = ph.x == kPlanMagicPrefix && ph.y == a.num_seqs;
+    if (!planned && threadIdx.x == 0 && blockIdx.x == 0 && yrow == 0) flag(a.status, PKV_DEV_BAD_PLAN);
+    int ft = planned ? __ldg(a.prefix_tokens + s) : 0;
+    if (ft < 0 || ft > max_len || (ft & (kBlock - 1))) {
+      flag(a.status, PKV_DEV_BAD_PLAN);
+      ft = 0;
+    }
+    if (ft > 0) {
+      if (L <= ft) return;  // no own tokens: the prefix kernel writes this sequence
+      tr.first = tr.aligned = ft;
+      nparts = 2;
+      pslot = 1;
+    }
+  }
   trace_mark(tm, 2);
   if (L == 0) {
     T* o = static_cast<T*>(a.out) + (size_t(s) * a.num_q_heads + hq0) * D;
@@ -290,7 +323,7 @@ paged_decode_mma_kernel(const DecodeArgs a, const __grid_constant__ PoolMaps map
   };
   int ids = 0;
   if (lane < n_my) {
-    ids = a.window == 0 ? ids_early : __ldg(trow + warp + lane * NW);
+    ids = (a.window == 0 && !a.prefix_tokens) ? ids_early : __ldg(trow + warp + lane * NW);
     if (ids < 0 || ids >= a.num_blocks) {
       flag(a.status, PKV_DEV_BAD_BLOCK_ID);
       ids = 0;
@@ -390,7 +423,7 @@ paged_decode_mma_kernel(const DecodeArgs a, const __grid_constant__ PoolMaps map
     }
   }
   __syncthreads();
-  finish_chunk<T, D, G, NW>(a, smem, size_t(STAGES) * C::STAGE_BYTES, s, g, part, nparts);
+  finish_chunk<T, D, G, NW>(a, smem, size_t(STAGES) * C::STAGE_BYTES, s, g, pslot, nparts);
   trace_write(a, tm, s, nb);
 }
 

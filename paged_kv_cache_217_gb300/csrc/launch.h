@@ -38,6 +38,13 @@ int decode_sk_max_seqs(int head_dim, int gpad);
 cudaError_t launch_seq_order(const int32_t* lens, int num_seqs, int max_len, int window, bool short_last,
                              int4* plan, cudaStream_t stream);
 
+// The prefix plan of the shared-prefix schedule (decode_prefix.cuh): header,
+// groups int4[num_seqs / 2], shared tokens int32[num_seqs], and the merge
+// counters [num_seqs][num_kv_heads] zeroed. num_seqs <= 1024, tables of at
+// most 256 blocks; groups of at most max_members sequences.
+cudaError_t launch_prefix_plan(const int32_t* lens, const int32_t* tables, int num_seqs, int max_blocks,
+                               int num_kv_heads, int max_members, int4* header, int4* groups, int32_t* prefix_tokens,
+                               unsigned int* counters, cudaStream_t stream);
 // One warp that waits on an mbarrier no copy completes (bounded-wait self-test).
 cudaError_t launch_bounded_wait_selftest(unsigned long long limit_ns, unsigned int* status, cudaStream_t stream);
 cudaError_t launch_trace_stamp(unsigned long long* dst, cudaStream_t stream);

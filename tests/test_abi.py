@@ -70,6 +70,14 @@ def test_workspace_and_partition_choice():
     assert B.workspace_size(2, 8, 8, 128, 2048) == _split_bytes(2, 8, 8, 128, 38) + 32
     assert B.resolved_partition(4, 4, 4, 64, 100) == 256            # 16 pairs, 1600 tokens
     assert B.resolved_partition(4, 4, 4, 64, 16) == -1              # 256 tokens: one pass
+    # the shared-prefix schedule, on request: two partial slots, then the
+    # prefix plan (header, groups int4[S / 2], shared tokens int32[S])
+    assert B.resolved_partition(128, 72, 72, 128, 80, B.SHARED_PREFIX) == B.SHARED_PREFIX
+    assert B.workspace_size(128, 72, 72, 128, 80, B.SHARED_PREFIX) == \
+        _split_bytes(128, 72, 72, 128, 2) + 16 + 64 * 16 + 512
+    assert B.resolved_partition(128, 64, 8, 128, 80, B.SHARED_PREFIX) == 0     # 8 query heads per KV head
+    assert B.resolved_partition(1, 8, 8, 128, 80, B.SHARED_PREFIX) == 0        # one sequence
+    assert B.resolved_partition(8, 8, 8, 128, 257, B.SHARED_PREFIX) == 0       # tables wider than 256 blocks
     # the balanced persistent schedule, on request
     assert B.resolved_partition(64, 40, 40, 128, 32, -2) == B.BALANCED
     assert B.workspace_size(64, 40, 40, 128, 32, -2) == _balanced_bytes(64, 40, 40, 128)
@@ -172,11 +180,16 @@ def test_binding_scratch_size_matches_the_header():
 
 def test_plan_rejects_bad_arguments_before_launch():
     plan = B.lib().pkv_paged_attention_plan
-    assert plan(None, 4, 4, 4, 64, 4, 0, FAKE, 64, None) == 1          # no lengths
-    assert plan(FAKE + 2, 4, 4, 4, 64, 4, 0, FAKE, 64, None) == 1      # misaligned lengths
-    assert plan(FAKE, 4, 6, 4, 64, 4, 0, FAKE, 64, None) == 1          # not a multiple
-    assert plan(FAKE, 4, 4, 4, 64, 4, 0, None, 0, None) == 5           # needs the plan region
-    assert plan(FAKE, 4, 4, 4, 64, 4, 0, FAKE, 31, None) == 5          # 16 + 16 bytes
-    assert plan(FAKE, 4, 4, 4, 64, 4, 24, FAKE, 64, None) == 1         # bad partition
-    assert plan(FAKE, 0, 4, 4, 64, 4, 0, None, 0, None) == 0           # nothing to plan
-    assert plan(FAKE, 1, 4, 4, 64, 4, 0, None, 0, None) == 0           # one sequence: nothing to plan
+    assert plan(None, None, 4, 4, 4, 64, 4, 0, FAKE, 64, None) == 1          # no lengths
+    assert plan(FAKE + 2, None, 4, 4, 4, 64, 4, 0, FAKE, 64, None) == 1      # misaligned lengths
+    assert plan(FAKE, None, 4, 6, 4, 64, 4, 0, FAKE, 64, None) == 1          # not a multiple
+    assert plan(FAKE, None, 4, 4, 4, 64, 4, 0, None, 0, None) == 5           # needs the plan region
+    assert plan(FAKE, None, 4, 4, 4, 64, 4, 0, FAKE, 31, None) == 5          # 16 + 16 bytes
+    assert plan(FAKE, None, 4, 4, 4, 64, 4, 24, FAKE, 64, None) == 1         # bad partition
+    assert plan(FAKE, None, 0, 4, 4, 64, 4, 0, None, 0, None) == 0           # nothing to plan
+    assert plan(FAKE, None, 1, 4, 4, 64, 4, 0, None, 0, None) == 0           # one sequence: nothing to plan
+    # the shared-prefix plan reads the tables
+    assert plan(FAKE, None, 4, 4, 4, 64, 4, -5, FAKE, 1 << 20, None) == 1
+    assert plan(FAKE, FAKE, 4, 16, 2, 64, 4, -5, FAKE, 1 << 20, None) == 2   # 8 query heads per KV head
+    assert plan(FAKE, FAKE, 4, 4, 4, 64, 300, -5, FAKE, 1 << 30, None) == 2  # tables wider than 256 blocks
+    assert plan(FAKE, FAKE, 4, 4, 4, 64, 4, -5, FAKE, 64, None) == 5         # workspace too small

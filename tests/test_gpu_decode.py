@@ -438,7 +438,7 @@ def test_planned_decode_matches_the_oracle_and_the_unplanned_call(S, hq, hkv, d,
     mb = case.tables.shape[1]
     need = B.workspace_size(S, hq, hkv, d, mb, part)
     ws = torch.full((need,), 0xAB, dtype=torch.uint8, device="cuda")
-    B.paged_attention_plan(case.lens, hq, hkv, d, mb, part, workspace=ws)
+    B.paged_attention_plan(case.lens, case.tables, hq, hkv, d, part, workspace=ws)
     parts = 1 if part == 0 else -(-mb * 16 // part)
     if S * hkv * parts <= 4096:     # a grid that starts long sequences first has a plan
         at = need - (4 * S + 15) // 16 * 16
@@ -478,10 +478,136 @@ def test_a_plan_of_other_lengths_is_still_correct():
     mb = case.tables.shape[1]
     ws = torch.empty((B.workspace_size(256, 32, 8, 128, mb),), dtype=torch.uint8, device="cuda")
     other = torch.from_numpy(np.roll(lens, 17)).cuda()   # same batch size, other lengths
-    B.paged_attention_plan(other, 32, 8, 128, mb, workspace=ws)
+    B.paged_attention_plan(other, case.tables, 32, 8, 128, workspace=ws)
     out = case.new_out()
     B.paged_attention_decode(out, case.q, case.k_pool, case.v_pool, case.tables, case.lens, case.scale,
                              workspace=ws, planned=True)
     torch.cuda.synchronize()
     assert B.device_status(clear=True) == 0
     H.assert_attention_close(H.to_f64(out), H.oracle_full(case), "stale plan")
+
+
+# ---------------------------------------------------------------------------
+# the shared-prefix schedule: sibling sequences read their shared prompt
+# blocks once per group
+# ---------------------------------------------------------------------------
+PREFIX_MAGIC = 0x504B5831  # the first word of a prefix plan's header
+
+
+def _sampling_case(num_prompts, n, prompt_range, tail_range, hq, hkv, d, dtype, seed):
+    """Sequences from the block manager after parallel sampling (prompt added,
+    forked n-1 times, tails appended with copy-on-write), pools filled with
+    seeded values, copy-on-write pairs applied."""
+    trace = W.ParallelSamplingTrace("sampling", dtype, hq, hkv, d,
+                                    np.random.default_rng(seed).integers(*prompt_range, size=num_prompts,
+                                                                         endpoint=True).astype(np.int32),
+                                    np.random.default_rng(seed + 1).integers(*tail_range, size=(num_prompts, n),
+                                                                             endpoint=True).astype(np.int32))
+    nb = trace.block_budget()
+    bm = B.BlockManager(nb, W.shuffled_free_order(nb, seed))
+    plan = W.drive_parallel_sampling(trace, bm)
+    kp = W.normal_values((nb, hkv, 16, d), dtype, seed * 3 + 1, "cuda")
+    vp = W.normal_values((nb, hkv, 16, d), dtype, seed * 3 + 2, "cuda")
+    if plan.pairs:
+        B.copy_blocks(kp, vp, torch.tensor(plan.pairs, dtype=torch.int64, device="cuda").reshape(-1, 2))
+    mb = max(-(-L // 16) for L in plan.final_lens.values())
+    tables, lens = bm.block_tables(plan.seq_ids, mb)
+    q = W.normal_values((len(plan.seq_ids), hq, d), dtype, seed * 3 + 3, "cuda")
+    return H.DecodeCase(q, kp, vp, torch.from_numpy(tables).cuda(), torch.from_numpy(lens).cuda(), d ** -0.5,
+                        dtype), trace
+
+
+def _prefix_layout(S, hq, hkv, d):
+    split = (S * hq * 2 * (d * 4 + 8) + S * hkv * 4 + 15) // 16 * 16
+    groups = split + 16
+    tokens = groups + max(S // 2, 1) * 16
+    return dict(header=split, groups=groups, tokens=tokens, total=tokens + (4 * S + 15) // 16 * 16)
+
+
+@pytest.mark.parametrize("n,hq,hkv,d,dtype", [(4, 8, 8, 128, "f16"), (3, 16, 8, 64, "bf16"),
+                                              (10, 4, 4, 256, "bf16"), (2, 16, 4, 128, "f16")])
+def test_shared_prefix_schedule_matches_the_oracle(n, hq, hkv, d, dtype):
+    case, trace = _sampling_case(6, n, (70, 300), (0, 40), hq, hkv, d, dtype, seed=n * 7 + d)
+    S, mb = case.q.shape[0], case.tables.shape[1]
+    assert B.resolved_partition(S, hq, hkv, d, mb, B.SHARED_PREFIX) == B.SHARED_PREFIX
+    lay = _prefix_layout(S, hq, hkv, d)
+    assert B.workspace_size(S, hq, hkv, d, mb, B.SHARED_PREFIX) == lay["total"]
+    ws = torch.full((lay["total"],), 0x3C, dtype=torch.uint8, device="cuda")
+    B.paged_attention_plan(case.lens, case.tables, hq, hkv, d, B.SHARED_PREFIX, workspace=ws)
+    torch.cuda.synchronize()
+    # the plan: each prompt's samples are consecutive sequences; groups of at
+    # most 8 / (query heads per KV head) members share the prompt's full blocks
+    max_members = 8 // (hq // hkv)
+    hdr = ws[lay["header"]:lay["header"] + 16].view(torch.int32).cpu().tolist()
+    want_groups = []
+    for i, P in enumerate(trace.prompt_lens.tolist()):
+        if P // 16 < 4:
+            continue
+        for g0 in range(0, n, max_members):
+            m = min(max_members, n - g0)
+            if m >= 2:
+                want_groups.append([i * n + g0, m, P // 16, 0])
+    assert hdr == [PREFIX_MAGIC, S, len(want_groups), 0]
+    groups = ws[lay["groups"]:lay["groups"] + 16 * len(want_groups)].view(torch.int32).cpu().tolist()
+    assert [groups[4 * k:4 * k + 4] for k in range(len(want_groups))] == want_groups
+    tokens = ws[lay["tokens"]:lay["tokens"] + 4 * S].view(torch.int32).cpu().tolist()
+    want_tokens = [0] * S
+    for s0, m, P, _ in want_groups:
+        for k in range(m):
+            want_tokens[s0 + k] = 16 * P
+    assert tokens == want_tokens
+    # two layers with the one plan, then an unplanned call: identical bits, the oracle's values
+    outs = []
+    for _ in range(2):
+        out = case.new_out()
+        B.paged_attention_decode(out, case.q, case.k_pool, case.v_pool, case.tables, case.lens, case.scale,
+                                 partition_size=B.SHARED_PREFIX, workspace=ws, planned=True)
+        outs.append(out)
+    plain = _run(case, B.SHARED_PREFIX)
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], plain)
+    H.assert_attention_close(H.to_f64(outs[0]), H.oracle_full(case), f"shared prefix n={n} {hq}/{hkv} d={d}")
+    assert B.device_status(clear=True) == 0
+
+
+def test_shared_prefix_siblings_with_one_query_are_bit_identical():
+    # samples whose own tokens are empty take their output straight from the
+    # prefix kernel; with one query for all of them the outputs agree bit for bit
+    case, trace = _sampling_case(3, 4, (200, 400), (0, 0), 8, 8, 128, "f16", seed=5)
+    q1 = case.q[0:1].expand_as(case.q).contiguous()
+    same = H.DecodeCase(q1, case.k_pool, case.v_pool, case.tables, case.lens, case.scale, "f16")
+    out = _run(same, B.SHARED_PREFIX)
+    n = trace.n
+    for i in range(3):
+        for c in range(1, n):
+            assert torch.equal(out[i * n + c], out[i * n])
+    H.assert_attention_close(H.to_f64(out), H.oracle_full(same), "siblings without own tokens")
+
+
+def test_shared_prefix_without_sharing_is_one_pass_per_sequence():
+    # no groups: every sequence in one pass of the tensor-core kernel
+    case = H.make_case([37, 300, 1000, 12, 0, 515], 8, 8, 128, "bf16", seed=8)
+    out = _run(case, B.SHARED_PREFIX)
+    H.assert_attention_close(H.to_f64(out), H.oracle_full(case), "no sharing")
+    assert torch.all(out[4] == 0)
+    assert B.device_status(clear=True) == 0
+
+
+def test_shared_prefix_without_a_plan_is_flagged_and_still_correct():
+    case, _ = _sampling_case(4, 4, (100, 200), (1, 30), 8, 8, 64, "f16", seed=9)
+    S, mb = case.q.shape[0], case.tables.shape[1]
+    ws = torch.full((B.workspace_size(S, 8, 8, 64, mb, B.SHARED_PREFIX),), 0x55, dtype=torch.uint8, device="cuda")
+    out = case.new_out()
+    B.paged_attention_decode(out, case.q, case.k_pool, case.v_pool, case.tables, case.lens, case.scale,
+                             partition_size=B.SHARED_PREFIX, workspace=ws, planned=True)
+    torch.cuda.synchronize()
+    assert B.device_status(clear=True) == 0x20
+    H.assert_attention_close(H.to_f64(out), H.oracle_full(case), "no prefix plan")
+
+
+def test_shared_prefix_full_size_parallel_sampling():
+    # the OPT-66B-shaped batch: 32 prompts x 4 samples, 72 heads, head_dim 128
+    case, _ = _sampling_case(32, 4, (512, 1024), (0, 256), 72, 72, 128, "f16", seed=21)
+    out = _run(case, B.SHARED_PREFIX)
+    _check_sampled(case, out, 300, seed=13)
+    H.assert_attention_close(H.to_f64(out), H.to_f64(_run(case, -1)), "shared prefix against the grid")
+    assert B.device_status(clear=True) == 0

@@ -19,9 +19,11 @@ OPT-175B-shaped long-context layer (batch 8, 96 heads MHA, head_dim 128, fp16,
 lengths uniform in [16384, 32768], blocks scattered through a shuffled pool).
 The same run also times the decode call of the LLaMA-13B, Llama-3-8B and
 OPT-66B parallel-sampling layers and reports each against the HBM roofline
-(``per_config``); for the sampling batch, whose sibling sequences share their
-prompt blocks, the roofline figure counts each shared block once (unique
-bytes), with the per-sequence (logical) figure beside it.
+(``per_config``). The sampling batch (and the beam-search batch), whose
+sibling sequences share their prompt blocks, runs the shared-prefix schedule
+(partition_size -5: each group of siblings reads its shared blocks once, its
+prefix plan made once per step); its roofline figure counts each shared
+block once (unique bytes), with the per-sequence (logical) figure beside it.
 
 value = algorithmic KV bytes read per step (sum over sequences of
 L * num_kv_heads * head_dim * 2 (K and V) * 2 bytes) / device time per step,
@@ -535,6 +537,14 @@ def cpu_baseline(wl, budget_s=12.0):
 # arms
 # ---------------------------------------------------------------------------
 PER_CONFIG = ["llama13b", "llama3_8b", "opt66b_sampling", "opt175b_long"]
+# Batches whose sibling sequences share prompt blocks run the shared-prefix
+# schedule (partition_size -5): each group of siblings reads its shared blocks
+# once. Every other workload takes the library's choice (0).
+SHARED_PREFIX_WORKLOADS = ("opt66b_sampling", "llama13b_beam")
+
+
+def default_partition(name, kv, window, B):
+    return B.SHARED_PREFIX if name in SHARED_PREFIX_WORKLOADS and kv == "native" and window == 0 else 0
 
 
 def launches_per_step(wl, B):
@@ -546,6 +556,9 @@ def launches_per_step(wl, B):
     batches of 128..1024 sequences (see pkv_paged_attention_decode). Sets
     wl.planned."""
     part = B.resolved_partition(wl.num_seqs, wl.hq, wl.hkv, wl.d, wl.tables_h.shape[1], wl.partition)
+    if part == B.SHARED_PREFIX:   # the prefix plan, made once per step
+        wl.planned = True
+        return part, 3
     parts = 1 if part in (-1, B.BALANCED) else -(-wl.tables_h.shape[1] * 16 // part)
     fits = part != B.BALANCED and wl.num_seqs <= 1024 and wl.num_seqs * wl.hkv * parts <= 4096
     wl.planned = wl.kv == "native" and wl.window == 0 and fits and wl.num_seqs >= 2
@@ -597,7 +610,7 @@ def traffic_key(name, kv, window):
 def per_config_entry(name, args, device, B, flush, stream, peak):
     import torch
     wl = build_workload(name, args.seed, device, args.kv, 0)
-    wl.partition = 0
+    wl.partition = default_partition(name, args.kv, 0, B)
     device_inputs(wl, device)
     part, _ = launches_per_step(wl, B)
     for _ in range(max(3, args.warmup)):
@@ -622,6 +635,7 @@ def per_config_entry(name, args, device, B, flush, stream, peak):
 
 def schedule_name(part, B):
     return ("balanced persistent (equal tiles per warp)" if part == B.BALANCED else
+            "shared prefix (each group of siblings reads its shared blocks once)" if part == B.SHARED_PREFIX else
             "one pass per (sequence, KV head)" if part == -1 else f"split-K, {part}-token partitions")
 
 
@@ -647,7 +661,8 @@ def run_ours(args):
     if args.window > 0 and args.kv != "native":
         raise SystemExit("--window runs on the native cache only")
     wl = build_workload(args.workload, args.seed, device, args.kv, args.window)
-    wl.partition = args.partition
+    wl.partition = (args.partition if args.partition is not None
+                    else default_partition(args.workload, args.kv, args.window, B))
     device_inputs(wl, device)
     # L2 eviction buffer: read (not written) between timed steps, so the next
     # step starts with L2 full of clean, unrelated lines and pays no write-backs.
@@ -728,7 +743,9 @@ def run_ours(args):
             "kv_bytes_per_step": wl.kv_bytes,
             "schedule": schedule_name(part, B),
             "launch_plan": ("made once per step by pkv_paged_attention_plan (inside the step's events, outside "
-                            "the decode call's), used by pkv_paged_attention_decode_planned") if wl.planned else
+                            "the decode call's), used by pkv_paged_attention_decode_planned"
+                            + (": the sibling groups of the shared-prefix schedule" if part == B.SHARED_PREFIX
+                               else "")) if wl.planned else
                            "none (or made inside the decode call)",
             "l2": f"KV working set {wl.kv_bytes / 1e6:.0f} MB > 129 MB L2, and L2 flushed "
                   f"(a {L2_FLUSH_BYTES >> 20} MB read) between timed steps outside the timed events",
@@ -777,7 +794,7 @@ def run_ours(args):
                       "traffic": line["roofline"]["traffic"],
                       "meets_70pct_of_measured": fig["frac"] >= 0.70,
                       "meets_70pct_of_nominal": fig["pct_of_nominal_8000GBs"] >= 70.0}
-        keep_main = args.partition == 0 and args.workload in PER_CONFIG
+        keep_main = args.partition is None and args.kv == "native" and args.workload in PER_CONFIG
         del wl
         torch.cuda.empty_cache()
         per = {}
@@ -849,9 +866,10 @@ def main(argv=None):
                     help="sliding-window decode over the last W tokens of each sequence (0 = full attention)")
     ap.add_argument("--kv", choices=["native", "int8"], default="native",
                     help="KV cache storage: native (the workload's fp16/bf16) or int8 codes with row scales")
-    ap.add_argument("--partition", type=int, default=0,
-                    help="decode schedule: 0 = library choice, -1 = one CTA per (sequence, KV head), "
-                         "N = split-K partitions of N tokens")
+    ap.add_argument("--partition", type=int, default=None,
+                    help="decode schedule: 0 = library choice, -1 = one CTA per (sequence, KV head), -2 = "
+                         "balanced, -5 = shared prefix, N = split-K partitions of N tokens (default: -5 for the "
+                         "sampling and beam batches, else 0)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-config", action="store_true",
                     help="skip timing the decode call of the other target layers (per_config)")

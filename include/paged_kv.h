@@ -145,6 +145,22 @@ pkv_status_t pkv_selftest_bounded_wait(uint32_t limit_us, pkv_stream_t stream);
  *       the batch's 16-token tiles; items split between warps are merged by
  *       log-sum-exp (for heavily skewed length mixes; batches of up to 2048
  *       sequences at head_dim 128);
+ *  -5   shared-prefix schedule, for parallel sampling and beam search
+ *       ([S] "並列サンプリングやビームサーチでの共有": siblings' tables hold
+ *       the same physical blocks for their common prompt): a one-CTA plan
+ *       kernel groups consecutive sequences whose tables start with the same
+ *       >= 4 physical blocks (at most 8 query rows a group: 8 / (query heads
+ *       per KV head) members); one CTA per (group, KV head) copies each
+ *       shared K/V tile once, multiplies it with every member's queries on
+ *       the tensor cores, then streams each member's own blocks for that
+ *       member's rows only. When the grid would be under one wave of
+ *       resident CTAs, a group's blocks are split over up to 4 CTAs whose
+ *       partials the last to finish merges by log-sum-exp. Sequences outside
+ *       any group take one CTA each. Takes 2..1024 sequences, at most 4 query
+ *       heads per KV head, tables of at most 256 blocks; groups form only
+ *       from equal leading table entries, so a batch without sharing is
+ *       still computed exactly. Siblings of one group with equal lengths and
+ *       contents get bit-identical outputs;
  *  N>0  (multiple of 16) split-K partitions of N tokens, one CTA each, whose
  *       partial (max, sum, weighted V) are merged by log-sum-exp.
  * The result does not depend on the schedule beyond fp32 rounding.
@@ -191,8 +207,12 @@ pkv_status_t pkv_paged_attention_decode(
 /* Bytes of workspace pkv_paged_attention_decode (and _decode_planned) needs
  * for these sizes: the split-K partials and counters, then the launch plan
  * (a 16-byte header and int32[num_seqs]) of batches of 2 to 1024 sequences in
- * grids of at most 4096 CTAs (see above); 0 for calls without either.
- * Returns 0 for invalid sizes as well. */
+ * grids of at most 4096 CTAs (see above); 0 for calls without either. For
+ * the shared-prefix schedule (-5): the split-K layout with 4 partitions (the
+ * partials of split groups and one arrival counter per (sequence, KV head)),
+ * then its plan: a 16-byte header, int4 groups[num_seqs / 2], int4
+ * chunks[num_seqs] and int32[num_seqs] rounded up to 16 bytes.
+ * Returns 0 for invalid sizes (and sizes -5 does not take) as well. */
 size_t pkv_paged_attention_workspace_size(
     int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
     int max_blocks_per_seq, int partition_size);
@@ -241,8 +261,10 @@ pkv_status_t pkv_paged_attention_decode_planned(
     pkv_stream_t stream);
 
 /* The schedule a call with these sizes runs: -2 for the balanced persistent
- * schedule, -1 for one CTA per (sequence, KV head), else the split-K
- * partition in tokens; 0 for invalid sizes. Resolves partition_size == 0. */
+ * schedule, -5 for the shared-prefix schedule, -1 for one CTA per (sequence,
+ * KV head), else the split-K partition in tokens; 0 for invalid sizes (and
+ * for -2 or -5 where those schedules do not take the sizes). Resolves
+ * partition_size == 0 (never to -2 or -5). */
 int pkv_paged_attention_partition(
     int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
     int max_blocks_per_seq, int partition_size);
@@ -296,8 +318,9 @@ pkv_status_t pkv_paged_attention_decode_noalloc(
  * Block-table entries of blocks wholly before that range are never read (the
  * block manager may have released them, see pkv_bm_release_before).
  * sliding_window <= 0 means no window. partition_size as for
- * pkv_paged_attention_decode except -2 (balanced), which returns
- * PKV_ERR_UNSUPPORTED; the split covers the window, not the whole length.
+ * pkv_paged_attention_decode except -2 (balanced) and -5 (shared prefix),
+ * which return PKV_ERR_UNSUPPORTED with a window; the split covers the
+ * window, not the whole length.
  * The workspace must hold pkv_paged_attention_sliding_workspace_size bytes.
  */
 pkv_status_t pkv_paged_attention_decode_sliding(
@@ -412,7 +435,8 @@ pkv_status_t pkv_reshape_and_cache_int8(
  * Decode over the INT8 cache: pkv_paged_attention_decode with every K row
  * read as c_K * s_K and every V row as c_V * s_V. q and out are T = dtype.
  * Same block tables, lengths, GQA rule, partition_size values (except -2,
- * the balanced schedule, which returns PKV_ERR_UNSUPPORTED), workspace
+ * the balanced schedule, and -5, the shared-prefix schedule, which return
+ * PKV_ERR_UNSUPPORTED), workspace
  * (pkv_paged_attention_workspace_size with the same arguments) and error
  * behaviour. Internally the scores are q . c_K scaled by s_K, and s_V is
  * folded into each softmax weight.

@@ -109,22 +109,47 @@ bool prefix_fits(int num_seqs, int num_q_heads, int num_kv_heads, int max_blocks
 }
 int prefix_max_members(int num_q_heads, int num_kv_heads) { return pkv::kPrefixRows / (num_q_heads / num_kv_heads); }
 
-// Workspace of the shared-prefix schedule: the split-K layout with two
-// partitions (shared prefix, own tokens), then the prefix plan: header int4,
-// groups int4[num_seqs / 2], shared tokens int32[num_seqs] (16-byte rounded).
+// Workspace of the shared-prefix schedule: the split-K layout with
+// kPrefixMaxParts partitions (the partials of split groups, one arrival
+// counter per (group's first sequence, KV head)), then the prefix plan:
+// header int4, groups int4[num_seqs / 2], chunks int4[num_seqs], the
+// sequences outside any group int32[num_seqs] (16-byte rounded).
 struct PrefixLayout {
-  size_t header_offset, groups_offset, tokens_offset, total;
-  int max_groups;
+  size_t header_offset, groups_offset, chunks_offset, others_offset, total;
+  int max_chunks;
 };
 
 PrefixLayout prefix_layout(size_t split_total, int num_seqs) {
   PrefixLayout l;
-  l.max_groups = num_seqs / 2 > 0 ? num_seqs / 2 : 1;
+  const int max_groups = num_seqs / 2 > 0 ? num_seqs / 2 : 1;
+  l.max_chunks = num_seqs;
   l.header_offset = split_total;
   l.groups_offset = l.header_offset + 16;
-  l.tokens_offset = l.groups_offset + size_t(l.max_groups) * 16;
-  l.total = l.tokens_offset + (size_t(num_seqs) * sizeof(int32_t) + 15) / 16 * 16;
+  l.chunks_offset = l.groups_offset + size_t(max_groups) * 16;
+  l.others_offset = l.chunks_offset + size_t(l.max_chunks) * 16;
+  l.total = l.others_offset + (size_t(num_seqs) * sizeof(int32_t) + 15) / 16 * 16;
   return l;
+}
+
+// CTAs of the shared-prefix grid resident at once on the current device, per
+// head_dim (64, 128, 256), looked up once per device.
+pkv_status_t prefix_slots(int head_dim, int* slots) {
+  static std::mutex mu;
+  static int cache[pkv::kMaxDevices][3] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= pkv::kMaxDevices)
+    return pkv::fail(PKV_ERR_CUDA, "no usable current CUDA device");
+  const int i = head_dim == 64 ? 0 : head_dim == 128 ? 1 : 2;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache[dev][i] <= 0) {
+    int n = 0;
+    const cudaError_t err = pkv::prefix_resident_ctas(head_dim, &n);
+    if (err != cudaSuccess)
+      return pkv::fail(PKV_ERR_CUDA, "occupancy of the shared-prefix grid: %s", cudaGetErrorString(err));
+    cache[dev][i] = n > 0 ? n : 1;
+  }
+  *slots = cache[dev][i];
+  return PKV_OK;
 }
 
 bool balanced_fits(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim) {
@@ -165,12 +190,7 @@ pkv_status_t plan_decode(int max_blocks_per_seq, int partition, Plan* plan) {
     plan->max_parts = 0;
     return PKV_OK;
   }
-  if (partition == kSharedPrefix) {  // two partial slots: the shared prefix and the own tokens
-    plan->part_tokens = int(max_ctx);
-    plan->max_parts = 2;
-    return PKV_OK;
-  }
-  if (partition == -1) {
+  if (partition == -1 || partition == kSharedPrefix) {
     plan->part_tokens = int(max_ctx);
     plan->max_parts = 1;
     return PKV_OK;
@@ -260,6 +280,26 @@ pkv_status_t cuda_status(cudaError_t err, const char* what) {
   return pkv::fail(PKV_ERR_CUDA, "%s: %s", what, cudaGetErrorString(err));
 }
 
+// Launches the prefix plan kernel into a shared-prefix workspace (its layout
+// as prefix_layout gives it for these sizes).
+pkv_status_t launch_prefix_plan_ws(const int32_t* context_lens, const int32_t* block_tables, int num_seqs,
+                                   int num_q_heads, int num_kv_heads, int head_dim, int max_blocks_per_seq,
+                                   char* ws, cudaStream_t stream) {
+  const SplitLayout split = split_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, pkv::kPrefixMaxParts);
+  const PrefixLayout pre = prefix_layout(split.total, num_seqs);
+  int slots = 0;
+  const pkv_status_t st = prefix_slots(head_dim, &slots);
+  if (st != PKV_OK) return st;
+  return cuda_status(pkv::launch_prefix_plan(context_lens, block_tables, num_seqs, max_blocks_per_seq, num_kv_heads,
+                                             slots, prefix_max_members(num_q_heads, num_kv_heads),
+                                             reinterpret_cast<int4*>(ws + pre.header_offset),
+                                             reinterpret_cast<int4*>(ws + pre.groups_offset),
+                                             reinterpret_cast<int4*>(ws + pre.chunks_offset),
+                                             reinterpret_cast<int32_t*>(ws + pre.others_offset),
+                                             reinterpret_cast<unsigned int*>(ws + split.counter_offset), stream),
+                     "prefix plan");
+}
+
 bool supported_head_dim(int d) { return d == 64 || d == 128 || d == 256; }
 
 // Trace buffer of PKV_TRACE builds (pkv_set_trace_buffer), per process.
@@ -334,7 +374,9 @@ size_t pkv_paged_attention_workspace_size(int num_seqs, int num_q_heads, int num
   }
   if (p == kSharedPrefix) {
     if (!prefix_fits(num_seqs, num_q_heads, num_kv_heads, max_blocks_per_seq)) return 0;
-    return prefix_layout(split_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, 2).total, num_seqs).total;
+    return prefix_layout(split_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, pkv::kPrefixMaxParts).total,
+                         num_seqs)
+        .total;
   }
   return split_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, plan.max_parts).total +
          plan_bytes(num_seqs, num_kv_heads, plan.max_parts);
@@ -398,7 +440,8 @@ pkv_status_t decode_impl(void* out, const void* q, const void* k_pool, const voi
   const SplitLayout lay = split_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, plan.max_parts);
   const SkLayout sk = sk_layout(num_seqs, num_q_heads, num_kv_heads, head_dim);
   const size_t ord = (balanced || shared_prefix) ? 0 : plan_bytes(num_seqs, num_kv_heads, plan.max_parts);
-  const PrefixLayout pre = prefix_layout(lay.total, num_seqs);
+  const SplitLayout pre_split = split_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, pkv::kPrefixMaxParts);
+  const PrefixLayout pre = prefix_layout(pre_split.total, num_seqs);
   const size_t need = balanced ? sk.total : shared_prefix ? pre.total : lay.total + ord;
   if (int64_t(num_blocks) * num_kv_heads * PKV_BLOCK_SIZE > INT32_MAX)
     return pkv::fail(PKV_ERR_UNSUPPORTED, "num_blocks * num_kv_heads * 16 exceeds 2^31 rows");
@@ -492,28 +535,28 @@ pkv_status_t decode_impl(void* out, const void* q, const void* k_pool, const voi
   cudaError_t err = cudaSuccess;
   if (shared_prefix) {
     // The prefix plan (made here, or by pkv_paged_attention_plan for a planned
-    // call) zeroes the merge counters; the prefix kernel reads shared prompt
-    // blocks once per group of siblings, the grid kernels the rest of every
-    // sequence, and the later of the two for a sequence merges them.
+    // call) groups siblings and zeroes the merge counters; a chunk's CTA reads
+    // its group's shared prompt blocks once and each member's own blocks, the
+    // other CTAs take the sequences outside any group.
     char* ws = static_cast<char*>(workspace);
-    int4* hdr = reinterpret_cast<int4*>(ws + pre.header_offset);
-    int4* groups = reinterpret_cast<int4*>(ws + pre.groups_offset);
-    int32_t* ptok = reinterpret_cast<int32_t*>(ws + pre.tokens_offset);
     a.long_first = 0;
     a.order = nullptr;
     a.plan = nullptr;
-    a.prefix_tokens = ptok;
-    a.prefix_header = hdr;
+    a.part_o = reinterpret_cast<float*>(ws);
+    a.part_ml = reinterpret_cast<float2*>(ws + pre_split.ml_offset);
+    a.counters = reinterpret_cast<unsigned int*>(ws + pre_split.counter_offset);
+    a.prefix_header = reinterpret_cast<int4*>(ws + pre.header_offset);
+    a.prefix_groups = reinterpret_cast<int4*>(ws + pre.groups_offset);
+    a.prefix_chunks = reinterpret_cast<int4*>(ws + pre.chunks_offset);
+    a.prefix_others = reinterpret_cast<int32_t*>(ws + pre.others_offset);
+    a.prefix_slots = pre.max_chunks;
     if (!planned) {
-      err = pkv::launch_prefix_plan(context_lens, block_tables, num_seqs, max_blocks_per_seq, num_kv_heads,
-                                    prefix_max_members(num_q_heads, num_kv_heads), hdr, groups, ptok, a.counters,
-                                    stream);
-      if (err != cudaSuccess) return cuda_status(err, "prefix plan");
+      st = launch_prefix_plan_ws(context_lens, block_tables, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                 max_blocks_per_seq, ws, stream);
+      if (st != PKV_OK) return st;
     }
-    a.prefix_groups = groups;
-    a.prefix_slots = pre.max_groups;
-    // one launch of the tensor-core kernel with rows for groups of up to
-    // kPrefixRows query rows: the group CTAs first, then every sequence's own tokens
+    // one launch of the tensor-core kernel with rows of kPrefixRows query rows:
+    // the chunk CTAs first, then the sequences outside any group
     err = dtype == PKV_F16 ? pkv::launch_decode_f16(a, head_dim, pkv::kPrefixRows, kmap, vmap, stream)
                            : pkv::launch_decode_bf16(a, head_dim, pkv::kPrefixRows, kmap, vmap, stream);
     return cuda_status(err, "paged_attention_decode launch");
@@ -582,19 +625,13 @@ pkv_status_t pkv_paged_attention_plan(const int32_t* context_lens, const int32_t
       return pkv::fail(PKV_ERR_UNSUPPORTED, "these sizes take no shared-prefix schedule");
     if (!block_tables || !aligned(block_tables, 4))
       return pkv::fail(PKV_ERR_INVALID_ARG, "the shared-prefix plan reads block_tables (4-byte aligned)");
-    const SplitLayout lay2 = split_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, 2);
-    const PrefixLayout pre = prefix_layout(lay2.total, num_seqs);
+    const PrefixLayout pre = prefix_layout(
+        split_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, pkv::kPrefixMaxParts).total, num_seqs);
     if (!workspace || workspace_bytes < pre.total || !aligned(workspace, 16))
       return pkv::fail(PKV_ERR_WORKSPACE, "workspace of %zu bytes (16-byte aligned) required, got %zu at %p",
                        pre.total, workspace_bytes, workspace);
-    char* ws = static_cast<char*>(workspace);
-    return cuda_status(pkv::launch_prefix_plan(context_lens, block_tables, num_seqs, max_blocks_per_seq, num_kv_heads,
-                                               prefix_max_members(num_q_heads, num_kv_heads),
-                                               reinterpret_cast<int4*>(ws + pre.header_offset),
-                                               reinterpret_cast<int4*>(ws + pre.groups_offset),
-                                               reinterpret_cast<int32_t*>(ws + pre.tokens_offset),
-                                               reinterpret_cast<unsigned int*>(ws + lay2.counter_offset), stream),
-                       "prefix plan");
+    return launch_prefix_plan_ws(context_lens, block_tables, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                 max_blocks_per_seq, static_cast<char*>(workspace), stream);
   }
   const SplitLayout lay = split_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, plan.max_parts);
   const size_t ord = plan_bytes(num_seqs, num_kv_heads, plan.max_parts);

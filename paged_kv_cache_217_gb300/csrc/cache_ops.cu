@@ -12,6 +12,7 @@
 // threads consecutive vectors, so loads and stores are fully coalesced.
 #include <cuda_runtime.h>
 
+#include <climits>
 #include <cstdint>
 
 #include "decode.cuh"
@@ -266,71 +267,108 @@ seq_order_kernel(const int32_t* __restrict__ lens, int S, int max_len, int windo
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+// Inclusive scan (sum, or max with MAX) over the threads of a CTA of up to
+// 1024 threads; every thread calls it. Warp 0 scans the warps' totals.
+template <bool MAX>
+__device__ __forceinline__ int cta_inclusive_scan(int v, int* warp_tot) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = int(blockDim.x >> 5);
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(kFull, v, o);
+    if (lane >= o) v = MAX ? max(v, n) : v + n;
+  }
+  __syncthreads();  // earlier readers of warp_tot are done
+  if (lane == 31) warp_tot[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    const int x0 = lane < nwarps ? warp_tot[lane] : (MAX ? INT_MIN : 0);
+    int x = x0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(kFull, x, o);
+      if (lane >= o) x = MAX ? max(x, n) : x + n;
+    }
+    const int before = __shfl_up_sync(kFull, x, 1);  // the scan of the warps before this lane's
+    if (lane < nwarps) warp_tot[lane] = lane == 0 ? (MAX ? INT_MIN : 0) : before;
+  }
+  __syncthreads();
+  return MAX ? max(v, warp_tot[warp]) : v + warp_tot[warp];
+}
+
 // The prefix plan of a batch for the shared-prefix schedule
-// (decode_prefix.cuh). For each sequence s > 0, lcp[s] = the number of whole
-// blocks at the start of its table that hold the same physical ids as its
-// predecessor's (at most the whole blocks of either length). Sequence s
-// continues its predecessor's group when lcp[s] >= min_blocks; runs of such
-// sequences are cut into groups of at most max_members, each sharing the
-// smallest lcp of its links. Writes the groups {first, members, shared
-// blocks, 0}, each sequence's shared tokens (16 x shared blocks, 0 outside a
-// group), the header {kPlanMagicPrefix, S, groups, 0}, and zeroes the merge
-// counters [S][Hkv]. One CTA of 1024 threads, S <= 1024, tables of at most
-// kPrefixMaxBlocks blocks; launched like seq_order_kernel.
+// (decode_prefix.cuh).
+//  * Groups: for each sequence s > 0, lcp[s] = the number of whole blocks at
+//    the start of its table that hold the same physical ids as its
+//    predecessor's (at most the whole blocks of either length). Sequence s
+//    continues its predecessor's run when lcp[s] >= min_blocks; runs are cut
+//    into groups of at most max_members, each sharing the smallest lcp P of
+//    its links. A group's work is its tiles: P shared ones, then each
+//    member's own.
+//  * Chunks: when the grid (groups and other sequences, times Hkv) is less
+//    than one wave of `slots` (CTAs the decode grid holds at once), a group
+//    is split into parts = ceil(work / c) chunks (1..kPrefixMaxParts), c =
+//    max(kPrefixMinChunk, W x Hkv / slots) for W the batch's tiles (groups
+//    counted as above, other sequences whole); else every group is one
+//    chunk. A part is a range of block indices [jb, je) of equal work;
+//    chunks are written longest first (LPT), a group's parts together.
+//  * Others: the sequences outside any group, in batch order.
+// Writes groups {first, members, P, parts} (batch order), chunks {group,
+// part, jb, je}, others, the header {kPlanMagicPrefix, S, chunks, others},
+// and zeroes the merge counters [S][Hkv]. One CTA of 1024 threads, S <= 1024,
+// tables of at most kPrefixMaxBlocks blocks; launched like seq_order_kernel.
 __global__ void __launch_bounds__(1024)
 prefix_plan_kernel(const int32_t* __restrict__ lens, const int32_t* __restrict__ tables, int S, int max_blocks,
-                   int Hkv, int min_blocks, int max_members, int4* __restrict__ header, int4* __restrict__ groups,
-                   int32_t* __restrict__ prefix_tokens, unsigned int* __restrict__ counters) {
+                   int Hkv, int slots, int min_blocks, int max_members, int4* __restrict__ header,
+                   int4* __restrict__ groups, int4* __restrict__ chunks, int32_t* __restrict__ others,
+                   unsigned int* __restrict__ counters) {
   asm volatile("griddepcontrol.launch_dependents;");
-  __shared__ int full[kOrderMaxSeqs];
+  __shared__ int slen[kOrderMaxSeqs];       // clamped lengths
   __shared__ int lcp[kOrderMaxSeqs];
-  __shared__ int warp_val[32];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = int(blockDim.x >> 5);
+  __shared__ int cwork[kOrderMaxSeqs / 2];  // per group: tiles of one chunk
+  __shared__ int rparts[kOrderMaxSeqs / 2]; // per rank: parts of the group of that rank
+  __shared__ int warp_tot[32];
+  const int tid = threadIdx.x;
   const int max_len = max_blocks * kBlock;
   for (int s = tid; s < S; s += blockDim.x) {
     int L = __ldg(lens + s);
-    L = L < 0 ? 0 : (L > max_len ? max_len : L);
-    full[s] = L / kBlock;
-    prefix_tokens[s] = 0;
+    slen[s] = L < 0 ? 0 : (L > max_len ? max_len : L);
   }
   for (int i = tid; i < S * Hkv; i += blockDim.x) counters[i] = 0u;
   __syncthreads();
-  // lcp, one warp per sequence, 32 table entries per step (all loads in flight)
-  for (int s = warp; s < S; s += nwarps) {
-    int n = 0;
-    if (s > 0) {
-      const int m = min(full[s], full[s - 1]);
-      const int32_t* ra = tables + size_t(s) * max_blocks;
-      const int32_t* rb = tables + size_t(s - 1) * max_blocks;
-      n = m;
-#pragma unroll 4
-      for (int j0 = 0; j0 < m; j0 += 32) {
-        const int j = j0 + lane;
-        const int x = j < m ? __ldg(ra + j) : 0, y = j < m ? __ldg(rb + j) : 0;
-        const unsigned d = __ballot_sync(kFull, x != y);
-        if (d && n == m) n = j0 + __ffs(int(d)) - 1;
-      }
+  for (int s = tid; s < S; s += blockDim.x) lcp[s] = s > 0 ? min(slen[s], slen[s - 1]) / kBlock : 0;
+  __syncthreads();
+  // lcp: every table entry j < lcp[s] of every sequence at once (one pass of
+  // loads), the first mismatch with the predecessor's entry kept by atomicMin
+  const int entries = S * max_blocks;
+  constexpr int U = 8;  // entries a thread has in flight
+  for (int i0 = tid; i0 < entries; i0 += U * int(blockDim.x)) {
+    int x[U], y[U], si[U], ji[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int i = i0 + u * int(blockDim.x);
+      si[u] = i < entries ? i / max_blocks : 0;
+      ji[u] = i - si[u] * max_blocks;
+      const bool on = i < entries && si[u] > 0 && ji[u] < lcp[si[u]];
+      const int32_t* ra = tables + size_t(si[u]) * max_blocks + ji[u];
+      x[u] = on ? __ldg(ra) : 0;
+      y[u] = on ? __ldg(ra - max_blocks) : 0;
     }
-    if (lane == 0) lcp[s] = n;
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (x[u] != y[u]) atomicMin(&lcp[si[u]], ji[u]);
   }
   __syncthreads();
   // the start of each sequence's run: an inclusive max-scan of (s if it starts a run, else -1)
   const int s = tid;
   const bool in_batch = s < S;
   const bool link = in_batch && s > 0 && lcp[s] >= min_blocks;
-  int v = (in_batch && !link) ? s : -1;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int n = __shfl_up_sync(kFull, v, o);
-    if (lane >= o) v = max(v, n);
-  }
-  if (lane == 31) warp_val[warp] = v;
-  __syncthreads();
-  int run_start = v;
-  for (int w = 0; w < warp; ++w) run_start = max(run_start, warp_val[w]);
-  // group leaders: every max_members-th sequence of a run
-  int members = 0, shared = 0;
-  if (in_batch && (s - run_start) % max_members == 0) {
+  const int run_start = cta_inclusive_scan<true>((in_batch && !link) ? s : -1, warp_tot);
+  // group leaders: every max_members-th sequence of a run; a sequence is in a
+  // group unless it leads one of a single member
+  const int lead = in_batch ? run_start + (s - run_start) / max_members * max_members : 0;
+  const bool grouped = in_batch && (s != lead || (s + 1 < S && lcp[s + 1] >= min_blocks));
+  int members = 0, shared = 0, work = 0, tiles[kPrefixRows];
+  if (in_batch && s == lead && grouped) {
     members = 1;
     shared = kPrefixMaxBlocks;
     while (members < max_members && s + members < S && lcp[s + members] >= min_blocks) {
@@ -339,22 +377,91 @@ prefix_plan_kernel(const int32_t* __restrict__ lens, const int32_t* __restrict__
     }
   }
   const bool leader = members >= 2;
-  // compact the groups: index = leaders before this one
-  const unsigned lb = __ballot_sync(kFull, leader);
-  __syncthreads();
-  if (lane == 0) warp_val[warp] = __popc(lb);
-  __syncthreads();
-  int before = __popc(lb & ((1u << lane) - 1u));
-  int total = 0;
-  for (int w = 0; w < nwarps; ++w) {
-    if (w < warp) before += warp_val[w];
-    total += warp_val[w];
-  }
   if (leader) {
-    groups[before] = make_int4(s, members, shared, 0);
-    for (int m = 0; m < members; ++m) prefix_tokens[s + m] = shared * kBlock;
+    work = shared;
+#pragma unroll
+    for (int m = 0; m < kPrefixRows; ++m) {
+      tiles[m] = m < members ? (slen[s + m] + kBlock - 1) / kBlock : 0;
+      if (m < members) work += tiles[m] - shared;
+    }
+  } else if (in_batch && !grouped) {
+    work = (slen[s] + kBlock - 1) / kBlock;
   }
-  if (tid == 0) *header = make_int4(kPlanMagicPrefix, S, total, 0);
+  // group index (leaders before this one), other-sequence index, batch tiles
+  const int gi = cta_inclusive_scan<false>(leader ? 1 : 0, warp_tot) - (leader ? 1 : 0);
+  __shared__ int totals[3];
+  if (tid == blockDim.x - 1) totals[0] = gi + (leader ? 1 : 0);
+  const int oi = cta_inclusive_scan<false>((in_batch && !grouped) ? 1 : 0, warp_tot) - ((in_batch && !grouped) ? 1 : 0);
+  if (tid == blockDim.x - 1) totals[1] = oi + ((in_batch && !grouped) ? 1 : 0);
+  const int wsum = cta_inclusive_scan<false>(work, warp_tot);
+  if (tid == blockDim.x - 1) totals[2] = wsum;
+  __syncthreads();
+  const int G = totals[0], n_others = totals[1];
+  const int64_t W = totals[2];
+  if (in_batch && !grouped) others[oi] = s;
+  // parts: only a grid of less than one wave of resident CTAs splits groups,
+  // into chunks of about one wave's share of the batch's tiles
+  const int sl = slots > 0 ? slots : 1;
+  const bool split = int64_t(G + n_others) * Hkv < sl;
+  const int c = int(max(int64_t(kPrefixMinChunk), (W * Hkv + sl - 1) / sl));
+  int parts = leader ? (split ? min(kPrefixMaxParts, (work + c - 1) / c) : 1) : 0;
+  // at most S chunks: groups are at most S / 2, so two parts a group always fit
+  const int psum = cta_inclusive_scan<false>(parts, warp_tot);
+  if (tid == blockDim.x - 1) totals[2] = psum;
+  __syncthreads();
+  if (totals[2] > S) parts = min(parts, 2);
+  if (leader) cwork[gi] = (work + parts - 1) / parts;
+  __syncthreads();
+  // rank of this group by chunk work (longest first, ties in batch order)
+  int rank = 0;
+  if (leader) {
+    const int w = cwork[gi];
+    for (int j = 0; j < G; ++j) {
+      const int x = cwork[j];
+      rank += (x > w || (x == w && j < gi)) ? 1 : 0;
+    }
+    rparts[rank] = parts;
+  }
+  __syncthreads();
+  const int rp = tid < G ? rparts[tid] : 0;
+  const int rincl = cta_inclusive_scan<false>(rp, warp_tot);
+  __syncthreads();
+  if (tid < G) cwork[tid] = rincl - rp;  // chunk index of the first part of the group of rank tid
+  if (tid == blockDim.x - 1) totals[0] = rincl;
+  __syncthreads();
+  const int nchunks = totals[0];
+  if (leader) {
+    groups[gi] = make_int4(s, members, shared, parts);
+    const int base = cwork[rank];
+    int maxn = shared;
+#pragma unroll
+    for (int m = 0; m < kPrefixRows; ++m)
+      if (m < members) maxn = max(maxn, tiles[m]);
+    // F(j): work of blocks [0, j); part q starts at the first j with F(j) >= floor(q * work / parts)
+    auto F = [&](int j) {
+      int f = min(j, shared);
+#pragma unroll
+      for (int m = 0; m < kPrefixRows; ++m)
+        if (m < members) f += max(0, min(tiles[m], j) - shared);
+      return f;
+    };
+    int jb = 0;
+    for (int q = 0; q < parts; ++q) {
+      int je = maxn;
+      if (q + 1 < parts) {
+        const int target = int(int64_t(q + 1) * work / parts);
+        int lo = jb, hi = maxn;  // the first j in [lo, hi] with F(j) >= target
+        while (lo < hi) {
+          const int mid = (lo + hi) >> 1;
+          if (F(mid) >= target) hi = mid; else lo = mid + 1;
+        }
+        je = lo;
+      }
+      chunks[base + q] = make_int4(gi, q, jb, je);
+      jb = je;
+    }
+  }
+  if (tid == 0) *header = make_int4(kPlanMagicPrefix, S, nchunks, n_others);
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
@@ -377,8 +484,8 @@ cudaError_t launch_seq_order(const int32_t* lens, int num_seqs, int max_len, int
 }
 
 cudaError_t launch_prefix_plan(const int32_t* lens, const int32_t* tables, int num_seqs, int max_blocks,
-                               int num_kv_heads, int max_members, int4* header, int4* groups, int32_t* prefix_tokens,
-                               unsigned int* counters, cudaStream_t stream) {
+                               int num_kv_heads, int slots, int max_members, int4* header, int4* groups, int4* chunks,
+                               int32_t* others, unsigned int* counters, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(1);
   cfg.blockDim = dim3(1024);
@@ -389,8 +496,8 @@ cudaError_t launch_prefix_plan(const int32_t* lens, const int32_t* tables, int n
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, prefix_plan_kernel, lens, tables, num_seqs, max_blocks, num_kv_heads,
-                            kPrefixMinBlocks, max_members, header, groups, prefix_tokens, counters);
+  return cudaLaunchKernelEx(&cfg, prefix_plan_kernel, lens, tables, num_seqs, max_blocks, num_kv_heads, slots,
+                            kPrefixMinBlocks, max_members, header, groups, chunks, others, counters);
 }
 
 namespace {

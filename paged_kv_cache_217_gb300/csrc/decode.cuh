@@ -73,10 +73,11 @@ struct DecodeArgs {
   unsigned long long* trace;  // PKV_TRACE builds: per-CTA phase timestamps (8 words a CTA), or null
   int trace_records;          // CTAs the trace buffer holds
   int window;           // sliding window: attend over the last `window` tokens (0 = all)
-  const int32_t* prefix_tokens;  // shared-prefix schedule: tokens of each sequence done by the prefix kernel, or null
-  const int4* prefix_header;     // ... and the header of the plan that holds them
-  const int4* prefix_groups;     // ... and its groups {first member, members, shared blocks, 0}
-  int prefix_slots;              // grid rows taken by group CTAs (ahead of the sequences' rows)
+  const int4* prefix_header;     // shared-prefix schedule: the prefix plan's header {magic, S, chunks, others}, or null
+  const int4* prefix_groups;     // ... its groups {first member, members, shared blocks, parts}
+  const int4* prefix_chunks;     // ... its chunks {group, part, first block, end block}, longest first
+  const int32_t* prefix_others;  // ... the sequences outside any group
+  int prefix_slots;              // ... and the grid rows reserved for chunks (num_seqs)
   float scale_log2;     // scale * log2(e)
 };
 
@@ -150,6 +151,15 @@ constexpr int kPlanMagicPrefix = 0x504b5831;  // "PKX1"
 constexpr int kPrefixMinBlocks = 4;    // shared prefixes shorter than this stay in the members' own CTAs
 constexpr int kPrefixMaxBlocks = 256;  // table widths the prefix plan compares
 constexpr int kPrefixRows = 8;         // query rows per group (members x query heads per KV head)
+// A group's tiles may be split over up to kPrefixMaxParts CTAs (merged by
+// log-sum-exp) so that a batch of few groups still fills the GPU: only when
+// the grid is under one wave of resident CTAs, in chunks of at least
+// kPrefixMinChunk tiles. Measured on GB300 (LLaMA-13B beam batch, 640 group
+// CTAs for 608 resident): chunks aimed at 1 or 3 waves took 61.8 and
+// 67.6 us against 61.1 us unsplit -- each chunk pays a CTA's start-up and a
+// merge.
+constexpr int kPrefixMaxParts = 4;
+constexpr int kPrefixMinChunk = 8;
 // A sequence is "long" when its tile count is at least kLongFirstX2 / 2 times
 // the batch mean (2x). Measured on GB300 (threshold x mean -> decode call µs):
 // Llama-3-8B-shaped layer 1.5 -> 43.7, 2 -> 43.4, 2.5 -> 43.6, 4 -> 46.7;
@@ -544,7 +554,7 @@ paged_decode_kernel(const DecodeArgs a) {
   // not depend on the length: read them together with it (entries past the
   // sequence are never used).
   int ids_early = 0;
-  if (a.window == 0 && !a.prefix_tokens) {
+  if (a.window == 0) {
     const int j0 = (blockIdx.z * a.part_tokens) / kBlock + warp + lane * NW;
     if (j0 < a.max_blocks_per_seq) ids_early = __ldg(a.block_tables + size_t(s) * a.max_blocks_per_seq + j0);
   }
@@ -554,30 +564,10 @@ paged_decode_kernel(const DecodeArgs a) {
     if (threadIdx.x == 0 && part == 0 && g == 0) flag(a.status, PKV_DEV_BAD_CONTEXT_LEN);
     L = L < 0 ? 0 : max_len;
   }
-  TokenRange tr = token_range(L, a.window);
-  int nparts = L == 0 ? 1 : (L - tr.aligned + a.part_tokens - 1) / a.part_tokens;
+  const TokenRange tr = token_range(L, a.window);
+  const int nparts = L == 0 ? 1 : (L - tr.aligned + a.part_tokens - 1) / a.part_tokens;
   if (part >= nparts) return;
-  int pslot = part;  // partition slot of this CTA's partial in the workspace
-  if (a.prefix_tokens) {
-    // Shared-prefix schedule: the first prefix_tokens[s] tokens (whole blocks)
-    // are shared with sibling sequences and done by the prefix kernel, whose
-    // partial takes slot 0; this CTA takes the rest (one pass) as slot 1.
-    // Without a prefix plan of this batch every CTA takes its whole sequence.
-    const int4 ph = __ldg(a.prefix_header);
-    const bool planned = ph.x == kPlanMagicPrefix && ph.y == a.num_seqs;
-    if (!planned && threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) flag(a.status, PKV_DEV_BAD_PLAN);
-    int ft = planned ? __ldg(a.prefix_tokens + s) : 0;
-    if (ft < 0 || ft > max_len || (ft & (kBlock - 1))) {
-      flag(a.status, PKV_DEV_BAD_PLAN);
-      ft = 0;
-    }
-    if (ft > 0) {
-      if (L <= ft) return;  // no own tokens: the prefix kernel writes this sequence
-      tr.first = tr.aligned = ft;
-      nparts = 2;
-      pslot = 1;
-    }
-  }
+  const int pslot = part;  // partition slot of this CTA's partial in the workspace
   trace_mark(tm, 2);
 
   if (L == 0) {  // empty sequence: zeros
@@ -634,7 +624,7 @@ paged_decode_kernel(const DecodeArgs a) {
   };
   int ids = 0;
   if (lane < n_my) {
-    ids = (a.window == 0 && !a.prefix_tokens) ? ids_early : __ldg(trow + warp + lane * NW);
+    ids = a.window == 0 ? ids_early : __ldg(trow + warp + lane * NW);
     if (ids < 0 || ids >= a.num_blocks) {
       flag(a.status, PKV_DEV_BAD_BLOCK_ID);
       ids = 0;

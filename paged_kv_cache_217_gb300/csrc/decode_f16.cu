@@ -19,4 +19,13 @@ int decode_sk_max_seqs(int head_dim, int gpad) {
     default: return 0;
   }
 }
+cudaError_t prefix_resident_ctas(int head_dim, int* ctas) {
+  // fp16 and bf16 instantiations have the same shape and shared memory.
+  switch (head_dim) {
+    case 64: return prefix_resident_ctas_d<__half, 64>(ctas);
+    case 128: return prefix_resident_ctas_d<__half, 128>(ctas);
+    case 256: return prefix_resident_ctas_d<__half, 256>(ctas);
+    default: return cudaErrorInvalidValue;
+  }
+}
 }  // namespace pkv

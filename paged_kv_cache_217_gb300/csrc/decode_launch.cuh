@@ -79,9 +79,9 @@ cudaError_t launch_decode_dg(const DecodeArgs& a, const CUtensorMap* kmap, const
   constexpr int NW = kGridWarps;
   constexpr int STAGES = kGridStages;
   static bool configured[kMaxDevices] = {};
-  // (the shared-prefix schedule's partials take two slots, its grid one pass)
-  const dim3 grid(unsigned(a.num_kv_heads), unsigned(a.num_seqs + (a.prefix_tokens ? a.prefix_slots : 0)),
-                  a.prefix_tokens ? 1u : unsigned(a.max_parts));
+  // (the shared-prefix schedule: rows for its chunks, then the sequences, one pass)
+  const dim3 grid(unsigned(a.num_kv_heads), unsigned(a.num_seqs + (a.prefix_header ? a.prefix_slots : 0)),
+                  a.prefix_header ? 1u : unsigned(a.max_parts));
   if constexpr (G == 1) {
     const int64_t ctas = int64_t(grid.x) * grid.y * grid.z;
     cudaError_t err = ctas >= kWideGridCtas ? launch_cuda_core_grid<T, D, G, kWideGridWarps, 1>(a, grid, stream)
@@ -102,6 +102,26 @@ cudaError_t launch_decode_dg(const DecodeArgs& a, const CUtensorMap* kmap, const
     if (err != cudaSuccess) return err;
   }
   return cudaGetLastError();
+}
+
+// CTAs of the shared-prefix grid kernel (group rows kPrefixRows) that one SM
+// holds at once, times the SMs of the current device.
+template <typename T, int D>
+cudaError_t prefix_resident_ctas_d(int* ctas) {
+  using C = MmaCfg<T, D, kMmaWarps, kMmaStages>;
+  auto kern = paged_decode_mma_kernel<T, D, kPrefixRows, kMmaWarps, kMmaStages>;
+  static bool configured[kMaxDevices] = {};
+  cudaError_t err = configure_once(kern, C::SMEM_BYTES, configured);
+  if (err != cudaSuccess) return err;
+  int per_sm = 0, dev = 0, sms = 0;
+  err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kMmaWarps * 32, C::SMEM_BYTES);
+  if (err != cudaSuccess) return err;
+  err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (err != cudaSuccess) return err;
+  *ctas = per_sm * sms;
+  return cudaSuccess;
 }
 
 template <typename T, int D>

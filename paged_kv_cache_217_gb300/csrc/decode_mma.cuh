@@ -120,11 +120,13 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
   return uint32_t((chunk >> 3) * (kBlock * 128) + row * 128 + (((chunk & 7) ^ (row & 7)) << 4));
 }
 
-// One 16-row tile for the G heads of this warp's lane row g = lane/4.
+// One 16-row tile for the G heads of this warp's lane row g = lane/4. A lane
+// whose row_on is false takes nothing from the tile (its scores are -inf):
+// its weights are exactly 0 and its running max, sum and output unchanged.
 template <typename T, int D, int NW, int STAGES, bool MASK>
 __device__ __forceinline__ void mma_tile(uint32_t kt, uint32_t vt, int lo, int rows, const uint32_t (&qa)[D / 16][2],
                                          float (&o)[D / 8][4], float& mrun, float& lrun, float scale_log2,
-                                         int lane) {
+                                         int lane, bool row_on = true) {
   using C = MmaCfg<T, D, NW, STAGES>;
   const int t = lane & 3;
   const int mi = lane >> 3, rr = lane & 7;
@@ -150,12 +152,16 @@ __device__ __forceinline__ void mma_tile(uint32_t kt, uint32_t vt, int lo, int r
     if (8 + 2 * t < lo || 8 + 2 * t >= rows) x[2] = -INFINITY;
     if (9 + 2 * t < lo || 9 + 2 * t >= rows) x[3] = -INFINITY;
   }
+  if (!row_on) x[0] = x[1] = x[2] = x[3] = -INFINITY;  // this lane's row (query) does not attend to this tile
   float mt = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
   mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 1));
   mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 2));
   const float mn = fmaxf(mrun, mt);
+  // A row that has seen no valid score yet keeps mrun = -inf; exponents are
+  // taken against 0 there so that every weight is exactly 0 (not NaN).
+  const float mref = mn == -INFINITY ? 0.f : mn;
   if (__any_sync(kFull, mn > mrun)) {
-    const float alpha = fast_exp2(mrun - mn);  // 1 for rows whose max did not move
+    const float alpha = fast_exp2(mrun - mref);  // 1 for rows whose max did not move
     lrun *= alpha;
 #pragma unroll
     for (int nd = 0; nd < C::NTILES; ++nd) {
@@ -166,7 +172,7 @@ __device__ __forceinline__ void mma_tile(uint32_t kt, uint32_t vt, int lo, int r
   }
   float p[4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) p[i] = fast_exp2(x[i] - mn);
+  for (int i = 0; i < 4; ++i) p[i] = fast_exp2(x[i] - mref);
   lrun += (p[0] + p[1]) + (p[2] + p[3]);
   float r0, r1, r2, r3, d0, d1, d2, d3;
   const uint32_t hi01 = Mma<T>::pack(p[0], p[1], r0, r1);
@@ -223,15 +229,36 @@ paged_decode_mma_kernel(const DecodeArgs a, const __grid_constant__ PoolMaps map
   TraceMarks tm{};
   trace_mark(tm, 0);
   const int g = blockIdx.x;
-  // shared-prefix schedule: the first grid rows are the sibling groups' CTAs
-  if constexpr (G == kPrefixRows) {
-    if (a.prefix_tokens && int(blockIdx.y) < a.prefix_slots) {
-      prefix_cta<T, D, G, NW, STAGES>(a, maps, smem, int(blockIdx.y));
+  // Shared-prefix schedule: the plan's chunks take the first grid rows
+  // (longest first), the sequences outside any group the next ones; the last
+  // rows (room for S chunks and S sequences, fewer used) have nothing to do.
+  // Without a prefix plan of this batch the first S rows take every sequence
+  // whole.
+  int s;
+  if (a.prefix_header) {
+    const int4 ph = __ldg(a.prefix_header);
+    const bool planned = ph.x == kPlanMagicPrefix && ph.y == a.num_seqs;
+    const int nchunks = planned ? min(max(ph.z, 0), a.prefix_slots) : 0;
+    const int nothers = planned ? min(max(ph.w, 0), a.num_seqs) : a.num_seqs;
+    if (!planned && threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) flag(a.status, PKV_DEV_BAD_PLAN);
+    if constexpr (G == kPrefixRows) {
+      if (int(blockIdx.y) < nchunks) {
+        prefix_cta<T, D, G, NW, STAGES>(a, maps, smem, int(blockIdx.y));
+        return;
+      }
+    }
+    const int r = int(blockIdx.y) - nchunks;
+    if (r >= nothers) return;
+    s = planned ? __ldg(a.prefix_others + r) : r;
+    if (s < 0 || s >= a.num_seqs) {
+      if (threadIdx.x == 0 && blockIdx.x == 0) flag(a.status, PKV_DEV_BAD_PLAN);
       return;
     }
+  } else {
+    if (int(blockIdx.y) >= a.num_seqs) return;
+    s = long_first_seq<NW>(a, int(blockIdx.y));
   }
-  const int yrow = int(blockIdx.y) - (a.prefix_tokens ? a.prefix_slots : 0);
-  const int s = long_first_seq<NW>(a, yrow), part = blockIdx.z;
+  const int part = blockIdx.z;
   trace_mark(tm, 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int hq0 = g * a.group;
@@ -241,7 +268,7 @@ paged_decode_mma_kernel(const DecodeArgs a, const __grid_constant__ PoolMaps map
   // not depend on the length: read them together with it (entries past the
   // sequence are never used).
   int ids_early = 0;
-  if (a.window == 0 && !a.prefix_tokens) {
+  if (a.window == 0 && !a.prefix_header) {
     const int j0 = (blockIdx.z * a.part_tokens) / kBlock + warp + lane * NW;
     if (j0 < a.max_blocks_per_seq) ids_early = __ldg(a.block_tables + size_t(s) * a.max_blocks_per_seq + j0);
   }
@@ -251,30 +278,10 @@ paged_decode_mma_kernel(const DecodeArgs a, const __grid_constant__ PoolMaps map
     if (threadIdx.x == 0 && part == 0 && g == 0) flag(a.status, PKV_DEV_BAD_CONTEXT_LEN);
     L = L < 0 ? 0 : max_len;
   }
-  TokenRange tr = token_range(L, a.window);
-  int nparts = L == 0 ? 1 : (L - tr.aligned + a.part_tokens - 1) / a.part_tokens;
+  const TokenRange tr = token_range(L, a.window);
+  const int nparts = L == 0 ? 1 : (L - tr.aligned + a.part_tokens - 1) / a.part_tokens;
   if (part >= nparts) return;
-  int pslot = part;  // partition slot of this CTA's partial in the workspace
-  if (a.prefix_tokens) {
-    // Shared-prefix schedule: the first prefix_tokens[s] tokens (whole blocks)
-    // are shared with sibling sequences and done by the prefix kernel, whose
-    // partial takes slot 0; this CTA takes the rest (one pass) as slot 1.
-    // Without a prefix plan of this batch every CTA takes its whole sequence.
-    const int4 ph = __ldg(a.prefix_header);
-    const bool planned = ph.x == kPlanMagicPrefix && ph.y == a.num_seqs;
-    if (!planned && threadIdx.x == 0 && blockIdx.x == 0 && yrow == 0) flag(a.status, PKV_DEV_BAD_PLAN);
-    int ft = planned ? __ldg(a.prefix_tokens + s) : 0;
-    if (ft < 0 || ft > max_len || (ft & (kBlock - 1))) {
-      flag(a.status, PKV_DEV_BAD_PLAN);
-      ft = 0;
-    }
-    if (ft > 0) {
-      if (L <= ft) return;  // no own tokens: the prefix kernel writes this sequence
-      tr.first = tr.aligned = ft;
-      nparts = 2;
-      pslot = 1;
-    }
-  }
+  const int pslot = part;  // partition slot of this CTA's partial in the workspace
   trace_mark(tm, 2);
   if (L == 0) {
     T* o = static_cast<T*>(a.out) + (size_t(s) * a.num_q_heads + hq0) * D;
@@ -323,7 +330,7 @@ paged_decode_mma_kernel(const DecodeArgs a, const __grid_constant__ PoolMaps map
   };
   int ids = 0;
   if (lane < n_my) {
-    ids = (a.window == 0 && !a.prefix_tokens) ? ids_early : __ldg(trow + warp + lane * NW);
+    ids = (a.window == 0 && !a.prefix_header) ? ids_early : __ldg(trow + warp + lane * NW);
     if (ids < 0 || ids >= a.num_blocks) {
       flag(a.status, PKV_DEV_BAD_BLOCK_ID);
       ids = 0;

@@ -11,55 +11,136 @@
 // only its work is arranged so that each shared tile is read once:
 //
 //  * The step's plan (prefix_plan_kernel) finds groups of consecutive
-//    sequences whose tables start with the same physical blocks, and for each
-//    member the number of shared tokens (whole blocks, at most every member's
-//    length rounded down to a block).
-//  * One CTA per (KV head, group) (prefix_cta, run by the first CTA rows of
-//    the tensor-core grid kernel): the members' query rows
-//    of the KV head (members x query heads per KV head, at most 8) form the M
-//    rows of the tensor-core tile (mma_tile), so each shared K/V tile is
-//    copied into shared memory once and multiplied with every sibling's
-//    queries. Its result per row is a partial (max, sum, unnormalised V sum)
-//    over the shared tokens, in workspace slot 0 of that row.
-//  * The grid's other CTAs take each member's remaining tokens (slot 1); the
-//    last of the two to finish (an arrival counter per sequence and KV head)
-//    merges them by log-sum-exp. A member without tokens of its own gets its
-//    output straight from its group's CTA. The group CTAs come first in the
-//    grid (they are the long ones), so the members' short CTAs fill the GPU
-//    around them.
+//    sequences whose tables start with the same physical blocks (P shared
+//    whole blocks), and splits each group's work into 1..kPrefixMaxParts
+//    chunks -- ranges of block indices -- when the batch has too few groups
+//    to fill the GPU.
+//  * One CTA per (KV head, chunk) (prefix_cta, run by the first CTA rows of
+//    the tensor-core grid kernel): the members' query rows of the KV head
+//    (members x query heads per KV head, at most 8) form the M rows of the
+//    tensor-core tile (mma_tile), so each shared K/V tile is copied into
+//    shared memory once and multiplied with every sibling's queries; the
+//    members' own tiles in the chunk follow, each masked out of the other
+//    members' rows. A group of one chunk writes its outputs directly; the
+//    chunks of a split group leave partials that the last to finish merges
+//    by log-sum-exp. The chunk CTAs come first in the grid, longest first;
+//    the grid's later rows take the sequences outside any group.
 #pragma once
 
 #include "decode_mma.cuh"
 
 namespace pkv {
 
-// One CTA of the shared-prefix schedule: the group of blockIdx.y (a slot of
-// the plan's group list; past the list, nothing), KV head blockIdx.x. Called
-// by the tensor-core grid kernel, whose CTAs past the group slots take the
-// members' own tokens; `smem` is that kernel's 1024-byte-aligned shared
-// memory (rings of NW warps x STAGES stages).
+// One CTA of the shared-prefix schedule: chunk ci of a valid prefix plan, KV
+// head blockIdx.x. Called by the tensor-core grid kernel; `smem` is that
+// kernel's 1024-byte-aligned shared memory (rings of NW warps x STAGES
+// stages).
+//
+// The chunk covers block indices [jb, je) of its group: the shared blocks
+// among them (read through the first member's table) and each member's own
+// blocks among them (read through its own table). A warp takes a run of the
+// shared blocks, then each member's own blocks j = warp (mod NW) in order. A
+// member's row attends to the shared tiles and to its own; other members'
+// tiles are masked out of it (they change nothing in that row). Siblings of
+// one group with equal lengths and contents therefore get bit-identical
+// outputs.
 template <typename T, int D, int G, int NW, int STAGES>
-__device__ __forceinline__ void prefix_cta(const DecodeArgs& a, const PoolMaps& maps, unsigned char* smem, int gi) {
+__device__ __forceinline__ void prefix_cta(const DecodeArgs& a, const PoolMaps& maps, unsigned char* smem, int ci) {
   using C = MmaCfg<T, D, NW, STAGES>;
   static_assert(G == kPrefixRows, "a group's rows fill the tile's G rows");
-  constexpr int CHUNKS = D / 8;
 
   const int g = blockIdx.x;
-  const int4 hdr = __ldg(a.prefix_header);
-  if (hdr.x != kPlanMagicPrefix || hdr.y != a.num_seqs) {  // no plan: the sequences' CTAs do everything
-    if (threadIdx.x == 0 && g == 0 && gi == 0) flag(a.status, PKV_DEV_BAD_PLAN);
-    return;
-  }
-  if (gi >= hdr.z) return;
-  const int4 grp = __ldg(a.prefix_groups + gi);
-  const int s0 = grp.x, members = grp.y, P = grp.z;
+  const int4 ch = __ldg(a.prefix_chunks + ci);
+  const int gi = ch.x, part = ch.y, jb = ch.z, je = ch.w;
+  const int max_groups = a.num_seqs / 2 > 0 ? a.num_seqs / 2 : 1;
+  int4 grp = make_int4(-1, 0, 0, 0);
+  if (gi >= 0 && gi < max_groups) grp = __ldg(a.prefix_groups + gi);
+  const int s0 = grp.x, members = grp.y, P = grp.z, parts = grp.w;
   const int rows = members * a.group;
-  if (s0 < 0 || members < 2 || s0 + members > a.num_seqs || rows > G || P < 1 || P > a.max_blocks_per_seq) {
+  if (gi < 0 || gi >= max_groups || s0 < 0 || members < 2 || s0 + members > a.num_seqs || rows > G ||
+      P < kPrefixMinBlocks || P > a.max_blocks_per_seq || parts < 1 || parts > kPrefixMaxParts || part < 0 ||
+      part >= parts || jb < 0 || je < jb || je > a.max_blocks_per_seq) {
     if (threadIdx.x == 0 && g == 0) flag(a.status, PKV_DEV_BAD_PLAN);
     return;
   }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gr = lane >> 2, t = lane & 3;  // MMA row and column pair of this lane
+  const int max_len = a.max_blocks_per_seq * kBlock;
+
+  // Members' lengths, and this warp's tiles: sh_n shared ones, then own[m] of
+  // each member m. A member's own blocks j go to warp j mod NW (the same for
+  // every member, so equal siblings see equal tiles in equal warps); the
+  // shared blocks of the chunk are cut into NW consecutive runs that even out
+  // the warps' totals (water-filling over the own counts).
+  auto count_below = [&](int x, int w) { return x > w ? (x - w + NW - 1) / NW : 0; };  // j < x, j = w (mod NW)
+  int len[kPrefixRows], own[kPrefixRows], own_w[NW];
+#pragma unroll
+  for (int w = 0; w < NW; ++w) own_w[w] = 0;
+  const int sh_end = min(je, P), own_lo = max(jb, P);
+  const int sh_total = jb < sh_end ? sh_end - jb : 0;
+#pragma unroll
+  for (int m = 0; m < kPrefixRows; ++m) {
+    int L = m < members ? __ldg(a.context_lens + s0 + m) : 0;
+    L = L < 0 ? 0 : (L > max_len ? max_len : L);
+    if (m < members && L < P * kBlock) {  // the plan promised P whole blocks of every member
+      if (threadIdx.x == 0 && g == 0) flag(a.status, PKV_DEV_BAD_PLAN);
+      L = P * kBlock;
+    }
+    len[m] = L;
+    const int hi = min(je, (L + kBlock - 1) / kBlock);
+    own[m] = 0;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+      const int c = (m < members && own_lo < hi) ? count_below(hi, w) - count_below(own_lo, w) : 0;
+      own_w[w] += c;
+      if (w == warp) own[m] = c;
+    }
+  }
+  // the smallest level L with sum_w max(0, L - own_w) >= sh_total; warps
+  // below L - 1 fill up to it, the first few at L - 1 take the remainder
+  int lo = 0, hi = sh_total;
+#pragma unroll
+  for (int w = 0; w < NW; ++w) hi = max(hi, own_w[w] + sh_total);
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    int fill = 0;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) fill += max(0, mid - own_w[w]);
+    if (fill >= sh_total) hi = mid; else lo = mid + 1;
+  }
+  int sh_n = 0, sh_first = jb, rest = sh_total;
+#pragma unroll
+  for (int w = 0; w < NW; ++w) rest -= max(0, lo - 1 - own_w[w]);
+#pragma unroll
+  for (int w = 0; w < NW; ++w) {
+    int n = max(0, lo - 1 - own_w[w]);
+    if (rest > 0 && own_w[w] <= lo - 1) {
+      ++n;
+      --rest;
+    }
+    if (w < warp) sh_first += n;
+    if (w == warp) sh_n = n;
+  }
+  int n_my = sh_n;
+#pragma unroll
+  for (int m = 0; m < kPrefixRows; ++m) n_my += own[m];
+  const int j_own = own_lo + ((warp - own_lo) % NW + NW) % NW;  // the first own block j >= own_lo of this warp
+  // Tile k of this warp: (member, block) -- member -1 for a shared tile.
+  auto locate = [&](int k, int& m, int& j) {
+    m = -1;
+    j = sh_first + k;
+    if (k < sh_n) return;
+    int r = k - sh_n;
+#pragma unroll
+    for (int mm = 0; mm < kPrefixRows; ++mm) {
+      if (m < 0 && r < own[mm]) {
+        m = mm;
+        j = j_own + r * NW;
+      }
+      if (m < 0) r -= own[mm];
+    }
+  };
+  auto tile_rows = [&](int m, int j) -> int { return m < 0 ? kBlock : min(kBlock, len[m] - j * kBlock); };
 
   unsigned char* ring = smem + size_t(warp) * STAGES * C::STAGE_BYTES;
   const uint32_t ring_s = smem_addr(ring);
@@ -73,10 +154,11 @@ __device__ __forceinline__ void prefix_cta(const DecodeArgs& a, const PoolMaps& 
 
   // The A operand: row r is query head g * group + r % group of member r / group.
   uint32_t qa[C::KSTEPS][2];
+  const int my_member = gr / a.group;
   {
-    const int m = gr / a.group, h = g * a.group + gr % a.group;
+    const int h = g * a.group + gr % a.group;
     const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
-        static_cast<const T*>(a.q) + (size_t(s0 + (gr < rows ? m : 0)) * a.num_q_heads + h) * D);
+        static_cast<const T*>(a.q) + (size_t(s0 + (gr < rows ? my_member : 0)) * a.num_q_heads + h) * D);
 #pragma unroll
     for (int ks = 0; ks < C::KSTEPS; ++ks) {
       qa[ks][0] = gr < rows ? __ldg(qrow + 8 * ks + t) : 0u;
@@ -84,14 +166,13 @@ __device__ __forceinline__ void prefix_cta(const DecodeArgs& a, const PoolMaps& 
     }
   }
 
-  // Tiles j = warp, warp + NW, ... of the shared blocks, read through the
-  // first member's table (every member's table holds the same ids there).
-  const int n_my = P > warp ? (P - warp + NW - 1) / NW : 0;
-  const int32_t* trow = a.block_tables + size_t(s0) * a.max_blocks_per_seq;
+  // lane l of a batch holds the block id of this warp's tile k = batch * 32 + l
   auto load_ids = [&](int batch) -> int {
     const int k = batch * 32 + lane;
     if (k >= n_my) return 0;
-    int id = __ldg(trow + warp + k * NW);
+    int m, j;
+    locate(k, m, j);
+    int id = __ldg(a.block_tables + size_t(s0 + (m < 0 ? 0 : m)) * a.max_blocks_per_seq + j);
     if (id < 0 || id >= a.num_blocks) {
       flag(a.status, PKV_DEV_BAD_BLOCK_ID);
       id = 0;
@@ -101,7 +182,7 @@ __device__ __forceinline__ void prefix_cta(const DecodeArgs& a, const PoolMaps& 
   int ids = load_ids(0);
   int ids_next = n_my > 32 ? load_ids(1) : 0;
   int id_batch = 0;
-  auto issue = [&](int k) {  // warp-uniform; k increases by one per call; every tile is full
+  auto issue = [&](int k) {  // warp-uniform; k increases by one per call
     if ((k >> 5) != id_batch) {
       ids = ids_next;
       ++id_batch;
@@ -109,15 +190,34 @@ __device__ __forceinline__ void prefix_cta(const DecodeArgs& a, const PoolMaps& 
     }
     const int id = __shfl_sync(kFull, ids, k & 31);
     if (lane == 0) {
+      int m, j;
+      locate(k, m, j);
+      const int cover = min(kBlock, (tile_rows(m, j) + 3) & ~3);  // rows copied, a multiple of 4
       const int st = k % STAGES;
       const uint32_t bar = bar_s + 8 * st;
       const uint32_t dst = ring_s + st * C::STAGE_BYTES;
       const int y = (id * a.num_kv_heads + g) * kBlock;
-      mbar_arrive_expect_tx(bar, C::STAGE_BYTES);
+      mbar_arrive_expect_tx(bar, uint32_t(cover) * (C::STAGE_BYTES / kBlock));
+      if (cover == kBlock) {
 #pragma unroll
-      for (int j = 0; j < C::BOXES; ++j) {
-        tma_load_2d(dst + j * C::BOX_BYTES, &maps.k[0], 64 * j, y, bar);
-        tma_load_2d(dst + C::TILE_BYTES + j * C::BOX_BYTES, &maps.v[0], 64 * j, y, bar);
+        for (int jb2 = 0; jb2 < C::BOXES; ++jb2) {
+          tma_load_2d(dst + jb2 * C::BOX_BYTES, &maps.k[0], 64 * jb2, y, bar);
+          tma_load_2d(dst + C::TILE_BYTES + jb2 * C::BOX_BYTES, &maps.v[0], 64 * jb2, y, bar);
+        }
+      } else {
+#pragma unroll
+        for (int jb2 = 0; jb2 < C::BOXES; ++jb2) {
+          const uint32_t o = jb2 * C::BOX_BYTES;
+          if (cover & 8) {
+            tma_load_2d(dst + o, &maps.k[1], 64 * jb2, y, bar);
+            tma_load_2d(dst + C::TILE_BYTES + o, &maps.v[1], 64 * jb2, y, bar);
+          }
+          if (cover & 4) {
+            const int r0 = cover & 8;
+            tma_load_2d(dst + o + r0 * 128, &maps.k[2], 64 * jb2, y + r0, bar);
+            tma_load_2d(dst + C::TILE_BYTES + o + r0 * 128, &maps.v[2], 64 * jb2, y + r0, bar);
+          }
+        }
       }
     }
   };
@@ -137,15 +237,27 @@ __device__ __forceinline__ void prefix_cta(const DecodeArgs& a, const PoolMaps& 
       for (int kk = k; kk < last; ++kk) mbar_wait_bounded(bar_s + 8 * (kk % STAGES), (kk / STAGES) & 1);
       break;
     }
+    int m, j;
+    locate(k, m, j);
+    const int valid = tile_rows(m, j);
+    const bool row_on = m < 0 || my_member == m;
     const uint32_t kt = ring_s + st * C::STAGE_BYTES;
-    mma_tile<T, D, NW, STAGES, false>(kt, kt + C::TILE_BYTES, 0, kBlock, qa, o, mrun, lrun, a.scale_log2, lane);
+    if (valid == kBlock) {
+      mma_tile<T, D, NW, STAGES, false>(kt, kt + C::TILE_BYTES, 0, kBlock, qa, o, mrun, lrun, a.scale_log2, lane,
+                                        row_on);
+    } else {
+      zero_rows_outside<D>(kt + C::TILE_BYTES, 0, valid, lane);
+      mma_tile<T, D, NW, STAGES, true>(kt, kt + C::TILE_BYTES, 0, valid, qa, o, mrun, lrun, a.scale_log2, lane,
+                                       row_on);
+    }
     __syncwarp();
     if (k + STAGES < n_my) issue(k + STAGES);
   }
   lrun += __shfl_xor_sync(kFull, lrun, 1);
   lrun += __shfl_xor_sync(kFull, lrun, 2);
 
-  // Publish (acc[G][D], m[G], l[G]) in this warp's ring, as the grid kernels do.
+  // Publish (acc[G][D], m[G], l[G]) in this warp's ring, as the grid kernels
+  // do, and merge the warps: a row's (M, den, num = unnormalised output).
   float* wsm = reinterpret_cast<float*>(ring);
 #pragma unroll
   for (int nd = 0; nd < C::NTILES; ++nd)
@@ -155,14 +267,10 @@ __device__ __forceinline__ void prefix_cta(const DecodeArgs& a, const PoolMaps& 
     wsm[G * D + G + gr] = lrun;
   }
   __syncthreads();
-
-  // Merge the warps; each row's result is its member's output (no own
-  // tokens) or the member's partial in slot 0.
-  const int max_len = a.max_blocks_per_seq * kBlock;
+  constexpr int CHUNKS = D / 8;
   const size_t area = size_t(STAGES) * C::STAGE_BYTES;
   for (int it = threadIdx.x; it < rows * CHUNKS; it += NW * 32) {
     const int r = it / CHUNKS, c8 = it % CHUNKS;
-    const int s = s0 + r / a.group, hq = g * a.group + r % a.group;
     float M = -INFINITY;
 #pragma unroll
     for (int w = 0; w < NW; ++w) M = fmaxf(M, reinterpret_cast<const float*>(smem + size_t(w) * area)[G * D + r]);
@@ -187,54 +295,46 @@ __device__ __forceinline__ void prefix_cta(const DecodeArgs& a, const PoolMaps& 
       num[6] = fmaf(wt, x1.z, num[6]);
       num[7] = fmaf(wt, x1.w, num[7]);
     }
-    int L = __ldg(a.context_lens + s);
-    L = L < 0 ? 0 : (L > max_len ? max_len : L);
-    const size_t row = size_t(s) * a.num_q_heads + hq;
-    if (L <= P * kBlock) {  // the shared tokens are all of this member's tokens
+    const size_t row = size_t(s0 + r / a.group) * a.num_q_heads + g * a.group + r % a.group;
+    if (parts == 1) {  // every row has seen its shared tiles: den > 0
       const float inv = 1.f / den;
 #pragma unroll
       for (int c = 0; c < 8; ++c) num[c] *= inv;
       reinterpret_cast<uint4*>(static_cast<T*>(a.out) + row * D)[c8] = Vec8<T>::from_float(num);
-    } else {
-      float4* dst = reinterpret_cast<float4*>(a.part_o + (row * a.max_parts + 0) * D + c8 * 8);
+    } else {  // a row without tiles in this chunk leaves M = -inf, which the merge skips
+      float4* dst = reinterpret_cast<float4*>(a.part_o + (row * kPrefixMaxParts + part) * D + c8 * 8);
       dst[0] = make_float4(num[0], num[1], num[2], num[3]);
       dst[1] = make_float4(num[4], num[5], num[6], num[7]);
-      if (c8 == 0) a.part_ml[row * a.max_parts + 0] = make_float2(M, den);
+      if (c8 == 0) a.part_ml[row * kPrefixMaxParts + part] = make_float2(M, den);
     }
   }
+  if (parts == 1) return;
 
-  // One arrival per member with tokens of its own; the last of the two
-  // partitions of a (sequence, KV head) merges them.
-  __shared__ int last_m[kPrefixRows];
+  // The last chunk of the group to finish (for this KV head) merges the parts.
+  __shared__ unsigned int prefix_last;
   __threadfence();
   __syncthreads();
-  if (threadIdx.x < members) {
-    const int s = s0 + threadIdx.x;
-    int L = __ldg(a.context_lens + s);
-    L = L < 0 ? 0 : (L > max_len ? max_len : L);
-    last_m[threadIdx.x] = 0;
-    if (L > P * kBlock)
-      last_m[threadIdx.x] = atomicAdd(a.counters + size_t(s) * a.num_kv_heads + g, 1u) == 1u ? 1 : 0;
-  }
+  unsigned int* counter = a.counters + size_t(s0) * a.num_kv_heads + g;
+  if (threadIdx.x == 0) prefix_last = atomicAdd(counter, 1u) == unsigned(parts - 1) ? 1u : 0u;
   __syncthreads();
+  if (!prefix_last) return;
   __threadfence();
   for (int it = threadIdx.x; it < rows * CHUNKS; it += NW * 32) {
     const int r = it / CHUNKS, c8 = it % CHUNKS;
-    if (!last_m[r / a.group]) continue;
-    const int s = s0 + r / a.group, hq = g * a.group + r % a.group;
-    const size_t row = size_t(s) * a.num_q_heads + hq;
-    const float2* ml = a.part_ml + row * a.max_parts;
-    const float* po = a.part_o + row * a.max_parts * D + c8 * 8;
+    const size_t row = size_t(s0 + r / a.group) * a.num_q_heads + g * a.group + r % a.group;
+    const float2* ml = a.part_ml + row * kPrefixMaxParts;
+    const float* po = a.part_o + row * kPrefixMaxParts * D + c8 * 8;
     float M = -INFINITY;
-    for (int q = 0; q < 2; ++q) M = fmaxf(M, __ldcg(&ml[q].x));
+    for (int p = 0; p < parts; ++p) M = fmaxf(M, __ldcg(&ml[p].x));
     float den = 0.f, num[8];
 #pragma unroll
     for (int c = 0; c < 8; ++c) num[c] = 0.f;
-    for (int q = 0; q < 2; ++q) {
-      const float2 x = __ldcg(ml + q);
+    for (int p = 0; p < parts; ++p) {
+      const float2 x = __ldcg(ml + p);
+      if (x.x == -INFINITY) continue;  // no tile of this row in that chunk
       const float w = fast_exp2(x.x - M);
       den = fmaf(w, x.y, den);
-      const float4* src = reinterpret_cast<const float4*>(po + size_t(q) * D);
+      const float4* src = reinterpret_cast<const float4*>(po + size_t(p) * D);
       const float4 x0 = __ldcg(src), x1 = __ldcg(src + 1);
       num[0] = fmaf(w, x0.x, num[0]);
       num[1] = fmaf(w, x0.y, num[1]);
@@ -250,9 +350,7 @@ __device__ __forceinline__ void prefix_cta(const DecodeArgs& a, const PoolMaps& 
     for (int c = 0; c < 8; ++c) num[c] *= inv;
     reinterpret_cast<uint4*>(static_cast<T*>(a.out) + row * D)[c8] = Vec8<T>::from_float(num);
   }
-  __syncthreads();
-  if (threadIdx.x < members && last_m[threadIdx.x])
-    a.counters[size_t(s0 + threadIdx.x) * a.num_kv_heads + g] = 0u;  // ready for the next call
+  if (threadIdx.x == 0) *counter = 0u;  // leave the workspace ready for the next call
 }
 
 }  // namespace pkv

@@ -39,12 +39,15 @@ cudaError_t launch_seq_order(const int32_t* lens, int num_seqs, int max_len, int
                              int4* plan, cudaStream_t stream);
 
 // The prefix plan of the shared-prefix schedule (decode_prefix.cuh): header,
-// groups int4[num_seqs / 2], shared tokens int32[num_seqs], and the merge
-// counters [num_seqs][num_kv_heads] zeroed. num_seqs <= 1024, tables of at
-// most 256 blocks; groups of at most max_members sequences.
+// groups int4[num_seqs / 2], chunks int4[num_seqs], the sequences outside any
+// group int32[num_seqs], and the merge counters [num_seqs][num_kv_heads]
+// zeroed. num_seqs <= 1024, tables of at most 256 blocks; groups of at most
+// max_members sequences; slots = CTAs the decode grid holds at once.
 cudaError_t launch_prefix_plan(const int32_t* lens, const int32_t* tables, int num_seqs, int max_blocks,
-                               int num_kv_heads, int max_members, int4* header, int4* groups, int32_t* prefix_tokens,
-                               unsigned int* counters, cudaStream_t stream);
+                               int num_kv_heads, int slots, int max_members, int4* header, int4* groups, int4* chunks,
+                               int32_t* others, unsigned int* counters, cudaStream_t stream);
+// CTAs of the shared-prefix decode grid (head_dim 64/128/256) resident at once on the current device.
+cudaError_t prefix_resident_ctas(int head_dim, int* ctas);
 // One warp that waits on an mbarrier no copy completes (bounded-wait self-test).
 cudaError_t launch_bounded_wait_selftest(unsigned long long limit_ns, unsigned int* status, cudaStream_t stream);
 cudaError_t launch_trace_stamp(unsigned long long* dst, cudaStream_t stream);

@@ -74,7 +74,7 @@ def test_workspace_and_partition_choice():
     # prefix plan (header, groups int4[S / 2], shared tokens int32[S])
     assert B.resolved_partition(128, 72, 72, 128, 80, B.SHARED_PREFIX) == B.SHARED_PREFIX
     assert B.workspace_size(128, 72, 72, 128, 80, B.SHARED_PREFIX) == \
-        _split_bytes(128, 72, 72, 128, 2) + 16 + 64 * 16 + 512
+        _split_bytes(128, 72, 72, 128, 4) + 16 + 64 * 16 + 128 * 16 + 512   # partials of 4 chunks, the plan
     assert B.resolved_partition(128, 64, 8, 128, 80, B.SHARED_PREFIX) == 0     # 8 query heads per KV head
     assert B.resolved_partition(1, 8, 8, 128, 80, B.SHARED_PREFIX) == 0        # one sequence
     assert B.resolved_partition(8, 8, 8, 128, 257, B.SHARED_PREFIX) == 0       # tables wider than 256 blocks

@@ -89,16 +89,23 @@ def test_full_size_beam_search_sampled():
     q = W.normal_values((len(st.beam_ids), trace.num_q_heads, d), "bf16", 3, "cuda")
     case = H.DecodeCase(q, kp, vp, torch.from_numpy(tables).cuda(), torch.from_numpy(lens).cuda(),
                         trace.scale, "bf16")
-    out = case.new_out()
-    B.paged_attention_decode(out, q, kp, vp, case.tables, case.lens, case.scale)
-    torch.cuda.synchronize()
     rng = np.random.default_rng(4)
-    pairs = sorted({(int(s), int(h)) for s, h in zip(rng.integers(0, len(st.beam_ids), 16),
-                                                      rng.integers(0, trace.num_q_heads, 16))})
+    S = len(st.beam_ids)
+    pairs = sorted({(int(s), int(h)) for s, h in zip(rng.integers(0, S, 16), rng.integers(0, trace.num_q_heads, 16))}
+                   | {(s, int(h)) for s, h in zip(range(S), rng.integers(0, trace.num_q_heads, S))})
     want = H.oracle_sampled(case, pairs)
-    got = H.to_f64(out)
-    for (s, h), w in want.items():
-        H.assert_attention_close(got[s, h], w, f"beam {s} head {h}")
+    # the default schedule, and the shared-prefix schedule (beams of a prompt
+    # grouped; few groups, so each group's work is split over several CTAs)
+    outs = []
+    for partition in (0, B.SHARED_PREFIX):
+        out = case.new_out()
+        B.paged_attention_decode(out, q, kp, vp, case.tables, case.lens, case.scale, partition_size=partition)
+        torch.cuda.synchronize()
+        got = H.to_f64(out)
+        for (s, h), w in want.items():
+            H.assert_attention_close(got[s, h], w, f"partition {partition}: beam {s} head {h}")
+        outs.append(got)
+    H.assert_attention_close(outs[1], outs[0], "shared prefix against the default schedule")
     # beams share most of their blocks: far fewer unique blocks than table entries
     used = tables[tables >= 0]
     assert np.unique(used).size < 0.5 * used.size

@@ -214,9 +214,10 @@ def test_cow_siblings_bit_identical_over_shared_prefix():
     q = W.normal_values((1, hkv, d), "f16", 14, "cuda").expand(n, hkv, d).contiguous()
     shared = H.DecodeCase(q, kp, vp, torch.from_numpy(tables).cuda(),
                           torch.full((n,), prompt, dtype=torch.int32, device="cuda"), d ** -0.5, "f16")
-    out = _run(shared)
-    for s in range(1, n):
-        assert torch.equal(out[s], out[0])
+    for partition in (0, B.SHARED_PREFIX):   # the default schedule and the shared-prefix one
+        out = _run(shared, partition)
+        for s in range(1, n):
+            assert torch.equal(out[s], out[0]), f"partition {partition}: sibling {s}"
     grown = H.DecodeCase(q, kp, vp, torch.from_numpy(tables).cuda(), torch.from_numpy(lens).cuda(),
                          d ** -0.5, "f16")
     H.assert_attention_close(H.to_f64(_run(grown)), H.oracle_full(grown), "siblings after append")
@@ -518,10 +519,50 @@ def _sampling_case(num_prompts, n, prompt_range, tail_range, hq, hkv, d, dtype, 
 
 
 def _prefix_layout(S, hq, hkv, d):
-    split = (S * hq * 2 * (d * 4 + 8) + S * hkv * 4 + 15) // 16 * 16
+    # partials of up to 4 chunks a group (fp32 acc[d], (max, sum)) and one
+    # counter per (sequence, KV head), then the prefix plan: header int4,
+    # groups int4[S / 2], chunks int4[S], the other sequences int32[S]
+    split = (S * hq * 4 * (4 * d + 8) + 4 * S * hkv + 15) // 16 * 16
     groups = split + 16
-    tokens = groups + max(S // 2, 1) * 16
-    return dict(header=split, groups=groups, tokens=tokens, total=tokens + (4 * S + 15) // 16 * 16)
+    chunks = groups + max(S // 2, 1) * 16
+    others = chunks + 16 * S
+    return dict(header=split, groups=groups, chunks=chunks, others=others, total=others + (4 * S + 15) // 16 * 16)
+
+
+def _read_prefix_plan(ws, lay, S):
+    """(header, groups, chunks, others) of a prefix plan in the workspace."""
+    hdr = ws[lay["header"]:lay["header"] + 16].view(torch.int32).cpu().tolist()
+    ng = max(S // 2, 1)
+    groups = ws[lay["groups"]:lay["groups"] + 16 * ng].view(torch.int32).reshape(ng, 4).cpu().tolist()
+    chunks = ws[lay["chunks"]:lay["chunks"] + 16 * S].view(torch.int32).reshape(S, 4).cpu().tolist()
+    others = ws[lay["others"]:lay["others"] + 4 * S].view(torch.int32).cpu().tolist()
+    chunks = chunks[:max(hdr[2], 0)]
+    ngroups = max((c[0] for c in chunks), default=-1) + 1   # every group has a chunk
+    return hdr, groups[:ngroups], chunks, others[:max(hdr[3], 0)]
+
+
+def _check_chunks(groups, chunks, nchunks, tiles):
+    """Every group's parts 0..parts-1 appear once, as consecutive block ranges
+    from 0 to the group's last block, and chunks come in non-increasing work."""
+    assert nchunks == sum(g[3] for g in groups)
+    assert len(chunks) == nchunks
+    seen = {}
+    for gi, q, jb, je in chunks:
+        seen.setdefault(gi, {})[q] = (jb, je)
+    assert sorted(seen) == list(range(len(groups)))
+    for gi, (s0, m, P, parts) in enumerate(groups):
+        assert 1 <= parts <= 4 and sorted(seen[gi]) == list(range(parts))
+        maxn = max(tiles[s0 + k] for k in range(m))
+        edges = [seen[gi][q] for q in range(parts)]
+        assert edges[0][0] == 0 and edges[-1][1] == maxn
+        assert all(edges[q][1] == edges[q + 1][0] for q in range(parts - 1))
+
+    def work(gi, jb, je):
+        s0, m, P, _ = groups[gi]
+        return max(0, min(je, P) - jb) + sum(max(0, min(je, tiles[s0 + k]) - max(jb, P)) for k in range(m))
+    # groups ranked by ceil(work / parts); a group's chunks together
+    ranked = [-(-work(gi, 0, 10 ** 9) // groups[gi][3]) for gi, q, _, _ in chunks if q == 0]
+    assert ranked == sorted(ranked, reverse=True)
 
 
 @pytest.mark.parametrize("n,hq,hkv,d,dtype", [(4, 8, 8, 128, "f16"), (3, 16, 8, 64, "bf16"),
@@ -536,26 +577,26 @@ def test_shared_prefix_schedule_matches_the_oracle(n, hq, hkv, d, dtype):
     B.paged_attention_plan(case.lens, case.tables, hq, hkv, d, B.SHARED_PREFIX, workspace=ws)
     torch.cuda.synchronize()
     # the plan: each prompt's samples are consecutive sequences; groups of at
-    # most 8 / (query heads per KV head) members share the prompt's full blocks
+    # most 8 / (query heads per KV head) members share the prompt's full
+    # blocks (batch order); the rest are the other sequences
     max_members = 8 // (hq // hkv)
-    hdr = ws[lay["header"]:lay["header"] + 16].view(torch.int32).cpu().tolist()
-    want_groups = []
+    hdr, groups, chunks, others = _read_prefix_plan(ws, lay, S)
+    tiles = [-(-L // 16) for L in case.lens.cpu().tolist()]
+    want_groups, grouped = [], set()
     for i, P in enumerate(trace.prompt_lens.tolist()):
         if P // 16 < 4:
             continue
         for g0 in range(0, n, max_members):
             m = min(max_members, n - g0)
             if m >= 2:
-                want_groups.append([i * n + g0, m, P // 16, 0])
-    assert hdr == [PREFIX_MAGIC, S, len(want_groups), 0]
-    groups = ws[lay["groups"]:lay["groups"] + 16 * len(want_groups)].view(torch.int32).cpu().tolist()
-    assert [groups[4 * k:4 * k + 4] for k in range(len(want_groups))] == want_groups
-    tokens = ws[lay["tokens"]:lay["tokens"] + 4 * S].view(torch.int32).cpu().tolist()
-    want_tokens = [0] * S
-    for s0, m, P, _ in want_groups:
-        for k in range(m):
-            want_tokens[s0 + k] = 16 * P
-    assert tokens == want_tokens
+                want_groups.append([i * n + g0, m, P // 16])
+                grouped.update(range(i * n + g0, i * n + g0 + m))
+    assert hdr[0] == PREFIX_MAGIC and hdr[1] == S
+    assert [g[:3] for g in groups] == want_groups
+    assert others == [s for s in range(S) if s not in grouped] and hdr[3] == len(others)
+    _check_chunks(groups, chunks, hdr[2], tiles)
+    # a grid this small (under one wave) splits its groups into chunks
+    assert any(g[3] > 1 for g in groups)
     # two layers with the one plan, then an unplanned call: identical bits, the oracle's values
     outs = []
     for _ in range(2):
@@ -570,8 +611,9 @@ def test_shared_prefix_schedule_matches_the_oracle(n, hq, hkv, d, dtype):
 
 
 def test_shared_prefix_siblings_with_one_query_are_bit_identical():
-    # samples whose own tokens are empty take their output straight from the
-    # prefix kernel; with one query for all of them the outputs agree bit for bit
+    # siblings of one group with equal lengths see the same tiles in the same
+    # warps (the others' own tiles are masked out of a row exactly), so with
+    # one query for all of them the outputs agree bit for bit
     case, trace = _sampling_case(3, 4, (200, 400), (0, 0), 8, 8, 128, "f16", seed=5)
     q1 = case.q[0:1].expand_as(case.q).contiguous()
     same = H.DecodeCase(q1, case.k_pool, case.v_pool, case.tables, case.lens, case.scale, "f16")
@@ -581,6 +623,7 @@ def test_shared_prefix_siblings_with_one_query_are_bit_identical():
         for c in range(1, n):
             assert torch.equal(out[i * n + c], out[i * n])
     H.assert_attention_close(H.to_f64(out), H.oracle_full(same), "siblings without own tokens")
+    assert B.device_status(clear=True) == 0
 
 
 def test_shared_prefix_without_sharing_is_one_pass_per_sequence():

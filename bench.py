@@ -71,6 +71,8 @@ NOMINAL_HBM_GBS = 8000.0
 L2_FLUSH_BYTES = 512 << 20
 KERNEL_SOURCES = ["paged_kv_cache_217_gb300/csrc/decode.cuh",
                   "paged_kv_cache_217_gb300/csrc/decode_mma.cuh",
+                  "paged_kv_cache_217_gb300/csrc/decode_prefix.cuh",
+                  "paged_kv_cache_217_gb300/csrc/cache_ops.cu",
                   "paged_kv_cache_217_gb300/csrc/decode_sk.cuh",
                   "paged_kv_cache_217_gb300/csrc/device_common.cuh",
                   "paged_kv_cache_217_gb300/csrc/decode_launch.cuh",
@@ -94,7 +96,7 @@ def kernel_sha():
     return h.hexdigest()[:16]
 
 
-def build_workload(name, seed, device, kv="native", window=0):
+def build_workload(name, seed, device, kv="native", window=0, max_seqs=0):
     import torch
     from paged_kv_cache_217_gb300 import binding as B
     from paged_kv_cache_217_gb300 import workloads as W
@@ -150,11 +152,13 @@ def build_workload(name, seed, device, kv="native", window=0):
         shape = W.CONFIGS[name](seed)
         hq, hkv, d, dtype = shape.num_q_heads, shape.num_kv_heads, shape.head_dim, shape.dtype
         lens = shape.context_lens
+        if max_seqs > 0:   # profiling a smaller case of the same layer
+            lens = lens[:max_seqs]
         nb = W.pool_size(lens, shape.pool_factor)
         tables, mb = W.scattered_tables(lens, nb, seed)
         k_pool = W.normal_values((nb, hkv, 16, d), dtype, seed * 11 + 1, device)
         v_pool = W.normal_values((nb, hkv, 16, d), dtype, seed * 11 + 2, device)
-        wl.description = shape.name
+        wl.description = shape.name + (f" (first {lens.size} sequences)" if max_seqs > 0 else "")
         scale = shape.scale
         wl.unique_kv_bytes = None
     S = lens.shape[0]
@@ -660,7 +664,7 @@ def run_ours(args):
 
     if args.window > 0 and args.kv != "native":
         raise SystemExit("--window runs on the native cache only")
-    wl = build_workload(args.workload, args.seed, device, args.kv, args.window)
+    wl = build_workload(args.workload, args.seed, device, args.kv, args.window, args.max_seqs)
     wl.partition = (args.partition if args.partition is not None
                     else default_partition(args.workload, args.kv, args.window, B))
     device_inputs(wl, device)
@@ -870,6 +874,9 @@ def main(argv=None):
                     help="decode schedule: 0 = library choice, -1 = one CTA per (sequence, KV head), -2 = "
                          "balanced, -5 = shared prefix, N = split-K partitions of N tokens (default: -5 for the "
                          "sampling and beam batches, else 0)")
+    ap.add_argument("--max-seqs", type=int, default=0,
+                    help="profiling only: the first N sequences of a fixed-shape layer's batch (a smaller case "
+                         "of the same kernel for ncu captures; not a benchmark configuration)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-config", action="store_true",
                     help="skip timing the decode call of the other target layers (per_config)")

@@ -236,7 +236,7 @@ def plan(wl, B):
 def decode(wl, B):
     if wl.kv == "int8":
         B.paged_attention_decode_int8(wl.out, wl.q, wl.k_cache, wl.v_cache, wl.k_scale, wl.v_scale, wl.tables,
-                                      wl.lens, wl.scale, partition_size=wl.partition)
+                                      wl.lens, wl.scale, partition_size=wl.partition, planned=wl.planned)
     elif wl.window > 0:
         B.paged_attention_decode_sliding(wl.out, wl.q, wl.k_pool, wl.v_pool, wl.tables, wl.lens, wl.scale,
                                          wl.window, partition_size=wl.partition)
@@ -548,24 +548,24 @@ SHARED_PREFIX_WORKLOADS = ("opt66b_sampling", "llama13b_beam")
 
 
 def default_partition(name, kv, window, B):
-    return B.SHARED_PREFIX if name in SHARED_PREFIX_WORKLOADS and kv == "native" and window == 0 else 0
+    return B.SHARED_PREFIX if name in SHARED_PREFIX_WORKLOADS and window == 0 else 0
 
 
 def launches_per_step(wl, B):
     """This library's kernels in one step: the cache write, the decode (its
     split-K merge runs inside it), and the one-CTA kernel that orders the
-    batch -- the step's launch plan (native cache, full attention; batches of
-    2..1024 sequences in grids of at most 4096 CTAs), or, for the INT8 cache
-    and sliding windows, the ordering that the decode call itself launches for
-    batches of 128..1024 sequences (see pkv_paged_attention_decode). Sets
-    wl.planned."""
+    batch -- the step's launch plan (full attention, either cache; batches of
+    2..1024 sequences in grids of at most 4096 CTAs; the prefix plan of the
+    shared-prefix schedule), or, for sliding windows, the ordering that the
+    decode call itself launches for batches of 128..1024 sequences (see
+    pkv_paged_attention_decode). Sets wl.planned."""
     part = B.resolved_partition(wl.num_seqs, wl.hq, wl.hkv, wl.d, wl.tables_h.shape[1], wl.partition)
     if part == B.SHARED_PREFIX:   # the prefix plan, made once per step
-        wl.planned = True
+        wl.planned = wl.window == 0
         return part, 3
     parts = 1 if part in (-1, B.BALANCED) else -(-wl.tables_h.shape[1] * 16 // part)
     fits = part != B.BALANCED and wl.num_seqs <= 1024 and wl.num_seqs * wl.hkv * parts <= 4096
-    wl.planned = wl.kv == "native" and wl.window == 0 and fits and wl.num_seqs >= 2
+    wl.planned = wl.window == 0 and fits and wl.num_seqs >= 2
     ordered = wl.planned or (fits and wl.num_seqs >= 128)
     return part, 2 + (1 if ordered else 0)
 

@@ -435,13 +435,31 @@ pkv_status_t pkv_reshape_and_cache_int8(
  * Decode over the INT8 cache: pkv_paged_attention_decode with every K row
  * read as c_K * s_K and every V row as c_V * s_V. q and out are T = dtype.
  * Same block tables, lengths, GQA rule, partition_size values (except -2,
- * the balanced schedule, and -5, the shared-prefix schedule, which return
- * PKV_ERR_UNSUPPORTED), workspace
+ * the balanced schedule, which returns PKV_ERR_UNSUPPORTED; -5, the
+ * shared-prefix schedule, runs as described there), workspace
  * (pkv_paged_attention_workspace_size with the same arguments) and error
  * behaviour. Internally the scores are q . c_K scaled by s_K, and s_V is
- * folded into each softmax weight.
+ * folded into each softmax weight (with a power of two per warp that keeps
+ * the weights inside the fp16 range).
  */
 pkv_status_t pkv_paged_attention_decode_int8(
+    void* out, const void* q, const int8_t* k_cache, const int8_t* v_cache,
+    const float* k_scale, const float* v_scale, const int32_t* block_tables,
+    const int32_t* context_lens, int num_seqs, int num_q_heads, int num_kv_heads,
+    int head_dim, int max_blocks_per_seq, int num_blocks, float scale,
+    pkv_dtype_t dtype, int partition_size, void* workspace,
+    size_t workspace_bytes, pkv_stream_t stream);
+
+/*
+ * pkv_paged_attention_decode_int8 with the launch plan that
+ * pkv_paged_attention_plan left in `workspace` for the same sizes (the plan
+ * does not depend on the cache's element type): same arguments, semantics
+ * and results; the decision of when each sequence starts (and, for -5, the
+ * sibling groups) is read from the plan instead of made in the call. A
+ * workspace without a plan of this batch flags PKV_DEV_BAD_PLAN and runs
+ * every sequence in natural order, still computing every output.
+ */
+pkv_status_t pkv_paged_attention_decode_int8_planned(
     void* out, const void* q, const int8_t* k_cache, const int8_t* v_cache,
     const float* k_scale, const float* v_scale, const int32_t* block_tables,
     const int32_t* context_lens, int num_seqs, int num_q_heads, int num_kv_heads,

@@ -70,6 +70,8 @@ _SIGS = {
     "pkv_reshape_and_cache_int8": ([_c_p, _c_p, _c_int] + [_c_p] * 5 + [_c_int] * 4 + [_c_p], _c_int),
     "pkv_paged_attention_decode_int8": ([_c_p] * 8 + [_c_int] * 6 + [_c_f, _c_int, _c_int, _c_p, _c_sz, _c_p],
                                         _c_int),
+    "pkv_paged_attention_decode_int8_planned": ([_c_p] * 8 + [_c_int] * 6 + [_c_f, _c_int, _c_int, _c_p, _c_sz,
+                                                                            _c_p], _c_int),
     "pkv_copy_blocks_int8": ([_c_p] * 5 + [_c_int] * 4 + [_c_p], _c_int),
     "pkv_selftest_bounded_wait": ([ctypes.c_uint32, _c_p], _c_int),
     "pkv_trace_enabled": ([], _c_int),
@@ -385,8 +387,10 @@ def reshape_and_cache_int8(k, v, k_cache, v_cache, k_scale, v_scale, slot_mappin
 
 
 def paged_attention_decode_int8(out, q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens, scale,
-                                partition_size=0, workspace=None):
-    """paged_attention_decode over the INT8 cache (K = c_K * s_K, V = c_V * s_V per row)."""
+                                partition_size=0, workspace=None, planned=False):
+    """paged_attention_decode over the INT8 cache (K = c_K * s_K, V = c_V * s_V per row). ``planned``
+    runs pkv_paged_attention_decode_int8_planned with the plan paged_attention_plan left in the same
+    workspace."""
     import torch
     _need_cuda(out, q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens)
     dt = _dtype_code(q)
@@ -406,7 +410,8 @@ def paged_attention_decode_int8(out, q, k_cache, v_cache, k_scale, v_scale, bloc
     if need:
         ws = workspace if workspace is not None else _workspace(q.device, need)
         ws_ptr, ws_bytes = ws.data_ptr(), ws.numel() * ws.element_size()
-    _launch(q.device, "paged_attention_decode_int8", lib().pkv_paged_attention_decode_int8,
+    fn = lib().pkv_paged_attention_decode_int8_planned if planned else lib().pkv_paged_attention_decode_int8
+    _launch(q.device, "paged_attention_decode_int8_planned" if planned else "paged_attention_decode_int8", fn,
             out.data_ptr(), q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), k_scale.data_ptr(),
             v_scale.data_ptr(), block_tables.data_ptr(), context_lens.data_ptr(), S, Hq, hkv, D, mb, nb,
             float(scale), dt, int(partition_size), ws_ptr, ws_bytes)

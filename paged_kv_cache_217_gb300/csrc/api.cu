@@ -664,13 +664,14 @@ size_t pkv_paged_attention_sliding_workspace_size(int num_seqs, int num_q_heads,
                                             window_blocks(max_blocks_per_seq, sliding_window), partition_size);
 }
 
-pkv_status_t pkv_paged_attention_decode_int8(void* out, const void* q, const int8_t* k_cache,
-                                             const int8_t* v_cache, const float* k_scale, const float* v_scale,
-                                             const int32_t* block_tables, const int32_t* context_lens,
-                                             int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
-                                             int max_blocks_per_seq, int num_blocks, float scale,
-                                             pkv_dtype_t dtype, int partition_size, void* workspace,
-                                             size_t workspace_bytes, pkv_stream_t stream) {
+namespace {
+
+pkv_status_t decode_int8_impl(void* out, const void* q, const int8_t* k_cache, const int8_t* v_cache,
+                              const float* k_scale, const float* v_scale, const int32_t* block_tables,
+                              const int32_t* context_lens, int num_seqs, int num_q_heads, int num_kv_heads,
+                              int head_dim, int max_blocks_per_seq, int num_blocks, float scale, pkv_dtype_t dtype,
+                              int partition_size, void* workspace, size_t workspace_bytes, bool planned,
+                              cudaStream_t stream) {
   if (num_seqs < 0) return pkv::fail(PKV_ERR_INVALID_ARG, "num_seqs < 0");
   if (num_seqs == 0) return pkv::ok();
   if (num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0)
@@ -693,15 +694,24 @@ pkv_status_t pkv_paged_attention_decode_int8(void* out, const void* q, const int
     return pkv::fail(PKV_ERR_INVALID_ARG, "block_tables and context_lens must be 4-byte aligned");
   const int p = choose_partition(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, partition_size);
   if (p == kBalanced) return pkv::fail(PKV_ERR_UNSUPPORTED, "the INT8 cache has no balanced schedule");
-  if (p == kSharedPrefix) return pkv::fail(PKV_ERR_UNSUPPORTED, "the INT8 cache has no shared-prefix schedule");
+  const bool shared_prefix = p == kSharedPrefix;
+  if (shared_prefix && !prefix_fits(num_seqs, num_q_heads, num_kv_heads, max_blocks_per_seq))
+    return pkv::fail(PKV_ERR_UNSUPPORTED,
+                     "the shared-prefix schedule takes 2..%d sequences, at most 4 query heads per KV head and "
+                     "tables of at most %d blocks",
+                     pkv::kOrderMaxSeqs, pkv::kPrefixMaxBlocks);
+  if (shared_prefix && !pkv::decode_int8_uses_tensor_maps())
+    return pkv::fail(PKV_ERR_UNSUPPORTED, "the shared-prefix schedule needs the tensor-core INT8 tile");
   Plan plan;
   pkv_status_t st = plan_decode(max_blocks_per_seq, p, &plan);
   if (st != PKV_OK) return st;
   if (int64_t(num_blocks) * num_kv_heads * PKV_BLOCK_SIZE > INT32_MAX)
     return pkv::fail(PKV_ERR_UNSUPPORTED, "num_blocks * num_kv_heads * 16 exceeds 2^31 rows");
   const SplitLayout lay = split_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, plan.max_parts);
-  const size_t ord = plan_bytes(num_seqs, num_kv_heads, plan.max_parts);
-  const size_t need = lay.total + ord;
+  const size_t ord = shared_prefix ? 0 : plan_bytes(num_seqs, num_kv_heads, plan.max_parts);
+  const SplitLayout pre_split = split_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, pkv::kPrefixMaxParts);
+  const PrefixLayout pre = prefix_layout(pre_split.total, num_seqs);
+  const size_t need = shared_prefix ? pre.total : lay.total + ord;
   if (need > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, 16)))
     return pkv::fail(PKV_ERR_WORKSPACE, "workspace of %zu bytes (16-byte aligned) required, got %zu at %p",
                      need, workspace_bytes, workspace);
@@ -722,11 +732,14 @@ pkv_status_t pkv_paged_attention_decode_int8(void* out, const void* q, const int
   a.part_ml = lay.total > 0 ? reinterpret_cast<float2*>(static_cast<char*>(workspace) + lay.ml_offset) : nullptr;
   a.counters = lay.total > 0 ? reinterpret_cast<unsigned int*>(static_cast<char*>(workspace) + lay.counter_offset)
                              : nullptr;
-  int4* plan_hdr =
-      ord > 0 && num_seqs >= kOrderKernelMinSeqs ? reinterpret_cast<int4*>(static_cast<char*>(workspace) + lay.total)
-                                                 : nullptr;
-  a.order = plan_hdr ? reinterpret_cast<const int32_t*>(plan_hdr + 1) : nullptr;
-  a.plan = plan_hdr;
+  // The launch plan, as for the 16-bit cache: made here for batches of at
+  // least kOrderKernelMinSeqs sequences, read as the caller made it for a
+  // planned call, else ranked in every CTA.
+  int4* plan_hdr = ord > 0 ? reinterpret_cast<int4*>(static_cast<char*>(workspace) + lay.total) : nullptr;
+  const bool make_plan = plan_hdr && !planned && num_seqs >= kOrderKernelMinSeqs;
+  const bool use_plan = plan_hdr && (planned || make_plan);
+  a.order = use_plan ? reinterpret_cast<const int32_t*>(plan_hdr + 1) : nullptr;
+  a.plan = use_plan ? plan_hdr : nullptr;
   a.status = status;
   a.num_seqs = num_seqs;
   a.num_q_heads = num_q_heads;
@@ -747,16 +760,68 @@ pkv_status_t pkv_paged_attention_decode_int8(void* out, const void* q, const int
     if (st != PKV_OK) return st;
   }
   cudaError_t err = cudaSuccess;
-  if (lay.total > 0) {
-    err = cudaMemsetAsync(a.counters, 0, lay.counter_bytes, stream);
-    if (err != cudaSuccess) return cuda_status(err, "clear split-K counters");
+  int gpad = round_pow2_group(group);
+  if (shared_prefix) {
+    // The prefix plan (made here, or by pkv_paged_attention_plan for a planned
+    // call; its layout does not depend on the cache's element type).
+    char* ws = static_cast<char*>(workspace);
+    a.long_first = 0;
+    a.order = nullptr;
+    a.plan = nullptr;
+    a.part_o = reinterpret_cast<float*>(ws);
+    a.part_ml = reinterpret_cast<float2*>(ws + pre_split.ml_offset);
+    a.counters = reinterpret_cast<unsigned int*>(ws + pre_split.counter_offset);
+    a.prefix_header = reinterpret_cast<int4*>(ws + pre.header_offset);
+    a.prefix_groups = reinterpret_cast<int4*>(ws + pre.groups_offset);
+    a.prefix_chunks = reinterpret_cast<int4*>(ws + pre.chunks_offset);
+    a.prefix_others = reinterpret_cast<int32_t*>(ws + pre.others_offset);
+    a.prefix_slots = pre.max_chunks;
+    if (!planned) {
+      st = launch_prefix_plan_ws(context_lens, block_tables, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                 max_blocks_per_seq, ws, stream);
+      if (st != PKV_OK) return st;
+    }
+    gpad = pkv::kPrefixRows;
+  } else {
+    if (lay.total > 0) {
+      err = cudaMemsetAsync(a.counters, 0, lay.counter_bytes, stream);
+      if (err != cudaSuccess) return cuda_status(err, "clear split-K counters");
+    }
+    if (make_plan) {
+      err = pkv::launch_seq_order(context_lens, num_seqs, max_blocks_per_seq * PKV_BLOCK_SIZE, 0, true, plan_hdr,
+                                  stream);
+      if (err != cudaSuccess) return cuda_status(err, "launch plan");
+    }
   }
-  if (plan_hdr) {
-    err = pkv::launch_seq_order(context_lens, num_seqs, max_blocks_per_seq * PKV_BLOCK_SIZE, 0, true, plan_hdr, stream);
-    if (err != cudaSuccess) return cuda_status(err, "launch plan");
-  }
-  err = pkv::launch_decode_int8(a, dtype == PKV_BF16, head_dim, round_pow2_group(group), &kmap, &vmap, stream);
+  err = pkv::launch_decode_int8(a, dtype == PKV_BF16, head_dim, gpad, &kmap, &vmap, stream);
   return cuda_status(err, "paged_attention_decode_int8 launch");
+}
+
+}  // namespace
+
+pkv_status_t pkv_paged_attention_decode_int8(void* out, const void* q, const int8_t* k_cache,
+                                             const int8_t* v_cache, const float* k_scale, const float* v_scale,
+                                             const int32_t* block_tables, const int32_t* context_lens,
+                                             int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                             int max_blocks_per_seq, int num_blocks, float scale,
+                                             pkv_dtype_t dtype, int partition_size, void* workspace,
+                                             size_t workspace_bytes, pkv_stream_t stream) {
+  return decode_int8_impl(out, q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens, num_seqs,
+                          num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, num_blocks, scale, dtype,
+                          partition_size, workspace, workspace_bytes, false, static_cast<cudaStream_t>(stream));
+}
+
+pkv_status_t pkv_paged_attention_decode_int8_planned(void* out, const void* q, const int8_t* k_cache,
+                                                     const int8_t* v_cache, const float* k_scale,
+                                                     const float* v_scale, const int32_t* block_tables,
+                                                     const int32_t* context_lens, int num_seqs, int num_q_heads,
+                                                     int num_kv_heads, int head_dim, int max_blocks_per_seq,
+                                                     int num_blocks, float scale, pkv_dtype_t dtype,
+                                                     int partition_size, void* workspace, size_t workspace_bytes,
+                                                     pkv_stream_t stream) {
+  return decode_int8_impl(out, q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens, num_seqs,
+                          num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, num_blocks, scale, dtype,
+                          partition_size, workspace, workspace_bytes, true, static_cast<cudaStream_t>(stream));
 }
 
 pkv_status_t pkv_reshape_and_cache_int8(const void* k, const void* v, pkv_dtype_t dtype, int8_t* k_cache,

@@ -27,7 +27,9 @@ cudaError_t launch_int8_dg(const DecodeArgs& a, const CUtensorMap* kmap, const C
   constexpr int NW = (PKV_INT8_MMA && G >= 2) ? kInt8GqaWarps : kGridWarps;
   constexpr int STAGES = kInt8Stages;
   static bool configured[kMaxDevices] = {};
-  const dim3 grid(unsigned(a.num_kv_heads), unsigned(a.num_seqs), unsigned(a.max_parts));
+  // (the shared-prefix schedule: rows for its chunks, then the sequences, one pass)
+  const dim3 grid(unsigned(a.num_kv_heads), unsigned(a.num_seqs + (a.prefix_header ? a.prefix_slots : 0)),
+                  a.prefix_header ? 1u : unsigned(a.max_parts));
   cudaError_t err = cudaSuccess;
   if constexpr (PKV_INT8_MMA) {
     using C = I8Cfg<D, NW, STAGES>;

@@ -268,7 +268,7 @@ paged_decode_mma_kernel(const DecodeArgs a, const __grid_constant__ PoolMaps map
   // not depend on the length: read them together with it (entries past the
   // sequence are never used).
   int ids_early = 0;
-  if (a.window == 0 && !a.prefix_header) {
+  if (a.window == 0) {
     const int j0 = (blockIdx.z * a.part_tokens) / kBlock + warp + lane * NW;
     if (j0 < a.max_blocks_per_seq) ids_early = __ldg(a.block_tables + size_t(s) * a.max_blocks_per_seq + j0);
   }
@@ -330,7 +330,7 @@ paged_decode_mma_kernel(const DecodeArgs a, const __grid_constant__ PoolMaps map
   };
   int ids = 0;
   if (lane < n_my) {
-    ids = (a.window == 0 && !a.prefix_header) ? ids_early : __ldg(trow + warp + lane * NW);
+    ids = a.window == 0 ? ids_early : __ldg(trow + warp + lane * NW);
     if (ids < 0 || ids >= a.num_blocks) {
       flag(a.status, PKV_DEV_BAD_BLOCK_ID);
       ids = 0;

@@ -14,20 +14,26 @@
 //    max|q| to [2^13, 2^14), so bf16 queries are exact in fp16); the fp32
 //    scores are then multiplied by s_K of their token, the inverse power of
 //    two and scale * log2(e).
-//    The contraction runs over a permuted order of the head dims: k-slots
-//    2t, 2t+1, 2t+8, 2t+9 of a 16-dim chunk hold dims 4t .. 4t+3, so each
-//    K fragment is one 32-bit shared-memory word.
-//  * O += P . V~ with V~ = c_V * s_V rounded to fp16 (the exact code pair
-//    times the fp16 pair of scales), P rounded to fp16 once. Each
-//    lane loads one 32-bit word (4 dims) from each of its 4 token rows and
-//    regroups the bytes so that output column slot s of n-tile 4g + i holds
-//    head dim 32g + 4s + i; the epilogue undoes that permutation.
+//    The contraction runs over a permuted order of the head dims: lane t
+//    reads 16-byte chunks 2t, 2t+1 (and 2t+8, 2t+9 at D = 256; chunk t at
+//    D = 64) of its two token rows with one 16-byte load each, and word r of
+//    the q-th such chunk feeds k-slots 2t, 2t+1, 2t+8, 2t+9 of k-step 4q + r.
+//  * O += P~ . C_V with P~ = p * s_V * 2^e rounded to fp16 once and the V
+//    codes exact in fp16: the V scale of each token rides on its softmax
+//    weight. e is a per-warp power of two that keeps every P~ below 2^14
+//    (s_V below 2^(14 - e)): it only falls, when a tile brings a larger
+//    scale, and the accumulator is rescaled by the same exact power of two
+//    together with the softmax rescale. Each lane loads one 16-byte chunk
+//    (8 bytes at D = 64) from each of its 4 token rows; column slot c of
+//    n-tile j holds head dim 16c + j (8c + j at D = 64; n-tiles 16..31 at
+//    D = 256: 128 + 16c + j - 16), which the epilogue undoes.
 //  * K and V tiles arrive by TMA tensor copies of uint8 boxes (16 rows x
 //    min(D, 128) bytes) with the 128-byte swizzle (64-byte at D = 64), which
-//    keeps the word loads above free of bank conflicts; the 16 K and 16 V
-//    scales of the tile arrive by two 64-byte bulk copies.
-// Rounding V~ and P to fp16 each adds at most 2^-12 relative error per term,
-// far below the quantisation step of the codes.
+//    keeps the 16-byte loads above free of bank conflicts (2-way for the V
+//    loads at D = 64); the 16 K and 16 V scales of the tile arrive by two
+//    64-byte bulk copies.
+// Rounding P~ to fp16 adds at most 2^-11 relative error per term, far below
+// the quantisation step of the codes.
 #pragma once
 
 #include <cuda.h>
@@ -35,6 +41,7 @@
 
 #include "decode.cuh"
 #include "decode_mma.cuh"
+#include "decode_prefix.cuh"
 
 namespace pkv {
 
@@ -47,7 +54,6 @@ struct I8Cfg {
   static constexpr int STAGE_BYTES = 2 * TILE_BYTES;  // K tile then V tile
   static constexpr int SCALE_STAGE = 2 * kBlock * 4;  // 16 K scales then 16 V scales
   static constexpr int KCHUNKS = D / 16;              // QK k-steps
-  static constexpr int VGROUPS = D / 32;              // PV groups of 4 n-tiles
   static constexpr int NTILES = D / 8;
   static constexpr size_t RING_BYTES = size_t(NW) * STAGES * STAGE_BYTES;
   static constexpr size_t SCALE_BYTES = size_t(NW) * STAGES * SCALE_STAGE;
@@ -98,96 +104,317 @@ __device__ __forceinline__ void codes_to_f16x2(uint32_t w, uint32_t& lo, uint32_
   hi = hsub2_u32(__byte_perm(x, kF16Magic, 0x5342), kF16Bias);
 }
 
+// 16-byte chunk of a code row that lane t reads for its q-th QK load, and the
+// head dim that k-step c = 4q + r, word r, byte i of lane t stands for.
+template <int D>
+__device__ __forceinline__ int i8_k_chunk(int q, int t) {
+  return D == 64 ? t : 2 * t + (q & 1) + 8 * (q >> 1);
+}
+// Head dim of column slot c of PV n-tile j (the permutation the V loads make).
+template <int D>
+__host__ __device__ constexpr int i8_v_dim(int j, int c) {
+  return D == 64 ? 8 * c + j : 128 * (j / 16) + 16 * c + (j % 16);
+}
+
+// Running V-scale state of a warp: P~ = p * s_V * vmul with vmul = 2^(14 - E)
+// for every s_V seen below vbound = 2^E.
+struct VScale {
+  float vbound = 0x1p-100f;
+  float vmul = 0x1p114f;
+};
+
 template <int D, int NW, int STAGES, bool MASK>
 __device__ __forceinline__ void mma_tile_int8(uint32_t kt, uint32_t vt, uint32_t st_scale, int lo, int rows,
                                               const uint32_t (&qa)[D / 16][2], float (&o)[D / 8][4],
-                                              float& mrun, float& lrun, float qmul, int lane) {
+                                              float& mrun, float& lrun, VScale& vs, float qmul, int lane,
+                                              bool row_on = true) {
   using C = I8Cfg<D, NW, STAGES>;
   const int t = lane & 3, gr = lane >> 2;
 
   // S = Q~ . C_K^T: n-tile 0 = tokens 0..7 (this lane's token gr), n-tile 1 = tokens 8..15.
   float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-  for (int c = 0; c < C::KCHUNKS; ++c) {
-    const uint32_t w0 = lds32(kt + i8_swz<D>(gr, c) + 4 * t);
-    const uint32_t w1 = lds32(kt + i8_swz<D>(gr + 8, c) + 4 * t);
-    uint32_t b0, b1, b2, b3;
-    codes_to_f16x2(w0, b0, b1);
-    codes_to_f16x2(w1, b2, b3);
-    Mma<__half>::run(s0, qa[c][0], 0u, qa[c][1], 0u, b0, b1);
-    Mma<__half>::run(s1, qa[c][0], 0u, qa[c][1], 0u, b2, b3);
+  for (int q = 0; q < C::KCHUNKS / 4; ++q) {
+    const int ch = i8_k_chunk<D>(q, t);
+    const uint4 w0 = lds128(kt + i8_swz<D>(gr, ch));
+    const uint4 w1 = lds128(kt + i8_swz<D>(gr + 8, ch));
+    const uint32_t a0[4] = {w0.x, w0.y, w0.z, w0.w}, a1[4] = {w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      uint32_t b0, b1, b2, b3;
+      codes_to_f16x2(a0[r], b0, b1);
+      codes_to_f16x2(a1[r], b2, b3);
+      Mma<__half>::run(s0, qa[4 * q + r][0], 0u, qa[4 * q + r][1], 0u, b0, b1);
+      Mma<__half>::run(s1, qa[4 * q + r][0], 0u, qa[4 * q + r][1], 0u, b2, b3);
+    }
   }
 
   // Scores of head gr for tokens 2t, 2t+1, 8+2t, 9+2t, in the log2 domain.
   const float2 ka = lds_f32x2(st_scale + 8 * t);
   const float2 kb = lds_f32x2(st_scale + 32 + 8 * t);
   float x[4] = {s0[0] * ka.x * qmul, s0[1] * ka.y * qmul, s1[0] * kb.x * qmul, s1[1] * kb.y * qmul};
+  // V scales of the same tokens; rows outside [lo, rows) get 0 (their stale
+  // codes and scales then contribute exactly nothing).
+  const float2 va = lds_f32x2(st_scale + 64 + 8 * t);
+  const float2 vb = lds_f32x2(st_scale + 96 + 8 * t);
+  float sv[4] = {va.x, va.y, vb.x, vb.y};
   if (MASK) {
-    if (2 * t < lo || 2 * t >= rows) x[0] = -INFINITY;
-    if (2 * t + 1 < lo || 2 * t + 1 >= rows) x[1] = -INFINITY;
-    if (8 + 2 * t < lo || 8 + 2 * t >= rows) x[2] = -INFINITY;
-    if (9 + 2 * t < lo || 9 + 2 * t >= rows) x[3] = -INFINITY;
+    if (2 * t < lo || 2 * t >= rows) x[0] = -INFINITY, sv[0] = 0.f;
+    if (2 * t + 1 < lo || 2 * t + 1 >= rows) x[1] = -INFINITY, sv[1] = 0.f;
+    if (8 + 2 * t < lo || 8 + 2 * t >= rows) x[2] = -INFINITY, sv[2] = 0.f;
+    if (9 + 2 * t < lo || 9 + 2 * t >= rows) x[3] = -INFINITY, sv[3] = 0.f;
   }
+  if (!row_on) x[0] = x[1] = x[2] = x[3] = -INFINITY;  // this lane's row does not attend to this tile
   float mt = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
   mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 1));
   mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 2));
   const float mn = fmaxf(mrun, mt);
-  if (__any_sync(kFull, mn > mrun)) {
-    const float alpha = fast_exp2(mrun - mn);
+  const float mref = mn == -INFINITY ? 0.f : mn;  // a row with no valid score yet: weights exactly 0
+  // The tile's largest V scale (the 16 tokens are spread over t), warp-uniform.
+  float ms = fmaxf(fmaxf(sv[0], sv[1]), fmaxf(sv[2], sv[3]));
+  ms = fmaxf(ms, __shfl_xor_sync(kFull, ms, 1));
+  ms = fmaxf(ms, __shfl_xor_sync(kFull, ms, 2));
+  float vratio = 1.f;
+  const bool vgrow = ms >= vs.vbound;
+  if (vgrow) {  // ms in [2^(E-1), 2^E): vbound = 2^E, vmul = 2^(14 - E)
+    const int E = min(max(int((__float_as_uint(ms) >> 23) & 0xffu) - 126, -99), 113);
+    const float nmul = __uint_as_float(uint32_t(127 + 14 - E) << 23);
+    vratio = nmul / vs.vmul;  // a power of two: exact
+    vs.vmul = nmul;
+    vs.vbound = __uint_as_float(uint32_t(127 + E) << 23);
+  }
+  if (vgrow || __any_sync(kFull, mn > mrun)) {
+    const float alpha = fast_exp2(mrun - mref);  // 1 for rows whose max did not move
     lrun *= alpha;
+    const float oa = alpha * vratio;
 #pragma unroll
     for (int nd = 0; nd < C::NTILES; ++nd) {
-      o[nd][0] *= alpha;
-      o[nd][1] *= alpha;
+      o[nd][0] *= oa;
+      o[nd][1] *= oa;
     }
     mrun = mn;
   }
   float p[4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) p[i] = fast_exp2(x[i] - mn);
+  for (int i = 0; i < 4; ++i) p[i] = fast_exp2(x[i] - mref);
   lrun += (p[0] + p[1]) + (p[2] + p[3]);
-  const __half2 p01 = __floats2half2_rn(p[0], p[1]);
-  const __half2 p23 = __floats2half2_rn(p[2], p[3]);
+  const __half2 p01 = __floats2half2_rn(p[0] * (sv[0] * vs.vmul), p[1] * (sv[1] * vs.vmul));
+  const __half2 p23 = __floats2half2_rn(p[2] * (sv[2] * vs.vmul), p[3] * (sv[3] * vs.vmul));
   const uint32_t a01 = *reinterpret_cast<const uint32_t*>(&p01);
   const uint32_t a23 = *reinterpret_cast<const uint32_t*>(&p23);
 
-  // V scales of tokens (2t, 2t+1) and (2t+8, 2t+9) as fp16 pairs; rows outside
-  // [lo, rows) get scale 0 so their (stale) codes contribute exactly nothing.
-  const float2 va = lds_f32x2(st_scale + 64 + 8 * t);
-  const float2 vb = lds_f32x2(st_scale + 96 + 8 * t);
-  float sv[4] = {va.x, va.y, vb.x, vb.y};
-  if (MASK) {
-    if (2 * t < lo || 2 * t >= rows) sv[0] = 0.f;
-    if (2 * t + 1 < lo || 2 * t + 1 >= rows) sv[1] = 0.f;
-    if (8 + 2 * t < lo || 8 + 2 * t >= rows) sv[2] = 0.f;
-    if (9 + 2 * t < lo || 9 + 2 * t >= rows) sv[3] = 0.f;
-  }
-  const __half2 s01 = __floats2half2_rn(sv[0], sv[1]);
-  const __half2 s23 = __floats2half2_rn(sv[2], sv[3]);
-  const uint32_t sc01 = *reinterpret_cast<const uint32_t*>(&s01), sc23 = *reinterpret_cast<const uint32_t*>(&s23);
-
-  // O += P . V~ over groups of 32 dims: this lane reads dims 32g + 4gr .. +3 of
-  // tokens 2t, 2t+1, 8+2t, 9+2t and feeds n-tiles 4g .. 4g+3.
+  // O += P~ . C_V: this lane reads its 16-byte chunk (8 bytes at D = 64) of
+  // tokens 2t, 2t+1, 8+2t, 9+2t and feeds column gr of every n-tile.
+  constexpr int VW = D == 64 ? 8 : 16;        // bytes a lane takes from a row per load
+  constexpr int VLOADS = D == 256 ? 2 : 1;    // loads per row
 #pragma unroll
-  for (int g = 0; g < C::VGROUPS; ++g) {
-    const int ch = 2 * g + (gr >> 2);
-    const uint32_t off = 4 * (gr & 3);
-    const uint32_t wa = lds32(vt + i8_swz<D>(2 * t, ch) + off) ^ 0x80808080u;
-    const uint32_t wb = lds32(vt + i8_swz<D>(2 * t + 1, ch) + off) ^ 0x80808080u;
-    const uint32_t wc = lds32(vt + i8_swz<D>(2 * t + 8, ch) + off) ^ 0x80808080u;
-    const uint32_t wd = lds32(vt + i8_swz<D>(2 * t + 9, ch) + off) ^ 0x80808080u;
-    // Interleave the two tokens of each pair: [a_i, b_i, a_j, b_j].
-    const uint32_t ab01 = __byte_perm(wa, wb, 0x5140), ab23 = __byte_perm(wa, wb, 0x7362);
-    const uint32_t cd01 = __byte_perm(wc, wd, 0x5140), cd23 = __byte_perm(wc, wd, 0x7362);
+  for (int v = 0; v < VLOADS; ++v) {
+    uint32_t wa[VW / 4], wb[VW / 4], wc[VW / 4], wd[VW / 4];
+    if constexpr (D == 64) {
+      const uint32_t off = 8 * (gr & 1);
+      const uint2 xa = lds64(vt + i8_swz<D>(2 * t, gr >> 1) + off);
+      const uint2 xb = lds64(vt + i8_swz<D>(2 * t + 1, gr >> 1) + off);
+      const uint2 xc = lds64(vt + i8_swz<D>(2 * t + 8, gr >> 1) + off);
+      const uint2 xd = lds64(vt + i8_swz<D>(2 * t + 9, gr >> 1) + off);
+      wa[0] = xa.x, wa[1] = xa.y, wb[0] = xb.x, wb[1] = xb.y;
+      wc[0] = xc.x, wc[1] = xc.y, wd[0] = xd.x, wd[1] = xd.y;
+    } else {
+      const int ch = 8 * v + gr;
+      const uint4 xa = lds128(vt + i8_swz<D>(2 * t, ch));
+      const uint4 xb = lds128(vt + i8_swz<D>(2 * t + 1, ch));
+      const uint4 xc = lds128(vt + i8_swz<D>(2 * t + 8, ch));
+      const uint4 xd = lds128(vt + i8_swz<D>(2 * t + 9, ch));
+      wa[0] = xa.x, wa[1] = xa.y, wa[2] = xa.z, wa[3] = xa.w;
+      wb[0] = xb.x, wb[1] = xb.y, wb[2] = xb.z, wb[3] = xb.w;
+      wc[0] = xc.x, wc[1] = xc.y, wc[2] = xc.z, wc[3] = xc.w;
+      wd[0] = xd.x, wd[1] = xd.y, wd[2] = xd.z, wd[3] = xd.w;
+    }
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint32_t ab = i < 2 ? ab01 : ab23, cd = i < 2 ? cd01 : cd23;
-      const uint32_t sel = (i & 1) ? 0x5342 : 0x5140;
-      const uint32_t b0 = hmul2_u32(hsub2_u32(__byte_perm(ab, kF16Magic, sel), kF16Bias), sc01);
-      const uint32_t b1 = hmul2_u32(hsub2_u32(__byte_perm(cd, kF16Magic, sel), kF16Bias), sc23);
-      Mma<__half>::run(o[4 * g + i], a01, 0u, a23, 0u, b0, b1);
+    for (int w = 0; w < VW / 4; ++w) {
+      // Interleave the two tokens of each pair: [a_i, b_i, a_j, b_j].
+      const uint32_t xa = wa[w] ^ 0x80808080u, xb = wb[w] ^ 0x80808080u;
+      const uint32_t xc = wc[w] ^ 0x80808080u, xd = wd[w] ^ 0x80808080u;
+      const uint32_t ab01 = __byte_perm(xa, xb, 0x5140), ab23 = __byte_perm(xa, xb, 0x7362);
+      const uint32_t cd01 = __byte_perm(xc, xd, 0x5140), cd23 = __byte_perm(xc, xd, 0x7362);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t ab = i < 2 ? ab01 : ab23, cd = i < 2 ? cd01 : cd23;
+        const uint32_t sel = (i & 1) ? 0x5342 : 0x5140;
+        const uint32_t b0 = hsub2_u32(__byte_perm(ab, kF16Magic, sel), kF16Bias);
+        const uint32_t b1 = hsub2_u32(__byte_perm(cd, kF16Magic, sel), kF16Bias);
+        Mma<__half>::run(o[VW * v + 4 * w + i], a01, 0u, a23, 0u, b0, b1);
+      }
     }
   }
+}
+
+// Q~ of one query row as the A operand, dims permuted as the K loads are:
+// k-step c = 4q + r takes dims d, d+1 (qa[c][0]) and d+2, d+3 (qa[c][1]),
+// d = 16 * i8_k_chunk(q, t) + 4r; the row is scaled by a power of two that
+// brings max|q| to [2^13, 2^14) (exact for bf16 and fp16 queries), and
+// `qmul` = scale * log2(e) / that power. `qrow` null: a zero row.
+template <typename T, int D>
+__device__ __forceinline__ void i8_query(const T* qrow, int t, uint32_t (&qa)[D / 16][2], float& qmul,
+                                         float scale_log2) {
+  constexpr int KCHUNKS = D / 16;
+  float qf[KCHUNKS][4];
+  float m = 0.f;
+#pragma unroll
+  for (int c = 0; c < KCHUNKS; ++c) {
+    if (qrow) {
+      const int d0 = 16 * i8_k_chunk<D>(c / 4, t) + 4 * (c % 4);
+      const uint2 u = __ldg(reinterpret_cast<const uint2*>(qrow + d0));
+      const T* e = reinterpret_cast<const T*>(&u);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) qf[c][i] = float(e[i]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) qf[c][i] = 0.f;
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) m = fmaxf(m, fabsf(qf[c][i]));
+  }
+  m = fmaxf(m, __shfl_xor_sync(kFull, m, 1));
+  m = fmaxf(m, __shfl_xor_sync(kFull, m, 2));
+  // m < 2^E with E from m's exponent field (clamped for tiny or zero q);
+  // scale by 2^(14 - E).
+  const int E = max(int((__float_as_uint(m) >> 23) & 0xffu) - 126, -100);
+  const float up = __uint_as_float(uint32_t(127 + 14 - E) << 23);
+  qmul = scale_log2 * __uint_as_float(uint32_t(127 - 14 + E) << 23);
+#pragma unroll
+  for (int c = 0; c < KCHUNKS; ++c) {
+    const __half2 h0 = __floats2half2_rn(qf[c][0] * up, qf[c][1] * up);
+    const __half2 h1 = __floats2half2_rn(qf[c][2] * up, qf[c][3] * up);
+    qa[c][0] = *reinterpret_cast<const uint32_t*>(&h0);
+    qa[c][1] = *reinterpret_cast<const uint32_t*>(&h1);
+  }
+}
+
+// Publishes a warp's (acc[G][D], m[G], l[G]) at the start of its ring in
+// head-dim order, with the V-scale power of two taken out (exact).
+template <int D, int G>
+__device__ __forceinline__ void i8_publish(float* wsm, const float (&o)[D / 8][4], float mrun, float lrun,
+                                           const VScale& vs, int lane) {
+  const int t = lane & 3, gr = lane >> 2;
+  if (gr < G) {
+    const float unmul = 1.f / vs.vmul;
+#pragma unroll
+    for (int j = 0; j < D / 8; ++j) {
+      wsm[gr * D + i8_v_dim<D>(j, 2 * t)] = o[j][0] * unmul;
+      wsm[gr * D + i8_v_dim<D>(j, 2 * t + 1)] = o[j][1] * unmul;
+    }
+    if (t == 0) {
+      wsm[G * D + gr] = mrun;
+      wsm[G * D + G + gr] = lrun;
+    }
+  }
+}
+
+// One CTA of the shared-prefix schedule over the INT8 cache (the 16-bit
+// version, prefix_cta in decode_prefix.cuh, describes the chunk): the
+// members' query rows share each K/V code tile, copied once.
+template <typename T, int D, int G, int NW, int STAGES>
+__device__ __forceinline__ void prefix_cta_int8(const DecodeArgs& a, const CUtensorMap& kmap,
+                                                const CUtensorMap& vmap, unsigned char* smem, int ci) {
+  using C = I8Cfg<D, NW, STAGES>;
+  static_assert(G == kPrefixRows, "a group's rows fill the tile's G rows");
+  const int g = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gr = lane >> 2, t = lane & 3;
+  PrefixChunk<NW> c;
+  if (!c.init(a, ci, warp)) return;
+
+  unsigned char* ring = smem + size_t(warp) * STAGES * C::STAGE_BYTES;
+  const uint32_t ring_s = smem_addr(ring);
+  const uint32_t scale_s = smem_addr(smem + C::RING_BYTES) + warp * STAGES * C::SCALE_STAGE;
+  const uint32_t bar_s = smem_addr(smem + C::RING_BYTES + C::SCALE_BYTES) + warp * STAGES * 8;
+  if (lane == 0) {
+#pragma unroll
+    for (int st = 0; st < STAGES; ++st) mbar_init(bar_s + 8 * st, 1);
+    mbar_init_fence();
+  }
+  __syncwarp();
+
+  // Row r: query head g * group + r % group of member r / group.
+  const int my_member = gr / a.group;
+  uint32_t qa[C::KCHUNKS][2];
+  float qmul;
+  i8_query<T, D>(gr < c.rows ? static_cast<const T*>(a.q) +
+                                   (size_t(c.s0 + my_member) * a.num_q_heads + g * a.group + gr % a.group) * D
+                             : nullptr,
+                 t, qa, qmul, a.scale_log2);
+
+  const int n_my = c.n_my;
+  auto load_ids = [&](int batch) -> int {
+    const int k = batch * 32 + lane;
+    if (k >= n_my) return 0;
+    int m, j;
+    c.locate(k, m, j);
+    return c.block_id(a, m, j);
+  };
+  int ids = load_ids(0);
+  int ids_next = n_my > 32 ? load_ids(1) : 0;
+  int id_batch = 0;
+  auto issue = [&](int k) {  // warp-uniform; k increases by one per call
+    if ((k >> 5) != id_batch) {
+      ids = ids_next;
+      ++id_batch;
+      ids_next = (id_batch + 1) * 32 < n_my ? load_ids(id_batch + 1) : 0;
+    }
+    const int id = __shfl_sync(kFull, ids, k & 31);
+    if (lane == 0) {
+      const int st = k % STAGES;
+      const uint32_t bar = bar_s + 8 * st;
+      const uint32_t dst = ring_s + st * C::STAGE_BYTES;
+      const uint32_t sdst = scale_s + st * C::SCALE_STAGE;
+      const size_t row0 = (size_t(id) * a.num_kv_heads + g) * kBlock;
+      mbar_arrive_expect_tx(bar, C::STAGE_BYTES + C::SCALE_STAGE);
+#pragma unroll
+      for (int jb = 0; jb < C::BOXES; ++jb) {
+        tma_load_2d(dst + jb * C::BOX_BYTES, &kmap, C::BOX_COLS * jb, int(row0), bar);
+        tma_load_2d(dst + C::TILE_BYTES + jb * C::BOX_BYTES, &vmap, C::BOX_COLS * jb, int(row0), bar);
+      }
+      bulk_g2s(sdst, a.k_scale + row0, kBlock * 4, bar);
+      bulk_g2s(sdst + kBlock * 4, a.v_scale + row0, kBlock * 4, bar);
+    }
+  };
+
+  float o[C::NTILES][4];
+#pragma unroll
+  for (int nd = 0; nd < C::NTILES; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
+  float mrun = -INFINITY, lrun = 0.f;
+  VScale vs;
+  const int pre = n_my < STAGES ? n_my : STAGES;
+  for (int k = 0; k < pre; ++k) issue(k);
+  for (int k = 0; k < n_my; ++k) {
+    const int st = k % STAGES;
+    const bool ok = mbar_wait_bounded(bar_s + 8 * st, (k / STAGES) & 1);
+    if (!__all_sync(kFull, ok)) {
+      if (lane == 0) flag(a.status, PKV_DEV_WAIT_TIMEOUT);
+      const int last = min(n_my, k + STAGES);
+      for (int kk = k; kk < last; ++kk) mbar_wait_bounded(bar_s + 8 * (kk % STAGES), (kk / STAGES) & 1);
+      break;
+    }
+    int m, j;
+    c.locate(k, m, j);
+    const int valid = c.tile_rows(m, j);
+    const bool row_on = m < 0 || my_member == m;
+    const uint32_t kt = ring_s + st * C::STAGE_BYTES;
+    const uint32_t sc = scale_s + st * C::SCALE_STAGE;
+    if (valid == kBlock)
+      mma_tile_int8<D, NW, STAGES, false>(kt, kt + C::TILE_BYTES, sc, 0, kBlock, qa, o, mrun, lrun, vs, qmul,
+                                          lane, row_on);
+    else
+      mma_tile_int8<D, NW, STAGES, true>(kt, kt + C::TILE_BYTES, sc, 0, valid, qa, o, mrun, lrun, vs, qmul, lane,
+                                         row_on);
+    __syncwarp();
+    if (k + STAGES < n_my) issue(k + STAGES);
+  }
+  lrun += __shfl_xor_sync(kFull, lrun, 1);
+  lrun += __shfl_xor_sync(kFull, lrun, 2);
+  i8_publish<D, G>(reinterpret_cast<float*>(ring), o, mrun, lrun, vs, lane);
+  __syncthreads();
+  prefix_finish<T, D, G, NW>(a, c, smem, size_t(STAGES) * C::STAGE_BYTES);
 }
 
 template <typename T, int D, int G, int NW, int STAGES>
@@ -202,7 +429,32 @@ paged_decode_mma_int8_kernel(const DecodeArgs a, const __grid_constant__ CUtenso
 
   wait_for_predecessor();
   const int g = blockIdx.x;
-  const int s = long_first_seq<NW>(a, blockIdx.y), part = blockIdx.z;
+  // Shared-prefix schedule: the plan's chunks take the first grid rows, the
+  // sequences outside any group the next ones (as in the 16-bit kernel).
+  int s;
+  if (a.prefix_header) {
+    const int4 ph = __ldg(a.prefix_header);
+    const bool planned = ph.x == kPlanMagicPrefix && ph.y == a.num_seqs;
+    const int nchunks = planned ? min(max(ph.z, 0), a.prefix_slots) : 0;
+    const int nothers = planned ? min(max(ph.w, 0), a.num_seqs) : a.num_seqs;
+    if (!planned && threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) flag(a.status, PKV_DEV_BAD_PLAN);
+    if constexpr (G == kPrefixRows) {
+      if (int(blockIdx.y) < nchunks) {
+        prefix_cta_int8<T, D, G, NW, STAGES>(a, kmap, vmap, smem, int(blockIdx.y));
+        return;
+      }
+    }
+    const int r = int(blockIdx.y) - nchunks;
+    if (r >= nothers) return;
+    s = planned ? __ldg(a.prefix_others + r) : r;
+    if (s < 0 || s >= a.num_seqs) {
+      if (threadIdx.x == 0 && blockIdx.x == 0) flag(a.status, PKV_DEV_BAD_PLAN);
+      return;
+    }
+  } else {
+    s = long_first_seq<NW>(a, blockIdx.y);
+  }
+  const int part = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int hq0 = g * a.group;
   const int gr = lane >> 2, t = lane & 3;
@@ -243,43 +495,11 @@ paged_decode_mma_int8_kernel(const DecodeArgs a, const __grid_constant__ CUtenso
   }
   __syncwarp();
 
-  // Q~ of head hq0 + gr as the A operand, dims permuted per 16-dim chunk:
-  // qa[c][0] = (dims 16c + 4t, +1), qa[c][1] = (dims 16c + 4t + 2, +3).
+  // Q~ of head hq0 + gr as the A operand (rows past the group zero).
   uint32_t qa[C::KCHUNKS][2];
   float qmul;
-  {
-    float qf[C::KCHUNKS][4];
-    float m = 0.f;
-#pragma unroll
-    for (int c = 0; c < C::KCHUNKS; ++c) {
-      if (gr < a.group) {
-        const uint2 u = __ldg(reinterpret_cast<const uint2*>(
-            static_cast<const T*>(a.q) + (size_t(s) * a.num_q_heads + hq0 + gr) * D + 16 * c + 4 * t));
-        const T* e = reinterpret_cast<const T*>(&u);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) qf[c][i] = float(e[i]);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) qf[c][i] = 0.f;
-      }
-#pragma unroll
-      for (int i = 0; i < 4; ++i) m = fmaxf(m, fabsf(qf[c][i]));
-    }
-    m = fmaxf(m, __shfl_xor_sync(kFull, m, 1));
-    m = fmaxf(m, __shfl_xor_sync(kFull, m, 2));
-    // m < 2^E with E from m's exponent field (clamped for tiny or zero q);
-    // scale by 2^(14 - E).
-    const int E = max(int((__float_as_uint(m) >> 23) & 0xffu) - 126, -100);
-    const float up = __uint_as_float(uint32_t(127 + 14 - E) << 23);
-    qmul = a.scale_log2 * __uint_as_float(uint32_t(127 - 14 + E) << 23);
-#pragma unroll
-    for (int c = 0; c < C::KCHUNKS; ++c) {
-      const __half2 h0 = __floats2half2_rn(qf[c][0] * up, qf[c][1] * up);
-      const __half2 h1 = __floats2half2_rn(qf[c][2] * up, qf[c][3] * up);
-      qa[c][0] = *reinterpret_cast<const uint32_t*>(&h0);
-      qa[c][1] = *reinterpret_cast<const uint32_t*>(&h1);
-    }
-  }
+  i8_query<T, D>(gr < a.group ? static_cast<const T*>(a.q) + (size_t(s) * a.num_q_heads + hq0 + gr) * D : nullptr,
+                 t, qa, qmul, a.scale_log2);
 
   const int n_my = nb > warp ? (nb - warp + NW - 1) / NW : 0;
   const int32_t* trow = a.block_tables + size_t(s) * a.max_blocks_per_seq + t0 / kBlock;
@@ -332,6 +552,7 @@ paged_decode_mma_int8_kernel(const DecodeArgs a, const __grid_constant__ CUtenso
 #pragma unroll
   for (int nd = 0; nd < C::NTILES; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
   float mrun = -INFINITY, lrun = 0.f;
+  VScale vs;
 
   const int pre = n_my < STAGES ? n_my : STAGES;
   for (int k = 0; k < pre; ++k) issue(k);
@@ -352,9 +573,9 @@ paged_decode_mma_int8_kernel(const DecodeArgs a, const __grid_constant__ CUtenso
     const uint32_t kt = ring_s + st * C::STAGE_BYTES;
     const uint32_t sc = scale_s + st * C::SCALE_STAGE;
     if (rows == kBlock && lo == 0)
-      mma_tile_int8<D, NW, STAGES, false>(kt, kt + C::TILE_BYTES, sc, 0, rows, qa, o, mrun, lrun, qmul, lane);
+      mma_tile_int8<D, NW, STAGES, false>(kt, kt + C::TILE_BYTES, sc, 0, rows, qa, o, mrun, lrun, vs, qmul, lane);
     else
-      mma_tile_int8<D, NW, STAGES, true>(kt, kt + C::TILE_BYTES, sc, lo, rows, qa, o, mrun, lrun, qmul, lane);
+      mma_tile_int8<D, NW, STAGES, true>(kt, kt + C::TILE_BYTES, sc, lo, rows, qa, o, mrun, lrun, vs, qmul, lane);
     __syncwarp();
     if (k + STAGES < n_my) issue(k + STAGES);
   }
@@ -362,22 +583,7 @@ paged_decode_mma_int8_kernel(const DecodeArgs a, const __grid_constant__ CUtenso
   lrun += __shfl_xor_sync(kFull, lrun, 1);
   lrun += __shfl_xor_sync(kFull, lrun, 2);
 
-  // Publish (acc[G][D], m[G], l[G]); n-tile 4q + i, column slot c holds dim 32q + 4c + i.
-  float* wsm = reinterpret_cast<float*>(ring);
-  if (gr < G) {
-#pragma unroll
-    for (int q = 0; q < C::VGROUPS; ++q) {
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        wsm[gr * D + 32 * q + 4 * (2 * t) + i] = o[4 * q + i][0];
-        wsm[gr * D + 32 * q + 4 * (2 * t + 1) + i] = o[4 * q + i][1];
-      }
-    }
-    if (t == 0) {
-      wsm[G * D + gr] = mrun;
-      wsm[G * D + G + gr] = lrun;
-    }
-  }
+  i8_publish<D, G>(reinterpret_cast<float*>(ring), o, mrun, lrun, vs, lane);
   __syncthreads();
   finish_chunk<T, D, G, NW>(a, smem, size_t(STAGES) * C::STAGE_BYTES, s, g, part, nparts);
 }

@@ -219,6 +219,152 @@ def test_decode_int8_full_size_sampled(name):
     assert B.device_status(clear=True) == 0
 
 
+def test_decode_int8_large_v_rows_on_the_tensor_cores():
+    # V rows whose dequantised values exceed the fp16 range (possible for bf16
+    # inputs): the V scale rides on the softmax weight (with a power of two per
+    # warp), the codes stay exact in fp16, so nothing overflows
+    big = Int8Case([40, 300, 17], 4, 4, 128, "bf16", seed=91)
+    big.vc.fill_(100)
+    big.vs.mul_(65536.0)
+    want = big.oracle()
+    assert np.abs(want).max() > 65504.0
+    H.assert_attention_close(H.to_f64(big.run()), want, "int8 large V rows")
+    assert B.device_status(clear=True) == 0
+
+
+def test_decode_int8_v_scales_spanning_many_magnitudes():
+    # scales from 2^-30 to 2^20 in random blocks: the warps' power of two falls
+    # tile after tile and the accumulator is rescaled with it (bf16 outputs:
+    # values past the fp16 range stay finite)
+    case = Int8Case([700, 1200, 33, 16, 2000], 8, 2, 128, "bf16", seed=92)
+    rng = np.random.default_rng(5)
+    nb = case.vs.shape[0]
+    mags = torch.from_numpy(np.exp2(rng.integers(-30, 21, size=(nb, 1, 1))).astype(np.float32)).cuda()
+    case.vs.mul_(mags)
+    case.ks.mul_(torch.from_numpy(np.exp2(rng.integers(-3, 4, size=(nb, 1, 1))).astype(np.float32)).cuda())
+    want = case.oracle()
+    # Each weight enters the tensor cores as one fp16 value (11 significant
+    # bits), so an output element that is a near-cancelling sum of terms up to
+    # 2^27 carries an error of ~2^-11 of those terms, not of itself: the bound
+    # is taken against the largest output of its row (a lost rescale or an
+    # overflow would be off by the whole row).
+    row_max = np.abs(want).max(axis=-1, keepdims=True)
+    for p in (0, -1, 64):
+        got = H.to_f64(case.run(p))
+        assert np.all(np.isfinite(got)), p
+        assert np.all(np.abs(got - want) <= 2e-3 * row_max + 1e-2 * np.abs(want)), \
+            (p, float(np.max(np.abs(got - want) / row_max)))
+    assert B.device_status(clear=True) == 0
+
+
+def test_decode_int8_planned():
+    # the step's launch plan (made by paged_attention_plan, shared with the
+    # 16-bit cache) used by the planned INT8 entry point; a workspace holding
+    # no plan flags BAD_PLAN and still computes every output
+    rng = np.random.default_rng(8)
+    lens = np.clip(np.round(150 * np.exp(0.6 * rng.standard_normal(200))), 8, 1024).astype(np.int32)
+    case = Int8Case(lens, 32, 8, 128, "bf16", seed=93)
+    S, mb = case.q.shape[0], case.tables.shape[1]
+    ws = torch.zeros((B.workspace_size(S, 32, 8, 128, mb),), dtype=torch.uint8, device="cuda")
+    B.paged_attention_plan(case.lens, case.tables, 32, 8, 128, workspace=ws)
+    want = case.oracle()
+    for planned_ws in (ws, torch.zeros_like(ws)):
+        out = torch.full_like(case.q, float("nan"))
+        B.paged_attention_decode_int8(out, case.q, case.kc, case.vc, case.ks, case.vs, case.tables, case.lens,
+                                      case.scale, workspace=planned_ws, planned=True)
+        torch.cuda.synchronize()
+        H.assert_attention_close(H.to_f64(out), want, "planned int8")
+        assert B.device_status(clear=True) == (0 if planned_ws is ws else 0x20)
+
+
+# ---- the shared-prefix schedule over the INT8 cache ----------------------------------
+def _int8_sampling_case(num_prompts, n, prompt_range, tail_range, hq, hkv, d, dtype, seed):
+    """Tables of parallel samples from the block manager (prompt added, forked
+    n-1 times, tails appended with copy-on-write) over a random INT8 cache."""
+    trace = W.ParallelSamplingTrace("sampling", dtype, hq, hkv, d,
+                                    np.random.default_rng(seed).integers(*prompt_range, size=num_prompts,
+                                                                         endpoint=True).astype(np.int32),
+                                    np.random.default_rng(seed + 1).integers(*tail_range, size=(num_prompts, n),
+                                                                             endpoint=True).astype(np.int32))
+    nb = trace.block_budget()
+    bm = B.BlockManager(nb, W.shuffled_free_order(nb, seed))
+    plan = W.drive_parallel_sampling(trace, bm)
+    mb = max(-(-L // 16) for L in plan.final_lens.values())
+    tables, lens = bm.block_tables(plan.seq_ids, mb)
+    case = Int8Case.__new__(Int8Case)
+    case.kc, case.vc, case.ks, case.vs = _int8_cache(nb, hkv, d, seed)
+    case.q = W.normal_values((len(plan.seq_ids), hq, d), dtype, seed * 5 + 7, "cuda")
+    case.tables = torch.from_numpy(tables).cuda()
+    case.lens = torch.from_numpy(lens).cuda()
+    case.scale = d ** -0.5
+    case.dtype, case.hkv = dtype, hkv
+    return case, trace
+
+
+@pytest.mark.parametrize("n,hq,hkv,d,dtype", [(4, 8, 8, 128, "f16"), (3, 16, 8, 64, "bf16"),
+                                              (10, 4, 4, 256, "bf16"), (2, 16, 4, 128, "f16")])
+def test_decode_int8_shared_prefix_matches_the_oracle(n, hq, hkv, d, dtype):
+    # small batches: the plan splits groups into chunks merged by log-sum-exp
+    case, _ = _int8_sampling_case(6, n, (70, 300), (0, 40), hq, hkv, d, dtype, seed=n * 7 + d)
+    want = case.oracle()
+    got = case.run(B.SHARED_PREFIX)
+    H.assert_attention_close(H.to_f64(got), want, f"int8 shared prefix n={n} {hq}/{hkv} d={d}")
+    H.assert_attention_close(H.to_f64(case.run(0)), want, "int8 default schedule")
+    assert B.device_status(clear=True) == 0
+
+
+def test_decode_int8_shared_prefix_siblings_are_bit_identical():
+    case, trace = _int8_sampling_case(3, 4, (200, 400), (0, 0), 8, 8, 128, "f16", seed=5)
+    case.q = case.q[0:1].expand_as(case.q).contiguous()
+    out = case.run(B.SHARED_PREFIX)
+    n = trace.n
+    for i in range(3):
+        for c in range(1, n):
+            assert torch.equal(out[i * n + c], out[i * n])
+    H.assert_attention_close(H.to_f64(out), case.oracle(), "int8 siblings")
+    assert B.device_status(clear=True) == 0
+
+
+def test_decode_int8_shared_prefix_planned_and_unplanned():
+    case, _ = _int8_sampling_case(5, 4, (100, 260), (1, 30), 8, 8, 64, "bf16", seed=9)
+    S, mb = case.q.shape[0], case.tables.shape[1]
+    want = case.oracle()
+    ws = torch.full((B.workspace_size(S, 8, 8, 64, mb, B.SHARED_PREFIX),), 0x55, dtype=torch.uint8, device="cuda")
+    # no plan in the workspace: flagged, every sequence whole
+    out = torch.full_like(case.q, float("nan"))
+    B.paged_attention_decode_int8(out, case.q, case.kc, case.vc, case.ks, case.vs, case.tables, case.lens,
+                                  case.scale, partition_size=B.SHARED_PREFIX, workspace=ws, planned=True)
+    torch.cuda.synchronize()
+    assert B.device_status(clear=True) == 0x20
+    H.assert_attention_close(H.to_f64(out), want, "int8 shared prefix without a plan")
+    # the plan of the 16-bit call serves the INT8 call; two layers with it
+    B.paged_attention_plan(case.lens, case.tables, 8, 8, 64, B.SHARED_PREFIX, workspace=ws)
+    outs = []
+    for _ in range(2):
+        out = torch.full_like(case.q, float("nan"))
+        B.paged_attention_decode_int8(out, case.q, case.kc, case.vc, case.ks, case.vs, case.tables, case.lens,
+                                      case.scale, partition_size=B.SHARED_PREFIX, workspace=ws, planned=True)
+        outs.append(out)
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0], outs[1])
+    H.assert_attention_close(H.to_f64(outs[0]), want, "int8 shared prefix planned")
+    assert B.device_status(clear=True) == 0
+
+
+def test_decode_int8_shared_prefix_full_size_sampling():
+    # the OPT-66B-shaped batch: 32 prompts x 4 samples, 72 heads, head_dim 128
+    case, _ = _int8_sampling_case(32, 4, (512, 1024), (0, 256), 72, 72, 128, "f16", seed=21)
+    got = case.run(B.SHARED_PREFIX)
+    S, Hq = case.q.shape[0], case.q.shape[1]
+    rng = np.random.default_rng(13)
+    pairs = sorted({(s, int(h)) for s, h in zip(range(S), rng.integers(0, Hq, S))})
+    rows = case.oracle_rows(pairs)
+    for (s, h), want in rows.items():
+        H.assert_attention_close(H.to_f64(got[s, h]), want, f"int8 shared prefix ({s}, {h})")
+    H.assert_attention_close(H.to_f64(got), H.to_f64(case.run(-1)), "int8 shared prefix against one pass")
+    assert B.device_status(clear=True) == 0
+
+
 # ---- the CUDA-core INT8 tile (a build with PKV_INT8_MMA=0) -------------------------
 @pytest.fixture(scope="module")
 def cuda_core_int8_lib(tmp_path_factory):
@@ -259,3 +405,10 @@ def test_cuda_core_int8_tile_partial_tiles_and_large_rows(cuda_core_int8_lib):
     assert np.abs(want).max() > 65504.0
     H.assert_attention_close(H.to_f64(big.run()), want, "cuda-core int8 large V rows")
     assert B.device_status(clear=True) == 0
+
+
+def test_cuda_core_int8_tile_has_no_shared_prefix_schedule(cuda_core_int8_lib):
+    case, _ = _int8_sampling_case(2, 4, (100, 200), (0, 10), 8, 8, 128, "bf16", seed=94)
+    with pytest.raises(B.PagedKVError) as ei:
+        case.run(B.SHARED_PREFIX)
+    assert ei.value.status == 2

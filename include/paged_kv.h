@@ -293,7 +293,8 @@ int pkv_paged_attention_partition(
  * cudaDeviceReset (or any other teardown of that context) in the same
  * process. Every call on a device shares the one array, which keeps the last
  * call's contents; the parts that must start at zero (the arrival counters of
- * the split-K and balanced schedules) are cleared on `stream` by every call,
+ * the split-K, balanced and shared-prefix schedules) are cleared on `stream`
+ * by every call (the last by its prefix plan kernel),
  * and everything else a call reads from the array it first writes itself.
  * Calls that overlap on the GPU (different streams, or different host
  * threads) race on it. No cudaMalloc, cudaFree or other allocating routine

@@ -495,27 +495,7 @@ def test_a_plan_of_other_lengths_is_still_correct():
 PREFIX_MAGIC = 0x504B5831  # the first word of a prefix plan's header
 
 
-def _sampling_case(num_prompts, n, prompt_range, tail_range, hq, hkv, d, dtype, seed):
-    """Sequences from the block manager after parallel sampling (prompt added,
-    forked n-1 times, tails appended with copy-on-write), pools filled with
-    seeded values, copy-on-write pairs applied."""
-    trace = W.ParallelSamplingTrace("sampling", dtype, hq, hkv, d,
-                                    np.random.default_rng(seed).integers(*prompt_range, size=num_prompts,
-                                                                         endpoint=True).astype(np.int32),
-                                    np.random.default_rng(seed + 1).integers(*tail_range, size=(num_prompts, n),
-                                                                             endpoint=True).astype(np.int32))
-    nb = trace.block_budget()
-    bm = B.BlockManager(nb, W.shuffled_free_order(nb, seed))
-    plan = W.drive_parallel_sampling(trace, bm)
-    kp = W.normal_values((nb, hkv, 16, d), dtype, seed * 3 + 1, "cuda")
-    vp = W.normal_values((nb, hkv, 16, d), dtype, seed * 3 + 2, "cuda")
-    if plan.pairs:
-        B.copy_blocks(kp, vp, torch.tensor(plan.pairs, dtype=torch.int64, device="cuda").reshape(-1, 2))
-    mb = max(-(-L // 16) for L in plan.final_lens.values())
-    tables, lens = bm.block_tables(plan.seq_ids, mb)
-    q = W.normal_values((len(plan.seq_ids), hq, d), dtype, seed * 3 + 3, "cuda")
-    return H.DecodeCase(q, kp, vp, torch.from_numpy(tables).cuda(), torch.from_numpy(lens).cuda(), d ** -0.5,
-                        dtype), trace
+_sampling_case = H.sampling_case
 
 
 def _prefix_layout(S, hq, hkv, d):

@@ -7,7 +7,8 @@ risk a device synchronisation). Its scratch -- split-K partials and arrival
 counters, the balanced schedule's slots and counters, and the launch order of
 batches of 128..1024 sequences -- is one fixed array inside the library that
 every call shares. These tests call it through the C ABI several times in a
-row, with shapes that put different layouts into that array, and compare
+row, with shapes and schedules (split-K, balanced, one pass with a launch
+order, shared prefix) that put different layouts into that array, and compare
 every result element by element with the float64 oracle (and with the
 workspace-taking entry point) at the attention tolerance of the other GPU
 tests, so stale contents left by one call cannot hide in the next.
@@ -85,6 +86,13 @@ def test_noalloc_matches_the_oracle_on_calls_in_a_row():
     # 4: split again, another shape and fewer partitions (counters at a new offset)
     d = H.make_case([400, 17, 1200], 8, 8, 128, "f16", seed=34)
     _check(d, 256, "call 4 (split 256)")
+
+    # 5: the shared-prefix schedule over parallel samples: its prefix plan,
+    #    the partials of groups split into chunks and their counters all land
+    #    on the stale contents of the calls before
+    e, _ = H.sampling_case(6, 4, (70, 300), (0, 40), 8, 8, 128, "bf16", seed=35)
+    assert B.resolved_partition(e.q.shape[0], 8, 8, 128, e.tables.shape[1], B.SHARED_PREFIX) == B.SHARED_PREFIX
+    _check(e, B.SHARED_PREFIX, "call 5 (shared prefix)")
     assert B.device_status(clear=True) == 0
 
 

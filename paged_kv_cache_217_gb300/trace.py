@@ -4,7 +4,8 @@
     python -m paged_kv_cache_217_gb300.trace --lib DIR/libpaged_kv.so --workload llama3_8b
 
 Runs the named layer's decode on the grid kernels (one CTA per sequence, KV
-head and partition; --partition -1 by default, or a split-K partition size),
+head and partition; --partition -1 by default, or a split-K partition size;
+with --planned the step's launch plan is made once, before the traced calls),
 with seeded synthetic inputs, blocks scattered through a shuffled pool and L2
 evicted between calls, with a trace buffer set
 (pkv_set_trace_buffer) and GPU clock stamps (pkv_trace_stamp) before and
@@ -45,6 +46,9 @@ def main(argv=None):
     ap.add_argument("--partition", type=int, default=-1,
                     help="-1 (one CTA per sequence and KV head) or a split-K partition size in tokens; the "
                          "persistent schedules record no trace")
+    ap.add_argument("--planned", action="store_true",
+                    help="make the step's launch plan once (pkv_paged_attention_plan) and trace the planned decode "
+                         "call, as bench.py times it")
     ap.add_argument("--replay", action="store_true", help="replay the CTA lifetimes under other row orders")
     args = ap.parse_args(argv)
 
@@ -72,13 +76,16 @@ def main(argv=None):
     flush = torch.ones((512 << 20) // 4, dtype=torch.int32, device=dev)
     stamps = torch.zeros(2, dtype=torch.int64, device=dev)
     anatomy = []
+    if args.planned:
+        B.paged_attention_plan(l_d, t_d, hq, hkv, d, partition_size=args.partition)
     B.set_trace_buffer(buf)
     try:
         for i in range(args.calls):
             buf.zero_()
             flush.sum()
             B.trace_stamp(stamps, 0)
-            B.paged_attention_decode(out, q, k_pool, v_pool, t_d, l_d, shape.scale, partition_size=args.partition)
+            B.paged_attention_decode(out, q, k_pool, v_pool, t_d, l_d, shape.scale, partition_size=args.partition,
+                                     planned=args.planned)
             B.trace_stamp(stamps, 1)
             torch.cuda.synchronize()
             r = buf.view(-1, 8).cpu().numpy()

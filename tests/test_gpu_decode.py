@@ -627,6 +627,65 @@ def test_shared_prefix_without_a_plan_is_flagged_and_still_correct():
     H.assert_attention_close(H.to_f64(out), H.oracle_full(case), "no prefix plan")
 
 
+def test_shared_prefix_largest_batch():
+    # 1024 sequences (the plan kernel's limit: one thread per sequence, up to
+    # 512 groups): 256 prompts x 4 samples
+    case, _ = _sampling_case(256, 4, (64, 120), (0, 20), 4, 4, 64, "f16", seed=40)
+    S, mb = case.q.shape[0], case.tables.shape[1]
+    assert S == 1024 and B.resolved_partition(S, 4, 4, 64, mb, B.SHARED_PREFIX) == B.SHARED_PREFIX
+    lay = _prefix_layout(S, 4, 4, 64)
+    ws = torch.zeros((lay["total"],), dtype=torch.uint8, device="cuda")
+    B.paged_attention_plan(case.lens, case.tables, 4, 4, 64, B.SHARED_PREFIX, workspace=ws)
+    out = case.new_out()
+    B.paged_attention_decode(out, case.q, case.k_pool, case.v_pool, case.tables, case.lens, case.scale,
+                             partition_size=B.SHARED_PREFIX, workspace=ws, planned=True)
+    torch.cuda.synchronize()
+    hdr, groups, chunks, others = _read_prefix_plan(ws, lay, S)
+    assert len(groups) == 256 and others == []
+    _check_chunks(groups, chunks, hdr[2], [-(-L // 16) for L in case.lens.cpu().tolist()])
+    H.assert_attention_close(H.to_f64(out), H.oracle_full(case), "1024 sequences, shared prefix")
+    assert B.device_status(clear=True) == 0
+
+
+def test_shared_prefix_siblings_apart_form_no_groups():
+    # the same samples with siblings no longer next to each other: no group
+    # forms (sharing that is not consecutive is left to L2) and every
+    # sequence runs whole
+    case, _ = _sampling_case(6, 4, (100, 300), (0, 40), 8, 8, 128, "bf16", seed=41)
+    S = case.q.shape[0]
+    perm = torch.from_numpy(np.arange(S).reshape(6, 4).T.reshape(-1).copy()).cuda()  # sibling i of every prompt, in turn
+    apart = H.DecodeCase(case.q[perm].contiguous(), case.k_pool, case.v_pool, case.tables[perm].contiguous(),
+                         case.lens[perm].contiguous(), case.scale, "bf16")
+    lay = _prefix_layout(S, 8, 8, 128)
+    ws = torch.zeros((lay["total"],), dtype=torch.uint8, device="cuda")
+    B.paged_attention_plan(apart.lens, apart.tables, 8, 8, 128, B.SHARED_PREFIX, workspace=ws)
+    torch.cuda.synchronize()
+    hdr, groups, chunks, others = _read_prefix_plan(ws, lay, S)
+    assert hdr[2] == 0 and others == list(range(S))
+    H.assert_attention_close(H.to_f64(_run(apart, B.SHARED_PREFIX)), H.oracle_full(apart), "siblings apart")
+    assert B.device_status(clear=True) == 0
+
+
+def test_shared_prefix_widest_tables():
+    # tables of 256 blocks (the widest the plan compares) and a prefix of over
+    # 240 shared blocks; a group this long in a grid this small is split
+    case, _ = _sampling_case(2, 2, (3900, 4000), (0, 90), 2, 2, 128, "f16", seed=42)
+    S, mb = case.q.shape[0], case.tables.shape[1]
+    assert mb <= 256
+    if mb < 256:   # pad the tables to exactly 256 columns (unused entries -1)
+        pad = torch.full((S, 256 - mb), -1, dtype=torch.int32, device="cuda")
+        case = H.DecodeCase(case.q, case.k_pool, case.v_pool, torch.cat([case.tables, pad], 1).contiguous(),
+                            case.lens, case.scale, "f16")
+    lay = _prefix_layout(S, 2, 2, 128)
+    ws = torch.zeros((lay["total"],), dtype=torch.uint8, device="cuda")
+    B.paged_attention_plan(case.lens, case.tables, 2, 2, 128, B.SHARED_PREFIX, workspace=ws)
+    torch.cuda.synchronize()
+    hdr, groups, chunks, _ = _read_prefix_plan(ws, lay, S)
+    assert len(groups) == 2 and all(g[2] >= 240 and g[3] > 1 for g in groups)
+    H.assert_attention_close(H.to_f64(_run(case, B.SHARED_PREFIX)), H.oracle_full(case), "256-block tables")
+    assert B.device_status(clear=True) == 0
+
+
 def test_shared_prefix_full_size_parallel_sampling():
     # the OPT-66B-shaped batch: 32 prompts x 4 samples, 72 heads, head_dim 128
     case, _ = _sampling_case(32, 4, (512, 1024), (0, 256), 72, 72, 128, "f16", seed=21)

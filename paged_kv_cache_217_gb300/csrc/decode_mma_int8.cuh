@@ -348,8 +348,8 @@ __device__ __forceinline__ void prefix_cta_int8(const DecodeArgs& a, const CUten
   auto load_ids = [&](int batch) -> int {
     const int k = batch * 32 + lane;
     if (k >= n_my) return 0;
-    int m, j;
-    c.locate(k, m, j);
+    int m, j, rows;
+    c.locate(k, m, j, rows);
     return c.block_id(a, m, j);
   };
   int ids = load_ids(0);
@@ -395,9 +395,8 @@ __device__ __forceinline__ void prefix_cta_int8(const DecodeArgs& a, const CUten
       for (int kk = k; kk < last; ++kk) mbar_wait_bounded(bar_s + 8 * (kk % STAGES), (kk / STAGES) & 1);
       break;
     }
-    int m, j;
-    c.locate(k, m, j);
-    const int valid = c.tile_rows(m, j);
+    int m, j, valid;
+    c.locate(k, m, j, valid);
     const bool row_on = m < 0 || my_member == m;
     const uint32_t kt = ring_s + st * C::STAGE_BYTES;
     const uint32_t sc = scale_s + st * C::SCALE_STAGE;

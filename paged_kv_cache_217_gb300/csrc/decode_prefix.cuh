@@ -45,7 +45,8 @@ namespace pkv {
 template <int NW>
 struct PrefixChunk {
   int s0, members, P, parts, part, rows;
-  int len[kPrefixRows], own[kPrefixRows];
+  // per member m: (length << 9) | this warp's own tiles (length <= 4096, own <= 256)
+  int mem[kPrefixRows];
   int sh_first, sh_n, j_own, n_my;
 
   // Reads and checks the chunk; false (after flagging PKV_DEV_BAD_PLAN) when
@@ -86,15 +87,15 @@ struct PrefixChunk {
         if (threadIdx.x == 0 && g == 0) flag(a.status, PKV_DEV_BAD_PLAN);
         L = P * kBlock;
       }
-      len[m] = L;
       const int hi = min(je, (L + kBlock - 1) / kBlock);
-      own[m] = 0;
+      int mine = 0;
 #pragma unroll
       for (int w = 0; w < NW; ++w) {
         const int c = (m < members && own_lo < hi) ? count_below(hi, w) - count_below(own_lo, w) : 0;
         own_w[w] += c;
-        if (w == warp) own[m] = c;
+        if (w == warp) mine = c;
       }
+      mem[m] = (L << 9) | mine;
     }
     // the smallest level L with sum_w max(0, L - own_w) >= sh_total; warps
     // below L - 1 fill up to it, the first few at L - 1 take the remainder
@@ -125,29 +126,30 @@ struct PrefixChunk {
     }
     n_my = sh_n;
 #pragma unroll
-    for (int m = 0; m < kPrefixRows; ++m) n_my += own[m];
+    for (int m = 0; m < kPrefixRows; ++m) n_my += mem[m] & 511;
     j_own = own_lo + ((warp - own_lo) % NW + NW) % NW;  // the first own block j >= own_lo of this warp
     return true;
   }
 
-  // Tile k of this warp: (member, block) -- member -1 for a shared tile.
-  __device__ __forceinline__ void locate(int k, int& m, int& j) const {
+  // Tile k of this warp: (member, block, valid rows) -- member -1 for a
+  // shared tile. (The arrays are indexed with unrolled constants only, so
+  // they stay in registers.)
+  __device__ __forceinline__ void locate(int k, int& m, int& j, int& rows) const {
     m = -1;
     j = sh_first + k;
+    rows = kBlock;
     if (k < sh_n) return;
     int r = k - sh_n;
 #pragma unroll
     for (int mm = 0; mm < kPrefixRows; ++mm) {
-      if (m < 0 && r < own[mm]) {
+      const int own = mem[mm] & 511;
+      if (m < 0 && r < own) {
         m = mm;
         j = j_own + r * NW;
+        rows = min(kBlock, (mem[mm] >> 9) - j * kBlock);
       }
-      if (m < 0) r -= own[mm];
+      if (m < 0) r -= own;
     }
-  }
-  // Valid rows of tile (m, j).
-  __device__ __forceinline__ int tile_rows(int m, int j) const {
-    return m < 0 ? kBlock : min(kBlock, len[m] - j * kBlock);
   }
   // Physical block of tile (m, j), checked against the pool (0 and flagged if bad).
   __device__ __forceinline__ int block_id(const DecodeArgs& a, int m, int j) const {
@@ -297,8 +299,8 @@ __device__ __forceinline__ void prefix_cta(const DecodeArgs& a, const PoolMaps& 
   auto load_ids = [&](int batch) -> int {
     const int k = batch * 32 + lane;
     if (k >= n_my) return 0;
-    int m, j;
-    c.locate(k, m, j);
+    int m, j, rows;
+    c.locate(k, m, j, rows);
     return c.block_id(a, m, j);
   };
   int ids = load_ids(0);
@@ -312,9 +314,9 @@ __device__ __forceinline__ void prefix_cta(const DecodeArgs& a, const PoolMaps& 
     }
     const int id = __shfl_sync(kFull, ids, k & 31);
     if (lane == 0) {
-      int m, j;
-      c.locate(k, m, j);
-      const int cover = min(kBlock, (c.tile_rows(m, j) + 3) & ~3);  // rows copied, a multiple of 4
+      int m, j, rows;
+      c.locate(k, m, j, rows);
+      const int cover = min(kBlock, (rows + 3) & ~3);  // rows copied, a multiple of 4
       const int st = k % STAGES;
       const uint32_t bar = bar_s + 8 * st;
       const uint32_t dst = ring_s + st * C::STAGE_BYTES;
@@ -359,9 +361,8 @@ __device__ __forceinline__ void prefix_cta(const DecodeArgs& a, const PoolMaps& 
       for (int kk = k; kk < last; ++kk) mbar_wait_bounded(bar_s + 8 * (kk % STAGES), (kk / STAGES) & 1);
       break;
     }
-    int m, j;
-    c.locate(k, m, j);
-    const int valid = c.tile_rows(m, j);
+    int m, j, valid;
+    c.locate(k, m, j, valid);
     const bool row_on = m < 0 || my_member == m;
     const uint32_t kt = ring_s + st * C::STAGE_BYTES;
     if (valid == kBlock) {

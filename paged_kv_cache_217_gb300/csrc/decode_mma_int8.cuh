@@ -310,6 +310,167 @@ __device__ __forceinline__ void i8_publish(float* wsm, const float (&o)[D / 8][4
   }
 }
 
+// One query row per KV head (group size 1, head_dim <= 128): QK^T on the
+// integer units instead of the tensor cores. The query becomes two int8
+// digit planes, q ~ s1 * d1 + s2 * d2 with s1 = max|q| / 127, d1 = rint(q /
+// s1), s2 = s1 / 254 and d2 = rint((q - s1 d1) / s2), so |q - (s1 d1 + s2
+// d2)| <= max|q| / 64516, and each K code word meets each plane in one
+// dp4a (four int8 products summed exactly in int32): no code is converted.
+// Lane l takes token l / 2 and head dims [D/2 * (l & 1), D/2 * (l & 1 + 1)).
+// PV stays on the tensor cores (the weights gathered into row 0 of the A
+// operand), exactly as in mma_tile_int8.
+template <int D>
+struct MhaQuery {
+  int p1[D / 8], p2[D / 8];  // this lane's half of the two planes, 4 dims a word
+  float s1, s2;              // plane scales times scale * log2(e)
+};
+
+template <typename T, int D>
+__device__ __forceinline__ void i8_query_mha(const T* qrow, int lane, float scale_log2, MhaQuery<D>& mq) {
+  // Lane l digitises dims 4l .. 4l+3 (lanes past D/4 repeat the first ones),
+  // then each lane gathers the words of its half by shuffles.
+  constexpr int W = D / 8;  // words of one half
+  const int wl = lane % (D / 4);
+  const uint2 u = __ldg(reinterpret_cast<const uint2*>(qrow + 4 * wl));
+  const T* e = reinterpret_cast<const T*>(&u);
+  float qf[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) qf[i] = float(e[i]);
+  float m = fmaxf(fmaxf(fabsf(qf[0]), fabsf(qf[1])), fmaxf(fabsf(qf[2]), fabsf(qf[3])));
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, off));
+  const float s1 = m / 127.f, s2 = s1 / 254.f;
+  const float inv1 = m > 0.f ? 127.f / m : 0.f, inv2 = m > 0.f ? 254.f * 127.f / m : 0.f;
+  uint32_t w1 = 0, w2 = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float d1 = rintf(qf[i] * inv1);
+    const float d2 = fminf(fmaxf(rintf((qf[i] - d1 * s1) * inv2), -127.f), 127.f);
+    w1 |= (uint32_t(int(d1)) & 0xffu) << (8 * i);
+    w2 |= (uint32_t(int(d2)) & 0xffu) << (8 * i);
+  }
+  const int h = lane & 1;
+#pragma unroll
+  for (int w = 0; w < W; ++w) {
+    mq.p1[w] = int(__shfl_sync(kFull, w1, W * h + w));
+    mq.p2[w] = int(__shfl_sync(kFull, w2, W * h + w));
+  }
+  mq.s1 = s1 * scale_log2;
+  mq.s2 = s2 * scale_log2;
+}
+
+template <int D, int NW, int STAGES, bool MASK>
+__device__ __forceinline__ void mma_tile_int8_mha(uint32_t kt, uint32_t vt, uint32_t st_scale, int lo, int rows,
+                                                  const MhaQuery<D>& mq, float (&o)[D / 8][4], float& mrun,
+                                                  float& lsum, VScale& vs, int lane) {
+  using C = I8Cfg<D, NW, STAGES>;
+  static_assert(D <= 128, "the integer QK^T keeps a half row of both planes in registers");
+  const int tk = lane >> 1, h = lane & 1;
+  const int t = lane & 3, gr = lane >> 2;
+
+  // S = q . C_K^T for token tk: this lane's half of the dims, then the pair's sum.
+  int acc1 = 0, acc2 = 0;
+#pragma unroll
+  for (int c = 0; c < D / 32; ++c) {
+    const uint4 w = lds128(kt + i8_swz<D>(tk, (D / 32) * h + c));
+    acc1 = __dp4a(int(w.x), mq.p1[4 * c], acc1);
+    acc2 = __dp4a(int(w.x), mq.p2[4 * c], acc2);
+    acc1 = __dp4a(int(w.y), mq.p1[4 * c + 1], acc1);
+    acc2 = __dp4a(int(w.y), mq.p2[4 * c + 1], acc2);
+    acc1 = __dp4a(int(w.z), mq.p1[4 * c + 2], acc1);
+    acc2 = __dp4a(int(w.z), mq.p2[4 * c + 2], acc2);
+    acc1 = __dp4a(int(w.w), mq.p1[4 * c + 3], acc1);
+    acc2 = __dp4a(int(w.w), mq.p2[4 * c + 3], acc2);
+  }
+  float sc = fmaf(mq.s1, float(acc1), mq.s2 * float(acc2));
+  sc += __shfl_xor_sync(kFull, sc, 1);
+  float x, sv;
+  {
+    float ks, vsc;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(ks) : "r"(st_scale + 4 * tk));
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(vsc) : "r"(st_scale + 64 + 4 * tk));
+    x = sc * ks;
+    sv = vsc;
+  }
+  if (MASK && (tk < lo || tk >= rows)) x = -INFINITY, sv = 0.f;
+  // the tile's max score and largest V scale, over the 16 tokens (lanes 2 apart)
+  float mt = x, ms = sv;
+#pragma unroll
+  for (int off = 2; off < 32; off <<= 1) {
+    mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, off));
+    ms = fmaxf(ms, __shfl_xor_sync(kFull, ms, off));
+  }
+  const float mn = fmaxf(mrun, mt);
+  const float mref = mn == -INFINITY ? 0.f : mn;
+  float vratio = 1.f;
+  const bool vgrow = ms >= vs.vbound;
+  if (vgrow) {  // ms in [2^(E-1), 2^E): vbound = 2^E, vmul = 2^(14 - E)
+    const int E = min(max(int((__float_as_uint(ms) >> 23) & 0xffu) - 126, -99), 113);
+    const float nmul = __uint_as_float(uint32_t(127 + 14 - E) << 23);
+    vratio = nmul / vs.vmul;
+    vs.vmul = nmul;
+    vs.vbound = __uint_as_float(uint32_t(127 + E) << 23);
+  }
+  if (vgrow || mn > mrun) {  // warp-uniform
+    const float alpha = fast_exp2(mrun - mref);
+    lsum *= alpha;
+    const float oa = alpha * vratio;
+#pragma unroll
+    for (int nd = 0; nd < C::NTILES; ++nd) {
+      o[nd][0] *= oa;
+      o[nd][1] *= oa;
+    }
+    mrun = mn;
+  }
+  const float p = fast_exp2(x - mref);
+  if (h == 0) lsum += p;  // each token once
+  const float pv = p * (sv * vs.vmul);
+  // Row 0 of the A operand: lanes 0..3 take the weights of tokens 2t, 2t+1, 2t+8, 2t+9.
+  const float w0 = __shfl_sync(kFull, pv, 4 * t), w1 = __shfl_sync(kFull, pv, 4 * t + 2);
+  const float w2 = __shfl_sync(kFull, pv, 4 * t + 16), w3 = __shfl_sync(kFull, pv, 4 * t + 18);
+  const __half2 p01 = __floats2half2_rn(w0, w1);
+  const __half2 p23 = __floats2half2_rn(w2, w3);
+  const uint32_t a01 = gr == 0 ? *reinterpret_cast<const uint32_t*>(&p01) : 0u;
+  const uint32_t a23 = gr == 0 ? *reinterpret_cast<const uint32_t*>(&p23) : 0u;
+
+  // O += P~ . C_V, as in mma_tile_int8.
+  constexpr int VW = D == 64 ? 8 : 16;
+  uint32_t wa[VW / 4], wb[VW / 4], wc[VW / 4], wd[VW / 4];
+  if constexpr (D == 64) {
+    const uint32_t off = 8 * (gr & 1);
+    const uint2 xa = lds64(vt + i8_swz<D>(2 * t, gr >> 1) + off);
+    const uint2 xb = lds64(vt + i8_swz<D>(2 * t + 1, gr >> 1) + off);
+    const uint2 xc = lds64(vt + i8_swz<D>(2 * t + 8, gr >> 1) + off);
+    const uint2 xd = lds64(vt + i8_swz<D>(2 * t + 9, gr >> 1) + off);
+    wa[0] = xa.x, wa[1] = xa.y, wb[0] = xb.x, wb[1] = xb.y;
+    wc[0] = xc.x, wc[1] = xc.y, wd[0] = xd.x, wd[1] = xd.y;
+  } else {
+    const uint4 xa = lds128(vt + i8_swz<D>(2 * t, gr));
+    const uint4 xb = lds128(vt + i8_swz<D>(2 * t + 1, gr));
+    const uint4 xc = lds128(vt + i8_swz<D>(2 * t + 8, gr));
+    const uint4 xd = lds128(vt + i8_swz<D>(2 * t + 9, gr));
+    wa[0] = xa.x, wa[1] = xa.y, wa[2] = xa.z, wa[3] = xa.w;
+    wb[0] = xb.x, wb[1] = xb.y, wb[2] = xb.z, wb[3] = xb.w;
+    wc[0] = xc.x, wc[1] = xc.y, wc[2] = xc.z, wc[3] = xc.w;
+    wd[0] = xd.x, wd[1] = xd.y, wd[2] = xd.z, wd[3] = xd.w;
+  }
+#pragma unroll
+  for (int w = 0; w < VW / 4; ++w) {
+    const uint32_t xa = wa[w] ^ 0x80808080u, xb = wb[w] ^ 0x80808080u;
+    const uint32_t xc = wc[w] ^ 0x80808080u, xd = wd[w] ^ 0x80808080u;
+    const uint32_t ab01 = __byte_perm(xa, xb, 0x5140), ab23 = __byte_perm(xa, xb, 0x7362);
+    const uint32_t cd01 = __byte_perm(xc, xd, 0x5140), cd23 = __byte_perm(xc, xd, 0x7362);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t ab = i < 2 ? ab01 : ab23, cd = i < 2 ? cd01 : cd23;
+      const uint32_t sel = (i & 1) ? 0x5342 : 0x5140;
+      const uint32_t b0 = hsub2_u32(__byte_perm(ab, kF16Magic, sel), kF16Bias);
+      const uint32_t b1 = hsub2_u32(__byte_perm(cd, kF16Magic, sel), kF16Bias);
+      Mma<__half>::run(o[4 * w + i], a01, 0u, a23, 0u, b0, b1);
+    }
+  }
+}
+
 // One CTA of the shared-prefix schedule over the INT8 cache (the 16-bit
 // version, prefix_cta in decode_prefix.cuh, describes the chunk): the
 // members' query rows share each K/V code tile, copied once.
@@ -494,11 +655,20 @@ paged_decode_mma_int8_kernel(const DecodeArgs a, const __grid_constant__ CUtenso
   }
   __syncwarp();
 
-  // Q~ of head hq0 + gr as the A operand (rows past the group zero).
+  // Group size 1 up to head_dim 128: QK^T on the integer units against the
+  // query's two digit planes (mma_tile_int8_mha); otherwise Q~ of head hq0 + gr
+  // as the tensor cores' A operand (rows past the group zero).
+  constexpr bool kMha = G == 1 && D <= 128;
   uint32_t qa[C::KCHUNKS][2];
-  float qmul;
-  i8_query<T, D>(gr < a.group ? static_cast<const T*>(a.q) + (size_t(s) * a.num_q_heads + hq0 + gr) * D : nullptr,
-                 t, qa, qmul, a.scale_log2);
+  float qmul = 0.f;
+  MhaQuery<D <= 128 ? D : 128> mq;
+  if constexpr (kMha) {
+    i8_query_mha<T, D>(static_cast<const T*>(a.q) + (size_t(s) * a.num_q_heads + hq0) * D, lane, a.scale_log2, mq);
+  } else {
+    i8_query<T, D>(gr < a.group ? static_cast<const T*>(a.q) + (size_t(s) * a.num_q_heads + hq0 + gr) * D
+                                : nullptr,
+                   t, qa, qmul, a.scale_log2);
+  }
 
   const int n_my = nb > warp ? (nb - warp + NW - 1) / NW : 0;
   const int32_t* trow = a.block_tables + size_t(s) * a.max_blocks_per_seq + t0 / kBlock;
@@ -571,16 +741,28 @@ paged_decode_mma_int8_kernel(const DecodeArgs a, const __grid_constant__ CUtenso
     const int lo = j == 0 ? head : 0;
     const uint32_t kt = ring_s + st * C::STAGE_BYTES;
     const uint32_t sc = scale_s + st * C::SCALE_STAGE;
-    if (rows == kBlock && lo == 0)
-      mma_tile_int8<D, NW, STAGES, false>(kt, kt + C::TILE_BYTES, sc, 0, rows, qa, o, mrun, lrun, vs, qmul, lane);
-    else
-      mma_tile_int8<D, NW, STAGES, true>(kt, kt + C::TILE_BYTES, sc, lo, rows, qa, o, mrun, lrun, vs, qmul, lane);
+    if constexpr (kMha) {
+      if (rows == kBlock && lo == 0)
+        mma_tile_int8_mha<D, NW, STAGES, false>(kt, kt + C::TILE_BYTES, sc, 0, rows, mq, o, mrun, lrun, vs, lane);
+      else
+        mma_tile_int8_mha<D, NW, STAGES, true>(kt, kt + C::TILE_BYTES, sc, lo, rows, mq, o, mrun, lrun, vs, lane);
+    } else {
+      if (rows == kBlock && lo == 0)
+        mma_tile_int8<D, NW, STAGES, false>(kt, kt + C::TILE_BYTES, sc, 0, rows, qa, o, mrun, lrun, vs, qmul, lane);
+      else
+        mma_tile_int8<D, NW, STAGES, true>(kt, kt + C::TILE_BYTES, sc, lo, rows, qa, o, mrun, lrun, vs, qmul, lane);
+    }
     __syncwarp();
     if (k + STAGES < n_my) issue(k + STAGES);
   }
 
-  lrun += __shfl_xor_sync(kFull, lrun, 1);
-  lrun += __shfl_xor_sync(kFull, lrun, 2);
+  if constexpr (kMha) {  // each lane summed the weights of its own token's tiles (h == 0 lanes only)
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) lrun += __shfl_xor_sync(kFull, lrun, off);
+  } else {
+    lrun += __shfl_xor_sync(kFull, lrun, 1);
+    lrun += __shfl_xor_sync(kFull, lrun, 2);
+  }
 
   i8_publish<D, G>(reinterpret_cast<float*>(ring), o, mrun, lrun, vs, lane);
   __syncthreads();

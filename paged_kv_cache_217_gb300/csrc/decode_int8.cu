@@ -13,8 +13,12 @@ namespace pkv {
 namespace {
 
 // Stages per warp of the INT8 kernels (an int8 stage is half the size of a
-// 16-bit one).
+// 16-bit one). The one-query tile (group size 1, head_dim <= 128: QK^T on
+// dp4a, see mma_tile_int8_mha) takes kInt8MhaStages and 4 CTAs per SM (at
+// most 128 registers): measured on GB300, the LLaMA-13B layer 87.1 -> 80.7 us
+// against 4 stages at 3 CTAs per SM, the OPT-175B layer 670.6 -> 691.9 us.
 constexpr int kInt8Stages = 4;
+constexpr int kInt8MhaStages = 3;
 // Warps per CTA of the INT8 tensor-core kernel for groups of 2..8 query
 // heads (group size 1 keeps kGridWarps). Measured on GB300: the
 // Llama-3-8B-shaped layer 39.1 us with 4 warps, 37.5 us with 3 (4 CTAs per
@@ -25,7 +29,7 @@ template <typename T, int D, int G>
 cudaError_t launch_int8_dg(const DecodeArgs& a, const CUtensorMap* kmap, const CUtensorMap* vmap,
                            cudaStream_t stream) {
   constexpr int NW = (PKV_INT8_MMA && G >= 2) ? kInt8GqaWarps : kGridWarps;
-  constexpr int STAGES = kInt8Stages;
+  constexpr int STAGES = (PKV_INT8_MMA && G == 1 && D <= 128) ? kInt8MhaStages : kInt8Stages;
   static bool configured[kMaxDevices] = {};
   // (the shared-prefix schedule: rows for its chunks, then the sequences, one pass)
   const dim3 grid(unsigned(a.num_kv_heads), unsigned(a.num_seqs + (a.prefix_header ? a.prefix_slots : 0)),

@@ -361,7 +361,7 @@ __device__ __forceinline__ void i8_query_mha(const T* qrow, int lane, float scal
 
 template <int D, int NW, int STAGES, bool MASK>
 __device__ __forceinline__ void mma_tile_int8_mha(uint32_t kt, uint32_t vt, uint32_t st_scale, int lo, int rows,
-                                                  const MhaQuery<D>& mq, float (&o)[D / 8][4], float& mrun,
+                                                  const MhaQuery<D>& mq, float (&o)[D / 16][4], float& mrun,
                                                   float& lsum, VScale& vs, int lane) {
   using C = I8Cfg<D, NW, STAGES>;
   static_assert(D <= 128, "the integer QK^T keeps a half row of both planes in registers");
@@ -416,24 +416,28 @@ __device__ __forceinline__ void mma_tile_int8_mha(uint32_t kt, uint32_t vt, uint
     lsum *= alpha;
     const float oa = alpha * vratio;
 #pragma unroll
-    for (int nd = 0; nd < C::NTILES; ++nd) {
-      o[nd][0] *= oa;
-      o[nd][1] *= oa;
+    for (int nb = 0; nb < D / 16; ++nb) {  // column 0 of each block (columns 1..7 stay zero)
+      o[nb][0] *= oa;
+      o[nb][2] *= oa;
     }
     mrun = mn;
   }
   const float p = fast_exp2(x - mref);
   if (h == 0) lsum += p;  // each token once
   const float pv = p * (sv * vs.vmul);
-  // Row 0 of the A operand: lanes 0..3 take the weights of tokens 2t, 2t+1, 2t+8, 2t+9.
+  // Column 0 of the B operand: lanes 0..3 (gr = 0) take the weights of tokens 2t, 2t+1, 2t+8, 2t+9.
   const float w0 = __shfl_sync(kFull, pv, 4 * t), w1 = __shfl_sync(kFull, pv, 4 * t + 2);
   const float w2 = __shfl_sync(kFull, pv, 4 * t + 16), w3 = __shfl_sync(kFull, pv, 4 * t + 18);
   const __half2 p01 = __floats2half2_rn(w0, w1);
   const __half2 p23 = __floats2half2_rn(w2, w3);
-  const uint32_t a01 = gr == 0 ? *reinterpret_cast<const uint32_t*>(&p01) : 0u;
-  const uint32_t a23 = gr == 0 ? *reinterpret_cast<const uint32_t*>(&p23) : 0u;
+  const uint32_t b01 = gr == 0 ? *reinterpret_cast<const uint32_t*>(&p01) : 0u;
+  const uint32_t b23 = gr == 0 ? *reinterpret_cast<const uint32_t*>(&p23) : 0u;
 
-  // O += P~ . C_V, as in mma_tile_int8.
+  // O^T += C_V^T . P~ on the tensor cores: M = 16 head dims, K = the 16
+  // tokens, N = 8 columns of which column 0 is the weights (lanes gr = 0 give
+  // the B operand). This lane reads its 16-byte chunk (8 bytes at D = 64) of
+  // tokens 2t, 2t+1, 8+2t, 9+2t; rows gr and gr + 8 of block b are head dims
+  // VW * gr + 2b and VW * gr + 2b + 1.
   constexpr int VW = D == 64 ? 8 : 16;
   uint32_t wa[VW / 4], wb[VW / 4], wc[VW / 4], wd[VW / 4];
   if constexpr (D == 64) {
@@ -456,18 +460,42 @@ __device__ __forceinline__ void mma_tile_int8_mha(uint32_t kt, uint32_t vt, uint
   }
 #pragma unroll
   for (int w = 0; w < VW / 4; ++w) {
+    // Interleave the two tokens of each pair: [a_i, b_i, a_j, b_j].
     const uint32_t xa = wa[w] ^ 0x80808080u, xb = wb[w] ^ 0x80808080u;
     const uint32_t xc = wc[w] ^ 0x80808080u, xd = wd[w] ^ 0x80808080u;
     const uint32_t ab01 = __byte_perm(xa, xb, 0x5140), ab23 = __byte_perm(xa, xb, 0x7362);
     const uint32_t cd01 = __byte_perm(xc, xd, 0x5140), cd23 = __byte_perm(xc, xd, 0x7362);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint32_t ab = i < 2 ? ab01 : ab23, cd = i < 2 ? cd01 : cd23;
-      const uint32_t sel = (i & 1) ? 0x5342 : 0x5140;
-      const uint32_t b0 = hsub2_u32(__byte_perm(ab, kF16Magic, sel), kF16Bias);
-      const uint32_t b1 = hsub2_u32(__byte_perm(cd, kF16Magic, sel), kF16Bias);
-      Mma<__half>::run(o[4 * w + i], a01, 0u, a23, 0u, b0, b1);
+    for (int half = 0; half < 2; ++half) {  // block 2w + half: bytes 2 half (row gr) and 2 half + 1 (row gr + 8)
+      const uint32_t ab = half ? ab23 : ab01, cd = half ? cd23 : cd01;
+      const uint32_t a0 = hsub2_u32(__byte_perm(ab, kF16Magic, 0x5140), kF16Bias);
+      const uint32_t a1 = hsub2_u32(__byte_perm(ab, kF16Magic, 0x5342), kF16Bias);
+      const uint32_t a2 = hsub2_u32(__byte_perm(cd, kF16Magic, 0x5140), kF16Bias);
+      const uint32_t a3 = hsub2_u32(__byte_perm(cd, kF16Magic, 0x5342), kF16Bias);
+      Mma<__half>::run(o[2 * w + half], a0, a1, a2, a3, b01, b23);
     }
+  }
+}
+
+// Publishes a warp's (acc[1][D], m, l) of the one-query tile in head-dim
+// order, with the V-scale power of two taken out (exact): column 0 of block
+// b sits in lanes t = 0, rows gr and gr + 8 = head dims VW * gr + 2b, + 1.
+template <int D>
+__device__ __forceinline__ void i8_publish_mha(float* wsm, const float (&o)[D / 16][4], float mrun, float lrun,
+                                               const VScale& vs, int lane) {
+  constexpr int VW = D == 64 ? 8 : 16;
+  const int t = lane & 3, gr = lane >> 2;
+  if (t == 0) {
+    const float unmul = 1.f / vs.vmul;
+#pragma unroll
+    for (int b = 0; b < D / 16; ++b) {
+      wsm[VW * gr + 2 * b] = o[b][0] * unmul;
+      wsm[VW * gr + 2 * b + 1] = o[b][2] * unmul;
+    }
+  }
+  if (lane == 0) {
+    wsm[D] = mrun;      // G = 1: m at acc[1][D], l after it
+    wsm[D + 1] = lrun;
   }
 }
 
@@ -578,7 +606,7 @@ __device__ __forceinline__ void prefix_cta_int8(const DecodeArgs& a, const CUten
 }
 
 template <typename T, int D, int G, int NW, int STAGES>
-__global__ void __launch_bounds__(NW * 32)
+__global__ void __launch_bounds__(NW * 32, (G == 1 && D <= 128) ? 4 : 0)  // one-query tile: 4 CTAs per SM
 paged_decode_mma_int8_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap kmap,
                              const __grid_constant__ CUtensorMap vmap) {
   using C = I8Cfg<D, NW, STAGES>;
@@ -717,9 +745,10 @@ paged_decode_mma_int8_kernel(const DecodeArgs a, const __grid_constant__ CUtenso
     }
   };
 
-  float o[C::NTILES][4];
+  constexpr int OROWS = kMha ? D / 16 : C::NTILES;  // accumulator blocks
+  float o[OROWS][4];
 #pragma unroll
-  for (int nd = 0; nd < C::NTILES; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
+  for (int nd = 0; nd < OROWS; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
   float mrun = -INFINITY, lrun = 0.f;
   VScale vs;
 
@@ -764,7 +793,10 @@ paged_decode_mma_int8_kernel(const DecodeArgs a, const __grid_constant__ CUtenso
     lrun += __shfl_xor_sync(kFull, lrun, 2);
   }
 
-  i8_publish<D, G>(reinterpret_cast<float*>(ring), o, mrun, lrun, vs, lane);
+  if constexpr (kMha)
+    i8_publish_mha<D>(reinterpret_cast<float*>(ring), o, mrun, lrun, vs, lane);
+  else
+    i8_publish<D, G>(reinterpret_cast<float*>(ring), o, mrun, lrun, vs, lane);
   __syncthreads();
   finish_chunk<T, D, G, NW>(a, smem, size_t(STAGES) * C::STAGE_BYTES, s, g, part, nparts);
 }

@@ -439,9 +439,12 @@ pkv_status_t pkv_reshape_and_cache_int8(
  * the balanced schedule, which returns PKV_ERR_UNSUPPORTED; -5, the
  * shared-prefix schedule, runs as described there), workspace
  * (pkv_paged_attention_workspace_size with the same arguments) and error
- * behaviour. Internally the scores are q . c_K scaled by s_K, and s_V is
- * folded into each softmax weight (with a power of two per warp that keeps
- * the weights inside the fp16 range).
+ * behaviour. Internally the scores are q . c_K scaled by s_K (with one query
+ * head per KV head and head_dim <= 128, q enters as two int8 digit planes,
+ * q ~ s1 d1 + s2 d2, within max|q| / 64516 of q, so that the products run as
+ * exact integer dot products), and s_V is folded into each softmax weight
+ * (with a power of two per warp that keeps the weights inside the fp16
+ * range).
  */
 pkv_status_t pkv_paged_attention_decode_int8(
     void* out, const void* q, const int8_t* k_cache, const int8_t* v_cache,

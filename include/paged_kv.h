@@ -364,6 +364,17 @@ pkv_status_t pkv_set_trace_buffer(unsigned long long* device_buffer, int records
  * launch's latency. PKV_ERR_INVALID_ARG for a NULL or misaligned word.
  */
 pkv_status_t pkv_trace_stamp(unsigned long long* device_word, void* stream);
+/*
+ * pkv_trace_empty_grid (every build) enqueues on `stream` a kernel of `ctas`
+ * CTAs of `threads` threads with `smem_bytes` of dynamic shared memory that
+ * reads and writes nothing, launched as the decode kernels are (programmatic
+ * stream serialization). Timed between two events it gives the fixed cost of
+ * a launch of that shape (dispatch of its CTAs and the kernel's completion),
+ * which a decode call of the same grid pays before and after its own work.
+ * PKV_ERR_INVALID_ARG unless ctas >= 1, 1 <= threads <= 1024 and
+ * 0 <= smem_bytes <= 227 KB; a launch error is returned as PKV_ERR_CUDA.
+ */
+pkv_status_t pkv_trace_empty_grid(int ctas, int threads, int smem_bytes, void* stream);
 
 /* ------------------------------------------------------------------------ */
 /* Cache writes and copy-on-write                                            */

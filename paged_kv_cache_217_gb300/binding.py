@@ -77,6 +77,7 @@ _SIGS = {
     "pkv_trace_enabled": ([], _c_int),
     "pkv_set_trace_buffer": ([_c_p, _c_int], _c_int),
     "pkv_trace_stamp": ([_c_p, _c_p], _c_int),
+    "pkv_trace_empty_grid": ([_c_int, _c_int, _c_int, _c_p], _c_int),
     "pkv_bm_create": ([_c_int, _c_int, _c_p, ctypes.POINTER(_c_p)], _c_int),
     "pkv_bm_destroy": ([_c_p], None),
     "pkv_bm_add_seq": ([_c_p, _c_i64, _c_i64], _c_int),
@@ -480,6 +481,18 @@ def trace_stamp(words, index):
         raise ValueError("trace_stamp takes a contiguous int64 tensor and an index into it")
     ptr = words.data_ptr() + 8 * int(index)
     _launch(words.device, "trace_stamp", lib().pkv_trace_stamp, ptr)
+
+
+def trace_empty_grid(device, ctas, threads, smem_bytes):
+    """Enqueues on ``device``'s current stream a kernel of ``ctas`` CTAs x
+    ``threads`` threads with ``smem_bytes`` of dynamic shared memory that does
+    nothing, launched as the decode kernels are: timed between two events it
+    is the fixed cost of a launch of that shape."""
+    import torch
+    device = torch.device(device)
+    if device.type != "cuda":
+        raise ValueError("trace_empty_grid needs a CUDA device")
+    _launch(device, "trace_empty_grid", lib().pkv_trace_empty_grid, int(ctas), int(threads), int(smem_bytes))
 
 
 def describe_device_flags(flags):

@@ -29,6 +29,7 @@ SOURCES = [
     "decode_bf16.cu",
     "decode_int8.cu",
     "cache_ops.cu",
+    "diag.cu",
     "block_manager.cpp",
     "status.cpp",
 ]

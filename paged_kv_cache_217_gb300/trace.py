@@ -16,6 +16,16 @@ mean, median, p90 and max of each phase of a CTA's life, CTAs resident per
 microsecond, and the phases by tile count. Needs a library built with
 PKV_TRACE=1; timings of traced calls are not benchmark numbers.
 
+--calibrate (any build; --lib optional) instead times, between CUDA events
+with L2 evicted before each launch, the layer's decode call, an empty
+one-CTA kernel, and an empty kernel with the decode grid's CTA count and the
+given threads and shared memory (pkv_trace_empty_grid; the defaults are the
+tensor-core kernel's 3 warps and bf16 d=128 rings), plus two clock stamps
+with nothing between: what any launch of that shape costs before and after
+its work, next to the call.
+
+    python -m paged_kv_cache_217_gb300.trace --calibrate --workload llama3_8b --planned
+
 --replay also fits the traced CTA lifetimes as a + b * tiles and replays
 the layer's CTAs through as many slots as were resident, rows dispatched in
 order, for several row orders (natural; long first; long first and short
@@ -39,7 +49,7 @@ SHORT_LAST_X8 = 5
 
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
-    ap.add_argument("--lib", required=True, help="a libpaged_kv.so built with PKV_TRACE=1")
+    ap.add_argument("--lib", help="a libpaged_kv.so built with PKV_TRACE=1 (optional with --calibrate)")
     ap.add_argument("--workload", default="llama3_8b", choices=["tiny", "llama13b", "llama3_8b", "opt175b_long"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--calls", type=int, default=20)
@@ -50,13 +60,21 @@ def main(argv=None):
                     help="make the step's launch plan once (pkv_paged_attention_plan) and trace the planned decode "
                          "call, as bench.py times it")
     ap.add_argument("--replay", action="store_true", help="replay the CTA lifetimes under other row orders")
+    ap.add_argument("--calibrate", action="store_true",
+                    help="time the decode call next to empty launches of its grid's shape (no trace needed)")
+    ap.add_argument("--threads", type=int, default=96, help="--calibrate: threads per CTA of the empty grid")
+    ap.add_argument("--smem", type=int, default=50224,
+                    help="--calibrate: dynamic shared memory (bytes) per CTA of the empty grid")
     args = ap.parse_args(argv)
 
     import torch
     from . import binding as B
     from . import workloads as W
-    B.LIB_PATH = os.path.abspath(args.lib)
-    if not B.trace_enabled():
+    if args.lib:
+        B.LIB_PATH = os.path.abspath(args.lib)
+    elif not args.calibrate:
+        raise SystemExit("--lib is required unless --calibrate is given")
+    if not args.calibrate and not B.trace_enabled():
         raise SystemExit(f"{args.lib} was not built with PKV_TRACE=1")
 
     dev = torch.device("cuda", 0)
@@ -78,6 +96,12 @@ def main(argv=None):
     anatomy = []
     if args.planned:
         B.paged_attention_plan(l_d, t_d, hq, hkv, d, partition_size=args.partition)
+    if args.calibrate:
+        def decode():
+            B.paged_attention_decode(out, q, k_pool, v_pool, t_d, l_d, shape.scale, partition_size=args.partition,
+                                     planned=args.planned)
+        calibrate(args, shape, decode, flush, stamps, lens.size * hkv)
+        return
     B.set_trace_buffer(buf)
     try:
         for i in range(args.calls):
@@ -124,6 +148,47 @@ def main(argv=None):
 
     if args.replay:
         replay(tiles, life, lens, shape.num_kv_heads, max(resident) if resident else 1)
+
+
+def calibrate(args, shape, decode, flush, stamps, ctas):
+    """Event-timed medians (and means) over args.calls launches, L2 evicted
+    before each launch and outside the events."""
+    import torch
+    from . import binding as B
+    dev = flush.device
+    calls = max(args.calls, 20)
+
+    def timed(fn):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(calls)]
+        for i in range(calls + 3):
+            flush.sum()
+            if i >= 3:
+                ev[i - 3][0].record()
+            fn()
+            if i >= 3:
+                ev[i - 3][1].record()
+        torch.cuda.synchronize()
+        t = np.array([a.elapsed_time(b) * 1e3 for a, b in ev])
+        return np.median(t), t.mean()
+
+    rows = [("decode call" + (" (planned)" if args.planned else ""), decode),
+            ("empty kernel, 1 CTA x 32 threads", lambda: B.trace_empty_grid(dev, 1, 32, 0)),
+            (f"empty kernel, {ctas} CTAs x {args.threads} threads, {args.smem} B shared",
+             lambda: B.trace_empty_grid(dev, ctas, args.threads, args.smem))]
+    for name, fn in rows:
+        med, mean = timed(fn)
+        print(f"{shape.name}: {name}: median {med:.2f} us, mean {mean:.2f} us ({calls} launches)")
+    gaps = []
+    for _ in range(calls):
+        flush.sum()
+        B.trace_stamp(stamps, 0)
+        B.trace_stamp(stamps, 1)
+        torch.cuda.synchronize()
+        s0, s1 = stamps.cpu().numpy()
+        gaps.append((s1 - s0) / 1e3)
+    print(f"{shape.name}: stamp -> stamp with nothing between: median {np.median(gaps):.2f} us")
+    if B.device_status(clear=True):
+        raise SystemExit("device checks tripped during the calibration")
 
 
 def modelled_span(order, seq_tiles, heads, slots, a, b):

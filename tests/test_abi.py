@@ -167,6 +167,9 @@ def test_tracing_is_off_in_the_default_build():
     # the clock stamp exists in every build and checks its word on the host
     assert B.lib().pkv_trace_stamp(None, None) == 1             # PKV_ERR_INVALID_ARG
     assert B.lib().pkv_trace_stamp(ctypes.c_void_p(12), None) == 1
+    # so does the empty grid (its shape is checked before any launch)
+    for ctas, threads, smem in [(0, 96, 0), (1, 0, 0), (1, 1025, 0), (1, 32, -1), (1, 32, 227 * 1024 + 1)]:
+        assert B.lib().pkv_trace_empty_grid(ctas, threads, smem, None) == 1, (ctas, threads, smem)
 
 
 def test_binding_scratch_size_matches_the_header():

@@ -62,3 +62,43 @@ def test_stamps_follow_the_stream():
         B.trace_stamp(words.to(torch.int32), 0)
     with pytest.raises(ValueError):
         B.trace_stamp(words, 4)
+
+
+def test_empty_grid_runs_in_stream_order():
+    """pkv_trace_empty_grid launches a kernel of the given shape that does
+    nothing: stamps around it are in order, the stream stays usable, and a
+    decode-shaped grid (2048 CTAs x 96 threads, 50 KB of shared memory) and
+    the largest shared-memory request both launch."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from paged_kv_cache_217_gb300 import binding as B
+    words = torch.zeros(2, dtype=torch.int64, device="cuda")
+    B.trace_stamp(words, 0)
+    B.trace_empty_grid("cuda", 2048, 96, 50224)
+    B.trace_empty_grid("cuda", 152, 1024, 227 * 1024)
+    B.trace_stamp(words, 1)
+    torch.cuda.synchronize()
+    w = words.cpu().tolist()
+    assert 0 < w[0] <= w[1], w
+    with pytest.raises(B.PagedKVError):
+        B.trace_empty_grid("cuda", 1, 32, 227 * 1024 + 1)
+    assert B.device_status(clear=True) == 0
+
+
+
+def test_calibration_on_the_default_build():
+    """--calibrate needs no trace build: it prints the decode call and the two
+    empty launches (median and mean, both positive) and the stamp gap."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    res = subprocess.run([sys.executable, "-m", "paged_kv_cache_217_gb300.trace", "--calibrate",
+                          "--workload", "tiny", "--calls", "20"],
+                         cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert res.returncode == 0, res.stderr[-2000:]
+    lines = [ln for ln in res.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 4, res.stdout
+    assert "decode call" in lines[0] and "1 CTA x 32 threads" in lines[1] and "16 CTAs x 96 threads" in lines[2]
+    for ln in lines[:3]:
+        med, mean = [float(x) for x in re.findall(r"([0-9.]+) us", ln)]
+        assert med > 0.0 and mean > 0.0, ln
+    assert float(re.findall(r"median ([0-9.]+) us", lines[3])[0]) > 0.0, lines[3]

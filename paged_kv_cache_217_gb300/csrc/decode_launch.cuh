@@ -34,6 +34,15 @@ constexpr int kGridWarps = 4;
 constexpr int kGridStages = 2;
 constexpr int kMmaWarps = 3;
 constexpr int kMmaStages = 2;
+// The shared-prefix schedule's CTAs (group rows) take 2 warps x 2 stages:
+// 32 KB of ring and 168 registers a thread hold 6 CTAs per SM (912), so the
+// LLaMA-13B beam batch's 640 group CTAs run in one wave: 57.0 us against
+// 59.5 us with 3 x 2 (4 per SM); the OPT-66B sampling batch (2304 group CTAs)
+// is 233.0 us either way. The plan's split rule still counts slots of the
+// 3 x 2 CTA (one wave of that shape's in-flight bytes): counting the 912 of
+// this one split the beam batch's groups and took 61.3 us.
+constexpr int kPrefixWarps = 2;
+constexpr int kPrefixStages = 2;
 
 // Launch with programmatic stream serialization: the grid may become resident
 // while the previous kernel in the stream finishes (the kernels wait for it
@@ -73,12 +82,27 @@ cudaError_t launch_cuda_core_grid(const DecodeArgs& a, dim3 grid, cudaStream_t s
   return launch_pdl(kern, grid, dim3(NW * 32), C::SMEM_BYTES, stream, a);
 }
 
+template <typename T, int D, int G, int MW, int MS>
+cudaError_t launch_mma_grid(const DecodeArgs& a, dim3 grid, const CUtensorMap* kmap, const CUtensorMap* vmap,
+                            cudaStream_t stream) {
+  using C = MmaCfg<T, D, MW, MS>;
+  auto kern = paged_decode_mma_kernel<T, D, G, MW, MS>;
+  static bool configured[kMaxDevices] = {};
+  cudaError_t err = configure_once(kern, C::SMEM_BYTES, configured);
+  if (err != cudaSuccess) return err;
+  PoolMaps maps;
+  for (int i = 0; i < 3; ++i) {
+    maps.k[i] = kmap[i];
+    maps.v[i] = vmap[i];
+  }
+  return launch_pdl(kern, grid, dim3(MW * 32), C::SMEM_BYTES, stream, a, maps);
+}
+
 template <typename T, int D, int G>
 cudaError_t launch_decode_dg(const DecodeArgs& a, const CUtensorMap* kmap, const CUtensorMap* vmap,
                              cudaStream_t stream) {
   constexpr int NW = kGridWarps;
   constexpr int STAGES = kGridStages;
-  static bool configured[kMaxDevices] = {};
   // (the shared-prefix schedule: rows for its chunks, then the sequences, one pass)
   const dim3 grid(unsigned(a.num_kv_heads), unsigned(a.num_seqs + (a.prefix_header ? a.prefix_slots : 0)),
                   a.prefix_header ? 1u : unsigned(a.max_parts));
@@ -88,24 +112,21 @@ cudaError_t launch_decode_dg(const DecodeArgs& a, const CUtensorMap* kmap, const
                                             : launch_cuda_core_grid<T, D, G, NW, STAGES>(a, grid, stream);
     if (err != cudaSuccess) return err;
   } else {
-    constexpr int MW = kMmaWarps, MS = kMmaStages;
-    using C = MmaCfg<T, D, MW, MS>;
-    auto kern = paged_decode_mma_kernel<T, D, G, MW, MS>;
-    cudaError_t err = configure_once(kern, C::SMEM_BYTES, configured);
-    if (err != cudaSuccess) return err;
-    PoolMaps maps;
-    for (int i = 0; i < 3; ++i) {
-      maps.k[i] = kmap[i];
-      maps.v[i] = vmap[i];
+    cudaError_t err;
+    if constexpr (G == kPrefixRows) {
+      err = a.prefix_header ? launch_mma_grid<T, D, G, kPrefixWarps, kPrefixStages>(a, grid, kmap, vmap, stream)
+                            : launch_mma_grid<T, D, G, kMmaWarps, kMmaStages>(a, grid, kmap, vmap, stream);
+    } else {
+      err = launch_mma_grid<T, D, G, kMmaWarps, kMmaStages>(a, grid, kmap, vmap, stream);
     }
-    err = launch_pdl(kern, grid, dim3(MW * 32), C::SMEM_BYTES, stream, a, maps);
     if (err != cudaSuccess) return err;
   }
   return cudaGetLastError();
 }
 
-// CTAs of the shared-prefix grid kernel (group rows kPrefixRows) that one SM
-// holds at once, times the SMs of the current device.
+// Slots the shared-prefix plan splits groups against: CTAs of the 3 x 2
+// group-row kernel that one SM holds at once, times the SMs of the current
+// device (the group CTAs themselves run 2 x 2, see kPrefixWarps).
 template <typename T, int D>
 cudaError_t prefix_resident_ctas_d(int* ctas) {
   using C = MmaCfg<T, D, kMmaWarps, kMmaStages>;

@@ -24,6 +24,13 @@ constexpr int kInt8MhaStages = 3;
 // Llama-3-8B-shaped layer 39.1 us with 4 warps, 37.5 us with 3 (4 CTAs per
 // SM); 3 warps for group size 1 made the LLaMA-13B layer 104.2 -> 113.7 us.
 constexpr int kInt8GqaWarps = 3;
+// One-query tile on one-pass grids of at most kLongGridCtas CTAs (few, long
+// CTAs, see kLongGridWarps): 8 warps x kInt8MhaStages (2 CTAs per SM, the
+// same 16 warps per SM), so the longest CTA streams at half its SM's rate
+// instead of a quarter. Measured on GB300, OPT-175B layer over INT8 (768
+// CTAs): 691.2-691.8 us with 4 x 3, 647.1-647.5 with 8 x 3, 649.2-649.3 with
+// 8 x 2, 675.5 with 6 x 3, 677.1-677.2 with 6 x 4.
+constexpr int kInt8LongWarps = 8;
 
 template <typename T, int D, int G>
 cudaError_t launch_int8_dg(const DecodeArgs& a, const CUtensorMap* kmap, const CUtensorMap* vmap,
@@ -36,6 +43,20 @@ cudaError_t launch_int8_dg(const DecodeArgs& a, const CUtensorMap* kmap, const C
                   a.prefix_header ? 1u : unsigned(a.max_parts));
   cudaError_t err = cudaSuccess;
   if constexpr (PKV_INT8_MMA) {
+    if constexpr (G == 1 && D <= 128) {
+      const int64_t ctas = int64_t(grid.x) * grid.y * grid.z;
+      if (grid.z == 1 && !a.prefix_header && ctas <= kLongGridCtas) {
+        using CL = I8Cfg<D, kInt8LongWarps, kInt8MhaStages>;
+        static_assert(CL::SMEM_BYTES <= 227 * 1024, "INT8 decode ring exceeds shared memory");
+        auto kern = paged_decode_mma_int8_kernel<T, D, G, kInt8LongWarps, kInt8MhaStages>;
+        static bool configured_long[kMaxDevices] = {};
+        err = configure_once(kern, CL::SMEM_BYTES, configured_long);
+        if (err != cudaSuccess) return err;
+        err = launch_pdl(kern, grid, dim3(kInt8LongWarps * 32), CL::SMEM_BYTES, stream, a, *kmap, *vmap);
+        if (err != cudaSuccess) return err;
+        return cudaGetLastError();
+      }
+    }
     using C = I8Cfg<D, NW, STAGES>;
     static_assert(C::SMEM_BYTES <= 227 * 1024, "INT8 decode ring exceeds shared memory");
     auto kern = paged_decode_mma_int8_kernel<T, D, G, NW, STAGES>;

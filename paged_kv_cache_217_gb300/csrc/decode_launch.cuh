@@ -71,6 +71,16 @@ cudaError_t launch_pdl(K kern, dim3 grid, dim3 block, size_t smem, cudaStream_t 
 // which keep the two-stage ring.
 constexpr int kWideGridWarps = 6;
 constexpr int64_t kWideGridCtas = 8192;
+// One-pass CUDA-core grids of at most kLongGridCtas CTAs (under two waves of
+// 4 x 2 CTAs at 3 per SM) hold few, long CTAs, and the longest CTA's own rate
+// (its share of its SM's copies: a third at 3 CTAs per SM) nears the whole
+// call: there the CTAs take 6 warps x 2 stages (2 per SM, the same 12 warps
+// and 192 KB of ring per SM). Measured on GB300, OPT-175B layer (768 CTAs):
+// 1177.0-1177.5 us with 4 x 2, 1160.4-1160.8 with 6 x 2, 1177.5-1177.9 with
+// 4 x 3 and 5 x 2, 1220.5-1221.0 with 3 x 2; LLaMA-13B layer (2560 CTAs):
+// 132.2-132.4 us with 4 x 2 against 133.7-133.8 with 6 x 2.
+constexpr int kLongGridWarps = 6;
+constexpr int64_t kLongGridCtas = 1024;
 
 template <typename T, int D, int G, int NW, int STAGES>
 cudaError_t launch_cuda_core_grid(const DecodeArgs& a, dim3 grid, cudaStream_t stream) {
@@ -108,7 +118,9 @@ cudaError_t launch_decode_dg(const DecodeArgs& a, const CUtensorMap* kmap, const
                   a.prefix_header ? 1u : unsigned(a.max_parts));
   if constexpr (G == 1) {
     const int64_t ctas = int64_t(grid.x) * grid.y * grid.z;
+    const bool long_grid = grid.z == 1 && !a.prefix_header && ctas <= kLongGridCtas;
     cudaError_t err = ctas >= kWideGridCtas ? launch_cuda_core_grid<T, D, G, kWideGridWarps, 1>(a, grid, stream)
+                      : long_grid           ? launch_cuda_core_grid<T, D, G, kLongGridWarps, STAGES>(a, grid, stream)
                                             : launch_cuda_core_grid<T, D, G, NW, STAGES>(a, grid, stream);
     if (err != cudaSuccess) return err;
   } else {

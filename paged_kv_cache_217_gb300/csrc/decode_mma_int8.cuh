@@ -606,7 +606,7 @@ __device__ __forceinline__ void prefix_cta_int8(const DecodeArgs& a, const CUten
 }
 
 template <typename T, int D, int G, int NW, int STAGES>
-__global__ void __launch_bounds__(NW * 32, (G == 1 && D <= 128) ? 4 : 0)  // one-query tile: 4 CTAs per SM
+__global__ void __launch_bounds__(NW * 32, (G == 1 && D <= 128) ? 16 / NW : 0)  // one-query tile: 128 registers
 paged_decode_mma_int8_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap kmap,
                              const __grid_constant__ CUtensorMap vmap) {
   using C = I8Cfg<D, NW, STAGES>;

@@ -79,8 +79,14 @@ constexpr int64_t kWideGridCtas = 8192;
 // 1177.0-1177.5 us with 4 x 2, 1160.4-1160.8 with 6 x 2, 1177.5-1177.9 with
 // 4 x 3 and 5 x 2, 1220.5-1221.0 with 3 x 2; LLaMA-13B layer (2560 CTAs):
 // 132.2-132.4 us with 4 x 2 against 133.7-133.8 with 6 x 2.
+// Split-K grids of at most kLongGridCtas CTAs take the same shape only when
+// their partitions are long: the first N sequences of the OPT-175B layer, 768
+// CTAs (672 for N = 1), 4 x 2 against 6 x 2: N = 4 (15168-token partitions)
+// 726.1 -> 713.7 us, N = 2 (7584) 396.9 -> 409.7 us, N = 1 (4336) 222.7 ->
+// 233.9 us; the change of sign lies near 12K tokens.
 constexpr int kLongGridWarps = 6;
 constexpr int64_t kLongGridCtas = 1024;
+constexpr int kLongSplitTokens = 12288;
 
 template <typename T, int D, int G, int NW, int STAGES>
 cudaError_t launch_cuda_core_grid(const DecodeArgs& a, dim3 grid, cudaStream_t stream) {
@@ -118,7 +124,8 @@ cudaError_t launch_decode_dg(const DecodeArgs& a, const CUtensorMap* kmap, const
                   a.prefix_header ? 1u : unsigned(a.max_parts));
   if constexpr (G == 1) {
     const int64_t ctas = int64_t(grid.x) * grid.y * grid.z;
-    const bool long_grid = grid.z == 1 && !a.prefix_header && ctas <= kLongGridCtas;
+    const bool long_ctas = grid.z == 1 || a.part_tokens >= kLongSplitTokens;
+    const bool long_grid = long_ctas && !a.prefix_header && ctas <= kLongGridCtas;
     cudaError_t err = ctas >= kWideGridCtas ? launch_cuda_core_grid<T, D, G, kWideGridWarps, 1>(a, grid, stream)
                       : long_grid           ? launch_cuda_core_grid<T, D, G, kLongGridWarps, STAGES>(a, grid, stream)
                                             : launch_cuda_core_grid<T, D, G, NW, STAGES>(a, grid, stream);

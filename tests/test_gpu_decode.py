@@ -190,6 +190,18 @@ def test_partition_size_invariance():
         assert np.abs(o - outs[0]).max() <= 4e-3
 
 
+def test_long_partitions_on_few_ctas():
+    """Grids of at most 1024 CTAs run 6-warp rings when each CTA streams a
+    long stretch: one pass, and split grids whose partitions hold at least
+    12288 tokens (12288 and 16384 here); 512-token partitions and the
+    library's own choice keep 4 warps. All against the oracle."""
+    case = H.make_case([25000, 12289], 2, 2, 128, "bf16", seed=21)
+    want = H.oracle_full(case)
+    outs = {p: H.to_f64(_run(case, p)) for p in (-1, 12288, 16384, 512, 0)}
+    for p, o in outs.items():
+        H.assert_attention_close(o, want, f"partition {p}")
+
+
 def test_cow_siblings_bit_identical_over_shared_prefix():
     hkv, d, prompt, n = 8, 128, 517, 4
     nb = 200

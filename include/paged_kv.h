@@ -184,12 +184,16 @@ pkv_status_t pkv_selftest_bounded_wait(uint32_t limit_us, pkv_stream_t stream);
  * workspace (see pkv_paged_attention_plan); it also puts sequences of at most
  * 5/8 of the mean length last (each group in natural order). Smaller batches
  * are ranked in every CTA. The order changes only when the work starts,
- * never the results.
- * That kernel reads context_lens without waiting for the previous kernel on
- * the stream to finish when that kernel allows programmatic early launch
- * (the library's cache writes do, and never touch context_lens): a kernel
- * that writes context_lens and allows early launch must not directly
- * precede this call.
+ * never the results. The plan also holds, per grid row, the sequence, its
+ * length and its first six block ids: the tensor-core kernel (groups of 2..8)
+ * starts its first tile copies from them before its own reads of the length
+ * and the table return, then compares them and copies again from the
+ * sequence's own values if they differ.
+ * That kernel reads context_lens and block_tables without waiting for the
+ * previous kernel on the stream to finish when that kernel allows
+ * programmatic early launch (the library's cache writes do, and touch
+ * neither): a kernel that writes context_lens or block_tables and allows
+ * early launch must not directly precede this call.
  *
  * Group size 1 runs on the CUDA cores; groups of 2..8 query heads per KV head
  * run the QK and PV products of each 16-token tile on the tensor cores (fp32
@@ -206,8 +210,10 @@ pkv_status_t pkv_paged_attention_decode(
 
 /* Bytes of workspace pkv_paged_attention_decode (and _decode_planned) needs
  * for these sizes: the split-K partials and counters, then the launch plan
- * (a 16-byte header and int32[num_seqs]) of batches of 2 to 1024 sequences in
- * grids of at most 4096 CTAs (see above); 0 for calls without either. For
+ * (a 16-byte header, int32[num_seqs] rounded up to 16 bytes, then int4[2 *
+ * num_seqs] of rows {sequence, length, block ids 0..5}) of batches of 2 to
+ * 1024 sequences in grids of at most 4096 CTAs (see above); 0 for calls
+ * without either. For
  * the shared-prefix schedule (-5): the split-K layout with 4 partitions (the
  * partials of split groups and one arrival counter per (sequence, KV head)),
  * then its plan: a 16-byte header, int4 groups[num_seqs / 2], int4
@@ -227,9 +233,11 @@ size_t pkv_paged_attention_workspace_size(
  * region of `workspace` (the bytes after the split-K scratch, see
  * pkv_paged_attention_workspace_size), and pkv_paged_attention_decode_planned
  * then uses it in every layer instead of ranking the batch itself.
- * Arguments as for pkv_paged_attention_decode; context_lens (and, for the
- * shared-prefix schedule, block_tables; otherwise it may be NULL) are read on
- * `stream` (device memory, the same values the decode calls will see). Does
+ * Arguments as for pkv_paged_attention_decode; context_lens and block_tables
+ * are read on `stream` (device memory, the same values the decode calls will
+ * see). block_tables may be NULL except for the shared-prefix schedule: the
+ * plan's rows then name no sequence and the decode reads every length and
+ * block id itself. Does
  * nothing when the sizes need no plan (one sequence, more than 1024, grids of
  * more than 4096 CTAs, the balanced schedule). For the shared-prefix schedule
  * (partition_size -5) the plan holds the sibling groups instead; its decode
@@ -245,8 +253,9 @@ pkv_status_t pkv_paged_attention_plan(const int32_t* context_lens, const int32_t
  * left in `workspace` for the same sizes: one kernel, no ranking. Same
  * arguments, semantics and results as pkv_paged_attention_decode (the plan
  * decides only when each sequence starts, never a result). A plan made from
- * other lengths of a batch of the same size is still correct (only the start
- * order is off). If the workspace holds no plan of this batch size, the
+ * other lengths or tables of a batch of the same size is still correct (the
+ * start order is off, and first tile copies made from the plan's rows are
+ * made again from the sequence's own length and ids). If the workspace holds no plan of this batch size, the
  * kernels flag PKV_DEV_BAD_PLAN and take the sequences in natural order,
  * still computing every output. The plan region must not be overwritten
  * between the plan and the decode calls that use it (a call with other sizes

@@ -93,10 +93,17 @@ constexpr int kOrderKernelMinSeqs = pkv::kRankInCtaMaxSeqs + 1;
 bool long_first_grid(int num_seqs, int num_kv_heads, int max_parts) {
   return int64_t(num_seqs) * num_kv_heads * max_parts <= kLongFirstMaxCtas;
 }
-// Plan region of the workspace: a 16-byte header, then int32[num_seqs].
+// Plan region of the workspace: a 16-byte header, int32[num_seqs] (the
+// order, rounded up to 16 bytes), then int4[2 * num_seqs] of rows {sequence,
+// length, block ids 0..5} in the order's ranks.
 size_t plan_bytes(int num_seqs, int num_kv_heads, int max_parts) {
   if (num_seqs < 2 || num_seqs > pkv::kOrderMaxSeqs || !long_first_grid(num_seqs, num_kv_heads, max_parts)) return 0;
-  return 16 + (size_t(num_seqs) * sizeof(int32_t) + 15) / 16 * 16;
+  return 16 + (size_t(num_seqs) * sizeof(int32_t) + 15) / 16 * 16 + size_t(num_seqs) * 32;
+}
+int4* plan_rows_of(int4* plan_hdr, int num_seqs) {
+  if (!plan_hdr) return nullptr;
+  return reinterpret_cast<int4*>(reinterpret_cast<char*>(plan_hdr) + 16 +
+                                 (size_t(num_seqs) * sizeof(int32_t) + 15) / 16 * 16);
 }
 
 // Sizes the shared-prefix schedule takes: batches the plan kernel covers,
@@ -513,6 +520,7 @@ pkv_status_t decode_impl(void* out, const void* q, const void* k_pool, const voi
   const bool use_plan = plan_hdr && (planned || make_plan);
   a.order = use_plan ? reinterpret_cast<const int32_t*>(plan_hdr + 1) : nullptr;
   a.plan = use_plan ? plan_hdr : nullptr;
+  a.plan_rows = use_plan && round_pow2_group(group) >= 2 && window <= 0 ? plan_rows_of(plan_hdr, num_seqs) : nullptr;
   a.status = status;
   a.num_seqs = num_seqs;
   a.num_q_heads = num_q_heads;
@@ -568,7 +576,7 @@ pkv_status_t decode_impl(void* out, const void* q, const void* k_pool, const voi
   }
   if (make_plan) {
     err = pkv::launch_seq_order(context_lens, num_seqs, max_blocks_per_seq * PKV_BLOCK_SIZE, a.window, true, plan_hdr,
-                                stream);
+                                block_tables, max_blocks_per_seq, plan_rows_of(plan_hdr, num_seqs), stream);
     if (err != cudaSuccess) return cuda_status(err, "launch plan");
   }
   err = dtype == PKV_F16 ? pkv::launch_decode_f16(a, head_dim, gpad, kmap, vmap, stream)
@@ -641,7 +649,8 @@ pkv_status_t pkv_paged_attention_plan(const int32_t* context_lens, const int32_t
                      lay.total + ord, workspace_bytes, workspace);
   int4* plan_hdr = reinterpret_cast<int4*>(static_cast<char*>(workspace) + lay.total);
   return cuda_status(pkv::launch_seq_order(context_lens, num_seqs, max_blocks_per_seq * PKV_BLOCK_SIZE, 0,
-                                           num_seqs >= kOrderKernelMinSeqs, plan_hdr, stream),
+                                           num_seqs >= kOrderKernelMinSeqs, plan_hdr, block_tables,
+                                           max_blocks_per_seq, plan_rows_of(plan_hdr, num_seqs), stream),
                      "launch plan");
 }
 
@@ -789,7 +798,7 @@ pkv_status_t decode_int8_impl(void* out, const void* q, const int8_t* k_cache, c
     }
     if (make_plan) {
       err = pkv::launch_seq_order(context_lens, num_seqs, max_blocks_per_seq * PKV_BLOCK_SIZE, 0, true, plan_hdr,
-                                  stream);
+                                  block_tables, max_blocks_per_seq, plan_rows_of(plan_hdr, num_seqs), stream);
       if (err != cudaSuccess) return cuda_status(err, "launch plan");
     }
   }

@@ -222,14 +222,16 @@ __global__ void bounded_wait_selftest_kernel(unsigned long long limit_ns, unsign
 // completion implies that predecessor's.
 __global__ void __launch_bounds__(1024)
 seq_order_kernel(const int32_t* __restrict__ lens, int S, int max_len, int window, int short_last,
-                 int32_t* __restrict__ order, int4* __restrict__ header) {
+                 int32_t* __restrict__ order, int4* __restrict__ header, const int32_t* __restrict__ tables,
+                 int max_blocks, int4* __restrict__ rows) {
   asm volatile("griddepcontrol.launch_dependents;");
   __shared__ long long part_tiles[32];
   __shared__ int part_long[32], part_rest[32], part_short[32];
   const int s = threadIdx.x, lane = s & 31, warp = s >> 5;
-  int tiles = 0;
+  int tiles = 0, raw_len = 0;
   if (s < S) {
     int L = __ldg(lens + s);
+    raw_len = L;
     L = L < 0 ? 0 : (L > max_len ? max_len : L);
     if (window > 0 && L > window) L = window;
     tiles = (L + kBlock - 1) / kBlock;
@@ -262,7 +264,17 @@ seq_order_kernel(const int32_t* __restrict__ lens, int S, int max_len, int windo
     n_long += part_long[w];
     n_rest += part_rest[w];
   }
-  if (s < S) order[b == 0 ? long_before : (b == 1 ? n_long + rest_before : n_long + n_rest + short_before)] = s;
+  if (s < S) {
+    const int rank = b == 0 ? long_before : (b == 1 ? n_long + rest_before : n_long + n_rest + short_before);
+    order[rank] = s;
+    if (rows) {  // the row of this rank: the sequence, its length and first six block ids (none without tables)
+      int id[6];
+#pragma unroll
+      for (int i = 0; i < 6; ++i) id[i] = tables && i < max_blocks ? __ldg(tables + size_t(s) * max_blocks + i) : -1;
+      rows[2 * rank] = make_int4(tables ? s : -1, raw_len, id[0], id[1]);
+      rows[2 * rank + 1] = make_int4(id[2], id[3], id[4], id[5]);
+    }
+  }
   if (s == 0) *header = make_int4(kPlanMagic, S, 0, 0);
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }
@@ -468,7 +480,7 @@ prefix_plan_kernel(const int32_t* __restrict__ lens, const int32_t* __restrict__
 }  // namespace
 
 cudaError_t launch_seq_order(const int32_t* lens, int num_seqs, int max_len, int window, bool short_last,
-                             int4* plan, cudaStream_t stream) {
+                             int4* plan, const int32_t* tables, int max_blocks, int4* rows, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(1);
   cfg.blockDim = dim3(unsigned((num_seqs + 31) / 32 * 32));
@@ -480,7 +492,8 @@ cudaError_t launch_seq_order(const int32_t* lens, int num_seqs, int max_len, int
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int32_t* order = reinterpret_cast<int32_t*>(plan + 1);
-  return cudaLaunchKernelEx(&cfg, seq_order_kernel, lens, num_seqs, max_len, window, short_last ? 1 : 0, order, plan);
+  return cudaLaunchKernelEx(&cfg, seq_order_kernel, lens, num_seqs, max_len, window, short_last ? 1 : 0, order, plan,
+                            tables, max_blocks, rows);
 }
 
 cudaError_t launch_prefix_plan(const int32_t* lens, const int32_t* tables, int num_seqs, int max_blocks,

@@ -70,6 +70,7 @@ struct DecodeArgs {
   int long_first;       // start sequences of twice the mean length first (long_first_seq)
   const int32_t* order; // long_first: grid row -> sequence from a launch plan (seq_order_kernel), or null
   const int4* plan;     // the plan's header {kPlanMagic, num_seqs, 0, 0}, checked before `order` is used
+  const int4* plan_rows; // launch plan rows {s, L, ids 0..5} per grid row (tensor-core one-pass grid), or null
   unsigned long long* trace;  // PKV_TRACE builds: per-CTA phase timestamps (8 words a CTA), or null
   int trace_records;          // CTAs the trace buffer holds
   int window;           // sliding window: attend over the last `window` tokens (0 = all)

@@ -235,6 +235,7 @@ paged_decode_mma_kernel(const DecodeArgs a, const __grid_constant__ PoolMaps map
   // Without a prefix plan of this batch the first S rows take every sequence
   // whole.
   int s;
+  int4 phdr = make_int4(0, 0, 0, 0), prow0 = make_int4(-1, 0, 0, 0), prow1 = make_int4(0, 0, 0, 0);
   if (a.prefix_header) {
     const int4 ph = __ldg(a.prefix_header);
     const bool planned = ph.x == kPlanMagicPrefix && ph.y == a.num_seqs;
@@ -256,44 +257,23 @@ paged_decode_mma_kernel(const DecodeArgs a, const __grid_constant__ PoolMaps map
     }
   } else {
     if (int(blockIdx.y) >= a.num_seqs) return;
+    if (a.plan_rows && a.window == 0 && gridDim.z == 1) {
+      phdr = __ldg(a.plan);
+      prow0 = __ldg(a.plan_rows + 2 * blockIdx.y);
+      prow1 = __ldg(a.plan_rows + 2 * blockIdx.y + 1);
+    }
     s = long_first_seq<NW>(a, int(blockIdx.y));
   }
+  const bool rows_ok = prow0.x == s && phdr.x == kPlanMagic && phdr.y == a.num_seqs;
   const int part = blockIdx.z;
   trace_mark(tm, 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int hq0 = g * a.group;
   const int gr = lane >> 2, t = lane & 3;   // MMA row (query head) and column pair of this lane
 
-  // Without a sliding window the first 32 block ids of this warp's tiles do
-  // not depend on the length: read them together with it (entries past the
-  // sequence are never used).
-  int ids_early = 0;
-  if (a.window == 0) {
-    const int j0 = (blockIdx.z * a.part_tokens) / kBlock + warp + lane * NW;
-    if (j0 < a.max_blocks_per_seq) ids_early = __ldg(a.block_tables + size_t(s) * a.max_blocks_per_seq + j0);
-  }
-  int L = a.context_lens[s];
-  const int max_len = a.max_blocks_per_seq * kBlock;
-  if (L < 0 || L > max_len) {
-    if (threadIdx.x == 0 && part == 0 && g == 0) flag(a.status, PKV_DEV_BAD_CONTEXT_LEN);
-    L = L < 0 ? 0 : max_len;
-  }
-  const TokenRange tr = token_range(L, a.window);
-  const int nparts = L == 0 ? 1 : (L - tr.aligned + a.part_tokens - 1) / a.part_tokens;
-  if (part >= nparts) return;
-  const int pslot = part;  // partition slot of this CTA's partial in the workspace
-  trace_mark(tm, 2);
-  if (L == 0) {
-    T* o = static_cast<T*>(a.out) + (size_t(s) * a.num_q_heads + hq0) * D;
-    for (int i = threadIdx.x; i < a.group * D / 8; i += NW * 32)
-      reinterpret_cast<uint4*>(o)[i] = make_uint4(0u, 0u, 0u, 0u);
-    return;
-  }
-  const int t0 = tr.aligned + part * a.part_tokens;
-  const int ntok = min(L, t0 + a.part_tokens) - t0;
-  const int nb = (ntok + kBlock - 1) / kBlock;
-  const int head = part == 0 ? tr.first - tr.aligned : 0;  // rows before the window in tile 0
-
+  // This warp's ring and barriers first: with a launch plan, the row of this
+  // grid row may start the warp's first copies before its own length and
+  // block ids arrive.
   unsigned char* ring = smem + size_t(warp) * STAGES * C::STAGE_BYTES;
   const uint32_t ring_s = smem_addr(ring);
   const uint32_t bar_s = smem_addr(smem + C::RING_BYTES) + warp * STAGES * 8;
@@ -304,55 +284,16 @@ paged_decode_mma_kernel(const DecodeArgs a, const __grid_constant__ PoolMaps map
   }
   __syncwarp();
 
-  // Q as the A operand: row gr holds query head hq0 + gr (zero past the group).
-  uint32_t qa[C::KSTEPS][2];
-  {
-    const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
-        static_cast<const T*>(a.q) + (size_t(s) * a.num_q_heads + hq0 + gr) * D);
-#pragma unroll
-    for (int ks = 0; ks < C::KSTEPS; ++ks) {
-      qa[ks][0] = gr < a.group ? __ldg(qrow + 8 * ks + t) : 0u;
-      qa[ks][1] = gr < a.group ? __ldg(qrow + 8 * ks + 4 + t) : 0u;
-    }
-  }
-
-  const int n_my = nb > warp ? (nb - warp + NW - 1) / NW : 0;
-  const int32_t* trow = a.block_tables + size_t(s) * a.max_blocks_per_seq + t0 / kBlock;
-  auto load_ids = [&](int batch) -> int {
-    const int k = batch * 32 + lane;
-    if (k >= n_my) return 0;
-    int id = __ldg(trow + warp + k * NW);
-    if (id < 0 || id >= a.num_blocks) {
-      flag(a.status, PKV_DEV_BAD_BLOCK_ID);
-      id = 0;
-    }
-    return id;
-  };
-  int ids = 0;
-  if (lane < n_my) {
-    ids = a.window == 0 ? ids_early : __ldg(trow + warp + lane * NW);
-    if (ids < 0 || ids >= a.num_blocks) {
-      flag(a.status, PKV_DEV_BAD_BLOCK_ID);
-      ids = 0;
-    }
-  }
-  int ids_next = n_my > 32 ? load_ids(1) : 0;
-  int id_batch = 0;
-
-  auto issue = [&](int k) {  // warp-uniform; k increases by one per call
-    if ((k >> 5) != id_batch) {
-      ids = ids_next;
-      ++id_batch;
-      ids_next = (id_batch + 1) * 32 < n_my ? load_ids(id_batch + 1) : 0;
-    }
-    const int id = __shfl_sync(kFull, ids, k & 31);
+  // Lane 0 copies tile k of this warp (table position warp + k * NW of a
+  // sequence stretch of ntk tokens) from physical block id.
+  auto copy_tile = [&](int k, int id, int ntk) {
     if (lane == 0) {
       const int st = k % STAGES;
       const uint32_t bar = bar_s + 8 * st;
       const uint32_t dst = ring_s + st * C::STAGE_BYTES;
       const int y = (id * a.num_kv_heads + g) * kBlock;
       // rows copied: all 16, or the valid rows rounded up to a multiple of 4
-      const int cover = min(kBlock, (ntok - (warp + k * NW) * kBlock + 3) & ~3);
+      const int cover = min(kBlock, (ntk - (warp + k * NW) * kBlock + 3) & ~3);
       mbar_arrive_expect_tx(bar, uint32_t(cover) * (C::STAGE_BYTES / kBlock));
       if (cover == kBlock) {
 #pragma unroll
@@ -380,13 +321,187 @@ paged_decode_mma_kernel(const DecodeArgs a, const __grid_constant__ PoolMaps map
     }
   };
 
+  // Without a sliding window the first 32 block ids of this warp's tiles do
+  // not depend on the length: read them together with it (entries past the
+  // sequence are never used).
+  const int max_len = a.max_blocks_per_seq * kBlock;
+  int ids_early = 0;
+  if (a.window == 0) {
+    const int j0 = (blockIdx.z * a.part_tokens) / kBlock + warp + lane * NW;
+    if (j0 < a.max_blocks_per_seq) ids_early = __ldg(a.block_tables + size_t(s) * a.max_blocks_per_seq + j0);
+  }
+  int L = a.context_lens[s];
+  // Q as the A operand: row gr holds query head hq0 + gr (zero past the group);
+  // the block ids, the length and Q are all requested before the speculative
+  // copies below and before anything waits for them.
+  uint32_t qa[C::KSTEPS][2];
+  {
+    const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
+        static_cast<const T*>(a.q) + (size_t(s) * a.num_q_heads + hq0 + gr) * D);
+#pragma unroll
+    for (int ks = 0; ks < C::KSTEPS; ++ks) {
+      qa[ks][0] = gr < a.group ? __ldg(qrow + 8 * ks + t) : 0u;
+      qa[ks][1] = gr < a.group ? __ldg(qrow + 8 * ks + 4 + t) : 0u;
+    }
+  }
+
+  // Speculative start: the plan row's length and first block ids (table
+  // positions 0..5) give this warp's first tiles. They are checked against
+  // the sequence's own length and ids before the first tile is used, and
+  // copied again from those if they differ (a plan made for other lengths or
+  // tables), so the plan never decides a result.
+  // spec: the CTA runs on the row's length (the same in every warp); spec_n:
+  // the tiles this warp started from the row (0 when it has none to start).
+  bool spec = false;
+  int spec_n = 0, spec_len = 0;
+  int spec_id[STAGES];
+#pragma unroll
+  for (int k = 0; k < STAGES; ++k) spec_id[k] = 0;
+  if constexpr (NW * STAGES <= 6) {
+    if (rows_ok && prow0.y > 0 && prow0.y <= max_len) {
+      spec = true;
+      spec_len = prow0.y;
+      const int nb_s = (spec_len + kBlock - 1) / kBlock;
+      const int n_s = min(nb_s > warp ? (nb_s - warp + NW - 1) / NW : 0, STAGES);
+#pragma unroll
+      for (int k = 0; k < STAGES; ++k) {
+        if (k >= n_s || spec_n < k) continue;
+        const int pos = warp + k * NW;
+        const int id = pos == 0 ? prow0.z : pos == 1 ? prow0.w : pos == 2 ? prow1.x : pos == 3 ? prow1.y
+                     : pos == 4 ? prow1.z : prow1.w;
+        if (id < 0 || id >= a.num_blocks) continue;  // stop here; the sequence's own ids are checked below
+        spec_id[k] = id;
+        copy_tile(k, id, spec_len);
+        spec_n = k + 1;
+      }
+    }
+  }
+  // Waits for the speculative copies to land (before their stages are reused or the CTA exits).
+  auto drain_spec = [&]() {
+#pragma unroll
+    for (int k = 0; k < STAGES; ++k)
+      if (k < spec_n && !mbar_wait_bounded(bar_s + 8 * k, 0) && lane == 0) flag(a.status, PKV_DEV_WAIT_TIMEOUT);
+    __syncwarp();
+  };
+
+  // The sequence's length: its own (checked), or with a speculative start
+  // the plan row's, compared with its own below before any tile is used.
+  auto checked_len = [&](int len) {
+    if (len < 0 || len > max_len) {
+      if (threadIdx.x == 0 && part == 0 && g == 0) flag(a.status, PKV_DEV_BAD_CONTEXT_LEN);
+      len = len < 0 ? 0 : max_len;
+    }
+    return len;
+  };
+  const int L_own = L;
+  if (spec)
+    L = spec_len;
+  else
+    L = checked_len(L_own);
+  auto write_zeros = [&]() {
+    T* o = static_cast<T*>(a.out) + (size_t(s) * a.num_q_heads + hq0) * D;
+    for (int i = threadIdx.x; i < a.group * D / 8; i += NW * 32)
+      reinterpret_cast<uint4*>(o)[i] = make_uint4(0u, 0u, 0u, 0u);
+  };
+  const TokenRange tr = token_range(L, a.window);
+  const int nparts = L == 0 ? 1 : (L - tr.aligned + a.part_tokens - 1) / a.part_tokens;
+  if (part >= nparts) return;  // (split grids only; no speculative copies there)
+  const int pslot = part;  // partition slot of this CTA's partial in the workspace
+  trace_mark(tm, 2);
+  if (L == 0) {  // (never on the row's length)
+    write_zeros();
+    return;
+  }
+  const int t0 = tr.aligned + part * a.part_tokens;
+  int ntok = min(L, t0 + a.part_tokens) - t0;
+  int nb = (ntok + kBlock - 1) / kBlock;
+  const int head = part == 0 ? tr.first - tr.aligned : 0;  // rows before the window in tile 0
+
+  int n_my = nb > warp ? (nb - warp + NW - 1) / NW : 0;
+  const int32_t* trow = a.block_tables + size_t(s) * a.max_blocks_per_seq + t0 / kBlock;
+  auto load_ids = [&](int batch) -> int {
+    const int k = batch * 32 + lane;
+    if (k >= n_my) return 0;
+    int id = __ldg(trow + warp + k * NW);
+    if (id < 0 || id >= a.num_blocks) {
+      flag(a.status, PKV_DEV_BAD_BLOCK_ID);
+      id = 0;
+    }
+    return id;
+  };
+  int ids = 0;
+  auto first_ids = [&]() {
+    ids = 0;
+    if (lane < n_my) {
+      ids = a.window == 0 ? ids_early : __ldg(trow + warp + lane * NW);
+      if (ids < 0 || ids >= a.num_blocks) {
+        flag(a.status, PKV_DEV_BAD_BLOCK_ID);
+        ids = 0;
+      }
+    }
+  };
+  int ids_next = 0, id_batch = 0;
+  if (!spec) {
+    first_ids();
+    ids_next = n_my > 32 ? load_ids(1) : 0;
+  }
+
+  auto issue = [&](int k) {  // warp-uniform; k increases by one per call
+    if ((k >> 5) != id_batch) {
+      ids = ids_next;
+      ++id_batch;
+      ids_next = (id_batch + 1) * 32 < n_my ? load_ids(id_batch + 1) : 0;
+    }
+    copy_tile(k, __shfl_sync(kFull, ids, k & 31), ntok);
+  };
+
   float o[C::NTILES][4];
 #pragma unroll
   for (int nd = 0; nd < C::NTILES; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
   float mrun = -INFINITY, lrun = 0.f;
 
-  const int pre = n_my < STAGES ? n_my : STAGES;
-  for (int k = 0; k < pre; ++k) issue(k);
+  // Keep the speculative copies only if they are exactly the first copies of
+  // this warp (same length, same block ids); else drain them, reset the
+  // barriers and copy from the sequence's own length and ids. The length
+  // test is the same in every warp of the CTA.
+  int pre = n_my < STAGES ? n_my : STAGES;
+  bool started = false;
+  if (spec) {  // (one pass, no window: ids_early holds table positions warp + lane * NW)
+    const int own = checked_len(L_own);
+    bool same = own == spec_len && spec_n == pre;
+#pragma unroll
+    for (int k = 0; k < STAGES; ++k)
+      if (k < spec_n) same = same && __shfl_sync(kFull, ids_early, k) == spec_id[k];
+    if (same) {
+      started = true;
+    } else {
+      drain_spec();
+      if (lane == 0) {
+#pragma unroll
+        for (int st = 0; st < STAGES; ++st) {
+          mbar_inval(bar_s + 8 * st);
+          mbar_init(bar_s + 8 * st, 1);
+        }
+        mbar_init_fence();
+      }
+      __syncwarp();
+      if (own != spec_len) {  // one pass, no window: the stretch is the whole sequence
+        if (own == 0) {  // every warp of the CTA comes here
+          write_zeros();
+          return;
+        }
+        L = own;
+        ntok = L;
+        nb = (ntok + kBlock - 1) / kBlock;
+        n_my = nb > warp ? (nb - warp + NW - 1) / NW : 0;
+        pre = n_my < STAGES ? n_my : STAGES;
+      }
+    }
+    first_ids();  // checked (and flagged) against the settled tile count only
+    ids_next = n_my > 32 ? load_ids(1) : 0;
+  }
+  if (!started)
+    for (int k = 0; k < pre; ++k) issue(k);
 
   for (int k = 0; k < n_my; ++k) {
     const int st = k % STAGES;

@@ -34,9 +34,11 @@ int decode_sk_max_seqs(int head_dim, int gpad);
 
 // The launch plan of a batch (num_seqs <= 1024) into `plan`: a 16-byte header
 // {magic, num_seqs, 0, 0}, then the long-first order int32[num_seqs] (grid row
-// -> sequence; the shortest sequences last with short_last).
+// -> sequence; the shortest sequences last with short_last); with `rows`, also
+// int4[2 * num_seqs] per rank {sequence, length, ids 0..5 of `tables`} (the
+// sequence -1 when tables is null).
 cudaError_t launch_seq_order(const int32_t* lens, int num_seqs, int max_len, int window, bool short_last,
-                             int4* plan, cudaStream_t stream);
+                             int4* plan, const int32_t* tables, int max_blocks, int4* rows, cudaStream_t stream);
 
 // The prefix plan of the shared-prefix schedule (decode_prefix.cuh): header,
 // groups int4[num_seqs / 2], chunks int4[num_seqs], the sequences outside any

@@ -51,23 +51,29 @@ def _balanced_bytes(S, hq, hkv, d):
     return _round16(2 * 2048 * slot_floats * 4 + S * hkv * 4)
 
 
+def _plan_bytes(S):
+    """Launch plan: a 16-byte header, the order int32[S] (16-byte rounded), then
+    int4[2 S] of rows {sequence, length, block ids 0..5}."""
+    return 16 + _round16(4 * S) + 32 * S
+
+
 def test_workspace_and_partition_choice():
     # automatic choice: one CTA per (sequence, KV head) with at least 608 pairs
     assert B.resolved_partition(64, 40, 40, 128, 32) == -1          # 2560 pairs
     assert B.resolved_partition(256, 32, 8, 128, 64) == -1          # 2048 pairs
     # 2..1024 sequences in a grid of at most 4096 CTAs: a launch plan region, a
-    # 16-byte header and int32[num_seqs] (16-byte rounded)
-    assert B.workspace_size(64, 40, 40, 128, 32) == 16 + 256
-    assert B.workspace_size(256, 32, 8, 128, 64) == 16 + 256 * 4
-    assert B.workspace_size(130, 8, 8, 128, 64) == 16 + 528          # 130 * 4 rounded up to 16
-    assert B.workspace_size(2, 8, 8, 128, 1) == 16 + 16
+    # 16-byte header, int32[num_seqs] (16-byte rounded) and two int4 rows a sequence
+    assert B.workspace_size(64, 40, 40, 128, 32) == 16 + 256 + 64 * 32
+    assert B.workspace_size(256, 32, 8, 128, 64) == 16 + 256 * 4 + 256 * 32
+    assert B.workspace_size(130, 8, 8, 128, 64) == 16 + 528 + 130 * 32    # 130 * 4 rounded up to 16
+    assert B.workspace_size(2, 8, 8, 128, 1) == _plan_bytes(2)
     assert B.workspace_size(1, 8, 8, 128, 1) == 0                    # one sequence: nothing to order
     assert B.workspace_size(512, 16, 16, 128, 64) == 0               # 8192 CTAs: no long-first order
     assert B.workspace_size(1025, 1, 1, 128, 64) == 0                # beyond the plan's 1024 sequences
     assert B.resolved_partition(8, 96, 96, 128, 2048) == -1         # 768 pairs
     # fewer pairs: partitions just large enough for 608 CTAs, at least 256 tokens
     assert B.resolved_partition(2, 8, 8, 128, 2048) == 864          # 16 pairs x 38 parts
-    assert B.workspace_size(2, 8, 8, 128, 2048) == _split_bytes(2, 8, 8, 128, 38) + 32
+    assert B.workspace_size(2, 8, 8, 128, 2048) == _split_bytes(2, 8, 8, 128, 38) + _plan_bytes(2)
     assert B.resolved_partition(4, 4, 4, 64, 100) == 256            # 16 pairs, 1600 tokens
     assert B.resolved_partition(4, 4, 4, 64, 16) == -1              # 256 tokens: one pass
     # the shared-prefix schedule, on request: two partial slots, then the
@@ -85,12 +91,12 @@ def test_workspace_and_partition_choice():
     # explicit choices
     assert B.resolved_partition(8, 96, 96, 128, 2048, -1) == -1
     assert B.resolved_partition(8, 96, 96, 128, 2048, 256) == 256
-    assert B.workspace_size(8, 96, 96, 128, 2048, -1) == 16 + 32       # 768 CTAs: the plan region
+    assert B.workspace_size(8, 96, 96, 128, 2048, -1) == _plan_bytes(8)   # 768 CTAs: the plan region
     assert B.workspace_size(8, 96, 96, 128, 2048, 512) == _split_bytes(8, 96, 96, 128, 64)  # 49152 CTAs
-    assert B.workspace_size(3, 6, 2, 64, 10, 16) == _split_bytes(3, 6, 2, 64, 10) + 32
+    assert B.workspace_size(3, 6, 2, 64, 10, 16) == _split_bytes(3, 6, 2, 64, 10) + _plan_bytes(3)
     # a partition that covers the whole context is one pass
     assert B.resolved_partition(4, 4, 4, 64, 4, 64) == -1
-    assert B.workspace_size(4, 4, 4, 64, 4, 64) == 32
+    assert B.workspace_size(4, 4, 4, 64, 4, 64) == _plan_bytes(4)
     # invalid partition sizes
     assert B.resolved_partition(4, 4, 4, 64, 4, 24) == 0
     assert B.workspace_size(0, 4, 4, 64, 4) == 0

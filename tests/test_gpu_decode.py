@@ -387,11 +387,28 @@ def _dispatch_order(lens, max_len, short_last=True):
     return longs + rest + shorts
 
 
+def _plan_at(need, S):
+    """Offset of the plan's order array: the plan region ends the workspace with
+    a 16-byte header, int32[S] (16-byte rounded), then int4[2 S] of rows."""
+    return need - 32 * S - (4 * S + 15) // 16 * 16
+
+
+def _plan_rows_want(order, lens, tables):
+    """The rows the plan promises, rank by rank: {sequence, its length, its
+    first six block ids (-1 past the table's width)}."""
+    t = tables.cpu().numpy()
+    rows = []
+    for s in order:
+        ids = [int(t[s, i]) if i < t.shape[1] else -1 for i in range(6)]
+        rows.append([s, int(lens[s])] + ids)
+    return rows
+
+
 @pytest.mark.parametrize("S,hkv,seed", [(128, 8, 0), (150, 4, 1), (256, 8, 2), (1024, 4, 3)])
 def test_ordering_kernel_writes_the_promised_order(S, hkv, seed):
-    # the order array (int32[S], the last 16-byte-rounded bytes of the
-    # workspace, after any split-K scratch) is index work: it must equal the
-    # host restatement exactly
+    # the order array (int32[S] after a 16-byte header) and the rows behind
+    # it (int4[2 S], the last bytes of the workspace, after any split-K
+    # scratch) are index work: they must equal the host restatement exactly
     rng = np.random.default_rng(40 + seed)
     lens = np.clip(np.round(150 * np.exp(0.6 * rng.standard_normal(S))), 8, 1024).astype(np.int32)
     lens[rng.integers(0, S, 3)] = 0
@@ -399,7 +416,7 @@ def test_ordering_kernel_writes_the_promised_order(S, hkv, seed):
     case = H.make_case(lens, 2 * hkv, hkv, 64, "f16", seed=50 + seed)
     mb = case.tables.shape[1]
     need = B.workspace_size(S, 2 * hkv, hkv, 64, mb)
-    at = need - (4 * S + 15) // 16 * 16
+    at = _plan_at(need, S)
     assert at >= 16 and at % 16 == 0
     ws = torch.full((need,), 0xFF, dtype=torch.uint8, device="cuda")
     out = torch.empty_like(case.q)
@@ -411,6 +428,8 @@ def test_ordering_kernel_writes_the_promised_order(S, hkv, seed):
     assert got == want
     assert ws[at - 16:at].view(torch.int32).cpu().tolist() == [PLAN_MAGIC, S, 0, 0]
     assert sorted(got) == list(range(S))
+    rows = ws[need - 32 * S:need].view(torch.int32).view(S, 8).cpu().tolist()
+    assert rows == _plan_rows_want(want, lens, case.tables)
     _check_sampled(case, out, 16, seed=seed)
     assert B.device_status(clear=True) == 0
 
@@ -454,7 +473,7 @@ def test_planned_decode_matches_the_oracle_and_the_unplanned_call(S, hq, hkv, d,
     B.paged_attention_plan(case.lens, case.tables, hq, hkv, d, part, workspace=ws)
     parts = 1 if part == 0 else -(-mb * 16 // part)
     if S * hkv * parts <= 4096:     # a grid that starts long sequences first has a plan
-        at = need - (4 * S + 15) // 16 * 16
+        at = _plan_at(need, S)
         assert ws[at - 16:at].view(torch.int32).cpu().tolist() == [PLAN_MAGIC, S, 0, 0]
         # smaller batches keep two buckets, batches of 128+ put the shortest last
         order = ws[at:at + 4 * S].view(torch.int32).cpu().tolist()
@@ -498,6 +517,66 @@ def test_a_plan_of_other_lengths_is_still_correct():
     torch.cuda.synchronize()
     assert B.device_status(clear=True) == 0
     H.assert_attention_close(H.to_f64(out), H.oracle_full(case), "stale plan")
+
+
+@pytest.mark.parametrize("change", ["all ids", "one id", "lengths and ids"])
+def test_a_plan_of_other_tables_is_still_correct(change):
+    """The tensor-core kernel starts its first copies from the plan's rows and
+    checks them against the sequence's own length and ids: a plan made from
+    other tables (every id, a single id of the first six, or lengths and
+    ids) gives the same outputs as a fresh plan, bit for bit, and no flag."""
+    lens = _lognormal_lens(256, seed=9)
+    case = H.make_case(lens, 32, 8, 128, "bf16", seed=79)
+    mb = case.tables.shape[1]
+    need = B.workspace_size(256, 32, 8, 128, mb)
+    ws = torch.empty((need,), dtype=torch.uint8, device="cuda")
+    B.paged_attention_plan(case.lens, case.tables, 32, 8, 128, workspace=ws)
+    fresh = case.new_out()
+    B.paged_attention_decode(fresh, case.q, case.k_pool, case.v_pool, case.tables, case.lens, case.scale,
+                             workspace=ws, planned=True)
+    tables = case.tables.clone()
+    plan_lens = case.lens
+    nb = case.k_pool.shape[0]
+    if change == "all ids":
+        tables = torch.where(tables >= 0, (tables + 7) % nb, tables)
+    elif change == "one id":
+        long_rows = (case.lens > 16 * 5).nonzero().flatten()
+        tables[long_rows, 5] = (tables[long_rows, 5] + 1) % nb
+    else:
+        tables = torch.roll(tables, 3, dims=0)
+        plan_lens = torch.roll(case.lens, 3)
+    B.paged_attention_plan(plan_lens, tables, 32, 8, 128, workspace=ws)
+    stale = case.new_out()
+    B.paged_attention_decode(stale, case.q, case.k_pool, case.v_pool, case.tables, case.lens, case.scale,
+                             workspace=ws, planned=True)
+    torch.cuda.synchronize()
+    assert B.device_status(clear=True) == 0
+    assert torch.equal(stale, fresh)
+    H.assert_attention_close(H.to_f64(stale), H.oracle_full(case), f"plan of other tables ({change})")
+
+
+def test_a_plan_without_tables_names_no_sequence():
+    """pkv_paged_attention_plan with NULL block_tables (allowed outside the
+    shared-prefix schedule) writes rows that name no sequence; the decode
+    reads every length and id itself, with the same outputs."""
+    lens = _lognormal_lens(200, seed=10)
+    case = H.make_case(lens, 16, 4, 128, "f16", seed=80)
+    S, mb = case.tables.shape
+    need = B.workspace_size(S, 16, 4, 128, mb)
+    ws = torch.full((need,), 0x11, dtype=torch.uint8, device="cuda")
+    st = B.lib().pkv_paged_attention_plan(case.lens.data_ptr(), None, S, 16, 4, 128, mb, 0, ws.data_ptr(), need,
+                                         torch.cuda.current_stream().cuda_stream)
+    assert st == 0
+    torch.cuda.synchronize()
+    rows = ws[need - 32 * S:need].view(torch.int32).view(S, 8).cpu().numpy()
+    assert (rows[:, 0] == -1).all() and (rows[:, 2:] == -1).all()
+    out = case.new_out()
+    B.paged_attention_decode(out, case.q, case.k_pool, case.v_pool, case.tables, case.lens, case.scale,
+                             workspace=ws, planned=True)
+    torch.cuda.synchronize()
+    assert B.device_status(clear=True) == 0
+    assert torch.equal(out, _run(case))
+    H.assert_attention_close(H.to_f64(out), H.oracle_full(case), "plan without tables")
 
 
 # ---------------------------------------------------------------------------

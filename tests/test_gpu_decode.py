@@ -463,6 +463,7 @@ def _lognormal_lens(S, seed, median=150, sigma=0.6, hi=1024):
 
 @pytest.mark.parametrize("S,hq,hkv,d,dtype,part", [(64, 40, 40, 128, "bf16", 0), (256, 32, 8, 128, "bf16", 0),
                                                    (150, 8, 4, 64, "f16", 0), (40, 16, 8, 128, "f16", 0),
+                                                   (320, 16, 2, 256, "bf16", 0), (180, 8, 4, 64, "bf16", 0),
                                                    (200, 4, 4, 64, "bf16", 256), (300, 4, 4, 64, "bf16", 128)])
 def test_planned_decode_matches_the_oracle_and_the_unplanned_call(S, hq, hkv, d, dtype, part):
     lens = _lognormal_lens(S, seed=S + d)

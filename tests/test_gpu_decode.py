@@ -556,6 +556,33 @@ def test_a_plan_of_other_tables_is_still_correct(change):
     H.assert_attention_close(H.to_f64(stale), H.oracle_full(case), f"plan of other tables ({change})")
 
 
+@pytest.mark.parametrize("mb", [1, 3, 5])
+def test_plan_rows_of_narrow_tables(mb):
+    """Tables narrower than the six block ids of a plan row: the row holds -1
+    past the table, the speculative start stops there and the rest of the
+    first tiles come from the sequence's own ids; one pass (-1) on the
+    tensor cores, exact against the oracle and against the unplanned call."""
+    rng = np.random.default_rng(30 + mb)
+    S = 200
+    lens = rng.integers(0, 16 * mb + 1, S).astype(np.int32)
+    case = H.make_case(lens, 8, 2, 64, "bf16", seed=90 + mb)
+    assert case.tables.shape[1] == mb
+    need = B.workspace_size(S, 8, 2, 64, mb, -1)
+    ws = torch.full((need,), 0x3C, dtype=torch.uint8, device="cuda")
+    B.paged_attention_plan(case.lens, case.tables, 8, 2, 64, -1, workspace=ws)
+    torch.cuda.synchronize()
+    order = ws[_plan_at(need, S):_plan_at(need, S) + 4 * S].view(torch.int32).cpu().tolist()
+    rows = ws[need - 32 * S:need].view(torch.int32).view(S, 8).cpu().tolist()
+    assert rows == _plan_rows_want(order, lens, case.tables)
+    out = case.new_out()
+    B.paged_attention_decode(out, case.q, case.k_pool, case.v_pool, case.tables, case.lens, case.scale,
+                             partition_size=-1, workspace=ws, planned=True)
+    torch.cuda.synchronize()
+    assert B.device_status(clear=True) == 0
+    assert torch.equal(out, _run(case, -1))
+    H.assert_attention_close(H.to_f64(out), H.oracle_full(case), f"narrow tables ({mb} blocks)")
+
+
 def test_a_plan_without_tables_names_no_sequence():
     """pkv_paged_attention_plan with NULL block_tables (allowed outside the
     shared-prefix schedule) writes rows that name no sequence; the decode

@@ -202,9 +202,12 @@ def test_decode_int8_balanced_rejected():
     assert ei.value.status == 2
 
 
-@pytest.mark.parametrize("name", ["llama13b", "llama3_8b"])
+@pytest.mark.parametrize("name", ["llama13b", "llama3_8b", "opt175b"])
 def test_decode_int8_full_size_sampled(name):
-    shape = {"llama13b": W.llama13b_mha_decode, "llama3_8b": W.llama3_8b_gqa_decode}[name](0)
+    # the OPT-175B layer (768 CTAs of 16-32k tokens) runs the 8-warp one-query
+    # tile, whose warps walk more than 32 blocks of ids each
+    shape = {"llama13b": W.llama13b_mha_decode, "llama3_8b": W.llama3_8b_gqa_decode,
+             "opt175b": W.opt175b_long_decode}[name](0)
     case = Int8Case(shape.context_lens, shape.num_q_heads, shape.num_kv_heads, shape.head_dim, shape.dtype,
                     seed=1)
     got = case.run()
